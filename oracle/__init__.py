@@ -1,0 +1,19 @@
+"""fp64 CPU oracle for the MARS hot path (test infrastructure only).
+
+Only the test suite, the package smoke check and the benchmark's CPU-baseline leg may
+import this package. The CUDA library never uses it.
+"""
+from .mars_oracle import (  # noqa: F401
+    accept_count,
+    ar_signal_fraction,
+    attn_dual_stream,
+    beta,
+    decode_attn,
+    gather_prefix,
+    head_accept,
+    head_logits,
+    kv_commit,
+    mask_M,
+    mask_rows,
+    maxprob_argmax,
+)

@@ -1,0 +1,291 @@
+"""Plain, slow, fp64 CPU oracle for the MARS block-masked attention and decode epilogue.
+
+TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the benchmark's
+CPU-baseline leg may import or run this module. The CUDA library and its Python binding
+never import it, and it imports nothing from them: the two share no code.
+
+What it follows. The method is "MARS (Mask AutoRegreSsion)" from the paper
+"MARS: Enabling Autoregressive Models Multi-Token Generation" (Jin, Wang, Luo, Sun,
+arXiv 2604.07023). Citations name the web page and its section:
+
+  [notes]  the papernotes.org NeurIPS 2026 reading notes of the paper (Chinese). The only
+           page that prints formulas. Sections used:
+             Key design 1 (关键设计 1): the 2L x 2L dual-stream mask M over z = [x; x~],
+               with the block index beta(t) = ceil(t / B);
+             Key design 2 (关键设计 2): the loss L_mask + L_AR and the AR-signal fractions;
+             Key design 3 (关键设计 3): left-to-right threshold acceptance;
+             Key design 4 (关键设计 4): the block-level KV cache.
+  [gist]   the gist.science English explainer, "2. Methodology", part C (Inference
+           Mechanism) and part D (Block-Level KV Caching).
+
+Readings taken where the pages are silent (each also listed in the design doc):
+  * indices: M is stated 1-indexed; mask_M keeps that form, arrays are 0-indexed;
+  * softmax scale: not stated, 1/sqrt(D);
+  * grouped-query attention: not on the pages, query head h uses KV head h // (Hq/Hkv);
+  * decode form: B [MASK] queries appended after the committed prefix; query k sees the
+    whole prefix and block keys 0..k (causal inside the block);
+  * "maximum probability": full-vocabulary softmax at temperature 1, argmax ties go to the
+    lowest vocabulary index;
+  * acceptance starts at block position 0, ">=" is inclusive, at least one token, at most B;
+    tau is a float32 value compared exactly in fp64;
+  * commit: each sequence's own N rows are written every step (per-sequence commit).
+
+Every function takes float64 numpy arrays (callers pass bf16-rounded values converted to
+float64) and returns float64 / int64 numpy arrays. Nothing is blocked, fused or reordered
+beyond what the definitions state; matmul (BLAS) is the only library primitive used.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+# ---------------------------------------------------------------------------------------
+# Key design 1 [notes]: block index and the dual-stream mask M.
+# ---------------------------------------------------------------------------------------
+
+def beta(t, B: int):
+    """Block index beta(t) = ceil(t / B) of a 1-indexed stream position t ([notes], Key
+    design 1, definition under eq. M). Works on ints and integer numpy arrays."""
+    return -((-np.asarray(t)) // B) if isinstance(t, np.ndarray) else -((-t) // B)
+
+
+def mask_M(L: int, B: int) -> np.ndarray:
+    """The 2L x 2L visibility matrix of mask M ([notes], Key design 1, eq. M).
+
+    Entry [i-1, j-1] is True where M_ij = 0 (key j visible to query i), for 1-indexed
+    i, j in 1..2L. Rows/cols 1..L are the clean stream x, L+1..2L the masked stream x~:
+      case 1: i, j <= L and j <= i                         (clean stream, causal)
+      case 2: i, j > L, beta(i-L) = beta(j-L), j <= i      (masked stream, causal in block)
+      case 3: i > L, j <= L, beta(j) < beta(i-L)           (masked -> strictly earlier
+                                                            clean blocks)
+      otherwise M_ij = -inf (not visible).
+    The last block is shorter when B does not divide L; beta stays ceil(t/B).
+    """
+    if L < 1 or B < 1:
+        raise ValueError("L and B must be >= 1")
+    i = np.arange(1, 2 * L + 1)[:, None]
+    j = np.arange(1, 2 * L + 1)[None, :]
+    case1 = (i <= L) & (j <= L) & (j <= i)
+    bi = beta(np.maximum(i - L, 1), B)   # clamp only keeps beta defined where it is unused
+    bj = beta(np.maximum(j - L, 1), B)
+    case2 = (i > L) & (j > L) & (bi == bj) & (j <= i)
+    case3 = (i > L) & (j <= L) & (beta(j, B) < bi)
+    return case1 | case2 | case3
+
+
+def mask_rows(L: int, B: int, rows) -> np.ndarray:
+    """Rows `rows` (0-indexed) of mask_M(L, B), built from the same three cases without
+    materialising the whole 2L x 2L matrix (used for sampled rows at large L)."""
+    i = (np.asarray(rows, dtype=np.int64) + 1)[:, None]
+    j = np.arange(1, 2 * L + 1)[None, :]
+    case1 = (i <= L) & (j <= L) & (j <= i)
+    bi = beta(np.maximum(i - L, 1), B)
+    bj = beta(np.maximum(j - L, 1), B)
+    case2 = (i > L) & (j > L) & (bi == bj) & (j <= i)
+    case3 = (i > L) & (j <= L) & (beta(j, B) < bi)
+    return case1 | case2 | case3
+
+
+# ---------------------------------------------------------------------------------------
+# Key design 2 [notes]: the AR-signal fraction, counted from M.
+# ---------------------------------------------------------------------------------------
+
+def ar_signal_fraction(L: int, B: int, combined: bool) -> float:
+    """Fraction of predicted positions whose context is the full clean history
+    ([notes], Key design 2: r_AR = 1/B with L_mask only, (1 + 1/B)/2 with L_mask + L_AR).
+
+    Counted directly from M: a masked-stream row i = L + t (t = 1..L) has a fully clean
+    context when its visible set is exactly the clean keys 1..t-1 plus itself; a clean row
+    i has one when its visible set is exactly clean keys 1..i. With L_mask only the L
+    masked rows carry loss; with L_mask + L_AR all 2L rows do.
+    """
+    vis = mask_M(L, B)
+    n = 2 * L
+    cols = np.arange(1, n + 1)
+    clean_ok = 0
+    for i in range(1, L + 1):
+        want = cols <= i
+        clean_ok += int(np.array_equal(vis[i - 1], want))
+    masked_ok = 0
+    for t in range(1, L + 1):
+        i = L + t
+        want = (cols <= t - 1) | (cols == i)
+        masked_ok += int(np.array_equal(vis[i - 1], want))
+    if combined:
+        return (clean_ok + masked_ok) / (2 * L)
+    return masked_ok / L
+
+
+# ---------------------------------------------------------------------------------------
+# Attention under M (training form): softmax(scale * Q K^T + M) V per (batch, q head).
+# ---------------------------------------------------------------------------------------
+
+def _masked_softmax_rows(S: np.ndarray, vis: np.ndarray) -> np.ndarray:
+    """Row softmax of S with entries where vis is False set to -inf first."""
+    S = np.where(vis, S, NEG_INF)
+    m = S.max(axis=1, keepdims=True)
+    P = np.exp(S - m)
+    return P / P.sum(axis=1, keepdims=True)
+
+
+def attn_dual_stream(q, k, v, L: int, B: int, scale: float | None = None, rows=None,
+                     heads=None, batches=None):
+    """Dual-stream attention output O for z = [x; x~] under mask M.
+
+    q: [b, 2L, Hq, D]; k, v: [b, 2L, Hkv, D] (float64). Returns O [b, 2L, Hq, D] float64,
+    or, when `rows` is given, O[:, rows] only ([notes], overall framework: both streams in
+    one forward; Key design 1, eq. M). `heads`/`batches` restrict the work to those query
+    heads / batch items (others left as NaN) so large shapes can be sampled.
+    """
+    b, n, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if n != 2 * L:
+        raise ValueError("sequence length of q must be 2L")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    vis = mask_rows(L, B, rows)
+    out = np.full((b, len(rows), Hq, D), np.nan)
+    for bi in (range(b) if batches is None else batches):
+        for h in (range(Hq) if heads is None else heads):
+            hk = h // g
+            S = scale * (q[bi, rows, h, :] @ k[bi, :, hk, :].T)
+            P = _masked_softmax_rows(S, vis)
+            out[bi, :, h, :] = P @ v[bi, :, hk, :]
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# Decode form ([gist] 2.C, 2.D; [notes] Key design 3, Key design 4): B [MASK] queries per
+# sequence over the committed prefix in a paged cache, causal inside the block.
+# ---------------------------------------------------------------------------------------
+
+def gather_prefix(pool, block_table_row, P: int, page_size: int):
+    """Logical rows 0..P-1 of one sequence's cache: pool[page, hkv, slot, :] with
+    page = block_table_row[t // page_size], slot = t % page_size. Returns [P, Hkv, D]."""
+    Hkv, D = pool.shape[1], pool.shape[3]
+    out = np.empty((P, Hkv, D))
+    for t in range(P):
+        page = int(block_table_row[t // page_size])
+        out[t] = pool[page, :, t % page_size, :]
+    return out
+
+
+def decode_attn(q, k_blk, v_blk, k_pool, v_pool, block_table, seq_lens, page_size: int,
+                scale: float | None = None, seqs=None):
+    """Attention output of the B appended [MASK] queries of each sequence.
+
+    q: [b, B, Hq, D]; k_blk, v_blk: [b, B, Hkv, D]; k_pool, v_pool: [pages, Hkv, page_size,
+    D]; block_table: [b, max_pages] int; seq_lens: [b] committed prefix lengths P_s.
+    Keys of sequence s: the P_s prefix rows, then the B block rows; query k sees every
+    prefix row and block rows 0..k. Returns O [b, B, Hq, D] float64 (NaN for sequences
+    not in `seqs`).
+    """
+    b, B, Hq, D = q.shape
+    Hkv = k_blk.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.full(q.shape, np.nan)
+    for s in (range(b) if seqs is None else seqs):
+        P = int(seq_lens[s])
+        K = np.concatenate([gather_prefix(k_pool, block_table[s], P, page_size), k_blk[s]])
+        V = np.concatenate([gather_prefix(v_pool, block_table[s], P, page_size), v_blk[s]])
+        j = np.arange(P + B)[None, :]
+        kq = np.arange(B)[:, None]
+        vis = (j < P) | ((j - P) <= kq)
+        for h in range(Hq):
+            hk = h // g
+            S = scale * (q[s, :, h, :] @ K[:, hk, :].T)
+            out[s, :, h, :] = _masked_softmax_rows(S, vis) @ V[:, hk, :]
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# Step epilogue: LM-head logits, max-prob and argmax, threshold acceptance
+# ([notes] Key design 3; [gist] 2.C "Confidence Thresholding").
+# ---------------------------------------------------------------------------------------
+
+def head_logits(h, w_vocab_major, chunk: int = 16384):
+    """logits[r, v] = sum_d h[r, d] * W[v, d] for h [R, H] and W stored [V, H]; computed
+    in vocabulary chunks to bound memory."""
+    R = h.shape[0]
+    V = w_vocab_major.shape[0]
+    out = np.empty((R, V))
+    for c0 in range(0, V, chunk):
+        out[:, c0:c0 + chunk] = h @ w_vocab_major[c0:c0 + chunk].T
+    return out
+
+
+def maxprob_argmax(logits):
+    """Per row: token = lowest index attaining the max logit; maxprob = max_v softmax(l)_v
+    = 1 / sum_v exp(l_v - max); gap = max minus the second-largest logit (0 on ties).
+    Returns (tokens int64 [R], maxprob float64 [R], gap float64 [R])."""
+    m = logits.max(axis=1)
+    tokens = np.argmax(logits, axis=1)          # first occurrence = lowest index
+    maxprob = 1.0 / np.exp(logits - m[:, None]).sum(axis=1)
+    part = np.partition(logits, -2, axis=1)
+    gap = part[:, -1] - part[:, -2]
+    return tokens.astype(np.int64), maxprob, gap
+
+
+def accept_count(maxprob_row, tau) -> int:
+    """Left-to-right acceptance for one sequence ([notes] Key design 3): walk positions
+    0, 1, ... accepting while maxprob >= tau, stop at the first position below tau; at
+    least one token is always accepted and at most B (the row length). tau is taken as
+    the float32 value the caller passes, compared in float64."""
+    t = float(np.float32(tau))
+    n = 0
+    for p in maxprob_row:
+        if p >= t:
+            n += 1
+        else:
+            break
+    return max(1, n)
+
+
+def head_accept(h, w_vocab_major, batch: int, B: int, tau):
+    """The whole epilogue for a step: h [batch*B, H] (row s*B + k = sequence s, block
+    position k), W [V, H]. Returns (tokens [batch, B], maxprob [batch, B], n_accept
+    [batch], gap [batch, B])."""
+    tokens, maxprob, gap = maxprob_argmax(head_logits(h, w_vocab_major))
+    tokens = tokens.reshape(batch, B)
+    maxprob = maxprob.reshape(batch, B)
+    gap = gap.reshape(batch, B)
+    n = np.array([accept_count(maxprob[s], tau) for s in range(batch)], dtype=np.int64)
+    return tokens, maxprob, n, gap
+
+
+# ---------------------------------------------------------------------------------------
+# Commit into the block-level KV cache ([notes] Key design 4; [gist] 2.D), per sequence.
+# ---------------------------------------------------------------------------------------
+
+def kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
+              page_size: int):
+    """Copy the first N_s block rows of sequence s into the paged cache and advance its
+    length: for i < N_s, pos = seq_len_s + i, page = block_table[s, pos // page_size],
+    slot = pos % page_size, pool[page, :, slot, :] = blk[s, i, :, :]. Returns (new k_pool,
+    new v_pool, new seq_lens, commit_slots [b, B]) with commit_slots = page * page_size +
+    slot for committed rows and -1 otherwise. Inputs are not modified."""
+    k_pool = k_pool.copy()
+    v_pool = v_pool.copy()
+    b, B = k_blk.shape[0], k_blk.shape[1]
+    slots = np.full((b, B), -1, dtype=np.int64)
+    new_lens = np.array(seq_lens, dtype=np.int64).copy()
+    for s in range(b):
+        for i in range(int(n_accept[s])):
+            pos = int(seq_lens[s]) + i
+            page = int(block_table[s][pos // page_size])
+            slot = pos % page_size
+            k_pool[page, :, slot, :] = k_blk[s, i]
+            v_pool[page, :, slot, :] = v_blk[s, i]
+            slots[s, i] = page * page_size + slot
+        new_lens[s] = int(seq_lens[s]) + int(n_accept[s])
+    return k_pool, v_pool, new_lens, slots

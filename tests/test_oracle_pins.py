@@ -1,0 +1,392 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: a hand enumeration of
+eq. M, the AR-signal percentages printed on the pages, a library routine (torch SDPA,
+softmax, argmax) in fp64, a brute-force scalar loop, or an identity between the two
+attention forms. The last section plants plausible mistakes in the oracle and checks
+that some pin catches each of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import mars_oracle
+from block_masked_token_gb300 import workloads as W
+from conftest import golden_lines
+
+
+def _read_mask(name):
+    lines = golden_lines(name)
+    L = int(lines[0].split()[1])
+    B = int(lines[1].split()[1])
+    rows = [[c == "1" for c in ln.strip()] for ln in lines[2:]]
+    return L, B, np.array(rows, dtype=bool)
+
+
+# ------------------------------------------------------------------ mask M (Key design 1)
+
+@pytest.mark.parametrize("name", ["mask_M_L4_B2.txt", "mask_M_L3_B2.txt",
+                                  "mask_M_L4_B4.txt", "mask_M_L3_B1.txt"])
+def test_mask_matches_hand_enumeration(name):
+    L, B, want = _read_mask(name)
+    assert want.shape == (2 * L, 2 * L)
+    np.testing.assert_array_equal(oracle.mask_M(L, B), want)
+
+
+def test_beta_is_ceil():
+    for B in range(1, 9):
+        for t in range(1, 40):
+            assert oracle.beta(t, B) == math.ceil(t / B)
+
+
+@pytest.mark.parametrize("L", list(range(1, 17)))
+def test_mask_invariants(L):
+    for B in range(1, L + 1):
+        vis = oracle.mask_M(L, B)
+        # every row sees itself, so no softmax row is empty
+        assert vis.diagonal().all()
+        # the clean stream never sees the masked stream, and is plainly causal
+        assert not vis[:L, L:].any()
+        np.testing.assert_array_equal(vis[:L, :L], np.tril(np.ones((L, L), bool)))
+        # nothing sees a later position in its own stream
+        assert not np.triu(vis[L:, L:], 1).any()
+        # masked row t sees t keys: t - B*(beta(t)-1) in its block plus B*(beta(t)-1)
+        # clean ones; the total is L(L+1)/2 (clean) + L(L+1)/2 (masked) = L(L+1)
+        assert vis.sum() == L * (L + 1)
+        if B == L:
+            assert not vis[L:, :L].any()
+        if B == 1:
+            for t in range(1, L + 1):
+                row = vis[L + t - 1]
+                assert row[:t - 1].all() and not row[t - 1:L].any()
+                assert row[L + t - 1] and row[L:].sum() == 1
+
+
+def test_mask_rows_equals_full_matrix():
+    for L, B in [(7, 3), (16, 4), (9, 9), (33, 5)]:
+        rows = np.arange(2 * L)
+        np.testing.assert_array_equal(oracle.mask_rows(L, B, rows), oracle.mask_M(L, B))
+
+
+# --------------------------------------------------------- AR-signal fraction (Key design 2)
+
+def test_ar_signal_fraction_printed_values():
+    for line in golden_lines("r_ar_printed.txt"):
+        B, mode, pct, dec = line.split()
+        B, pct, dec = int(B), float(pct), int(dec)
+        L = 64                                     # any L divisible by B
+        got = 100.0 * oracle.ar_signal_fraction(L, B, combined=(mode == "combined"))
+        assert abs(got - pct) <= 0.5 * 10.0 ** (-dec) + 1e-12, (B, mode, got, pct)
+
+
+def test_ar_signal_fraction_closed_form():
+    for B in (1, 2, 4, 8, 16):
+        L = 4 * B
+        assert oracle.ar_signal_fraction(L, B, False) == pytest.approx(1.0 / B)
+        assert oracle.ar_signal_fraction(L, B, True) == pytest.approx((1 + 1.0 / B) / 2)
+        assert oracle.ar_signal_fraction(L, B, True) > 0.5
+
+
+# ------------------------------------------------------------- dual-stream attention
+
+def _rand(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g, dtype=torch.float64).numpy()
+
+
+def _sdpa(q, k, v, mask=None, causal=False):
+    # q [n, D], k/v [n, D] for one head; fp64 library routine on CPU
+    Q = torch.from_numpy(q)[None, None]
+    K = torch.from_numpy(k)[None, None]
+    V = torch.from_numpy(v)[None, None]
+    m = None if mask is None else torch.from_numpy(mask)[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(
+        Q, K, V, attn_mask=m, is_causal=causal)[0, 0].numpy()
+
+
+@pytest.mark.parametrize("L,B,hq,hkv,D", [(5, 2, 2, 1, 8), (16, 4, 4, 2, 16),
+                                          (13, 16, 3, 3, 8), (24, 3, 6, 2, 32)])
+def test_dual_stream_against_sdpa(L, B, hq, hkv, D):
+    b = 2
+    q = _rand((b, 2 * L, hq, D), 1)
+    k = _rand((b, 2 * L, hkv, D), 2)
+    v = _rand((b, 2 * L, hkv, D), 3)
+    out = oracle.attn_dual_stream(q, k, v, L, B)
+    vis = oracle.mask_M(L, B)
+    g = hq // hkv
+    for bi in range(b):
+        for h in range(hq):
+            hk = h // g
+            # clean half: plain causal attention over the clean stream
+            ref_clean = _sdpa(q[bi, :L, h], k[bi, :L, hk], v[bi, :L, hk], causal=True)
+            np.testing.assert_allclose(out[bi, :L, h], ref_clean, rtol=1e-12, atol=1e-12)
+            ref = _sdpa(q[bi, :, h], k[bi, :, hk], v[bi, :, hk], mask=vis)
+            np.testing.assert_allclose(out[bi, :, h], ref, rtol=1e-12, atol=1e-12)
+
+
+def _brute_attention_row(qrow, K, V, visible, scale):
+    scores = []
+    for j in range(len(K)):
+        if visible[j]:
+            scores.append((j, scale * sum(a * b for a, b in zip(qrow, K[j]))))
+    m = max(s for _, s in scores)
+    w = [(j, math.exp(s - m)) for j, s in scores]
+    tot = sum(x for _, x in w)
+    D = len(V[0])
+    return [sum(x * V[j][d] for j, x in w) / tot for d in range(D)]
+
+
+def test_dual_stream_bruteforce_hand_mask():
+    L, B, vis = _read_mask("mask_M_L4_B2.txt")
+    D = 4
+    q = _rand((1, 2 * L, 2, D), 4)
+    k = _rand((1, 2 * L, 1, D), 5)
+    v = _rand((1, 2 * L, 1, D), 6)
+    out = oracle.attn_dual_stream(q, k, v, L, B, scale=0.7)
+    for h in range(2):
+        for i in range(2 * L):
+            ref = _brute_attention_row(q[0, i, h].tolist(), k[0, :, 0].tolist(),
+                                       v[0, :, 0].tolist(), vis[i], 0.7)
+            np.testing.assert_allclose(out[0, i, h], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_dual_stream_row_sampling_matches_full():
+    L, B = 20, 4
+    q = _rand((2, 2 * L, 4, 8), 7)
+    k = _rand((2, 2 * L, 2, 8), 8)
+    v = _rand((2, 2 * L, 2, 8), 9)
+    full = oracle.attn_dual_stream(q, k, v, L, B)
+    rows = [0, 3, 19, 20, 27, 39]
+    part = oracle.attn_dual_stream(q, k, v, L, B, rows=rows, heads=[1, 3], batches=[1])
+    np.testing.assert_allclose(part[1][:, [1, 3]], full[1][rows][:, [1, 3]], rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------------- decode form
+
+def _paged_from_logical(logical, page_size, perm, Hkv, D):
+    """Scatter logical rows [P, Hkv, D] into the pages listed in perm (test-side layout);
+    unused slots keep random values. Returns (pool, block-table row)."""
+    pool = _rand((max(perm) + 2, Hkv, page_size, D), 99)
+    for t in range(len(logical)):
+        pool[perm[t // page_size], :, t % page_size, :] = logical[t]
+    return pool, np.array(list(perm) + [-1, -1])
+
+
+@pytest.mark.parametrize("B,P,ps", [(4, 8, 4), (2, 6, 16), (8, 16, 16), (1, 5, 4), (3, 9, 2)])
+def test_decode_equals_masked_stream_row(B, P, ps):
+    """A decode query at a block-aligned prefix P equals the masked-stream row L + P + k
+    of the dual-stream form, with the prefix as the clean stream and the block keys as the
+    masked stream (Key design 1 vs Key design 3/4: same visibility)."""
+    assert P % B == 0
+    Hq, Hkv, D = 4, 2, 8
+    L = P + B + 3                           # extra positions after the block are masked
+    q2 = _rand((1, 2 * L, Hq, D), 10)
+    k2 = _rand((1, 2 * L, Hkv, D), 11)
+    v2 = _rand((1, 2 * L, Hkv, D), 12)
+    dual = oracle.attn_dual_stream(q2, k2, v2, L, B)
+    perm = list(np.random.default_rng(0).permutation(P // ps + 3))
+    kpool, bt = _paged_from_logical(k2[0, :P], ps, perm, Hkv, D)
+    vpool, _ = _paged_from_logical(v2[0, :P], ps, perm, Hkv, D)
+    qd = q2[:, L + P:L + P + B]
+    kb = k2[:, L + P:L + P + B]
+    vb = v2[:, L + P:L + P + B]
+    dec = oracle.decode_attn(qd, kb, vb, kpool, vpool, bt[None, :], np.array([P]), ps)
+    np.testing.assert_allclose(dec[0], dual[0, L + P:L + P + B], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_bruteforce():
+    B, Hq, Hkv, D, ps = 3, 2, 1, 4, 4
+    lens = [5, 0, 9]
+    b = len(lens)
+    q = _rand((b, B, Hq, D), 20)
+    kb = _rand((b, B, Hkv, D), 21)
+    vb = _rand((b, B, Hkv, D), 22)
+    kpool = _rand((12, Hkv, ps, D), 23)
+    vpool = _rand((12, Hkv, ps, D), 24)
+    bt = np.array([[3, 7, -1, -1], [1, -1, -1, -1], [11, 0, 5, -1]])
+    out = oracle.decode_attn(q, kb, vb, kpool, vpool, bt, np.array(lens), ps, scale=0.5)
+    for s in range(b):
+        keys = [kpool[bt[s][t // ps], 0, t % ps].tolist() for t in range(lens[s])]
+        vals = [vpool[bt[s][t // ps], 0, t % ps].tolist() for t in range(lens[s])]
+        keys += kb[s, :, 0].tolist()
+        vals += vb[s, :, 0].tolist()
+        for kq in range(B):
+            visible = [True] * lens[s] + [i <= kq for i in range(B)]
+            for h in range(Hq):
+                ref = _brute_attention_row(q[s, kq, h].tolist(), keys, vals, visible, 0.5)
+                np.testing.assert_allclose(out[s, kq, h], ref, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------- head, max-prob, acceptance
+
+def test_maxprob_argmax_against_torch():
+    g = torch.Generator().manual_seed(3)
+    logits = (torch.randn(64, 1000, generator=g, dtype=torch.float64) * 4).numpy()
+    logits[5, 10] = logits[5, 900] = logits[5].max() + 1.0       # exact tie
+    tok, p, gap = oracle.maxprob_argmax(logits)
+    T = torch.from_numpy(logits)
+    np.testing.assert_allclose(p, torch.softmax(T, dim=1).max(dim=1).values.numpy(),
+                               rtol=1e-13)
+    first_max = [int(np.flatnonzero(r == r.max())[0]) for r in logits]
+    np.testing.assert_array_equal(tok, first_max)
+    no_tie = np.arange(64) != 5
+    np.testing.assert_array_equal(tok[no_tie], T.argmax(dim=1).numpy()[no_tie])
+    assert tok[5] == 10 and gap[5] == 0.0
+    assert (p > 1.0 / 1000).all() and (p <= 1.0).all() and (gap >= 0).all()
+
+
+def test_head_logits_chunked_equals_matmul():
+    h = _rand((6, 40), 30)
+    w = _rand((1000, 40), 31)
+    np.testing.assert_allclose(oracle.head_logits(h, w, chunk=97), h @ w.T, rtol=1e-11, atol=1e-12)
+
+
+def test_acceptance_golden_cases():
+    for line in golden_lines("acceptance_cases.txt"):
+        tau, ps, n = [x.strip() for x in line.split("|")]
+        probs = [float(x) for x in ps.split()]
+        assert oracle.accept_count(probs, float(tau)) == int(n), line
+
+
+def test_acceptance_properties_on_seeded_inputs():
+    cfg = W.TINY_DECODE
+    inp = W.make_decode_inputs(cfg, seed=0)
+    h = W.to_f64(inp.h[0])
+    w = W.to_f64(inp.w)
+    tok, p, n1, gap = oracle.head_accept(h, w, cfg.batch, cfg.B, 1.0)
+    assert (n1 == 1).all()                                  # tau = 1.0: plain AR
+    assert (p < 1.0).all()
+    _, _, n0, _ = oracle.head_accept(h, w, cfg.batch, cfg.B, 0.0)
+    assert (n0 == cfg.B).all()                              # tau = 0: the whole block
+    _, _, nbig, _ = oracle.head_accept(h, w, cfg.batch, cfg.B, 1.5)
+    assert (nbig == 1).all()
+    prev = None
+    for tau in np.linspace(0.0, 1.0, 41):
+        n = np.array([oracle.accept_count(p[s], tau) for s in range(cfg.batch)])
+        assert ((n >= 1) & (n <= cfg.B)).all()
+        if prev is not None:
+            assert (n <= prev).all()                        # N non-increasing in tau
+        prev = n
+
+
+def test_tau_one_gives_one_token_at_7b_vocab():
+    """tau = 1.0 accepts exactly one token per step at the 7B vocabulary size, with the
+    synthetic h/W distribution (log-uniform scales up to 8)."""
+    g = torch.Generator().manual_seed(1)
+    H, V, R = 64, 152064, 16
+    s = torch.exp(math.log(0.5) + (math.log(8) - math.log(0.5)) * torch.rand(R, 1, generator=g))
+    h = (torch.randn(R, H, generator=g) * s).to(torch.bfloat16).double().numpy()
+    w = (torch.randn(V, H, generator=g) / math.sqrt(H)).to(torch.bfloat16).double().numpy()
+    _, p, n, _ = oracle.head_accept(h, w, 2, 8, 1.0)
+    assert (n == 1).all() and (p < 1).all()
+
+
+# ------------------------------------------------------------------------- commit
+
+def test_commit_golden_case():
+    kv = dict(ln.split(None, 1) for ln in golden_lines("commit_case.txt"))
+    ps = int(kv["page_size"])
+    bt = np.array([[int(x) for x in kv["block_table"].split()]])
+    sl = np.array([int(kv["seq_len"])])
+    B = int(kv["B"])
+    n = np.array([int(kv["N"])])
+    Hkv, D = 2, 3
+    kb = _rand((1, B, Hkv, D), 40)
+    vb = _rand((1, B, Hkv, D), 41)
+    kp = _rand((8, Hkv, ps, D), 42)
+    vp = _rand((8, Hkv, ps, D), 43)
+    kp2, vp2, sl2, slots = oracle.kv_commit(kb, vb, n, sl, bt, kp, vp, ps)
+    np.testing.assert_array_equal(slots[0], [int(x) for x in kv["slots"].split()])
+    assert sl2[0] == int(kv["new_seq_len"])
+    for i, sl_ in enumerate(slots[0]):
+        if sl_ >= 0:
+            np.testing.assert_array_equal(kp2[sl_ // ps, :, sl_ % ps], kb[0, i])
+            np.testing.assert_array_equal(vp2[sl_ // ps, :, sl_ % ps], vb[0, i])
+
+
+def test_commit_properties():
+    ps, Hkv, D, B = 4, 2, 5, 6
+    lens = np.array([0, 3, 7, 12])
+    n = np.array([6, 1, 4, 2])
+    b = len(lens)
+    bt = np.array([[0, 1, -1, -1, -1], [2, 3, -1, -1, -1], [4, 5, 6, -1, -1],
+                   [7, 8, 9, 10, 11]])
+    kb = _rand((b, B, Hkv, D), 50)
+    vb = _rand((b, B, Hkv, D), 51)
+    kp = _rand((13, Hkv, ps, D), 52)
+    vp = _rand((13, Hkv, ps, D), 53)
+    kp2, vp2, sl2, slots = oracle.kv_commit(kb, vb, n, lens, bt, kp, vp, ps)
+    np.testing.assert_array_equal(sl2, lens + n)
+    # page 12 is mapped to no sequence: untouched
+    np.testing.assert_array_equal(kp2[12], kp[12])
+    for s in range(b):
+        P2 = int(sl2[s])
+        got = oracle.gather_prefix(kp2, bt[s], P2, ps)
+        old = oracle.gather_prefix(kp, bt[s], int(lens[s]), ps)
+        np.testing.assert_array_equal(got[:lens[s]], old)        # prefix unchanged
+        np.testing.assert_array_equal(got[lens[s]:], kb[s, :n[s]])
+        assert (slots[s, n[s]:] == -1).all()
+
+
+# ------------------------------------------- planted mistakes: each must fail some pin
+
+def test_planted_floor_block_index_is_caught(monkeypatch):
+    monkeypatch.setattr(mars_oracle, "beta", lambda t, B: np.asarray(t) // B)
+    L, B, want = _read_mask("mask_M_L4_B2.txt")
+    assert not np.array_equal(mars_oracle.mask_M(L, B), want)
+
+
+def test_planted_inclusive_cross_stream_is_caught(monkeypatch):
+    real = mars_oracle.mask_M
+
+    def wrong(L, B):          # case 3 with <= instead of <: a row sees its own clean block
+        vis = real(L, B)
+        i = np.arange(1, 2 * L + 1)[:, None]
+        j = np.arange(1, 2 * L + 1)[None, :]
+        bi = mars_oracle.beta(np.maximum(i - L, 1), B)
+        return vis | ((i > L) & (j <= L) & (mars_oracle.beta(j, B) == bi))
+    monkeypatch.setattr(mars_oracle, "mask_M", wrong)
+    L, B, want = _read_mask("mask_M_L4_B2.txt")
+    assert not np.array_equal(mars_oracle.mask_M(L, B), want)
+    assert abs(100 * mars_oracle.ar_signal_fraction(64, 4, True) - 62.5) > 0.05
+
+
+def test_planted_transposed_softmax_is_caught(monkeypatch):
+    def wrong(S, vis):
+        S = np.where(vis, S, -np.inf)
+        P = np.exp(S - S.max(axis=0, keepdims=True))
+        return P / P.sum(axis=0, keepdims=True)
+    monkeypatch.setattr(mars_oracle, "_masked_softmax_rows", wrong)
+    with pytest.raises(AssertionError):
+        test_dual_stream_against_sdpa(5, 2, 2, 1, 8)
+
+
+def test_planted_strict_threshold_is_caught(monkeypatch):
+    def wrong(row, tau):
+        t = float(np.float32(tau))
+        n = 0
+        for p in row:
+            if p > t:
+                n += 1
+            else:
+                break
+        return max(1, n)
+    monkeypatch.setattr(oracle, "accept_count", wrong)
+    with pytest.raises(AssertionError):
+        test_acceptance_golden_cases()
+
+
+def test_planted_swapped_page_slot_is_caught(monkeypatch):
+    # (a slot permutation inside a page would not be caught by attention, which is
+    # order-invariant over the prefix; the commit pins cover slot order)
+    def wrong(pool, row, P, ps):         # page and slot indices swapped
+        out = np.empty((P, pool.shape[1], pool.shape[3]))
+        for t in range(P):
+            out[t] = pool[int(row[t % ps]), :, t // ps, :]
+        return out
+    monkeypatch.setattr(mars_oracle, "gather_prefix", wrong)
+    with pytest.raises(AssertionError):
+        test_decode_equals_masked_stream_row(4, 8, 4)
