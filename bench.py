@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of the MARS decode hot path on GB300 (one JSON line on stdout).
+
+A step is one MARS decode step of the sustained 7B-class workload (batch 128, prefixes
+uniform in 2048..8192, block B=16, 28 query / 4 KV heads, head_dim 128, LM head 3584 x
+152064, 16-token bf16 KV pages, tau cycling 1.0 / 0.95 / 0.9 / 0.8 every 16 steps):
+decode attention -> LM head + max-prob/argmax + acceptance -> KV commit, all through
+the C ABI on one stream. `value` is accepted tokens per second over the K timed steps
+with inputs resident in HBM. The dual-stream training-form attention (batch 2, 2L=8192,
+B=16, same heads) is timed in the same run and reported under "dual_stream".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mars|reference]
+
+Under torchrun (N > 1) every rank runs its own replica (seed = rank) of the workload on
+its GPU; no data crosses ranks except the final max-time / token-sum reduction.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from block_masked_token_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TFLOP/s"
+CFG = W.SUSTAINED_DECODE_7B
+DUAL = W.DUAL_STREAM_7B
+
+
+# ------------------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_job(dist, tokens: float, seconds: float, device=None):
+    """Whole-job aggregate: total accepted tokens over all ranks and the slowest rank's
+    time. Works with any backend (gloo on CPU in the tests, nccl on GPUs)."""
+    if dist is None:
+        return tokens, seconds
+    t = torch.tensor([tokens], dtype=torch.float64, device=device)
+    s = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(t.item()), float(s.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.cmd = ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- oracle baseline
+
+def oracle_decode_sample(inp, cfg, step, seqs, seq_lens):
+    """One decode step of the oracle for the sequences `seqs` (host fp64). Returns the
+    number of accepted tokens."""
+    import numpy as np
+    import oracle
+    f = W.to_f64
+    seqs = list(seqs)
+    rows = [s * cfg.B + k for s in seqs for k in range(cfg.B)]
+    bt = inp.block_table.numpy()
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    # gather only the pages these sequences use into a compact host pool
+    need = sorted({int(p) for s in seqs for p in bt[s] if p >= 0})
+    remap = {p: i for i, p in enumerate(need)}
+    idx = torch.tensor(need, dtype=torch.long, device=inp.k_pool.device)
+    kp = f(inp.k_pool.index_select(0, idx))
+    vp = f(inp.v_pool.index_select(0, idx))
+    bt_l = np.array([[remap.get(int(p), -1) for p in bt[s]] for s in seqs])
+    sel = torch.tensor(seqs, dtype=torch.long, device=inp.q[step].device)
+    q = f(inp.q[step].index_select(0, sel))
+    kb = f(inp.k_blk[step].index_select(0, sel))
+    vb = f(inp.v_blk[step].index_select(0, sel))
+    h = f(inp.h[step][rows])
+    w = inp._w64 if getattr(inp, "_w64", None) is not None else f(inp.w)
+    inp._w64 = w
+    t0 = time.perf_counter()
+    oracle.decode_attn(q, kb, vb, kp, vp, bt_l, lens[seqs], cfg.page_size)
+    _, _, n, _ = oracle.head_accept(h, w, len(seqs), cfg.B, cfg.tau_at(step))
+    oracle.kv_commit(kb, vb, n, lens[seqs], bt_l, kp, vp, cfg.page_size)
+    return int(n.sum()), time.perf_counter() - t0
+
+
+def cpu_baseline(inp, cfg, budget_s: float = 15.0):
+    """The fp64 oracle on the host cores over a bounded sample: step 0 of the workload for
+    as many sequences as fit in about `budget_s` seconds of oracle time."""
+    toks, secs, done = 0, 0.0, 0
+    lens = inp.prefix_lens.tolist()
+    for s in range(cfg.batch):
+        n, t = oracle_decode_sample(inp, cfg, 0, [s], lens)
+        toks += n
+        secs += t
+        done += 1
+        if secs > budget_s:
+            break
+    return {"value": toks / secs, "unit": "accepted tok/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"step 0 of the workload for {done} of {cfg.batch} sequences "
+                      f"(attention, LM head 3584x152064, acceptance, commit), numpy fp64, "
+                      f"{secs:.1f} s"}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def _ev():
+    return torch.cuda.Event(enable_timing=True)
+
+
+def decode_kv_bytes(seq_lens, cfg):
+    """Algorithmic HBM bytes of one decode-attention call: every committed K and V row
+    read once per KV head, the block K/V and Q read, O written (fp32)."""
+    kv = int(sum(seq_lens)) * cfg.hkv * cfg.d * 2 * 2
+    blk = cfg.batch * cfg.B * cfg.hkv * cfg.d * 2 * 2
+    q = cfg.batch * cfg.B * cfg.hq * cfg.d * 2
+    o = cfg.batch * cfg.B * cfg.hq * cfg.d * 4
+    return kv + blk + q + o
+
+
+def head_flops(cfg):
+    return 2.0 * cfg.batch * cfg.B * cfg.hidden * cfg.vocab
+
+
+def dual_flops(cfg):
+    """QK^T and PV over the visible pairs of M: L(L+1) per (batch, head), 4*d flops each."""
+    return 4.0 * cfg.d * cfg.L * (cfg.L + 1) * cfg.batch * cfg.hq
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class DecodeRunner:
+    def __init__(self, inp, cfg, device):
+        from block_masked_token_gb300 import mars
+        self.mars = mars
+        self.inp, self.cfg, self.dev = inp, cfg, device
+        b = cfg.batch
+        self.bt = inp.block_table.to(device)
+        self.seq_lens = torch.empty(b, dtype=torch.int32, device=device)
+        self.max_hint = int(inp.prefix_lens.max()) + cfg.B * cfg.steps
+        self.o = torch.empty(b, cfg.B, cfg.hq, cfg.d, dtype=torch.float32, device=device)
+        self.tokens = torch.empty(b, cfg.B, dtype=torch.int32, device=device)
+        self.maxprob = torch.empty(b, cfg.B, dtype=torch.float32, device=device)
+        self.n_acc = torch.empty(max(cfg.steps, 1), b, dtype=torch.int32, device=device)
+        self.slots = torch.empty(b, cfg.B, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws_attn = torch.empty(mars.mars_workspace_bytes(
+            mars.OP_DECODE_ATTN, b, cfg.B, cfg.hq, cfg.hkv, cfg.d, max_len=self.max_hint),
+            dtype=torch.uint8, device=device)
+        self.ws_head = torch.empty(mars.mars_workspace_bytes(
+            mars.OP_HEAD_ACCEPT, b, cfg.B, vocab=cfg.vocab), dtype=torch.uint8, device=device)
+        self.reset()
+
+    def reset(self):
+        self.seq_lens.copy_(self.inp.prefix_lens.to(self.dev))
+        self.status.zero_()
+
+    def step(self, i, q=None, kb=None, vb=None, h=None, events=None):
+        m, inp, cfg = self.mars, self.inp, self.cfg
+        s = i % cfg.steps
+        q = inp.q[s] if q is None else q
+        kb = inp.k_blk[s] if kb is None else kb
+        vb = inp.v_blk[s] if vb is None else vb
+        h = inp.h[s] if h is None else h
+        n = self.n_acc[s]
+        if events:
+            events[0].record()
+        m.mars_decode_attn(q, kb, vb, inp.k_pool, inp.v_pool, self.bt, self.seq_lens,
+                           self.max_hint, self.o, self.ws_attn, self.status)
+        if events:
+            events[1].record()
+        m.mars_head_accept(h, inp.w, cfg.batch, cfg.B, cfg.tau_at(s), self.tokens,
+                           self.maxprob, n, self.ws_head, self.status)
+        if events:
+            events[2].record()
+        m.mars_kv_commit(kb, vb, n, self.seq_lens, self.bt, inp.k_pool, inp.v_pool,
+                         self.slots, self.status)
+        if events:
+            events[3].record()
+
+
+def run_gpu(args, rank, world, local):
+    from block_masked_token_gb300 import mars
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    cfg = CFG
+    peaks = load_peaks()
+    inp = W.make_decode_inputs(cfg, seed=rank, device=device)
+    runner = DecodeRunner(inp, cfg, device)
+    K, Wm = args.steps, args.warmup
+    torch.cuda.synchronize()
+    for i in range(Wm):
+        runner.step(i)
+    torch.cuda.synchronize()
+    runner.reset()
+    lens_before = []
+    # per-step seq_lens (for the algorithmic bytes of each attention call)
+    ev = [[_ev() for _ in range(4)] for _ in range(K)]
+    start, stop = _ev(), _ev()
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    launches0 = mars.mars_launch_count()
+    with ClockSampler(local) as clk:
+        start.record()
+        for i in range(K):
+            runner.step(i, events=ev[i])
+        stop.record()
+        torch.cuda.synchronize()
+    launches = mars.mars_launch_count() - launches0
+    barrier(dist, device)
+    elapsed = start.elapsed_time(stop) / 1e3
+    n_acc = runner.n_acc[: min(K, cfg.steps)].to(torch.int64)
+    steps_done = K
+    tok_local = float(n_acc.sum().item()) if K <= cfg.steps else float("nan")
+    status = int(runner.status.item())
+    t_attn = [ev[i][0].elapsed_time(ev[i][1]) / 1e3 for i in range(K)]
+    t_head = [ev[i][1].elapsed_time(ev[i][2]) / 1e3 for i in range(K)]
+    t_commit = [ev[i][2].elapsed_time(ev[i][3]) / 1e3 for i in range(K)]
+    # algorithmic bytes of each attention call: prefix lengths before step i
+    prefix = inp.prefix_lens.to(torch.int64)
+    cum = torch.cumsum(n_acc.cpu(), dim=0)
+    for i in range(K):
+        lens_before.append(int(prefix.sum()) + (int(cum[i - 1].sum()) if i > 0 else 0))
+    attn_bytes = [decode_kv_bytes([lens_before[i]], cfg) for i in range(K)]
+    attn_gbs = sum(attn_bytes) / sum(t_attn) / 1e9
+    hf = head_flops(cfg)
+    head_tflops = hf / statistics.mean(t_head) / 1e12
+    tokens, seconds = reduce_job(dist, tok_local, elapsed, device)
+
+    # ---- end to end through the public API with host buffers (pinned), rank-local
+    e2e = run_e2e(runner, inp, cfg, K, Wm, device, dist)
+
+    # ---- dual-stream training-form attention, same run
+    dual = run_dual(device, peaks, reps=max(3, min(K, 10)), warm=max(3, Wm))
+
+    out = None
+    if rank == 0:
+        frac_head = head_tflops / peaks["bf16_tflops_sustained"]
+        out = {
+            "metric": METRIC, "value": tokens / seconds, "unit": "accepted tok/s",
+            "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": seconds / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "B": cfg.B,
+                       "prefix": [cfg.prefix_lo, cfg.prefix_hi], "hq": cfg.hq,
+                       "hkv": cfg.hkv, "d": cfg.d, "hidden": cfg.hidden, "vocab": cfg.vocab,
+                       "page_size": cfg.page_size, "taus": list(cfg.taus),
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (KV ~1.3 GB + W 1.09 GB read per step)"},
+            "decode_step_us": seconds / K * 1e6 if world == 1 else elapsed / K * 1e6,
+            "mean_accepted_per_seq_step": tok_local / (K * cfg.batch),
+            "decode_attn": {"us_per_call": statistics.mean(t_attn) * 1e6,
+                            "hbm_gbs": attn_gbs,
+                            "frac_hbm": attn_gbs / peaks["hbm_gbs"]},
+            "head_accept": {"us_per_call": statistics.mean(t_head) * 1e6,
+                            "tflops": head_tflops, "frac_tensor": frac_head},
+            "kv_commit": {"us_per_call": statistics.mean(t_commit) * 1e6},
+            "dual_stream": dual,
+            "roofline": {"kernel": "mars_head_accept (LM head GEMM + fused epilogue)",
+                         "bound": "tensor", "achieved": head_tflops,
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": frac_head, "traffic": None,
+                         "peak_source": peaks["source"] + " bf16 sustained",
+                         "algorithmic": f"2*{cfg.batch * cfg.B}*{cfg.hidden}*{cfg.vocab} "
+                                        "flop per call"},
+            "device_status": status,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            out["cpu_baseline"] = cpu_baseline(inp, cfg, budget_s=args.cpu_budget)
+        elif not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(inp, cfg, budget_s=args.cpu_budget)
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
+def run_e2e(runner, inp, cfg, K, Wm, device, dist):
+    """Same metric, end to end: every step copies its inputs (q, k_blk, v_blk, h) from
+    pinned host memory to the device and reads tokens, max-probs and N back."""
+    nbuf = min(cfg.steps, 4)
+    host = []
+    for s in range(nbuf):
+        host.append([t.cpu().pin_memory() for t in (inp.q[s], inp.k_blk[s], inp.v_blk[s],
+                                                     inp.h[s])])
+    dq = [torch.empty_like(t, device=device) for t in host[0]]
+    out_tok = torch.empty(cfg.batch, cfg.B, dtype=torch.int32).pin_memory()
+    out_p = torch.empty(cfg.batch, cfg.B, dtype=torch.float32).pin_memory()
+    out_n = torch.empty(cfg.batch, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    d2h = sum(t.numel() * t.element_size() for t in (out_tok, out_p, out_n))
+
+    def one(i):
+        src = host[i % nbuf]
+        for d_, h_ in zip(dq, src):
+            d_.copy_(h_, non_blocking=True)
+        runner.step(i, q=dq[0], kb=dq[1], vb=dq[2], h=dq[3])
+        out_tok.copy_(runner.tokens, non_blocking=True)
+        out_p.copy_(runner.maxprob, non_blocking=True)
+        out_n.copy_(runner.n_acc[i % cfg.steps], non_blocking=True)
+
+    for i in range(Wm):
+        one(i)
+    torch.cuda.synchronize()
+    runner.reset()
+    barrier(dist, device)
+    start, stop = _ev(), _ev()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(K):
+        one(i)
+    stop.record()
+    torch.cuda.synchronize()
+    sec = start.elapsed_time(stop) / 1e3
+    tok = float(runner.n_acc[: min(K, cfg.steps)].sum().item())
+    tok, sec = reduce_job(dist, tok, sec, device)
+    return {"value": tok / sec, "unit": "accepted tok/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def run_dual(device, peaks, reps=10, warm=3):
+    from block_masked_token_gb300 import mars
+    cfg = DUAL
+    x = W.make_dual_stream_inputs(cfg, seed=0, device=device)
+    o = torch.empty(x["q"].shape, dtype=torch.float32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    for _ in range(warm):
+        mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)                      # L2 flush between timed launches
+        a, b = _ev(), _ev()
+        a.record()
+        mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    t = statistics.median(times)
+    fl = dual_flops(cfg)
+    tf = fl / t / 1e12
+    return {"workload": cfg.name, "ms": t * 1e3, "tflops": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                         "traffic": None, "peak_source": peaks["source"] + " bf16 burst"},
+            "l2": "flushed (256 MB write) before each timed launch"}
+
+
+# ----------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, as it stands: each step is one decode step of
+    the workload for a bounded sample of sequences."""
+    if rank != 0:
+        return None
+    cfg = CFG
+    per_step_seqs = args.ref_seqs
+    inp = W.make_decode_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available()
+                               else "cpu")
+    lens = inp.prefix_lens.tolist()
+    for i in range(args.warmup):
+        oracle_decode_sample(inp, cfg, i % cfg.steps, range(per_step_seqs), lens)
+    toks, secs = 0, 0.0
+    for i in range(args.steps):
+        seqs = [(i * per_step_seqs + j) % cfg.batch for j in range(per_step_seqs)]
+        n, t = oracle_decode_sample(inp, cfg, i % cfg.steps, seqs, lens)
+        toks += n
+        secs += t
+    value = toks / secs
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "accepted tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "B": cfg.B,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "accepted tok/s",
+                             "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{per_step_seqs} of {cfg.batch} sequences per step, "
+                                       "numpy fp64"},
+            "e2e": {"value": value, "unit": "accepted tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mars", "reference"], default="mars")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-seqs", type=int, default=2)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps > CFG.steps:
+        ap.error(f"--steps must be <= {CFG.steps} (the sustained workload's length)")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_gpu(args, rank, world, local)
+    if out is not None and rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

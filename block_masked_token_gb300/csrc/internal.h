@@ -1,0 +1,51 @@
+// Internal launchers behind the C ABI (mars_api.cu). Arguments are validated there;
+// every launcher enqueues on `stream` and returns the cudaError_t of its launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mars {
+
+// Host-side count of kernels enqueued by the library (read by mars_launch_count()).
+void count_launches(int n);
+
+// ---- KV commit ([notes] Key design 4): one CTA per sequence.
+cudaError_t launch_kv_commit(const uint16_t* k_blk, const uint16_t* v_blk,
+                             const int32_t* n_accept, int32_t* seq_lens,
+                             const int32_t* block_table, int max_pages, uint16_t* k_pool,
+                             uint16_t* v_pool, int num_pages, int32_t* commit_slots,
+                             int batch, int B, int hkv, int d, int32_t* status,
+                             cudaStream_t stream);
+
+// ---- Decode attention: split-KV partials then a combine pass.
+struct DecodePlan {
+  int split_len;   // keys per split (multiple of 128)
+  int nsplit;      // splits per (sequence, kv head)
+  int rows;        // query rows per (sequence, kv head) = (hq / hkv) * B
+  size_t ws_bytes;
+};
+DecodePlan plan_decode(int batch, int B, int hq, int hkv, int d, int max_len);
+
+cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
+                               const uint16_t* v_blk, const uint16_t* k_pool,
+                               const uint16_t* v_pool, int num_pages,
+                               const int32_t* block_table, int max_pages,
+                               const int32_t* seq_lens, const DecodePlan& plan, float* o,
+                               int batch, int B, int hq, int hkv, int d, float scale,
+                               void* workspace, int32_t* status, cudaStream_t stream);
+
+// ---- LM head + max-prob/argmax + acceptance.
+size_t head_workspace_bytes(int batch, int B, int vocab);
+cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, int B,
+                               int hidden, int vocab, float tau, int32_t* tokens,
+                               float* maxprob, int32_t* n_accept, void* workspace,
+                               cudaStream_t stream);
+
+// ---- Dual-stream attention under mask M.
+cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               float* o, int batch, int L, int B, int hq, int hkv, int d,
+                               float scale, cudaStream_t stream);
+
+}  // namespace mars

@@ -1,0 +1,146 @@
+// C ABI of libmars (declared in include/mars.h): argument validation on the host, then
+// launches on the caller's stream. No allocation, no host synchronisation.
+#include <math.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mars {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace mars
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MARS_OK : MARS_ECUDA; }
+
+int check_heads(int hq, int hkv, int d) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv) return MARS_EINVAL;
+  if (d != 64 && d != 128) return MARS_EUNSUPPORTED;
+  return MARS_OK;
+}
+
+// Shared-memory bound of the decode split kernel: query rows per KV head.
+constexpr int kMaxDecodeRows = 128;
+
+}  // namespace
+
+extern "C" {
+
+size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
+                            int vocab, int max_len) {
+  (void)hidden;
+  if (batch <= 0 || B < 1 || B > 32) return 0;
+  if (op == MARS_OP_DECODE_ATTN) {
+    if (check_heads(hq, hkv, d) != MARS_OK || max_len < 0) return 0;
+    return mars::plan_decode(batch, B, hq, hkv, d, max_len).ws_bytes;
+  }
+  if (op == MARS_OP_HEAD_ACCEPT) {
+    if (vocab <= 0) return 0;
+    return mars::head_workspace_bytes(batch, B, vocab);
+  }
+  return 0;
+}
+
+int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                          float* o, int batch, int L, int B, int hq, int hkv, int d,
+                          float scale, void* stream) {
+  if (batch < 0 || L < 1 || B < 1) return MARS_EINVAL;
+  int rc = check_heads(hq, hkv, d);
+  if (rc) return rc;
+  if (batch == 0) return MARS_OK;
+  if (!q || !k || !v || !o) return MARS_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MARS_EALIGN;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+  if (isinf(scale)) return MARS_EINVAL;
+  return cuda_rc(mars::launch_dual_stream(q, k, v, o, batch, L, B, hq, hkv, d, scale,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int mars_decode_attn(const mars_bf16* q, const mars_bf16* k_blk, const mars_bf16* v_blk,
+                     const mars_bf16* k_pool, const mars_bf16* v_pool, int num_pages,
+                     const int32_t* block_table, int max_pages_per_seq,
+                     const int32_t* seq_lens, int max_len_hint, float* o, int batch, int B,
+                     int hq, int hkv, int d, int page_size, float scale, void* workspace,
+                     size_t ws_bytes, int32_t* status, void* stream) {
+  if (batch < 0 || B < 1 || B > 32 || max_len_hint < 0 || num_pages < 0 ||
+      max_pages_per_seq < 0)
+    return MARS_EINVAL;
+  int rc = check_heads(hq, hkv, d);
+  if (rc) return rc;
+  if (page_size != mars::kPageSize) return MARS_EUNSUPPORTED;
+  if ((hq / hkv) * B > kMaxDecodeRows) return MARS_EUNSUPPORTED;
+  if (batch == 0) return MARS_OK;
+  if (!q || !k_blk || !v_blk || !o || !seq_lens || !workspace) return MARS_EINVAL;
+  if (max_pages_per_seq > 0 && (!k_pool || !v_pool || !block_table)) return MARS_EINVAL;
+  if (!aligned16(q) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(o) ||
+      !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(workspace))
+    return MARS_EALIGN;
+  const mars::DecodePlan plan = mars::plan_decode(batch, B, hq, hkv, d, max_len_hint);
+  if (ws_bytes < plan.ws_bytes) return MARS_ENOSPACE;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+  if (isinf(scale)) return MARS_EINVAL;
+  return cuda_rc(mars::launch_decode_attn(q, k_blk, v_blk, k_pool, v_pool, num_pages,
+                                          block_table, max_pages_per_seq, seq_lens, plan, o,
+                                          batch, B, hq, hkv, d, scale, workspace, status,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
+                     int vocab, float tau, int32_t* tokens, float* maxprob,
+                     int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
+                     void* stream) {
+  (void)status;
+  if (batch < 0 || B < 1 || B > 32 || hidden < 8 || vocab < 1) return MARS_EINVAL;
+  if (isnan(tau) || isinf(tau)) return MARS_EINVAL;
+  if (hidden % 8) return MARS_EUNSUPPORTED;
+  if (batch == 0) return MARS_OK;
+  if (!h || !w || !tokens || !maxprob || !n_accept || !workspace) return MARS_EINVAL;
+  if (!aligned16(h) || !aligned16(w) || !aligned16(workspace)) return MARS_EALIGN;
+  if (ws_bytes < mars::head_workspace_bytes(batch, B, vocab)) return MARS_ENOSPACE;
+  return cuda_rc(mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, tokens,
+                                          maxprob, n_accept, workspace,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int mars_kv_commit(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t* n_accept,
+                   int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq,
+                   mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
+                   int32_t* commit_slots, int batch, int B, int hkv, int d, int page_size,
+                   int32_t* status, void* stream) {
+  if (batch < 0 || B < 1 || B > 32 || hkv < 1 || num_pages < 0 || max_pages_per_seq < 0)
+    return MARS_EINVAL;
+  if (d != 64 && d != 128) return MARS_EUNSUPPORTED;
+  if (page_size != mars::kPageSize) return MARS_EUNSUPPORTED;
+  if (batch == 0) return MARS_OK;
+  if (!k_blk || !v_blk || !n_accept || !seq_lens || !block_table || !k_pool || !v_pool)
+    return MARS_EINVAL;
+  if (!aligned16(k_blk) || !aligned16(v_blk) || !aligned16(k_pool) || !aligned16(v_pool))
+    return MARS_EALIGN;
+  return cuda_rc(mars::launch_kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table,
+                                        max_pages_per_seq, k_pool, v_pool, num_pages,
+                                        commit_slots, batch, B, hkv, d, status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+const char* mars_strerror(int code) {
+  switch (code) {
+    case MARS_OK: return "ok";
+    case MARS_EINVAL: return "invalid argument";
+    case MARS_EALIGN: return "tensor base pointer not 16-byte aligned";
+    case MARS_EUNSUPPORTED: return "unsupported size (d must be 64/128, page_size 16)";
+    case MARS_ECUDA: return "CUDA launch failed";
+    case MARS_ENOSPACE: return "workspace too small";
+    default: return "unknown error";
+  }
+}
+
+uint64_t mars_launch_count(void) { return mars::g_launches.load(std::memory_order_relaxed); }
+
+const char* mars_version(void) { return "libmars sm_103a v1 (cuda-core reference kernels)"; }
+
+}  // extern "C"

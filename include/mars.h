@@ -1,0 +1,149 @@
+/*
+ * mars.h — C ABI of libmars: the GB300 (sm_103a) hot path of MARS block-masked
+ * multi-token decoding ("MARS: Enabling Autoregressive Models Multi-Token Generation",
+ * Jin, Wang, Luo, Sun, arXiv 2604.07023).
+ *
+ * Sources cited below: [notes] = the papernotes.org NeurIPS 2026 reading notes of the
+ * paper (the page that prints the formulas), sections "Key design 1..4" (关键设计 1..4);
+ * [gist] = the gist.science explainer, "2. Methodology", parts C and D.
+ *
+ * Conventions shared by every entry point
+ *   - Tensor arguments are DEVICE pointers to caller-owned memory (for example PyTorch
+ *     tensors). Scalars are passed by value. The library never allocates, frees or
+ *     keeps a pointer after the call returns.
+ *   - bf16 tensors are raw bfloat16 bits (mars_bf16). All tensors are row-major and
+ *     contiguous in the layout stated per argument; base pointers must be 16-byte
+ *     aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued
+ *     on it and the call returns without synchronising the host.
+ *   - Return value: MARS_OK, or a negative MARS_E* code for an error found on the host
+ *     before anything was launched (nothing was enqueued then), or MARS_ECUDA if a launch
+ *     failed. mars_strerror() names each code.
+ *   - Errors only the device can see (a block-table entry outside the pool, a position
+ *     past the mapped pages) OR a MARS_ST_* bit into *status (a device int32 the caller
+ *     zeroes) and skip the offending write; nothing traps. status may be NULL where
+ *     stated.
+ *   - Head dimension d is 64 or 128; hq % hkv == 0 (query head h uses KV head
+ *     h / (hq / hkv), consecutive query heads share a KV head); 1 <= B <= 32.
+ */
+#ifndef MARS_H
+#define MARS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mars_bf16;
+
+#define MARS_OK 0
+#define MARS_EINVAL (-1)        /* bad argument: null pointer, size out of range, NaN tau */
+#define MARS_EALIGN (-2)        /* a tensor base pointer is not 16-byte aligned */
+#define MARS_EUNSUPPORTED (-3)  /* valid but not built: d not in {64,128}, page_size != 16 */
+#define MARS_ECUDA (-4)         /* a CUDA launch or driver call failed */
+#define MARS_ENOSPACE (-5)      /* workspace smaller than mars_workspace_bytes() */
+
+#define MARS_ST_NOPAGE 1        /* block-table entry < 0 or >= num_pages: write skipped */
+#define MARS_ST_OVERFLOW 2      /* position beyond max_pages_per_seq: write skipped */
+#define MARS_ST_TIMEOUT 4       /* an in-kernel pipeline wait passed its time limit (2 s);
+                                   the kernel stopped early and its outputs are invalid */
+
+#define MARS_OP_DECODE_ATTN 1
+#define MARS_OP_HEAD_ACCEPT 2
+
+/* Workspace (device scratch, caller-allocated, >= 256-byte aligned) needed by `op`.
+ * MARS_OP_DECODE_ATTN uses batch, B, hq, hkv, d, max_len (the max_len_hint of the call);
+ * MARS_OP_HEAD_ACCEPT uses batch, B, vocab. Other arguments are ignored. Returns 0 for an
+ * unknown op or invalid sizes. */
+size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
+                            int vocab, int max_len);
+
+/* Dual-stream (training-form) attention under mask M ([notes] Key design 1, eq. M, with
+ * beta(t) = ceil(t/B); overall framework: one forward over z = [x; x~]).
+ *   q  [batch, 2L, hq,  d] bf16   rows 0..L-1 clean stream x, rows L..2L-1 masked x~
+ *   k  [batch, 2L, hkv, d] bf16
+ *   v  [batch, 2L, hkv, d] bf16
+ *   o  [batch, 2L, hq,  d] float  (written)
+ * Row i attends to key j (0-indexed) iff: i,j < L and j <= i; or i,j >= L,
+ * (i-L)/B == (j-L)/B and j <= i; or i >= L, j < L and j/B < (i-L)/B. Softmax of
+ * scale * q.k over the visible keys, scale <= 0 meaning 1/sqrt(d). Fully masked key tiles
+ * are never loaded. L >= 1, 1 <= B <= L is not required (B > L gives one block). */
+int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                          float* o, int batch, int L, int B, int hq, int hkv, int d,
+                          float scale, void* stream);
+
+/* Decode-form attention ([gist] 2.C sliding window; [notes] Key design 3 and 4): each
+ * sequence s appends B [MASK] queries after its committed prefix of P_s = seq_lens[s]
+ * tokens held in a paged cache; block query k sees all P_s prefix keys and block keys
+ * 0..k.
+ *   q           [batch, B, hq,  d] bf16
+ *   k_blk,v_blk [batch, B, hkv, d] bf16   K/V of the B block positions
+ *   k_pool,v_pool [num_pages, hkv, page_size, d] bf16   the paged prefix cache
+ *   block_table [batch, max_pages_per_seq] int32        page of logical page p
+ *   seq_lens    [batch] int32 (device)                  P_s
+ *   max_len_hint  host upper bound on every P_s; it sizes the split-KV grid without a
+ *                 host sync. A larger P_s is still computed correctly (the last split
+ *                 runs to the end), only slower.
+ *   o           [batch, B, hq, d] float (written)
+ *   workspace   >= mars_workspace_bytes(MARS_OP_DECODE_ATTN, ...) bytes
+ *   status      may be NULL; MARS_ST_NOPAGE / MARS_ST_OVERFLOW when a needed page is
+ *               unmapped (those keys are then skipped).
+ * page_size must be 16. */
+int mars_decode_attn(const mars_bf16* q, const mars_bf16* k_blk, const mars_bf16* v_blk,
+                     const mars_bf16* k_pool, const mars_bf16* v_pool, int num_pages,
+                     const int32_t* block_table, int max_pages_per_seq,
+                     const int32_t* seq_lens, int max_len_hint, float* o, int batch, int B,
+                     int hq, int hkv, int d, int page_size, float scale, void* workspace,
+                     size_t ws_bytes, int32_t* status, void* stream);
+
+/* Step epilogue ([notes] Key design 3; [gist] 2.C "Confidence Thresholding"): LM-head
+ * logits l = h W^T for the B positions of each sequence, then per position the argmax
+ * token (lowest index on ties) and max-prob p = max_v softmax(l)_v = 1 / sum_v
+ * exp(l_v - max l), then N_s = the number of leading positions with p >= tau, at least 1
+ * and at most B. The logits never reach global memory.
+ *   h         [batch*B, hidden] bf16   row s*B + k = sequence s, block position k
+ *   w         [vocab, hidden] bf16     the LM head, vocabulary-major (row v = word v)
+ *   tau       the confidence threshold, per call (the live speed knob); finite
+ *   tokens    [batch, B] int32, maxprob [batch, B] float, n_accept [batch] int32 (written)
+ *   workspace >= mars_workspace_bytes(MARS_OP_HEAD_ACCEPT, ...) bytes
+ * hidden % 8 == 0 (row pitch of h and w a multiple of 16 bytes). status may be NULL. */
+int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
+                     int vocab, float tau, int32_t* tokens, float* maxprob,
+                     int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
+                     void* stream);
+
+/* Commit of the accepted tokens' K/V into the block-level cache ([notes] Key design 4;
+ * [gist] 2.D), per sequence every step: for i < N_s = n_accept[s] (clamped to [0, B]),
+ * pos = seq_lens[s] + i, page = block_table[s][pos / page_size], slot = pos % page_size;
+ * k_pool[page, :, slot, :] = k_blk[s, i] and the same for v; commit_slots[s][i] =
+ * page * page_size + slot, -1 for i >= N_s; then seq_lens[s] += (rows committed).
+ * A row whose page is unmapped (entry < 0 or >= num_pages, or past max_pages_per_seq)
+ * is not written, flags MARS_ST_NOPAGE / MARS_ST_OVERFLOW, gets slot -1, and ends the
+ * commit of that sequence (seq_lens advances by the rows before it).
+ *   k_blk,v_blk [batch, B, hkv, d] bf16; n_accept [batch] int32; seq_lens [batch] int32
+ *   (in/out); block_table [batch, max_pages_per_seq] int32; k_pool, v_pool [num_pages,
+ *   hkv, page_size, d] bf16 (updated in place); commit_slots [batch, B] int32 (written,
+ *   may be NULL). page_size must be 16. status may be NULL. */
+int mars_kv_commit(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t* n_accept,
+                   int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq,
+                   mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
+                   int32_t* commit_slots, int batch, int B, int hkv, int d, int page_size,
+                   int32_t* status, void* stream);
+
+/* Human-readable name of a return code. Never NULL. */
+const char* mars_strerror(int code);
+
+/* Library build string (architecture and kernel variants). Never NULL. */
+const char* mars_version(void);
+
+/* Number of kernels libmars has enqueued (all threads, all devices) since it was loaded.
+ * Host-side counter, read it to count the launches of a timed region. */
+uint64_t mars_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MARS_H */

@@ -1,0 +1,94 @@
+"""The C ABI library loads and exports every entry point include/mars.h declares, and its
+host-side argument checks reject bad calls before launching anything (CPU only: the
+calls below return an error code before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_masked_token_gb300 import mars
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(mars_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(mars._LIB_PATH):
+        from block_masked_token_gb300.build import build_library
+        build_library()
+    return mars.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert {"mars_attn_dual_stream", "mars_decode_attn", "mars_head_accept",
+            "mars_kv_commit"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+    for n in mars.EXPORTED:
+        assert n in names
+
+
+def test_strerror_and_version(L):
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert mars.mars_strerror(code)
+    assert "sm_103a" in mars.mars_version()
+
+
+def test_workspace_sizes(L):
+    assert mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, 2, 4, vocab=512) > 0
+    ws = mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, 32, 8, 28, 4, 128, max_len=2048)
+    assert ws > 0 and ws % 16 == 0
+    assert mars.mars_workspace_bytes(99, 1, 1) == 0
+    assert mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, 1, 4, 3, 2, 64) == 0   # hq % hkv
+    assert mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, 1, 33, 4, 2, 64) == 0  # B > 32
+
+
+def _p(v=16):
+    return ctypes.c_void_p(v)
+
+
+def test_host_validation_codes(L):
+    P = _p()
+    # dual stream: unsupported head dim, bad group, misaligned pointer, null pointer
+    assert L.mars_attn_dual_stream(P, P, P, P, 1, 8, 2, 4, 2, 96, 0.0, None) == mars.EUNSUPPORTED
+    assert L.mars_attn_dual_stream(P, P, P, P, 1, 8, 2, 3, 2, 64, 0.0, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream(P, _p(18), P, P, 1, 8, 2, 4, 2, 64, 0.0, None) == mars.EALIGN
+    assert L.mars_attn_dual_stream(None, P, P, P, 1, 8, 2, 4, 2, 64, 0.0, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream(P, P, P, P, 0, 8, 2, 4, 2, 64, 0.0, None) == mars.OK
+    # head: NaN / inf tau, hidden not a multiple of 8, workspace too small
+    nan = float("nan")
+    assert L.mars_head_accept(P, P, 1, 4, 256, 512, nan, P, P, P, P, 1 << 20, None, None) == mars.EINVAL
+    assert L.mars_head_accept(P, P, 1, 4, 256, 512, float("inf"), P, P, P, P, 1 << 20, None, None) == mars.EINVAL
+    assert L.mars_head_accept(P, P, 1, 4, 252, 512, 0.9, P, P, P, P, 1 << 20, None, None) == mars.EUNSUPPORTED
+    assert L.mars_head_accept(P, P, 1, 4, 256, 512, 0.9, P, P, P, P, 16, None, None) == mars.ENOSPACE
+    assert L.mars_head_accept(P, P, 1, 0, 256, 512, 0.9, P, P, P, P, 1 << 20, None, None) == mars.EINVAL
+    # decode: page size, B range, workspace too small
+    args = [P, P, P, P, P, 10, P, 4, P, 64, P, 2, 4, 4, 2, 64]
+    assert L.mars_decode_attn(*args, 8, 0.0, P, 1 << 30, None, None) == mars.EUNSUPPORTED
+    assert L.mars_decode_attn(*args, 16, 0.0, P, 16, None, None) == mars.ENOSPACE
+    bad_b = list(args)
+    bad_b[12] = 33
+    assert L.mars_decode_attn(*bad_b, 16, 0.0, P, 1 << 30, None, None) == mars.EINVAL
+    # commit: page size, null pool
+    assert L.mars_kv_commit(P, P, P, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 8, None, None) == mars.EUNSUPPORTED
+    assert L.mars_kv_commit(P, P, P, P, P, 4, None, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EINVAL
+
+
+def test_binding_rejects_cpu_tensors(L):
+    import torch
+    q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    o = torch.zeros(1, 8, 2, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        mars.mars_attn_dual_stream(q, q[:, :, :1].contiguous(), q[:, :, :1].contiguous(), o, L=4, B=2)

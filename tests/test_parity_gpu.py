@@ -1,0 +1,309 @@
+"""GPU-vs-oracle parity of the four C-ABI entry points (needs a GB300).
+
+Small cases run the oracle on every output; they span several tiles/splits and ragged
+tails. The configuration-sized cases compare sampled outputs the oracle computes one by
+one. Comparison rules are in parity_util.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_masked_token_gb300 import mars
+from block_masked_token_gb300 import workloads as W
+from parity_util import assert_attn_close, compare_head
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def f64(t):
+    return W.to_f64(t)
+
+
+def _ws(nbytes):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=DEV)
+
+
+# --------------------------------------------------------------------------- helpers
+
+def run_dual(q, k, v, L, B):
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    mars.mars_attn_dual_stream(q, k, v, o, L=L, B=B)
+    torch.cuda.synchronize()
+    return o
+
+
+def run_decode(inp, step, seq_lens, cfg, max_len_hint=None):
+    q = inp.q[step].to(DEV)
+    kb = inp.k_blk[step].to(DEV)
+    vb = inp.v_blk[step].to(DEV)
+    b = cfg.batch
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    hint = int(seq_lens.max()) if max_len_hint is None else max_len_hint
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, b, cfg.B, cfg.hq, cfg.hkv, cfg.d,
+                                       max_len=hint))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mars.mars_decode_attn(q, kb, vb, inp.k_pool_dev, inp.v_pool_dev, inp.bt_dev,
+                          seq_lens.to(DEV), hint, o, ws, st)
+    torch.cuda.synchronize()
+    return o, int(st.item())
+
+
+def run_head(h, w, batch, B, tau):
+    tokens = torch.empty(batch, B, dtype=torch.int32, device=DEV)
+    maxprob = torch.empty(batch, B, dtype=torch.float32, device=DEV)
+    n = torch.empty(batch, dtype=torch.int32, device=DEV)
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, batch, B, vocab=w.shape[0]))
+    mars.mars_head_accept(h, w, batch, B, tau, tokens, maxprob, n, ws)
+    torch.cuda.synchronize()
+    return tokens.cpu().numpy(), maxprob.cpu().numpy(), n.cpu().numpy()
+
+
+def _to_dev(inp):
+    inp.k_pool_dev = inp.k_pool.to(DEV)
+    inp.v_pool_dev = inp.v_pool.to(DEV)
+    inp.bt_dev = inp.block_table.to(DEV)
+    return inp
+
+
+# ------------------------------------------------------------------ dual-stream attention
+
+@pytest.mark.parametrize("b,L,B,hq,hkv,d", [
+    (1, 1, 1, 1, 1, 64),          # degenerate: one position per stream
+    (2, 4, 2, 2, 1, 64),
+    (1, 37, 4, 4, 2, 64),         # L not a multiple of B: short last block
+    (2, 130, 16, 4, 4, 128),      # spans several 128-row tiles + ragged tail
+    (1, 200, 3, 7, 1, 128),       # GQA 7, odd B
+    (1, 64, 64, 2, 2, 64),        # B = L: masked stream sees no clean key
+    (1, 50, 1, 2, 1, 64),         # B = 1
+    (1, 33, 40, 2, 1, 128),       # B > L: one block
+])
+def test_dual_stream_small(b, L, B, hq, hkv, d):
+    cfg = W.DualStreamConfig("t", b, L, B, hq, hkv, d)
+    x = W.make_dual_stream_inputs(cfg, seed=L * 7 + B)
+    o = run_dual(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), L, B)
+    ref = oracle.attn_dual_stream(f64(x["q"]), f64(x["k"]), f64(x["v"]), L, B)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_dual_stream_config_0p5b_full():
+    cfg = W.DUAL_STREAM_0P5B
+    x = W.make_dual_stream_inputs(cfg, seed=0)
+    o = run_dual(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), cfg.L, cfg.B)
+    ref = oracle.attn_dual_stream(f64(x["q"]), f64(x["k"]), f64(x["v"]), cfg.L, cfg.B)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_dual_stream_config_7b_sampled():
+    cfg = W.DUAL_STREAM_7B
+    x = W.make_dual_stream_inputs(cfg, seed=0, device=DEV)
+    o = run_dual(x["q"], x["k"], x["v"], cfg.L, cfg.B)
+    L = cfg.L
+    rows = sorted({0, 1, 127, 128, 4095, L, L + 1, L + 15, L + 16, L + 127, L + 128, 2 * L - 1,
+                   *np.random.default_rng(0).integers(0, 2 * L, 24).tolist()})
+    q, k, v = f64(x["q"]), f64(x["k"]), f64(x["v"])
+    for bb, h in [(0, 0), (1, 13), (1, 27)]:
+        ref = oracle.attn_dual_stream(q, k, v, L, cfg.B, rows=rows, heads=[h], batches=[bb])
+        got = o[bb, rows, h].cpu().numpy()
+        assert_attn_close(got, ref[bb, :, h], f"dual 7B b{bb} h{h}")
+
+
+# ------------------------------------------------------------------------ decode attention
+
+def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
+    inp = W.make_decode_inputs(cfg, seed=seed, steps=steps, with_head=False,
+                               extra_pages=extra_pages)
+    return _to_dev(inp)
+
+
+@pytest.mark.parametrize("cfg", [
+    W.TINY_DECODE,
+    W.DecodeConfig("d1", batch=3, prefix_lo=0, prefix_hi=40, prefixes=(0, 17, 300), B=1,
+                   hq=2, hkv=2, d=64, hidden=64, vocab=64),
+    W.DecodeConfig("d2", batch=4, prefix_lo=100, prefix_hi=1500, B=8, hq=28, hkv=4, d=128,
+                   hidden=64, vocab=64),
+    W.DecodeConfig("d3", batch=2, prefix_lo=1, prefix_hi=9, prefixes=(1, 9), B=16, hq=7,
+                   hkv=1, d=128, hidden=64, vocab=64),
+    W.DecodeConfig("d4", batch=5, prefix_lo=500, prefix_hi=3000, B=3, hq=8, hkv=2, d=64,
+                   hidden=64, vocab=64),
+])
+def test_decode_small(cfg):
+    inp = _decode_case(cfg, seed=1)
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
+    assert st == 0
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_decode_hint_smaller_than_length_is_still_correct():
+    cfg = W.DecodeConfig("d5", batch=3, prefix_lo=600, prefix_hi=2000, B=4, hq=4, hkv=2,
+                         d=64, hidden=64, vocab=64)
+    inp = _decode_case(cfg, seed=2)
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg, max_len_hint=100)
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size)
+    assert st == 0
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_decode_unmapped_page_sets_status():
+    cfg = W.TINY_DECODE
+    inp = _decode_case(cfg)
+    inp.block_table[1, 1] = -1
+    inp.bt_dev = inp.block_table.to(DEV)
+    _, st = run_decode(inp, 0, inp.prefix_lens, cfg)
+    assert st & mars.ST_NOPAGE
+
+
+def test_decode_config_7b_sampled():
+    cfg = W.DECODE_7B
+    inp = _to_dev(W.make_decode_inputs(cfg, seed=0, device=DEV, with_head=False))
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
+    assert st == 0
+    seqs = [0, 5, 17, 31]
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.cpu().numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size, seqs=seqs)
+    assert_attn_close(o.cpu().numpy()[seqs], ref[seqs], "decode 7B")
+
+
+# --------------------------------------------------------------------------------- head
+
+@pytest.mark.parametrize("batch,B,hidden,vocab,tau", [
+    (2, 4, 256, 512, 0.9),
+    (3, 5, 64, 1000, 0.5),          # ragged vocabulary tile
+    (1, 16, 128, 77, 0.0),          # tau 0: whole block
+    (4, 8, 512, 3000, 1.0),         # tau 1: plain AR
+    (2, 32, 96, 300, 0.3),
+])
+def test_head_small(batch, B, hidden, vocab, tau):
+    cfg = W.DecodeConfig("h", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
+                         hidden=hidden, vocab=vocab, taus=(tau,))
+    inp = W.make_decode_inputs(cfg, seed=3)
+    tok, p, n = run_head(inp.h[0].to(DEV), inp.w.to(DEV), batch, B, tau)
+    rt, rp, rn, gap = oracle.head_accept(f64(inp.h[0]), f64(inp.w), batch, B, tau)
+    compare_head(tok, p, n, rt, rp, rn, gap, tau)
+    if tau == 1.0:
+        assert (n == 1).all()
+    if tau == 0.0:
+        assert (n == B).all()
+
+
+def test_head_tie_goes_to_lowest_index():
+    batch, B, H, V = 1, 2, 64, 700
+    h = torch.zeros(batch * B, H, dtype=torch.bfloat16)
+    h[:, 0] = 1.0
+    w = torch.zeros(V, H, dtype=torch.bfloat16)
+    w[[5, 300, 650], 0] = 2.0               # equal logits in different vocabulary tiles
+    w[[7], 0] = -1.0
+    tok, p, n = run_head(h.to(DEV), w.to(DEV), batch, B, 0.5)
+    assert (tok == 5).all()
+    rt, rp, rn, _ = oracle.head_accept(f64(h), f64(w), batch, B, 0.5)
+    assert (rt == 5).all()
+    np.testing.assert_allclose(p, rp, atol=1e-4)
+
+
+def test_head_config_7b_sampled_rows():
+    cfg = W.DECODE_7B
+    g = torch.Generator(device=DEV).manual_seed(0)
+    inp = W.make_decode_inputs(W.DecodeConfig(**{**cfg.__dict__, "batch": 32}), seed=0,
+                               device=DEV, steps=1)
+    h, w = inp.h[0], inp.w
+    tok, p, n = run_head(h, w, cfg.batch, cfg.B, cfg.taus[0])
+    seqs = [0, 9, 31]
+    rows = [s * cfg.B + k for s in seqs for k in range(cfg.B)]
+    rt, rp, rn, gap = oracle.head_accept(f64(h[rows]), f64(w), len(seqs), cfg.B, cfg.taus[0])
+    compare_head(tok[seqs], p[seqs], n[seqs], rt, rp, rn, gap, cfg.taus[0])
+    del g
+
+
+# ------------------------------------------------------------------------------ commit
+
+def test_commit_matches_oracle_and_guards():
+    cfg = W.DecodeConfig("c", batch=5, prefix_lo=0, prefix_hi=60, B=8, hq=4, hkv=2, d=128,
+                         hidden=64, vocab=64)
+    inp = W.make_decode_inputs(cfg, seed=4, steps=2, with_head=False, extra_pages=4)
+    n = torch.tensor([1, 8, 3, 0, 5], dtype=torch.int32)
+    kp, vp = inp.k_pool.to(DEV), inp.v_pool.to(DEV)
+    sl = inp.prefix_lens.to(DEV)
+    slots = torch.empty(cfg.batch, cfg.B, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mars.mars_kv_commit(inp.k_blk[0].to(DEV), inp.v_blk[0].to(DEV), n.to(DEV), sl,
+                        inp.block_table.to(DEV), kp, vp, slots, st)
+    torch.cuda.synchronize()
+    rk, rv, rl, rs = oracle.kv_commit(f64(inp.k_blk[0]), f64(inp.v_blk[0]), n.numpy(),
+                                      inp.prefix_lens.numpy(), inp.block_table.numpy(),
+                                      f64(inp.k_pool), f64(inp.v_pool), cfg.page_size)
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(sl.cpu().numpy(), rl)
+    np.testing.assert_array_equal(slots.cpu().numpy(), rs)
+    # whole pools bit-exact, including the unmapped guard pages
+    np.testing.assert_array_equal(f64(kp.cpu()), rk)
+    np.testing.assert_array_equal(f64(vp.cpu()), rv)
+
+
+def test_commit_unmapped_page_is_skipped_and_flagged():
+    cfg = W.DecodeConfig("c2", batch=2, prefix_lo=0, prefix_hi=0, prefixes=(14, 3), B=4,
+                         hq=2, hkv=2, d=64, hidden=64, vocab=64)
+    inp = W.make_decode_inputs(cfg, seed=5, steps=1, with_head=False)
+    bt = inp.block_table.clone()
+    bt[0, 1] = -1                      # positions 16.. of sequence 0 have no page
+    kp, vp = inp.k_pool.to(DEV), inp.v_pool.to(DEV)
+    sl = inp.prefix_lens.to(DEV)
+    slots = torch.empty(2, 4, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    n = torch.tensor([4, 4], dtype=torch.int32, device=DEV)
+    mars.mars_kv_commit(inp.k_blk[0].to(DEV), inp.v_blk[0].to(DEV), n, sl, bt.to(DEV), kp, vp,
+                        slots, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mars.ST_NOPAGE
+    s = slots.cpu().numpy()
+    assert s[0, 0] >= 0 and s[0, 1] >= 0 and (s[0, 2:] == -1).all()
+    assert sl.cpu().tolist() == [16, 7]
+
+
+# -------------------------------------------------------------- whole decode step chain
+
+def test_tiny_decode_step_end_to_end():
+    """Config 1: attention, head + acceptance, commit, all against the oracle, for two
+    steps (the second step runs on the committed cache of the first)."""
+    cfg = W.TINY_DECODE
+    inp = W.make_decode_inputs(cfg, seed=0, steps=2, extra_pages=2)
+    kp, vp = inp.k_pool.to(DEV), inp.v_pool.to(DEV)
+    bt = inp.block_table.to(DEV)
+    sl = inp.prefix_lens.to(DEV)
+    w = inp.w.to(DEV)
+    rk, rv, rl = f64(inp.k_pool), f64(inp.v_pool), inp.prefix_lens.numpy().astype(np.int64)
+    for step in range(2):
+        tau = cfg.tau_at(step) if step == 0 else 0.0     # step 1 forces a multi-token commit
+        o = torch.empty(cfg.batch, cfg.B, cfg.hq, cfg.d, dtype=torch.float32, device=DEV)
+        ws = _ws(mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, cfg.batch, cfg.B, cfg.hq,
+                                           cfg.hkv, cfg.d, max_len=64))
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        mars.mars_decode_attn(inp.q[step].to(DEV), inp.k_blk[step].to(DEV),
+                              inp.v_blk[step].to(DEV), kp, vp, bt, sl, 64, o, ws, st)
+        ref_o = oracle.decode_attn(f64(inp.q[step]), f64(inp.k_blk[step]),
+                                   f64(inp.v_blk[step]), rk, rv, inp.block_table.numpy(), rl,
+                                   cfg.page_size)
+        tok, p, n = run_head(inp.h[step].to(DEV), w, cfg.batch, cfg.B, tau)
+        rt, rp, rn, gap = oracle.head_accept(f64(inp.h[step]), f64(inp.w), cfg.batch, cfg.B,
+                                             tau)
+        assert_attn_close(o.cpu().numpy(), ref_o)
+        compare_head(tok, p, n, rt, rp, rn, gap, tau)
+        slots = torch.empty(cfg.batch, cfg.B, dtype=torch.int32, device=DEV)
+        mars.mars_kv_commit(inp.k_blk[step].to(DEV), inp.v_blk[step].to(DEV),
+                            torch.from_numpy(n).to(DEV), sl, bt, kp, vp, slots, st)
+        rk, rv, rl, rs = oracle.kv_commit(f64(inp.k_blk[step]), f64(inp.v_blk[step]), rn, rl,
+                                          inp.block_table.numpy(), rk, rv, cfg.page_size)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        np.testing.assert_array_equal(slots.cpu().numpy(), rs)
+        np.testing.assert_array_equal(sl.cpu().numpy(), rl)
+    np.testing.assert_array_equal(f64(kp.cpu()), rk)
