@@ -41,7 +41,10 @@ size_t head_workspace_bytes(int batch, int B, int vocab);
 cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, int B,
                                int hidden, int vocab, float tau, int32_t* tokens,
                                float* maxprob, int32_t* n_accept, void* workspace,
-                               cudaStream_t stream);
+                               int32_t* status, cudaStream_t stream);
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
 
 // ---- Dual-stream attention under mask M.
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,

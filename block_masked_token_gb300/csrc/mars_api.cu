@@ -94,7 +94,6 @@ int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, i
                      int vocab, float tau, int32_t* tokens, float* maxprob,
                      int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
                      void* stream) {
-  (void)status;
   if (batch < 0 || B < 1 || B > 32 || hidden < 8 || vocab < 1) return MARS_EINVAL;
   if (isnan(tau) || isinf(tau)) return MARS_EINVAL;
   if (hidden % 8) return MARS_EUNSUPPORTED;
@@ -103,7 +102,7 @@ int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, i
   if (!aligned16(h) || !aligned16(w) || !aligned16(workspace)) return MARS_EALIGN;
   if (ws_bytes < mars::head_workspace_bytes(batch, B, vocab)) return MARS_ENOSPACE;
   return cuda_rc(mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, tokens,
-                                          maxprob, n_accept, workspace,
+                                          maxprob, n_accept, workspace, status,
                                           static_cast<cudaStream_t>(stream)));
 }
 
