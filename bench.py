@@ -474,8 +474,61 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """One entry point on one named workload, W untimed + K timed launches (CUDA events,
+    L2 flushed between launches). Used for ncu captures of a single kernel."""
+    from block_masked_token_gb300 import mars
+    device = torch.device("cuda", 0)
+    cfg = W.CONFIGS[args.config]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    if isinstance(cfg, W.DualStreamConfig):
+        x = W.make_dual_stream_inputs(cfg, seed=0, device=device)
+        o = torch.empty(x["q"].shape, dtype=torch.float32, device=device)
+
+        def call():
+            mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
+        work = {"flop": dual_flops(cfg)}
+    else:
+        inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1)
+        r = DecodeRunner(inp, cfg, device)
+        if args.case == "head":
+            def call():
+                mars.mars_head_accept(inp.h[0], inp.w, cfg.batch, cfg.B, cfg.taus[0], r.tokens,
+                                      r.maxprob, r.n_acc[0], r.ws_head, r.status)
+            work = {"flop": head_flops(cfg)}
+        elif args.case == "decode":
+            def call():
+                mars.mars_decode_attn(inp.q[0], inp.k_blk[0], inp.v_blk[0], inp.k_pool,
+                                      inp.v_pool, r.bt, r.seq_lens, r.max_hint, r.o, r.ws_attn,
+                                      r.status)
+            work = {"bytes": decode_kv_bytes(inp.prefix_lens.tolist(), cfg)}
+        else:
+            raise SystemExit(f"--case {args.case} needs a decode workload")
+    for _ in range(args.warmup):
+        call()
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = _ev(), _ev()
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    t = statistics.median(times)
+    out = {"case": args.case, "workload": cfg.name, "us": t * 1e6}
+    if "flop" in work:
+        out["tflops"] = work["flop"] / t / 1e12
+    if "bytes" in work:
+        out["gbs"] = work["bytes"] / t / 1e9
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=["head", "decode", "dual"], default=None,
+                    help="time one entry point on --config instead of the decode step")
+    ap.add_argument("--config", default=None, choices=sorted(W.CONFIGS))
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=3)
@@ -489,6 +542,11 @@ def main(argv=None):
     if args.steps > CFG.steps:
         ap.error(f"--steps must be <= {CFG.steps} (the sustained workload's length)")
     rank, world, local = dist_env()
+    if args.case is not None:
+        if args.config is None:
+            ap.error("--case needs --config")
+        print(json.dumps(run_case(args)), flush=True)
+        return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
     else:
