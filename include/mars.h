@@ -114,6 +114,30 @@ int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, i
                      int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
                      void* stream);
 
+/* Scratch reserved by mars_head_accept_noalloc on every GPU that loads the library. */
+#define MARS_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* mars_head_accept without a workspace argument. The paper has no counterpart: this is
+ * a deployment variant for callers that cannot allocate device memory when they run a
+ * decode step (memory reserved up front with no allocation allowed afterwards, a host
+ * framework that owns every device allocation, a real-time path where an allocation and
+ * its possible synchronisation are not allowed). Inputs, outputs and results are those
+ * of mars_head_accept; it allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library call).
+ * Scratch: one library-owned device array of MARS_NOALLOC_SCRATCH_BYTES per GPU, held
+ * from library load until the process exits. A call needing more than that
+ * (batch*B*ceil(vocab/256)*16 bytes, i.e. more than 882 rows at vocab 152064) returns
+ * MARS_ENOSPACE before anything is launched.
+ * The first call on a device (made while that device is current) looks up the array's
+ * device address; make that first call before any CUDA stream capture.
+ * Every call uses the same array and leaves its contents behind: calls whose kernels may
+ * overlap on the GPU (different streams without ordering between them) race on it and
+ * give wrong results, so order such calls on one stream. */
+int mars_head_accept_noalloc(const mars_bf16* h, const mars_bf16* w, int batch, int B,
+                             int hidden, int vocab, float tau, int32_t* tokens,
+                             float* maxprob, int32_t* n_accept, int32_t* status,
+                             void* stream);
+
 /* Commit of the accepted tokens' K/V into the block-level cache ([notes] Key design 4;
  * [gist] 2.D), per sequence every step: for i < N_s = n_accept[s] (clamped to [0, B]),
  * pos = seq_lens[s] + i, page = block_table[s][pos / page_size], slot = pos % page_size;
