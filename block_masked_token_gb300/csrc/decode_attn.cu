@@ -3,153 +3,234 @@
 // Enabling Autoregressive Models Multi-Token Generation", 2.C sliding window and 2.D
 // block-level KV cache; papernotes.org notes, Key design 3 and 4).
 //
-// Split-KV: grid (split, kv head, sequence). Each CTA serves all G*B query rows that
-// share one KV head (GQA grouping: every key/value byte is read from HBM once per
-// group), streams its split of the keys in 32-key chunks through shared memory, keeps
-// an online softmax per row and writes an unnormalised partial (m, l, O) to the
-// workspace. A second kernel merges the splits.
+// Split-KV over the prefix: grid (split, kv head, sequence). A CTA stacks the G*B query
+// rows that share one KV head (row r = block position r / G, head kvh*G + r % G) into one
+// 128-row tile, so every key/value byte is read from HBM once per KV head, and runs the
+// tcgen05 flash engine (flash_tc.cuh) over its split: prefix tiles of 128 keys gathered
+// page by page from the paged pool (8 producer lanes, one 16-token page each, TMA with
+// 128-byte swizzle), and for the last split one more tile with the B block keys (causal:
+// query k sees block keys 0..k). Each split writes an unnormalised partial
+// (m in log2 units, l, O) to the workspace; a second kernel merges the splits.
+#include <climits>
+
 #include "common.cuh"
+#include "flash_tc.cuh"
 #include "internal.h"
 
 namespace mars {
 
 namespace {
 
-constexpr int kChunk = 32;          // keys staged per iteration
-constexpr int kThreads = 256;       // 8 warps
+using flash::BKV;
+using flash::BQ;
+
 constexpr int kTargetCtas = 4 * kNumSMs;
+constexpr int kPagesPerTile = BKV / kPageSize;   // 8
 
 struct DecodeArgs {
-  const uint16_t* q;
-  const uint16_t* k_blk;
-  const uint16_t* v_blk;
-  const uint16_t* k_pool;
-  const uint16_t* v_pool;
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* ws;
   float* o;
   int32_t* status;
   int num_pages, max_pages, B, hq, hkv, G, R, split_len, nsplit;
-  float scale;
+  float scale_log2;
 };
 
-// Partial record per (sequence, kv head, split, row): m, l, 2 pad, then O[D].
+MARS_DEV bool page_ok(const DecodeArgs& a, const int32_t* bt_row, int lp) {
+  if (lp >= a.max_pages) return false;
+  const int e = bt_row[lp];
+  return e >= 0 && e < a.num_pages;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
-  extern __shared__ float smem[];
-  float* q_s = smem;                             // [R][D], pre-scaled
-  float* k_s = q_s + a.R * D;                    // [kChunk][D+1]
-  float* v_s = k_s + kChunk * (D + 1);           // [kChunk][D]
-  float* o_s = v_s + kChunk * D;                 // [R][D]
-  float* m_s = o_s + a.R * D;                    // [R]
-  float* l_s = m_s + a.R;                        // [R]
-  int* valid_s = reinterpret_cast<int*>(l_s + a.R);   // [kChunk]
+struct DecodePolicy {
+  const DecodeArgs* a;
+  const int32_t* bt_row;
+  float* part;           // [R][D + 4] records of this (sequence, kv head, split)
+  int P, start, n_prefix;
 
-  const int sp = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = a.seq_lens[s];
-  const int T = P + a.B;
-  const int t0 = sp * a.split_len;
-  const int t1 = (sp == a.nsplit - 1) ? T : min(T, t0 + a.split_len);
-
-  for (int idx = threadIdx.x; idx < a.R * D; idx += kThreads) {
-    const int r = idx / D, dd = idx - r * D;
-    const int g = r / a.B, k = r - g * a.B;
-    const int h = kvh * a.G + g;
-    q_s[idx] = a.scale * bf16_to_f32(a.q[(((size_t)s * a.B + k) * a.hq + h) * D + dd]);
-    o_s[idx] = 0.f;
+  struct Tile {
+    int kp0;             // logical key position of column 0
+    uint32_t pmask;      // prefix tile: bit i = page i of the tile is mapped
+    bool block;          // the block-key tile
+    bool full;
+  };
+  MARS_DEV bool row_valid(int row) const { return row < a->R; }
+  MARS_DEV flash::RowVis row_vis(int row) const { return {P, P, P + row / a->G}; }
+  MARS_DEV Tile tile(int j) const {
+    Tile t;
+    if (j < n_prefix) {
+      t.kp0 = start + j * BKV;
+      t.block = false;
+      t.pmask = 0;
+      for (int i = 0; i < kPagesPerTile; ++i)
+        if (page_ok(*a, bt_row, t.kp0 / kPageSize + i)) t.pmask |= 1u << i;
+      t.full = (t.kp0 + BKV <= P) && t.pmask == 0xffu;
+    } else {
+      t.kp0 = P;
+      t.block = true;
+      t.pmask = 0;
+      t.full = false;
+    }
+    return t;
   }
-  for (int r = threadIdx.x; r < a.R; r += kThreads) {
-    m_s[r] = -INFINITY;
-    l_s[r] = 0.f;
+  MARS_DEV flash::ColRange cols(const flash::RowVis& v, const Tile& t) const {
+    flash::ColRange c;
+    if (t.block) {                       // block keys 0..k (k = v.hi2 - P)
+      c.e1 = v.hi2 - P + 1;
+      c.pmask = 0xffu;
+    } else {                             // prefix keys below P on mapped pages
+      c.e1 = min(P - t.kp0, BKV);
+      c.pmask = t.pmask;
+    }
+    c.s2 = BKV;
+    c.e2 = -1;
+    return c;
   }
-  int st = 0;
-  for (int c0 = t0; c0 < t1; c0 += kChunk) {
-    __syncthreads();
-    // stage keys c0 .. c0+31 (prefix rows from the pool, block rows from k_blk)
-    for (int idx = threadIdx.x; idx < kChunk * (D / 8); idx += kThreads) {
-      const int j = idx / (D / 8), c = idx - j * (D / 8);
-      const int t = c0 + j;
-      float kf[8], vf[8];
-      bool ok = false;
-      if (t < t1) {
-        const uint16_t *kp = nullptr, *vp = nullptr;
-        if (t < P) {
-          const int lp = t / kPageSize;
-          const int page = lp < a.max_pages ? a.block_table[(size_t)s * a.max_pages + lp] : -1;
-          if (lp >= a.max_pages) st |= MARS_ST_OVERFLOW;
-          else if (page < 0 || page >= a.num_pages) st |= MARS_ST_NOPAGE;
-          else {
-            const size_t off = (((size_t)page * a.hkv + kvh) * kPageSize + t % kPageSize) * D;
-            kp = a.k_pool + off;
-            vp = a.v_pool + off;
-          }
-        } else {
-          const size_t off = (((size_t)s * a.B + (t - P)) * a.hkv + kvh) * D;
-          kp = a.k_blk + off;
-          vp = a.v_blk + off;
-        }
-        if (kp) {
-          unpack8(*reinterpret_cast<const uint4*>(kp + c * 8), kf);
-          unpack8(*reinterpret_cast<const uint4*>(vp + c * 8), vf);
-          ok = true;
-        }
-      }
+  MARS_DEV void store_chunk(int row, int col, const uint32_t (&r)[32], float, float m,
+                            float l) const {
+    float* rec = part + (size_t)row * (D + 4);
+    if (col == 0) {
+      rec[0] = m;
+      rec[1] = l;
+    }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        k_s[j * (D + 1) + c * 8 + e] = ok ? kf[e] : 0.f;
-        v_s[j * D + c * 8 + e] = ok ? vf[e] : 0.f;
-      }
-      if (c == 0) valid_s[j] = ok;
-    }
-    __syncthreads();
-    const int t = c0 + lane;
-    for (int r = warp; r < a.R; r += kThreads / 32) {
-      const int k = r % a.B;
-      const bool vis = valid_s[lane] && (t < P || (t - P) <= k);
-      float sc = -INFINITY;
-      if (vis) {
-        float acc = 0.f;
-        const float* qr = q_s + r * D;
-        const float* kr = k_s + lane * (D + 1);
-#pragma unroll 16
-        for (int dd = 0; dd < D; ++dd) acc = fmaf(qr[dd], kr[dd], acc);
-        sc = acc;
-      }
-      const float cmax = warp_max(sc);
-      const float m_old = m_s[r];
-      const float m_new = fmaxf(m_old, cmax);
-      if (m_new == -INFINITY) continue;
-      const float p = vis ? __expf(sc - m_new) : 0.f;
-      const float alpha = (m_old == -INFINITY) ? 0.f : __expf(m_old - m_new);
-      const float psum = warp_sum(p);
-      float* orow = o_s + r * D;
-      for (int dd = lane; dd < D; dd += 32) {
-        float acc = orow[dd] * alpha;
-#pragma unroll 8
-        for (int j = 0; j < kChunk; ++j) acc = fmaf(__shfl_sync(0xffffffffu, p, j), v_s[j * D + dd], acc);
-        orow[dd] = acc;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        m_s[r] = m_new;
-        l_s[r] = l_s[r] * alpha + psum;
-      }
-      __syncwarp();
-    }
+    for (int e = 0; e < 32; e += 4)
+      *reinterpret_cast<float4*>(rec + 4 + col + e) =
+          make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                      __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
   }
+};
+
+template <int D>
+__global__ void __launch_bounds__(flash::NUM_THREADS, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_kp,
+                 const __grid_constant__ CUtensorMap tm_vp,
+                 const __grid_constant__ CUtensorMap tm_kb,
+                 const __grid_constant__ CUtensorMap tm_vb, DecodeArgs a) {
+  using namespace sm100;
+  using S = flash::Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ flash::Barriers bar;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sp = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+
+  DecodePolicy<D> pol;
+  pol.a = &a;
+  pol.bt_row = a.block_table + (size_t)s * a.max_pages;
+  pol.part = a.ws + ((((size_t)s * a.hkv + kvh) * a.nsplit + sp) * a.R) * (D + 4);
+  pol.P = a.seq_lens[s];
+  pol.start = sp * a.split_len;
+  const bool last = sp == a.nsplit - 1;
+  const int end = last ? pol.P : min(pol.P, pol.start + a.split_len);
+  pol.n_prefix = end > pol.start ? (end - pol.start + BKV - 1) / BKV : 0;
+  const int n_total = pol.n_prefix + (last ? 1 : 0);
+  if (n_total == 0) {                // split past this sequence's prefix: empty partial
+    for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
+      pol.part[(size_t)r * (D + 4)] = -INFINITY;
+      pol.part[(size_t)r * (D + 4) + 1] = 0.f;
+    }
+    return;
+  }
+
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  if (threadIdx.x == 0) {
+    bar.abort = 0;
+    mbar_init(&bar.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_empty[i], 1);
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_free[i], flash::SOFTMAX_THREADS);
+      mbar_init(&bar.p_full[i], flash::SOFTMAX_THREADS);
+      mbar_init(&bar.pv_done[i], 1);
+    }
+    mbar_init(&bar.o_final, 1);
+    mbar_init(&bar.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar.tmem_base, S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  if (st && a.status) atomicOr(a.status, st);
-  const size_t rec = D + 4;
-  float* base = a.ws + ((((size_t)s * a.hkv + kvh) * a.nsplit + sp) * a.R) * rec;
-  for (int r = threadIdx.x; r < a.R; r += kThreads) {
-    base[r * rec + 0] = m_s[r];
-    base[r * rec + 1] = l_s[r];
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loader (8 lanes)
+    volatile int* ab = &bar.abort;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar.q_full, a.R * 128 * (D / 64));
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, kvh * a.G,
+                    s * a.B);
+    }
+    int last_tile[2] = {-1, -1};
+    int st_flags = 0;
+    for (int j = 0; j < n_total; ++j) {
+      const int st = j & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bar.kv_empty[st], ((j >> 1) & 1) ^ 1, ab, a.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      uint8_t* kb = smem + S::OFF_KV + st * S::STAGE_BYTES;
+      if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[st], S::STAGE_BYTES);
+      __syncwarp();
+      if (j < pol.n_prefix) {
+        if (lane < kPagesPerTile) {
+          const int kp = pol.start + j * BKV + lane * kPageSize;
+          const int lp = kp / kPageSize;
+          int page = 0;                      // unmapped pages load page 0 and are masked
+          if (page_ok(a, pol.bt_row, lp)) {
+            page = pol.bt_row[lp];
+          } else if (kp < pol.P) {
+            st_flags |= lp >= a.max_pages ? MARS_ST_OVERFLOW : MARS_ST_NOPAGE;
+          }
+          const int row = (page * a.hkv + kvh) * kPageSize;
+          for (int x = 0; x < D / 64; ++x) {
+            tma_load_2d(kb + x * (BKV * 128) + lane * (kPageSize * 128), &tm_kp,
+                        &bar.kv_full[st], x * 64, row);
+            tma_load_2d(kb + S::KV_BYTES + x * (BKV * 128) + lane * (kPageSize * 128), &tm_vp,
+                        &bar.kv_full[st], x * 64, row);
+          }
+        }
+      } else if (lane == 0) {
+        // block keys: a 128-row box from row s*B (rows past the batch are zero-filled)
+        for (int x = 0; x < D / 64; ++x) {
+          tma_load_3d(kb + x * (BKV * 128), &tm_kb, &bar.kv_full[st], x * 64, kvh, s * a.B);
+          tma_load_3d(kb + S::KV_BYTES + x * (BKV * 128), &tm_vb, &bar.kv_full[st], x * 64, kvh,
+                      s * a.B);
+        }
+      }
+      last_tile[st] = j;
+    }
+    if (st_flags && a.status) atomicOr(a.status, st_flags);
+    if (lane == 0) {
+      // never leave the CTA with copies in flight
+      mbar_wait(&bar.q_full, 0, nullptr, a.status);
+      for (int st = 0; st < 2; ++st)
+        if (last_tile[st] >= 0)
+          mbar_wait(&bar.kv_full[st], (last_tile[st] >> 1) & 1, nullptr, a.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      flash::mma_loop<D>(bar, smem, n_total, tmem, a.status);
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0, nullptr, a.status);
+    }
+  } else {
+    flash::softmax_loop<D>(bar, smem, pol, n_total, tmem, a.scale_log2, a.status);
   }
-  for (int idx = threadIdx.x; idx < a.R * D; idx += kThreads) {
-    const int r = idx / D, dd = idx - r * D;
-    base[r * rec + 4 + dd] = o_s[idx];
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TMEM_COLS);
   }
 }
 
@@ -158,13 +239,11 @@ template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs a) {
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int batch_rows = gridDim.y;   // unused guard helper
-  (void)batch_rows;
   const int s = blockIdx.y;
   if (gw >= a.hq * a.B) return;
   const int h = gw / a.B, k = gw - h * a.B;
   const int kvh = h / a.G, g = h - kvh * a.G;
-  const int r = g * a.B + k;
+  const int r = k * a.G + g;
   const size_t rec = D + 4;
   const float* base = a.ws + (((size_t)s * a.hkv + kvh) * a.nsplit) * a.R * rec + r * rec;
   float m = -INFINITY;
@@ -177,32 +256,72 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs a) {
     const float* pr = base + sp * a.R * rec;
     const float ms = pr[0];
     if (ms == -INFINITY) continue;
-    const float w = __expf(ms - m);
+    const float w = exp2f(ms - m);
     l += pr[1] * w;
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) acc[i] += pr[4 + lane + 32 * i] * w;
   }
-  const float inv = 1.f / l;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
   float* orow = a.o + (((size_t)s * a.B + k) * a.hq + h) * D;
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = acc[i] * inv;
 }
 
 template <int D>
-size_t split_smem_bytes(int R) {
-  return sizeof(float) * (size_t)(2 * R * D + kChunk * (D + 1) + kChunk * D + 2 * R) +
-         sizeof(int) * kChunk;
+cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
+                      const uint16_t* k_pool, const uint16_t* v_pool, DecodeArgs& a, int batch,
+                      cudaStream_t stream) {
+  using S = flash::Smem<D>;
+  CUtensorMap tq, tkp, tvp, tkb, tvb;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.hq, (uint64_t)batch * a.B};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.hq * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)a.B};
+    if (!encode_tmap_bf16(&tq, q, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t rows = (uint64_t)(a.num_pages > 0 ? a.num_pages : 1) * a.hkv * kPageSize;
+    const uint64_t dims[2] = {(uint64_t)D, rows};
+    const uint64_t str[1] = {(uint64_t)D * 2};
+    const uint32_t box[2] = {64, (uint32_t)kPageSize};
+    // an empty pool is never read (no prefix keys can be mapped); encode over q instead
+    const void* kp = a.num_pages > 0 ? (const void*)k_pool : (const void*)q;
+    const void* vp = a.num_pages > 0 ? (const void*)v_pool : (const void*)q;
+    const uint64_t dims_e[2] = {(uint64_t)D, (uint64_t)kPageSize};
+    if (!encode_tmap_bf16(&tkp, kp, 2, a.num_pages > 0 ? dims : dims_e, str, box))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tvp, vp, 2, a.num_pages > 0 ? dims : dims_e, str, box))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.hkv, (uint64_t)batch * a.B};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.hkv * D * 2};
+    const uint32_t box[3] = {64, 1, BKV};
+    if (!encode_tmap_bf16(&tkb, k_blk, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tvb, v_blk, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         S::TOTAL);
+    attr = true;
+  }
+  dim3 grid(a.nsplit, a.hkv, batch);
+  decode_tc_kernel<D><<<grid, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tkp, tvp, tkb, tvb, a);
+  dim3 cgrid((a.hq * a.B + 7) / 8, batch);
+  decode_combine_kernel<D><<<cgrid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 DecodePlan plan_decode(int batch, int B, int hq, int hkv, int d, int max_len) {
   DecodePlan p{};
-  const long long T = (long long)max_len + B;
+  const long long T = (long long)max_len > 0 ? max_len : 1;
   const long long pairs = (long long)batch * hkv;
   long long per = (pairs * T + kTargetCtas - 1) / kTargetCtas;
-  if (per < 256) per = 256;
-  per = (per + 127) / 128 * 128;
+  if (per < 4 * BKV) per = 4 * BKV;
+  per = (per + BKV - 1) / BKV * BKV;
   p.split_len = (int)per;
   p.nsplit = (int)((T + per - 1) / per);
   if (p.nsplit < 1) p.nsplit = 1;
@@ -218,24 +337,13 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
                                const int32_t* seq_lens, const DecodePlan& plan, float* o,
                                int batch, int B, int hq, int hkv, int d, float scale,
                                void* workspace, int32_t* status, cudaStream_t stream) {
-  DecodeArgs a{q, k_blk, v_blk, k_pool, v_pool, block_table, seq_lens,
-               static_cast<float*>(workspace), o, status, num_pages, max_pages, B, hq, hkv,
-               hq / hkv, plan.rows, plan.split_len, plan.nsplit, scale};
-  dim3 grid(plan.nsplit, hkv, batch);
-  dim3 cgrid((hq * B + 7) / 8, batch);
-  if (d == 64) {
-    const size_t sm = split_smem_bytes<64>(plan.rows);
-    cudaFuncSetAttribute(decode_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    decode_split_kernel<64><<<grid, kThreads, sm, stream>>>(a);
-    decode_combine_kernel<64><<<cgrid, 256, 0, stream>>>(a);
-  } else {
-    const size_t sm = split_smem_bytes<128>(plan.rows);
-    cudaFuncSetAttribute(decode_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    decode_split_kernel<128><<<grid, kThreads, sm, stream>>>(a);
-    decode_combine_kernel<128><<<cgrid, 256, 0, stream>>>(a);
-  }
+  DecodeArgs a{block_table, seq_lens, static_cast<float*>(workspace), o, status, num_pages,
+               max_pages, B, hq, hkv, hq / hkv, plan.rows, plan.split_len, plan.nsplit,
+               scale * 1.4426950408889634f};
+  const cudaError_t e = d == 64 ? launch_tc<64>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream)
+                                : launch_tc<128>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream);
   count_launches(2);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mars

@@ -4,118 +4,238 @@
 // forward over z = [x; x~]).
 //
 // In 0-indexed stream-local terms a query row sees one or two contiguous key ranges:
-//   clean row i < L:           keys [0, i]
-//   masked row L + t:          clean keys [0, B*(t/B)) and masked keys [L + B*(t/B), L + t]
-// so keys outside those ranges (fully masked under M) are never touched.
-//
-// Reference CUDA-core kernel: one warp per (batch, query head, row), 32 keys per step,
-// online softmax in registers.
+//   clean row t (global t):    keys [0, t]
+//   masked row t (global L+t): clean keys [0, B*(t/B)) and masked keys [L + B*(t/B), L + t]
+// A CTA owns 128 consecutive rows of one stream for one (batch, query head) and visits
+// only the 128-key tiles that intersect those ranges: for a clean tile the causal tiles
+// 0..t/128, for a masked tile the clean tiles below its block start plus the tile(s)
+// holding its own blocks. Fully masked tiles are never loaded; tiles every row sees in
+// full skip the per-key test. The tile engine (flash_tc.cuh) runs QK^T and PV on tcgen05
+// with S and O in TMEM.
+#include <climits>
+
 #include "common.cuh"
+#include "flash_tc.cuh"
 #include "internal.h"
 
 namespace mars {
 
 namespace {
 
-struct DualArgs {
-  const uint16_t* q;
-  const uint16_t* k;
-  const uint16_t* v;
+using flash::BKV;
+using flash::BQ;
+
+template <int D>
+struct DualPolicy {
   float* o;
-  int batch, L, B, hq, hkv, G;
-  float scale;
+  int L, B, hq, two_l;
+  int b, h, stream, r0;
+  int n_clean, n_total, mstart, full_limit;
+
+  MARS_DEV bool row_valid(int row) const { return r0 + row < L; }
+  MARS_DEV flash::RowVis row_vis(int row) const {
+    const int t = r0 + row;
+    if (stream == 0) return {t + 1, INT_MAX, -1};
+    const int bs = (t / B) * B;
+    return {bs, L + bs, L + t};
+  }
+  struct Tile {
+    int kg0;     // global key index of column 0
+    int kend;    // keys >= kend belong to another tile
+    bool full;
+  };
+  MARS_DEV int tile_key0(int j) const {
+    return j < n_clean ? j * BKV : mstart + (j - n_clean) * BKV;
+  }
+  // clean-segment tiles admit clean keys only (a tile starting at 0 can reach past L)
+  MARS_DEV Tile tile(int j) const {
+    return {tile_key0(j), j < n_clean ? L : INT_MAX, j < n_clean && (j + 1) * BKV <= full_limit};
+  }
+  // columns c with kg0 + c < kend and (kg0 + c < end1 or lo2 <= kg0 + c <= hi2)
+  MARS_DEV flash::ColRange cols(const flash::RowVis& v, const Tile& t) const {
+    const int lim = t.kend == INT_MAX ? BKV : min(BKV, t.kend - t.kg0);   // first col not owned
+    flash::ColRange c;
+    c.e1 = min(v.end1 - t.kg0, lim);
+    c.s2 = v.lo2 == INT_MAX ? BKV : v.lo2 - t.kg0;
+    c.e2 = min(v.hi2 - t.kg0, lim - 1);
+    c.pmask = 0xffu;
+    return c;
+  }
+  MARS_DEV void store_chunk(int row, int col, const uint32_t (&r)[32], float inv, float,
+                            float) const {
+    float* dst = o + (((size_t)b * two_l + (size_t)stream * L + r0 + row) * hq + h) * D + col;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4)
+      *reinterpret_cast<float4*>(dst + e) =
+          make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
+                      __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+  }
+};
+
+struct DualArgs {
+  float* o;
+  int batch, L, B, hq, hkv, G, nqt;
+  float scale_log2;
+  int32_t* status;
 };
 
 template <int D>
-__device__ void attend_range(const DualArgs& a, const float* qv, int b, int kvh, int j0,
-                             int j1, float& m, float& l, float* acc) {
-  const int lane = threadIdx.x & 31;
-  const size_t rs = (size_t)a.hkv * D;           // row stride of k / v in elements
-  const uint16_t* kb = a.k + ((size_t)b * 2 * a.L) * rs + (size_t)kvh * D;
-  const uint16_t* vb = a.v + ((size_t)b * 2 * a.L) * rs + (size_t)kvh * D;
-  for (int c0 = j0; c0 < j1; c0 += 32) {
-    const int j = c0 + lane;
-    float sc = -INFINITY;
-    if (j < j1) {
-      const uint16_t* kr = kb + (size_t)j * rs;
-      float acc2 = 0.f;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        float kf[8];
-        unpack8(*reinterpret_cast<const uint4*>(kr + c * 8), kf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc2 = fmaf(qv[c * 8 + e], kf[e], acc2);
+__global__ void __launch_bounds__(flash::NUM_THREADS, 1)
+dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, DualArgs a) {
+  using namespace sm100;
+  using S = flash::Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ flash::Barriers bar;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // heaviest query tiles first
+  int id = blockIdx.x;
+  const int b = id % a.batch;
+  id /= a.batch;
+  const int h = id % a.hq;
+  id /= a.hq;
+  const int stream = id & 1;
+  const int qt = a.nqt - 1 - (id >> 1);
+
+  DualPolicy<D> pol;
+  pol.o = a.o;
+  pol.L = a.L;
+  pol.B = a.B;
+  pol.hq = a.hq;
+  pol.two_l = 2 * a.L;
+  pol.b = b;
+  pol.h = h;
+  pol.stream = stream;
+  pol.r0 = qt * BQ;
+  const int t_last = min(pol.r0 + BQ - 1, a.L - 1);
+  if (stream == 0) {
+    pol.n_clean = t_last / BKV + 1;
+    pol.n_total = pol.n_clean;
+    pol.mstart = 0;
+    pol.full_limit = pol.r0 + 1;
+  } else {
+    const int clean_end = (t_last / a.B) * a.B;            // keys [0, clean_end)
+    const int bs0 = (pol.r0 / a.B) * a.B;
+    pol.n_clean = (clean_end + BKV - 1) / BKV;
+    pol.mstart = a.L + bs0;
+    pol.n_total = pol.n_clean + (t_last - bs0 + BKV) / BKV;
+    pol.full_limit = bs0;
+  }
+  const int kvh = h / a.G;
+  const int zb = b * 2 * a.L;
+
+  if (threadIdx.x == 0) {
+    bar.abort = 0;
+    mbar_init(&bar.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.kv_full[i], 1);
+      mbar_init(&bar.kv_empty[i], 1);
+      mbar_init(&bar.s_full[i], 1);
+      mbar_init(&bar.s_free[i], flash::SOFTMAX_THREADS);
+      mbar_init(&bar.p_full[i], flash::SOFTMAX_THREADS);
+      mbar_init(&bar.pv_done[i], 1);
+    }
+    mbar_init(&bar.o_final, 1);
+    mbar_init(&bar.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar.tmem_base, S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      volatile int* ab = &bar.abort;
+      mbar_arrive_expect_tx(&bar.q_full, S::Q_BYTES);
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, h,
+                    zb + stream * a.L + pol.r0);
+      int last[2] = {-1, -1};
+      for (int j = 0; j < pol.n_total; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&bar.kv_empty[st], ((j >> 1) & 1) ^ 1, ab, a.status)) break;
+        uint8_t* kb = smem + S::OFF_KV + st * S::STAGE_BYTES;
+        mbar_arrive_expect_tx(&bar.kv_full[st], S::STAGE_BYTES);
+        const int z = zb + pol.tile_key0(j);
+        for (int x = 0; x < D / 64; ++x) {
+          tma_load_3d(kb + x * (BKV * 128), &tm_k, &bar.kv_full[st], x * 64, kvh, z);
+          tma_load_3d(kb + S::KV_BYTES + x * (BKV * 128), &tm_v, &bar.kv_full[st], x * 64, kvh, z);
+        }
+        last[st] = j;
       }
-      sc = acc2;
+      // never leave the CTA with copies in flight
+      mbar_wait(&bar.q_full, 0, nullptr, a.status);
+      for (int st = 0; st < 2; ++st)
+        if (last[st] >= 0) mbar_wait(&bar.kv_full[st], (last[st] >> 1) & 1, nullptr, a.status);
     }
-    const float m_new = fmaxf(m, warp_max(sc));
-    const float p = (j < j1) ? __expf(sc - m_new) : 0.f;
-    const float alpha = (m == -INFINITY) ? 0.f : __expf(m - m_new);
-    l = l * alpha + warp_sum(p);
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] *= alpha;
-    const int n = min(32, j1 - c0);
-    for (int jj = 0; jj < n; ++jj) {
-      const float pj = __shfl_sync(0xffffffffu, p, jj);
-      const uint16_t* vr = vb + (size_t)(c0 + jj) * rs;
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(pj, bf16_to_f32(vr[lane + 32 * i]), acc[i]);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      flash::mma_loop<D>(bar, smem, pol.n_total, tmem, a.status);
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0, nullptr, a.status);
     }
-    m = m_new;
+  } else {
+    flash::softmax_loop<D>(bar, smem, pol, pol.n_total, tmem, a.scale_log2, a.status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TMEM_COLS);
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) dual_stream_rowwise_kernel(DualArgs a) {
-  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int n = 2 * a.L;
-  const long long total = (long long)a.batch * a.hq * n;
-  if (gw >= total) return;
-  const int i = (int)(gw % n);
-  const int h = (int)((gw / n) % a.hq);
-  const int b = (int)(gw / ((long long)n * a.hq));
-  const int kvh = h / a.G;
-  float qv[D];
-  const uint16_t* qr = a.q + (((size_t)b * n + i) * a.hq + h) * D;
-#pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
-    float f[8];
-    unpack8(*reinterpret_cast<const uint4*>(qr + c * 8), f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qv[c * 8 + e] = f[e] * a.scale;
+cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
+                      int batch, int L, int B, int hq, int hkv, float scale,
+                      int32_t* status, cudaStream_t stream) {
+  using S = flash::Smem<D>;
+  CUtensorMap tq, tk, tv;
+  const uint64_t rows = (uint64_t)batch * 2 * L;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hq, rows};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)hq * D * 2};
+    const uint32_t box[3] = {64, 1, BQ};
+    if (!encode_tmap_bf16(&tq, q, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  float m = -INFINITY, l = 0.f, acc[D / 32];
-#pragma unroll
-  for (int x = 0; x < D / 32; ++x) acc[x] = 0.f;
-  if (i < a.L) {
-    attend_range<D>(a, qv, b, kvh, 0, i + 1, m, l, acc);
-  } else {
-    const int t = i - a.L;
-    const int bs = (t / a.B) * a.B;
-    attend_range<D>(a, qv, b, kvh, 0, bs, m, l, acc);
-    attend_range<D>(a, qv, b, kvh, a.L + bs, i + 1, m, l, acc);
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hkv, rows};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)hkv * D * 2};
+    const uint32_t box[3] = {64, 1, BKV};
+    if (!encode_tmap_bf16(&tk, k, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tv, v, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  float* orow = a.o + (((size_t)b * n + i) * a.hq + h) * D;
-  const float inv = 1.f / l;
-#pragma unroll
-  for (int x = 0; x < D / 32; ++x) orow[lane + 32 * x] = acc[x] * inv;
+  DualArgs a{o, batch, L, B, hq, hkv, hq / hkv, (L + BQ - 1) / BQ,
+             scale * 1.4426950408889634f, status};
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(dual_stream_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         S::TOTAL);
+    attr = true;
+  }
+  const long long ctas = (long long)a.nqt * 2 * hq * batch;
+  dual_stream_tc_kernel<D><<<(unsigned)ctas, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* o, int batch, int L, int B, int hq, int hkv, int d,
-                               float scale, cudaStream_t stream) {
-  DualArgs a{q, k, v, o, batch, L, B, hq, hkv, hq / hkv, scale};
-  const long long warps = (long long)batch * hq * 2 * L;
-  const unsigned blocks = (unsigned)((warps + 7) / 8);
-  if (d == 64)
-    dual_stream_rowwise_kernel<64><<<blocks, 256, 0, stream>>>(a);
-  else
-    dual_stream_rowwise_kernel<128><<<blocks, 256, 0, stream>>>(a);
+                               float scale, int32_t* status, cudaStream_t stream) {
+  cudaError_t e = d == 64 ? launch_tc<64>(q, k, v, o, batch, L, B, hq, hkv, scale, status, stream)
+                          : launch_tc<128>(q, k, v, o, batch, L, B, hq, hkv, scale, status, stream);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mars

@@ -1,0 +1,285 @@
+// Flash-attention tile engine on tcgen05 shared by the dual-stream and decode kernels.
+//
+// One CTA owns a 128-row query tile held in shared memory and walks a list of 128-key
+// tiles. Roles (192 threads):
+//   warp 0      loader (written by each kernel): K/V tiles into a 2-stage ring (TMA,
+//               128-byte swizzle);
+//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two 128-column fp32
+//               TMEM buffers, then O += P_{j-1} V_{j-1} (O lives in TMEM, P in smem);
+//   warps 2..5  softmax: thread = query row. It reads its S_j row (tcgen05.ld) into
+//               registers, takes the row max, and writes P = exp2(S - m) as bf16 into the
+//               128-byte-swizzled K-major A-operand layout. The running max is raised lazily: O and l are
+//               rescaled (tcgen05.ld / st) only when the max grows by more than 2^8, which
+//               keeps P <= 256 and the result exact up to rounding.
+// S_{j+1} is issued before PV_j so the softmax of one tile overlaps the MMAs of the next.
+#pragma once
+
+#include "sm100.cuh"
+
+namespace mars {
+namespace flash {
+
+constexpr int BQ = 128;                    // query rows per CTA tile
+constexpr int BKV = 128;                   // keys per tile
+constexpr int NUM_THREADS = 192;
+constexpr int SOFTMAX_THREADS = 128;
+constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by > 2^8
+
+template <int D>
+struct Smem {
+  static constexpr int Q_BYTES = BQ * D * 2;         // D/64 swizzled regions of [128][64]
+  static constexpr int KV_BYTES = BKV * D * 2;       // K or V tile
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;   // K then V
+  static constexpr int P_BYTES = BQ * BKV * 2;       // 2 regions of [128][64]
+  static constexpr int STAGES = 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
+  static constexpr int TOTAL = OFF_P + 2 * P_BYTES + 1024;   // + alignment slack
+  static constexpr int TMEM_S = 0;                   // two S buffers at columns 0, 128
+  static constexpr int TMEM_O = 2 * BKV;             // O at column 256
+  static constexpr int TMEM_COLS = 512;
+};
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], pv_done[2];
+  uint64_t o_final, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Row-visibility of a query row: keys jg (in the kernel's key index space) with
+// jg < lo1_end, or lo2 <= jg <= hi2, are visible.
+struct RowVis {
+  int end1;     // first range [0, end1)
+  int lo2, hi2; // second range [lo2, hi2]
+};
+
+MARS_DEV bool visible(const RowVis& v, int jg) {
+  return jg < v.end1 || (jg >= v.lo2 && jg <= v.hi2);
+}
+
+// Visible columns of one row inside one key tile: [0, e1) or [s2, e2], restricted to the
+// 16-key groups whose bit is set in pmask (pages of a paged tile; all ones otherwise).
+struct ColRange {
+  int e1, s2, e2;
+  uint32_t pmask;
+};
+
+// Bits [lo, hi) of a 32-bit word (lo, hi clamped to [0, 32]).
+MARS_DEV uint32_t bit_range(int lo, int hi) {
+  lo = max(0, min(32, lo));
+  hi = max(0, min(32, hi));
+  if (hi <= lo) return 0u;
+  const uint32_t upto_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+  const uint32_t upto_lo = (1u << lo) - 1u;
+  return upto_hi & ~upto_lo;
+}
+
+// Visibility bits of columns 32c .. 32c+31 for one row.
+MARS_DEV uint32_t chunk_mask(const ColRange& cr, int c) {
+  const int base = c * 32;
+  uint32_t mk = bit_range(0, cr.e1 - base) | bit_range(cr.s2 - base, cr.e2 + 1 - base);
+  const uint32_t pg = cr.pmask >> (2 * c);            // two 16-key pages per chunk
+  mk &= ((pg & 1u) ? 0x0000ffffu : 0u) | ((pg & 2u) ? 0xffff0000u : 0u);
+  return mk;
+}
+
+// Swizzled byte offset of 16-byte chunk `chunk` (0..7) of row `r` inside a [rows][128 B]
+// region (the layout TMA writes with 128-byte swizzle).
+MARS_DEV uint32_t sw_off(int r, int chunk) {
+  return (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+MARS_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The MMA issuer (one thread). ntiles >= 1.
+template <int D>
+MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
+                       int32_t* status) {
+  using namespace sm100;
+  using S = Smem<D>;
+  const uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);   // S = Q K^T: B K-major
+  const uint32_t idesc_o = idesc_bf16_f32(BQ, D, true);      // O = P V:   B MN-major
+  const uint32_t q = smem_u32(smem + S::OFF_Q);
+  volatile int* ab = &bar.abort;
+  if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
+  auto issue_pv = [&](int j) -> bool {
+    const int pb = j & 1, st = j & 1;
+    if (!mbar_wait(&bar.p_full[pb], (j >> 1) & 1, ab, status)) return false;
+    tc_fence_after();
+    const uint32_t p = smem_u32(smem + S::OFF_P + pb * S::P_BYTES);
+    const uint32_t v = smem_u32(smem + S::OFF_KV + st * S::STAGE_BYTES + S::KV_BYTES);
+#pragma unroll
+    for (int k = 0; k < BKV / 16; ++k) {
+      // A = P [128 x 128 keys], K-major: 64-key regions of 16 KB, 32 B per K step
+      const uint64_t ad = sdesc_sw128(p + (k >> 2) * (BQ * 128) + (k & 3) * 32, 16, 1024);
+      // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
+      const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
+      mma_bf16_ss(tmem + S::TMEM_O, ad, bd, idesc_o, (j | k) != 0);
+    }
+    mma_commit(&bar.pv_done[pb]);
+    mma_commit(&bar.kv_empty[st]);
+    return true;
+  };
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j & 1, sb = j & 1;
+    if (!mbar_wait(&bar.kv_full[st], (j >> 1) & 1, ab, status)) return;
+    if (!mbar_wait(&bar.s_free[sb], ((j >> 1) & 1) ^ 1, ab, status)) return;
+    tc_fence_after();
+    const uint32_t kb = smem_u32(smem + S::OFF_KV + st * S::STAGE_BYTES);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
+      const uint32_t koff = (k >> 2) * (BKV * 128) + (k & 3) * 32;
+      mma_bf16_ss(tmem + S::TMEM_S + sb * BKV, sdesc_sw128(q + off, 16, 1024),
+                  sdesc_sw128(kb + koff, 16, 1024), idesc_s, k != 0);
+    }
+    mma_commit(&bar.s_full[sb]);
+    if (j > 0 && !issue_pv(j - 1)) return;
+  }
+  if (!issue_pv(ntiles - 1)) return;
+  mma_commit(&bar.o_final);
+}
+
+MARS_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Softmax + final normalisation for one query row per thread (threads 64..191).
+// Policy provides: row_valid(row), row_vis(row), tile(j) -> Tile (with .full set when
+// every row sees every key of tile j, so no per-key test runs), cols(vis, tile) ->
+// ColRange (the columns of tile j visible to the row; a tile must admit only keys it
+// owns, so no key is counted twice), store_chunk(row, col, 32 fp32 of O, 1/l, m, l).
+// Each tile's S row is read from TMEM once (4 loads, one wait) into registers.
+template <int D, class Policy>
+MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int ntiles,
+                           uint32_t tmem, float scale_log2, int32_t* status) {
+  using namespace sm100;
+  using S = Smem<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;               // TMEM lane = query row of the tile
+  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  volatile int* ab = &bar.abort;
+  const bool rv = pol.row_valid(row);
+  const RowVis vis = pol.row_vis(row);
+  float m = -INFINITY;                            // running max (log2 units, lazy)
+  float l = 0.f;
+  bool ok = true;
+  // tcgen05.ld / st are warp-collective (.sync.aligned): every branch around them below is
+  // warp-uniform, and so is every wait result (warp_wait).
+  auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(b, parity, ab, status));
+  };
+  for (int j = 0; j < ntiles && ok; ++j) {
+    const int sb = j & 1, pb = j & 1;
+    if (!(ok = warp_wait(&bar.s_full[sb], (j >> 1) & 1))) break;
+    tc_fence_after();
+    const uint32_t s_addr = tmem + S::TMEM_S + sb * BKV + lane_off;
+    uint32_t r[BKV];
+#pragma unroll
+    for (int c = 0; c < BKV / 32; ++c)
+      tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
+    tmem_ld_wait();
+    const typename Policy::Tile tile = pol.tile(j);
+    if (!rv || !tile.full) {
+      // visible columns of this row in this tile: [0, e1) or [s2, e2], on mapped pages
+      // (none for a padding row past the end of the query tile)
+      const ColRange cr = rv ? pol.cols(vis, tile) : ColRange{0, BKV, -1, 0u};
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) {
+        const uint32_t mk = chunk_mask(cr, c);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (!((mk >> e) & 1u)) r[c * 32 + e] = 0xff800000u;
+      }
+    }
+    // row max of the tile: 8 independent chains, then a tree
+    float pm[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pm[i] = __uint_as_float(r[i]);
+#pragma unroll
+    for (int k = 1; k < BKV / 8; ++k)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pm[i] = fmaxf(pm[i], __uint_as_float(r[k * 8 + i]));
+    const float tmax =
+        fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+              fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale_log2;
+    // lazy rescale of O and l: a row raises its max only when it grows by more than 2^8.
+    // Rows whose O already holds keys (m finite) rescale it in TMEM; the TMEM pass runs
+    // for the whole warp when any of its rows needs it (alpha = 1 for the others).
+    const bool raise = tmax > m + kRescaleLog2;
+    const bool rescale_o = raise && m != -INFINITY;
+    if (__any_sync(0xffffffffu, rescale_o)) {
+      // PV of the previous tile must have landed in O before O is rescaled
+      if (!(ok = warp_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
+      tc_fence_after();
+      const float alpha = rescale_o ? ex2_approx(m - tmax) : 1.f;
+      l *= alpha;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(tmem + S::TMEM_O + c * 32 + lane_off, o);
+      }
+      tmem_st_wait();
+    }
+    if (raise) m = tmax;
+    // P buffer pb was read by PV of tile j-2
+    if (!(ok = warp_wait(&bar.pv_done[pb], ((j >> 1) & 1) ^ 1))) break;
+    // P = exp2(S*scale - m) -> bf16 in the swizzled K-major layout, and the row sum
+    uint8_t* pbuf = smem + S::OFF_P + pb * S::P_BYTES;
+    const float neg_m = (m == -INFINITY) ? 0.f : -m;   // no visible key yet: all P are 0
+    float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < BKV / 32; ++c) {
+      uint32_t packed[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(r[c * 32 + e]), scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(r[c * 32 + e + 1]), scale_log2, neg_m));
+        packed[e >> 1] = pack_bf16x2(p0, p1);
+        ps[(e >> 1) & 3] += p0 + p1;
+      }
+      uint8_t* region = pbuf + (c >> 1) * (BQ * 128);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int chunk = (c & 1) * 4 + q4;
+        *reinterpret_cast<uint4*>(region + sw_off(row, chunk)) =
+            make_uint4(packed[q4 * 4], packed[q4 * 4 + 1], packed[q4 * 4 + 2], packed[q4 * 4 + 3]);
+      }
+    }
+    l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    fence_proxy_async_smem();     // generic-proxy smem writes -> visible to the MMA
+    tc_fence_before();
+    mbar_arrive(&bar.s_free[sb]);
+    mbar_arrive(&bar.p_full[pb]);
+  }
+  if (!ok) return;
+  if (!warp_wait(&bar.o_final, 0)) return;
+  tc_fence_after();
+  const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, o);
+    tmem_ld_wait();
+    if (rv) pol.store_chunk(row, c * 32, o, inv, m, l);
+  }
+}
+
+}  // namespace flash
+}  // namespace mars

@@ -140,7 +140,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       const int mb = tile % p.num_m, nb = tile / p.num_m;
       const int buf = t & 1;
       const uint32_t aph = (t >> 1) & 1;
-      if (!mbar_wait(&acc_full[buf], aph, &abort_s, p.status)) break;
+      // warp-uniform result: the tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], aph, &abort_s, p.status))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + buf * BN + ((uint32_t)(quad * 32) << 16);
       const int col0 = nb * BN;

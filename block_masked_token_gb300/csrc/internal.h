@@ -49,6 +49,6 @@ int num_sms();
 // ---- Dual-stream attention under mask M.
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* o, int batch, int L, int B, int hq, int hkv, int d,
-                               float scale, cudaStream_t stream);
+                               float scale, int32_t* status, cudaStream_t stream);
 
 }  // namespace mars

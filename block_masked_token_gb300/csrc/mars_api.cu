@@ -48,7 +48,7 @@ size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, in
 
 int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
                           float* o, int batch, int L, int B, int hq, int hkv, int d,
-                          float scale, void* stream) {
+                          float scale, int32_t* status, void* stream) {
   if (batch < 0 || L < 1 || B < 1) return MARS_EINVAL;
   int rc = check_heads(hq, hkv, d);
   if (rc) return rc;
@@ -57,7 +57,7 @@ int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf1
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MARS_EALIGN;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
   if (isinf(scale)) return MARS_EINVAL;
-  return cuda_rc(mars::launch_dual_stream(q, k, v, o, batch, L, B, hq, hkv, d, scale,
+  return cuda_rc(mars::launch_dual_stream(q, k, v, o, batch, L, B, hq, hkv, d, scale, status,
                                           static_cast<cudaStream_t>(stream)));
 }
 

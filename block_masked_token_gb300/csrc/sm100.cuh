@@ -110,17 +110,23 @@ MARS_DEV void prefetch_tmap(const CUtensorMap* map) {
 
 // --------------------------------------------------------------------- tcgen05 / TMEM
 
+// TMEM allocation is warp-collective (.sync.aligned): the helpers reconverge the warp
+// first, since a warp whose lanes took different paths before (for example one lane
+// issuing MMAs) is not guaranteed to be converged again.
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *dst.
 MARS_DEV void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  __syncwarp();
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(dst)),
                "r"(ncols)
                : "memory");
 }
 MARS_DEV void tmem_relinquish() {
+  __syncwarp();
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 MARS_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  __syncwarp();
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }

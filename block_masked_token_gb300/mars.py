@@ -39,7 +39,7 @@ def lib() -> ctypes.CDLL:
         L.mars_workspace_bytes.restype = S
         L.mars_workspace_bytes.argtypes = [I] * 9
         L.mars_attn_dual_stream.restype = I
-        L.mars_attn_dual_stream.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P]
+        L.mars_attn_dual_stream.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P]
         L.mars_decode_attn.restype = I
         L.mars_decode_attn.argtypes = [P, P, P, P, P, I, P, I, P, I, P, I, I, I, I, I, I, F,
                                        P, S, P, P]
@@ -106,7 +106,8 @@ def mars_workspace_bytes(op, batch, B, hq=1, hkv=1, d=64, hidden=8, vocab=1, max
     return int(lib().mars_workspace_bytes(op, batch, B, hq, hkv, d, hidden, vocab, max_len))
 
 
-def mars_attn_dual_stream(q, k, v, o, L: int, B: int, scale: float = 0.0, stream=None):
+def mars_attn_dual_stream(q, k, v, o, L: int, B: int, scale: float = 0.0, status=None,
+                          stream=None):
     """o[b, 2L, hq, d] (float32) = attention of q under mask M (see include/mars.h)."""
     b, n, hq, d = q.shape
     hkv = k.shape[2]
@@ -114,8 +115,11 @@ def mars_attn_dual_stream(q, k, v, o, L: int, B: int, scale: float = 0.0, stream
     _check(k, "k", torch.bfloat16, (b, 2 * L, hkv, d))
     _check(v, "v", torch.bfloat16, (b, 2 * L, hkv, d))
     _check(o, "o", torch.float32, (b, 2 * L, hq, d))
+    if status is not None:
+        _check(status, "status", torch.int32, (1,))
     _rc(lib().mars_attn_dual_stream(_ptr(q), _ptr(k), _ptr(v), _ptr(o), b, L, B, hq, hkv, d,
-                                    float(scale), _stream(stream)), "mars_attn_dual_stream")
+                                    float(scale), _ptr(status), _stream(stream)),
+        "mars_attn_dual_stream")
 
 
 def mars_decode_attn(q, k_blk, v_blk, k_pool, v_pool, block_table, seq_lens,

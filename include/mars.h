@@ -69,10 +69,11 @@ size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, in
  * Row i attends to key j (0-indexed) iff: i,j < L and j <= i; or i,j >= L,
  * (i-L)/B == (j-L)/B and j <= i; or i >= L, j < L and j/B < (i-L)/B. Softmax of
  * scale * q.k over the visible keys, scale <= 0 meaning 1/sqrt(d). Fully masked key tiles
- * are never loaded. L >= 1, 1 <= B <= L is not required (B > L gives one block). */
+ * are never loaded. L >= 1; B > L is allowed (one block). status may be NULL
+ * (MARS_ST_TIMEOUT only). */
 int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
                           float* o, int batch, int L, int B, int hq, int hkv, int d,
-                          float scale, void* stream);
+                          float scale, int32_t* status, void* stream);
 
 /* Decode-form attention ([gist] 2.C sliding window; [notes] Key design 3 and 4): each
  * sequence s appends B [MASK] queries after its committed prefix of P_s = seq_lens[s]

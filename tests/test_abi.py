@@ -62,11 +62,11 @@ def _p(v=16):
 def test_host_validation_codes(L):
     P = _p()
     # dual stream: unsupported head dim, bad group, misaligned pointer, null pointer
-    assert L.mars_attn_dual_stream(P, P, P, P, 1, 8, 2, 4, 2, 96, 0.0, None) == mars.EUNSUPPORTED
-    assert L.mars_attn_dual_stream(P, P, P, P, 1, 8, 2, 3, 2, 64, 0.0, None) == mars.EINVAL
-    assert L.mars_attn_dual_stream(P, _p(18), P, P, 1, 8, 2, 4, 2, 64, 0.0, None) == mars.EALIGN
-    assert L.mars_attn_dual_stream(None, P, P, P, 1, 8, 2, 4, 2, 64, 0.0, None) == mars.EINVAL
-    assert L.mars_attn_dual_stream(P, P, P, P, 0, 8, 2, 4, 2, 64, 0.0, None) == mars.OK
+    assert L.mars_attn_dual_stream(P, P, P, P, 1, 8, 2, 4, 2, 96, 0.0, None, None) == mars.EUNSUPPORTED
+    assert L.mars_attn_dual_stream(P, P, P, P, 1, 8, 2, 3, 2, 64, 0.0, None, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream(P, _p(18), P, P, 1, 8, 2, 4, 2, 64, 0.0, None, None) == mars.EALIGN
+    assert L.mars_attn_dual_stream(None, P, P, P, 1, 8, 2, 4, 2, 64, 0.0, None, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream(P, P, P, P, 0, 8, 2, 4, 2, 64, 0.0, None, None) == mars.OK
     # head: NaN / inf tau, hidden not a multiple of 8, workspace too small
     nan = float("nan")
     assert L.mars_head_accept(P, P, 1, 4, 256, 512, nan, P, P, P, P, 1 << 20, None, None) == mars.EINVAL

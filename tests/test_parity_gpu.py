@@ -112,6 +112,22 @@ def test_dual_stream_config_7b_sampled():
         assert_attn_close(got, ref[bb, :, h], f"dual 7B b{bb} h{h}")
 
 
+def test_dual_stream_divergent_rescale():
+    """One query row meets a key scoring far above its earlier maximum in a later key tile
+    while the other rows of its warp do not: the per-row running maximum is raised for
+    that row only (exercises the lazy rescale of O with rows that disagree)."""
+    cfg = W.DualStreamConfig("t", 1, 300, 4, 2, 1, 64)
+    x = W.make_dual_stream_inputs(cfg, seed=5)
+    q, k = x["q"].clone(), x["k"].clone()
+    qrow = q[0, 290, 0].float()
+    k[0, 280, 0] = (4.0 * qrow).to(torch.bfloat16)      # clean key tile 2, row 290 only
+    qm = q[0, 300 + 150, 1].float()
+    k[0, 140, 0] = (4.0 * qm).to(torch.bfloat16)        # masked row t=150: clean key tile 1
+    o = run_dual(q.to(DEV), k.to(DEV), x["v"].to(DEV), cfg.L, cfg.B)
+    ref = oracle.attn_dual_stream(f64(q), f64(k), f64(x["v"]), cfg.L, cfg.B)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
 # ------------------------------------------------------------------------ decode attention
 
 def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
@@ -133,6 +149,26 @@ def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
 ])
 def test_decode_small(cfg):
     inp = _decode_case(cfg, seed=1)
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
+    assert st == 0
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_decode_divergent_rescale():
+    """A prefix key far along the cache scores far above every earlier key for one query
+    row only (block position 0, head 0), so that row alone raises its running maximum
+    inside a warp of rows that do not."""
+    cfg = W.DecodeConfig("dr", batch=2, prefix_lo=0, prefix_hi=0, prefixes=(700, 333), B=4,
+                         hq=4, hkv=1, d=64, hidden=64, vocab=64)
+    inp = W.make_decode_inputs(cfg, seed=6, steps=1, with_head=False, extra_pages=2)
+    qrow = inp.q[0][0, 0, 0].float()
+    pos = 660                   # second key tile of the split that holds it
+    page = int(inp.block_table[0, pos // 16])
+    inp.k_pool[page, 0, pos % 16] = (4.0 * qrow).to(torch.bfloat16)
+    _to_dev(inp)
     o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
     assert st == 0
     ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
