@@ -489,7 +489,8 @@ def run_case(args):
             mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
         work = {"flop": dual_flops(cfg)}
     else:
-        inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1)
+        inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1,
+                                   with_head=args.case == "head")
         r = DecodeRunner(inp, cfg, device)
         if args.case == "head":
             def call():

@@ -24,7 +24,12 @@ namespace {
 using flash::BKV;
 using flash::BQ;
 
-constexpr int kTargetCtas = 4 * kNumSMs;
+// Split-KV sizing: aim for this many CTAs per SM over the host's length bound, so CTAs are
+// short enough to balance across SMs but long enough to amortise their set-up.
+#ifndef MARS_DECODE_CTAS_PER_SM
+#define MARS_DECODE_CTAS_PER_SM 8
+#endif
+constexpr int kTargetCtas = MARS_DECODE_CTAS_PER_SM * kNumSMs;
 constexpr int kPagesPerTile = BKV / kPageSize;   // 8
 
 struct DecodeArgs {
@@ -137,21 +142,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  if (threadIdx.x == 0) {
-    bar.abort = 0;
-    mbar_init(&bar.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.kv_empty[i], 1);
-      mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_free[i], flash::SOFTMAX_THREADS);
-      mbar_init(&bar.p_full[i], flash::SOFTMAX_THREADS);
-      mbar_init(&bar.pv_done[i], 1);
-    }
-    mbar_init(&bar.o_final, 1);
-    mbar_init(&bar.drain, 1);
-    fence_barrier_init();
-  }
+  if (threadIdx.x == 0) flash::init_barriers(bar);
   if (warp == 1) {
     tmem_alloc(&bar.tmem_base, S::TMEM_COLS);
     tmem_relinquish();
@@ -162,61 +153,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t tmem = bar.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ loader (8 lanes)
-    volatile int* ab = &bar.abort;
+    // ------------------------------------------------------------ loader
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, a.R * 128 * (D / 64));
       for (int x = 0; x < D / 64; ++x)
         tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, kvh * a.G,
                     s * a.B);
     }
-    int last_tile[2] = {-1, -1};
     int st_flags = 0;
-    for (int j = 0; j < n_total; ++j) {
-      const int st = j & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&bar.kv_empty[st], ((j >> 1) & 1) ^ 1, ab, a.status);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      uint8_t* kb = smem + S::OFF_KV + st * S::STAGE_BYTES;
-      if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[st], S::STAGE_BYTES);
-      __syncwarp();
-      if (j < pol.n_prefix) {
-        if (lane < kPagesPerTile) {
-          const int kp = pol.start + j * BKV + lane * kPageSize;
-          const int lp = kp / kPageSize;
-          int page = 0;                      // unmapped pages load page 0 and are masked
-          if (page_ok(a, pol.bt_row, lp)) {
-            page = pol.bt_row[lp];
-          } else if (kp < pol.P) {
-            st_flags |= lp >= a.max_pages ? MARS_ST_OVERFLOW : MARS_ST_NOPAGE;
+    // prefix tile j: lane i < 8 copies 16-token page i of the tile (unmapped pages load
+    // page 0 and are masked by the softmax); the block tile: lane 0 copies a 128-row box
+    // from row s*B of k_blk / v_blk (rows past the batch read as zeros)
+    auto issue = [&](const CUtensorMap* tm_pool, const CUtensorMap* tm_blk) {
+      return [&, tm_pool, tm_blk](int j, uint8_t* dst, uint64_t* b) {
+        if (j < pol.n_prefix) {
+          if (lane < kPagesPerTile) {
+            const int kp = pol.start + j * BKV + lane * kPageSize;
+            const int lp = kp / kPageSize;
+            int page = 0;
+            if (page_ok(a, pol.bt_row, lp)) {
+              page = pol.bt_row[lp];
+            } else if (kp < pol.P) {
+              st_flags |= lp >= a.max_pages ? MARS_ST_OVERFLOW : MARS_ST_NOPAGE;
+            }
+            const int row = (page * a.hkv + kvh) * kPageSize;
+            for (int x = 0; x < D / 64; ++x)
+              tma_load_2d(dst + x * (BKV * 128) + lane * (kPageSize * 128), tm_pool, b, x * 64,
+                          row);
           }
-          const int row = (page * a.hkv + kvh) * kPageSize;
-          for (int x = 0; x < D / 64; ++x) {
-            tma_load_2d(kb + x * (BKV * 128) + lane * (kPageSize * 128), &tm_kp,
-                        &bar.kv_full[st], x * 64, row);
-            tma_load_2d(kb + S::KV_BYTES + x * (BKV * 128) + lane * (kPageSize * 128), &tm_vp,
-                        &bar.kv_full[st], x * 64, row);
-          }
+        } else if (lane == 0) {
+          for (int x = 0; x < D / 64; ++x)
+            tma_load_3d(dst + x * (BKV * 128), tm_blk, b, x * 64, kvh, s * a.B);
         }
-      } else if (lane == 0) {
-        // block keys: a 128-row box from row s*B (rows past the batch are zero-filled)
-        for (int x = 0; x < D / 64; ++x) {
-          tma_load_3d(kb + x * (BKV * 128), &tm_kb, &bar.kv_full[st], x * 64, kvh, s * a.B);
-          tma_load_3d(kb + S::KV_BYTES + x * (BKV * 128), &tm_vb, &bar.kv_full[st], x * 64, kvh,
-                      s * a.B);
-        }
-      }
-      last_tile[st] = j;
-    }
+      };
+    };
+    flash::load_loop<D>(bar, smem, n_total, a.status, issue(&tm_kp, &tm_kb),
+                        issue(&tm_vp, &tm_vb));
     if (st_flags && a.status) atomicOr(a.status, st_flags);
-    if (lane == 0) {
-      // never leave the CTA with copies in flight
-      mbar_wait(&bar.q_full, 0, nullptr, a.status);
-      for (int st = 0; st < 2; ++st)
-        if (last_tile[st] >= 0)
-          mbar_wait(&bar.kv_full[st], (last_tile[st] >> 1) & 1, nullptr, a.status);
-    }
   } else if (warp == 1) {
     if (lane == 0) {
       flash::mma_loop<D>(bar, smem, n_total, tmem, a.status);

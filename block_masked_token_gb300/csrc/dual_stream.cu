@@ -128,21 +128,7 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int kvh = h / a.G;
   const int zb = b * 2 * a.L;
 
-  if (threadIdx.x == 0) {
-    bar.abort = 0;
-    mbar_init(&bar.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.kv_empty[i], 1);
-      mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.s_free[i], flash::SOFTMAX_THREADS);
-      mbar_init(&bar.p_full[i], flash::SOFTMAX_THREADS);
-      mbar_init(&bar.pv_done[i], 1);
-    }
-    mbar_init(&bar.o_final, 1);
-    mbar_init(&bar.drain, 1);
-    fence_barrier_init();
-  }
+  if (threadIdx.x == 0) flash::init_barriers(bar);
   if (warp == 1) {
     tmem_alloc(&bar.tmem_base, S::TMEM_COLS);
     tmem_relinquish();
@@ -154,29 +140,21 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (warp == 0) {
     if (lane == 0) {
-      volatile int* ab = &bar.abort;
       mbar_arrive_expect_tx(&bar.q_full, S::Q_BYTES);
       for (int x = 0; x < D / 64; ++x)
         tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, h,
                     zb + stream * a.L + pol.r0);
-      int last[2] = {-1, -1};
-      for (int j = 0; j < pol.n_total; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&bar.kv_empty[st], ((j >> 1) & 1) ^ 1, ab, a.status)) break;
-        uint8_t* kb = smem + S::OFF_KV + st * S::STAGE_BYTES;
-        mbar_arrive_expect_tx(&bar.kv_full[st], S::STAGE_BYTES);
-        const int z = zb + pol.tile_key0(j);
-        for (int x = 0; x < D / 64; ++x) {
-          tma_load_3d(kb + x * (BKV * 128), &tm_k, &bar.kv_full[st], x * 64, kvh, z);
-          tma_load_3d(kb + S::KV_BYTES + x * (BKV * 128), &tm_v, &bar.kv_full[st], x * 64, kvh, z);
-        }
-        last[st] = j;
-      }
-      // never leave the CTA with copies in flight
-      mbar_wait(&bar.q_full, 0, nullptr, a.status);
-      for (int st = 0; st < 2; ++st)
-        if (last[st] >= 0) mbar_wait(&bar.kv_full[st], (last[st] >> 1) & 1, nullptr, a.status);
     }
+    // one 3D box of 128 rows per 64-column half; rows past the batch read as zeros
+    auto issue = [&](const CUtensorMap* tm) {
+      return [&, tm](int j, uint8_t* dst, uint64_t* b) {
+        if (lane == 0) {
+          const int z = zb + pol.tile_key0(j);
+          for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * (BKV * 128), tm, b, x * 64, kvh, z);
+        }
+      };
+    };
+    flash::load_loop<D>(bar, smem, pol.n_total, a.status, issue(&tm_k), issue(&tm_v));
   } else if (warp == 1) {
     if (lane == 0) {
       flash::mma_loop<D>(bar, smem, pol.n_total, tmem, a.status);

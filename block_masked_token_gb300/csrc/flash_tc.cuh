@@ -2,15 +2,17 @@
 //
 // One CTA owns a 128-row query tile held in shared memory and walks a list of 128-key
 // tiles. Roles (192 threads):
-//   warp 0      loader (written by each kernel): K/V tiles into a 2-stage ring (TMA,
-//               128-byte swizzle);
+//   warp 0      loader (written by each kernel): K tiles and V tiles into two separate
+//               2-stage rings (TMA, 128-byte swizzle), K one tile ahead of V;
 //   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two 128-column fp32
-//               TMEM buffers, then O += P_{j-1} V_{j-1} (O lives in TMEM, P in smem);
+//               TMEM buffers, then O += P_{j-1} V_{j-1} (O lives in TMEM, P in smem). A K
+//               stage is released as soon as its QK^T finishes, a V stage after its PV,
+//               so the next loads start early;
 //   warps 2..5  softmax: thread = query row. It reads its S_j row (tcgen05.ld) into
 //               registers, takes the row max, and writes P = exp2(S - m) as bf16 into the
-//               128-byte-swizzled K-major A-operand layout. The running max is raised lazily: O and l are
-//               rescaled (tcgen05.ld / st) only when the max grows by more than 2^8, which
-//               keeps P <= 256 and the result exact up to rounding.
+//               128-byte-swizzled K-major A-operand layout. The running max is raised
+//               lazily: O and l are rescaled (tcgen05.ld / st) only when the max grows by
+//               more than 2^8, which keeps P <= 256 and the result exact up to rounding.
 // S_{j+1} is issued before PV_j so the softmax of one tile overlaps the MMAs of the next.
 #pragma once
 
@@ -28,14 +30,14 @@ constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by
 template <int D>
 struct Smem {
   static constexpr int Q_BYTES = BQ * D * 2;         // D/64 swizzled regions of [128][64]
-  static constexpr int KV_BYTES = BKV * D * 2;       // K or V tile
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;   // K then V
+  static constexpr int KV_BYTES = BKV * D * 2;       // one K or V tile
   static constexpr int P_BYTES = BQ * BKV * 2;       // 2 regions of [128][64]
   static constexpr int STAGES = 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
-  static constexpr int TOTAL = OFF_P + 2 * P_BYTES + 1024;   // + alignment slack
+  static constexpr int OFF_K = Q_BYTES;                          // K ring
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;        // V ring
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int TOTAL = OFF_P + 2 * P_BYTES + 1024;       // + alignment slack
   static constexpr int TMEM_S = 0;                   // two S buffers at columns 0, 128
   static constexpr int TMEM_O = 2 * BKV;             // O at column 256
   static constexpr int TMEM_COLS = 512;
@@ -43,13 +45,86 @@ struct Smem {
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_final, drain;
   uint32_t tmem_base;
   int abort;
 };
+
+// Thread 0: initialise every barrier (call before the CTA-wide sync that publishes them).
+MARS_DEV void init_barriers(Barriers& bar) {
+  using namespace sm100;
+  bar.abort = 0;
+  mbar_init(&bar.q_full, 1);
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&bar.k_full[i], 1);
+    mbar_init(&bar.k_empty[i], 1);
+    mbar_init(&bar.v_full[i], 1);
+    mbar_init(&bar.v_empty[i], 1);
+    mbar_init(&bar.s_full[i], 1);
+    mbar_init(&bar.s_free[i], SOFTMAX_THREADS);
+    mbar_init(&bar.p_full[i], SOFTMAX_THREADS);
+    mbar_init(&bar.pv_done[i], 1);
+  }
+  mbar_init(&bar.o_final, 1);
+  mbar_init(&bar.drain, 1);
+  fence_barrier_init();
+}
+
+// Loader skeleton shared by the kernels, run by the whole loader warp: lane 0 waits for
+// a free stage and arms its barrier with the tile's byte count, then every lane calls
+// `issue_k(j, dst, bar)` / `issue_v(j, dst, bar)` (the kernel decides which lanes issue
+// the TMA copies of tile j into dst, completing on bar). Order: K_0, then for each j:
+// K_{j+1}, V_j. Returns after waiting (bounded) for every copy it issued, so the CTA
+// never exits with copies in flight.
+template <int D, class IssueK, class IssueV>
+MARS_DEV void load_loop(Barriers& bar, uint8_t* smem, int ntiles, int32_t* status,
+                        IssueK issue_k, IssueV issue_v) {
+  using namespace sm100;
+  using S = Smem<D>;
+  const int lane = threadIdx.x & 31;
+  volatile int* ab = &bar.abort;
+  int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+  auto stage = [&](uint64_t* empty, uint64_t* full, int j) -> bool {
+    int ok = 1;
+    if (lane == 0) {
+      ok = mbar_wait(empty, ((j >> 1) & 1) ^ 1, ab, status);
+      if (ok) mbar_arrive_expect_tx(full, S::KV_BYTES);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok != 0;
+  };
+  auto load_k = [&](int j) -> bool {
+    const int st = j & 1;
+    if (!stage(&bar.k_empty[st], &bar.k_full[st], j)) return false;
+    issue_k(j, smem + S::OFF_K + st * S::KV_BYTES, &bar.k_full[st]);
+    last_k[st] = j;
+    return true;
+  };
+  auto load_v = [&](int j) -> bool {
+    const int st = j & 1;
+    if (!stage(&bar.v_empty[st], &bar.v_full[st], j)) return false;
+    issue_v(j, smem + S::OFF_V + st * S::KV_BYTES, &bar.v_full[st]);
+    last_v[st] = j;
+    return true;
+  };
+  if (ntiles > 0 && load_k(0)) {
+    for (int j = 0; j < ntiles; ++j) {
+      if (j + 1 < ntiles && !load_k(j + 1)) break;
+      if (!load_v(j)) break;
+    }
+  }
+  if (lane == 0) {
+    mbar_wait(&bar.q_full, 0, nullptr, status);
+    for (int st = 0; st < 2; ++st) {
+      if (last_k[st] >= 0) mbar_wait(&bar.k_full[st], (last_k[st] >> 1) & 1, nullptr, status);
+      if (last_v[st] >= 0) mbar_wait(&bar.v_full[st], (last_v[st] >> 1) & 1, nullptr, status);
+    }
+  }
+  __syncwarp();
+}
 
 // Row-visibility of a query row: keys jg (in the kernel's key index space) with
 // jg < lo1_end, or lo2 <= jg <= hi2, are visible.
@@ -113,10 +188,11 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
   auto issue_pv = [&](int j) -> bool {
     const int pb = j & 1, st = j & 1;
+    if (!mbar_wait(&bar.v_full[st], (j >> 1) & 1, ab, status)) return false;
     if (!mbar_wait(&bar.p_full[pb], (j >> 1) & 1, ab, status)) return false;
     tc_fence_after();
     const uint32_t p = smem_u32(smem + S::OFF_P + pb * S::P_BYTES);
-    const uint32_t v = smem_u32(smem + S::OFF_KV + st * S::STAGE_BYTES + S::KV_BYTES);
+    const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
     for (int k = 0; k < BKV / 16; ++k) {
       // A = P [128 x 128 keys], K-major: 64-key regions of 16 KB, 32 B per K step
@@ -126,15 +202,15 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
       mma_bf16_ss(tmem + S::TMEM_O, ad, bd, idesc_o, (j | k) != 0);
     }
     mma_commit(&bar.pv_done[pb]);
-    mma_commit(&bar.kv_empty[st]);
+    mma_commit(&bar.v_empty[st]);
     return true;
   };
   for (int j = 0; j < ntiles; ++j) {
     const int st = j & 1, sb = j & 1;
-    if (!mbar_wait(&bar.kv_full[st], (j >> 1) & 1, ab, status)) return;
+    if (!mbar_wait(&bar.k_full[st], (j >> 1) & 1, ab, status)) return;
     if (!mbar_wait(&bar.s_free[sb], ((j >> 1) & 1) ^ 1, ab, status)) return;
     tc_fence_after();
-    const uint32_t kb = smem_u32(smem + S::OFF_KV + st * S::STAGE_BYTES);
+    const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
@@ -143,6 +219,7 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
                   sdesc_sw128(kb + koff, 16, 1024), idesc_s, k != 0);
     }
     mma_commit(&bar.s_full[sb]);
+    mma_commit(&bar.k_empty[st]);      // K stage free once this QK^T completes
     if (j > 0 && !issue_pv(j - 1)) return;
   }
   if (!issue_pv(ntiles - 1)) return;
