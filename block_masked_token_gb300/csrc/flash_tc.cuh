@@ -27,25 +27,26 @@ constexpr int NUM_THREADS = 192;
 constexpr int SOFTMAX_THREADS = 128;
 constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by > 2^8
 
+constexpr int KV_STAGES = 3;               // depth of the K ring and of the V ring
+
 template <int D>
 struct Smem {
   static constexpr int Q_BYTES = BQ * D * 2;         // D/64 swizzled regions of [128][64]
   static constexpr int KV_BYTES = BKV * D * 2;       // one K or V tile
-  static constexpr int P_BYTES = BQ * BKV * 2;       // 2 regions of [128][64]
-  static constexpr int STAGES = 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;                          // K ring
-  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;        // V ring
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int TOTAL = OFF_P + 2 * P_BYTES + 1024;       // + alignment slack
-  static constexpr int TMEM_S = 0;                   // two S buffers at columns 0, 128
-  static constexpr int TMEM_O = 2 * BKV;             // O at column 256
+  static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;     // V ring
+  static constexpr int TOTAL = OFF_V + KV_STAGES * KV_BYTES + 1024;   // + alignment slack
+  // TMEM columns: S double buffer (fp32), O (fp32), P double buffer (bf16 pairs)
+  static constexpr int TMEM_S = 0;                   // S buffers at columns 0 and 128
+  static constexpr int TMEM_O = 2 * BKV;             // O at column 256 (D columns)
+  static constexpr int TMEM_P = 2 * BKV + 128;       // P buffers at 384 and 448 (64 each)
   static constexpr int TMEM_COLS = 512;
 };
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t k_full[KV_STAGES], k_empty[KV_STAGES], v_full[KV_STAGES], v_empty[KV_STAGES];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_final, drain;
@@ -58,11 +59,13 @@ MARS_DEV void init_barriers(Barriers& bar) {
   using namespace sm100;
   bar.abort = 0;
   mbar_init(&bar.q_full, 1);
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < KV_STAGES; ++i) {
     mbar_init(&bar.k_full[i], 1);
     mbar_init(&bar.k_empty[i], 1);
     mbar_init(&bar.v_full[i], 1);
     mbar_init(&bar.v_empty[i], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
     mbar_init(&bar.s_full[i], 1);
     mbar_init(&bar.s_free[i], SOFTMAX_THREADS);
     mbar_init(&bar.p_full[i], SOFTMAX_THREADS);
@@ -86,25 +89,26 @@ MARS_DEV void load_loop(Barriers& bar, uint8_t* smem, int ntiles, int32_t* statu
   using S = Smem<D>;
   const int lane = threadIdx.x & 31;
   volatile int* ab = &bar.abort;
-  int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+  int last_k[KV_STAGES], last_v[KV_STAGES];
+  for (int i = 0; i < KV_STAGES; ++i) last_k[i] = last_v[i] = -1;
   auto stage = [&](uint64_t* empty, uint64_t* full, int j) -> bool {
     int ok = 1;
     if (lane == 0) {
-      ok = mbar_wait(empty, ((j >> 1) & 1) ^ 1, ab, status);
+      ok = mbar_wait(empty, ((j / KV_STAGES) & 1) ^ 1, ab, status);
       if (ok) mbar_arrive_expect_tx(full, S::KV_BYTES);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     return ok != 0;
   };
   auto load_k = [&](int j) -> bool {
-    const int st = j & 1;
+    const int st = j % KV_STAGES;
     if (!stage(&bar.k_empty[st], &bar.k_full[st], j)) return false;
     issue_k(j, smem + S::OFF_K + st * S::KV_BYTES, &bar.k_full[st]);
     last_k[st] = j;
     return true;
   };
   auto load_v = [&](int j) -> bool {
-    const int st = j & 1;
+    const int st = j % KV_STAGES;
     if (!stage(&bar.v_empty[st], &bar.v_full[st], j)) return false;
     issue_v(j, smem + S::OFF_V + st * S::KV_BYTES, &bar.v_full[st]);
     last_v[st] = j;
@@ -118,9 +122,11 @@ MARS_DEV void load_loop(Barriers& bar, uint8_t* smem, int ntiles, int32_t* statu
   }
   if (lane == 0) {
     mbar_wait(&bar.q_full, 0, nullptr, status);
-    for (int st = 0; st < 2; ++st) {
-      if (last_k[st] >= 0) mbar_wait(&bar.k_full[st], (last_k[st] >> 1) & 1, nullptr, status);
-      if (last_v[st] >= 0) mbar_wait(&bar.v_full[st], (last_v[st] >> 1) & 1, nullptr, status);
+    for (int st = 0; st < KV_STAGES; ++st) {
+      if (last_k[st] >= 0)
+        mbar_wait(&bar.k_full[st], (last_k[st] / KV_STAGES) & 1, nullptr, status);
+      if (last_v[st] >= 0)
+        mbar_wait(&bar.v_full[st], (last_v[st] / KV_STAGES) & 1, nullptr, status);
     }
   }
   __syncwarp();
@@ -187,27 +193,26 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   volatile int* ab = &bar.abort;
   if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
   auto issue_pv = [&](int j) -> bool {
-    const int pb = j & 1, st = j & 1;
-    if (!mbar_wait(&bar.v_full[st], (j >> 1) & 1, ab, status)) return false;
+    const int pb = j & 1, st = j % KV_STAGES;
+    if (!mbar_wait(&bar.v_full[st], (j / KV_STAGES) & 1, ab, status)) return false;
     if (!mbar_wait(&bar.p_full[pb], (j >> 1) & 1, ab, status)) return false;
     tc_fence_after();
-    const uint32_t p = smem_u32(smem + S::OFF_P + pb * S::P_BYTES);
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
     for (int k = 0; k < BKV / 16; ++k) {
-      // A = P [128 x 128 keys], K-major: 64-key regions of 16 KB, 32 B per K step
-      const uint64_t ad = sdesc_sw128(p + (k >> 2) * (BQ * 128) + (k & 3) * 32, 16, 1024);
+      // A = P [128 rows x 128 keys] in TMEM: row = lane, 16 keys = 8 columns per K step
+      const uint32_t a = tmem + S::TMEM_P + pb * (BKV / 2) + k * 8;
       // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
       const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
-      mma_bf16_ss(tmem + S::TMEM_O, ad, bd, idesc_o, (j | k) != 0);
+      mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (j | k) != 0);
     }
     mma_commit(&bar.pv_done[pb]);
     mma_commit(&bar.v_empty[st]);
     return true;
   };
   for (int j = 0; j < ntiles; ++j) {
-    const int st = j & 1, sb = j & 1;
-    if (!mbar_wait(&bar.k_full[st], (j >> 1) & 1, ab, status)) return;
+    const int st = j % KV_STAGES, sb = j & 1;
+    if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
     if (!mbar_wait(&bar.s_free[sb], ((j >> 1) & 1) ^ 1, ab, status)) return;
     tc_fence_after();
     const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
@@ -317,30 +322,25 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     if (raise) m = tmax;
     // P buffer pb was read by PV of tile j-2
     if (!(ok = warp_wait(&bar.pv_done[pb], ((j >> 1) & 1) ^ 1))) break;
-    // P = exp2(S*scale - m) -> bf16 in the swizzled K-major layout, and the row sum
-    uint8_t* pbuf = smem + S::OFF_P + pb * S::P_BYTES;
+    // P = exp2(S*scale - m) -> bf16 pairs into the TMEM P buffer (row = lane, the A
+    // operand of the PV MMA), and the row sum
+    const uint32_t p_addr = tmem + S::TMEM_P + pb * (BKV / 2) + lane_off;
     const float neg_m = (m == -INFINITY) ? 0.f : -m;   // no visible key yet: all P are 0
     float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < BKV / 32; ++c) {
-      uint32_t packed[16];
+    for (int h = 0; h < BKV / 64; ++h) {               // 64 keys = 32 columns per store
+      uint32_t packed[32];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(r[c * 32 + e]), scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(r[c * 32 + e + 1]), scale_log2, neg_m));
+      for (int e = 0; e < 64; e += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(r[h * 64 + e]), scale_log2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(r[h * 64 + e + 1]), scale_log2, neg_m));
         packed[e >> 1] = pack_bf16x2(p0, p1);
         ps[(e >> 1) & 3] += p0 + p1;
       }
-      uint8_t* region = pbuf + (c >> 1) * (BQ * 128);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int chunk = (c & 1) * 4 + q4;
-        *reinterpret_cast<uint4*>(region + sw_off(row, chunk)) =
-            make_uint4(packed[q4 * 4], packed[q4 * 4 + 1], packed[q4 * 4 + 2], packed[q4 * 4 + 3]);
-      }
+      tmem_st32(p_addr + h * 32, packed);
     }
     l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-    fence_proxy_async_smem();     // generic-proxy smem writes -> visible to the MMA
+    tmem_st_wait();
     tc_fence_before();
     mbar_arrive(&bar.s_free[sb]);
     mbar_arrive(&bar.p_full[pb]);
