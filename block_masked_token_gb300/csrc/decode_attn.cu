@@ -152,9 +152,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ loader
-    if (lane == 0) {
+  if (warp == 0 || warp == flash::V_LOADER_WARP) {
+    // --------------------------------------------- loaders: K ring (warp 0, and Q first),
+    // V ring (its own warp)
+    const bool is_v = warp == flash::V_LOADER_WARP;
+    if (!is_v && lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, a.R * 128 * (D / 64));
       for (int x = 0; x < D / 64; ++x)
         tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, kvh * a.G,
@@ -187,8 +189,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       };
     };
-    flash::load_loop<D>(bar, smem, n_total, a.status, issue(&tm_kp, &tm_kb),
-                        issue(&tm_vp, &tm_vb));
+    if (is_v)
+      flash::load_ring<D>(bar, smem, n_total, a.status, true, issue(&tm_vp, &tm_vb));
+    else
+      flash::load_ring<D>(bar, smem, n_total, a.status, false, issue(&tm_kp, &tm_kb));
+    if (!is_v && lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
     if (st_flags && a.status) atomicOr(a.status, st_flags);
   } else if (warp == 1) {
     if (lane == 0) {

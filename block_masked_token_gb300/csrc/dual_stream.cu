@@ -138,6 +138,15 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
 
+  // one 3D box of 128 rows per 64-column half; rows past the batch read as zeros
+  auto issue = [&](const CUtensorMap* tm) {
+    return [&, tm](int j, uint8_t* dst, uint64_t* b) {
+      if (lane == 0) {
+        const int z = zb + pol.tile_key0(j);
+        for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * (BKV * 128), tm, b, x * 64, kvh, z);
+      }
+    };
+  };
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, S::Q_BYTES);
@@ -145,16 +154,10 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, h,
                     zb + stream * a.L + pol.r0);
     }
-    // one 3D box of 128 rows per 64-column half; rows past the batch read as zeros
-    auto issue = [&](const CUtensorMap* tm) {
-      return [&, tm](int j, uint8_t* dst, uint64_t* b) {
-        if (lane == 0) {
-          const int z = zb + pol.tile_key0(j);
-          for (int x = 0; x < D / 64; ++x) tma_load_3d(dst + x * (BKV * 128), tm, b, x * 64, kvh, z);
-        }
-      };
-    };
-    flash::load_loop<D>(bar, smem, pol.n_total, a.status, issue(&tm_k), issue(&tm_v));
+    flash::load_ring<D>(bar, smem, pol.n_total, a.status, false, issue(&tm_k));
+    if (lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
+  } else if (warp == flash::V_LOADER_WARP) {
+    flash::load_ring<D>(bar, smem, pol.n_total, a.status, true, issue(&tm_v));
   } else if (warp == 1) {
     if (lane == 0) {
       flash::mma_loop<D>(bar, smem, pol.n_total, tmem, a.status);

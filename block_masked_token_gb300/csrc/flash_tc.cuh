@@ -1,18 +1,19 @@
 // Flash-attention tile engine on tcgen05 shared by the dual-stream and decode kernels.
 //
 // One CTA owns a 128-row query tile held in shared memory and walks a list of 128-key
-// tiles. Roles (192 threads):
-//   warp 0      loader (written by each kernel): K tiles and V tiles into two separate
-//               2-stage rings (TMA, 128-byte swizzle), K one tile ahead of V;
+// tiles. Roles (224 threads):
+//   warp 0      Q loader, then K loader: K tiles into a 3-stage ring (TMA, 128-byte
+//               swizzle); warp 6 streams V tiles into their own 3-stage ring, so the two
+//               rings advance independently;
 //   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two 128-column fp32
-//               TMEM buffers, then O += P_{j-1} V_{j-1} (O lives in TMEM, P in smem). A K
-//               stage is released as soon as its QK^T finishes, a V stage after its PV,
-//               so the next loads start early;
+//               TMEM buffers, then O += P_{j-1} V_{j-1} with O and P in TMEM (P is the
+//               A operand, read from TMEM). A K stage is released as soon as its QK^T
+//               finishes, a V stage after its PV;
 //   warps 2..5  softmax: thread = query row. It reads its S_j row (tcgen05.ld) into
-//               registers, takes the row max, and writes P = exp2(S - m) as bf16 into the
-//               128-byte-swizzled K-major A-operand layout. The running max is raised
-//               lazily: O and l are rescaled (tcgen05.ld / st) only when the max grows by
-//               more than 2^8, which keeps P <= 256 and the result exact up to rounding.
+//               registers, takes the row max, and writes P = exp2(S - m) as bf16 pairs
+//               into a TMEM P buffer (tcgen05.st). The running max is raised lazily: O and
+//               l are rescaled (tcgen05.ld / st) only when the max grows by more than 2^8,
+//               which keeps P <= 256 and the result exact up to rounding.
 // S_{j+1} is issued before PV_j so the softmax of one tile overlaps the MMAs of the next.
 #pragma once
 
@@ -23,7 +24,8 @@ namespace flash {
 
 constexpr int BQ = 128;                    // query rows per CTA tile
 constexpr int BKV = 128;                   // keys per tile
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;          // 7 warps, roles below
+constexpr int V_LOADER_WARP = 6;
 constexpr int SOFTMAX_THREADS = 128;
 constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by > 2^8
 
@@ -76,58 +78,38 @@ MARS_DEV void init_barriers(Barriers& bar) {
   fence_barrier_init();
 }
 
-// Loader skeleton shared by the kernels, run by the whole loader warp: lane 0 waits for
-// a free stage and arms its barrier with the tile's byte count, then every lane calls
-// `issue_k(j, dst, bar)` / `issue_v(j, dst, bar)` (the kernel decides which lanes issue
-// the TMA copies of tile j into dst, completing on bar). Order: K_0, then for each j:
-// K_{j+1}, V_j. Returns after waiting (bounded) for every copy it issued, so the CTA
-// never exits with copies in flight.
-template <int D, class IssueK, class IssueV>
-MARS_DEV void load_loop(Barriers& bar, uint8_t* smem, int ntiles, int32_t* status,
-                        IssueK issue_k, IssueV issue_v) {
+// Loader skeleton shared by the kernels: one warp streams one ring (the K ring or the V
+// ring; the two run independently, so a slow V slot never holds back a K load). Lane 0
+// waits for a free stage and arms its barrier with the tile's byte count, then every lane
+// calls `issue(j, dst, bar)` (the kernel decides which lanes issue the TMA copies of tile
+// j into dst, completing on bar). Returns after waiting (bounded) for every copy it
+// issued, so the CTA never exits with copies in flight.
+template <int D, class Issue>
+MARS_DEV void load_ring(Barriers& bar, uint8_t* smem, int ntiles, int32_t* status, bool is_v,
+                        Issue issue) {
   using namespace sm100;
   using S = Smem<D>;
   const int lane = threadIdx.x & 31;
   volatile int* ab = &bar.abort;
-  int last_k[KV_STAGES], last_v[KV_STAGES];
-  for (int i = 0; i < KV_STAGES; ++i) last_k[i] = last_v[i] = -1;
-  auto stage = [&](uint64_t* empty, uint64_t* full, int j) -> bool {
+  uint64_t* full = is_v ? bar.v_full : bar.k_full;
+  uint64_t* empty = is_v ? bar.v_empty : bar.k_empty;
+  uint8_t* ring = smem + (is_v ? S::OFF_V : S::OFF_K);
+  int last[KV_STAGES];
+  for (int i = 0; i < KV_STAGES; ++i) last[i] = -1;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % KV_STAGES;
     int ok = 1;
     if (lane == 0) {
-      ok = mbar_wait(empty, ((j / KV_STAGES) & 1) ^ 1, ab, status);
-      if (ok) mbar_arrive_expect_tx(full, S::KV_BYTES);
+      ok = mbar_wait(&empty[st], ((j / KV_STAGES) & 1) ^ 1, ab, status);
+      if (ok) mbar_arrive_expect_tx(&full[st], S::KV_BYTES);
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    return ok != 0;
-  };
-  auto load_k = [&](int j) -> bool {
-    const int st = j % KV_STAGES;
-    if (!stage(&bar.k_empty[st], &bar.k_full[st], j)) return false;
-    issue_k(j, smem + S::OFF_K + st * S::KV_BYTES, &bar.k_full[st]);
-    last_k[st] = j;
-    return true;
-  };
-  auto load_v = [&](int j) -> bool {
-    const int st = j % KV_STAGES;
-    if (!stage(&bar.v_empty[st], &bar.v_full[st], j)) return false;
-    issue_v(j, smem + S::OFF_V + st * S::KV_BYTES, &bar.v_full[st]);
-    last_v[st] = j;
-    return true;
-  };
-  if (ntiles > 0 && load_k(0)) {
-    for (int j = 0; j < ntiles; ++j) {
-      if (j + 1 < ntiles && !load_k(j + 1)) break;
-      if (!load_v(j)) break;
-    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    issue(j, ring + st * S::KV_BYTES, &full[st]);
+    last[st] = j;
   }
   if (lane == 0) {
-    mbar_wait(&bar.q_full, 0, nullptr, status);
-    for (int st = 0; st < KV_STAGES; ++st) {
-      if (last_k[st] >= 0)
-        mbar_wait(&bar.k_full[st], (last_k[st] / KV_STAGES) & 1, nullptr, status);
-      if (last_v[st] >= 0)
-        mbar_wait(&bar.v_full[st], (last_v[st] / KV_STAGES) & 1, nullptr, status);
-    }
+    for (int st = 0; st < KV_STAGES; ++st)
+      if (last[st] >= 0) mbar_wait(&full[st], (last[st] / KV_STAGES) & 1, nullptr, status);
   }
   __syncwarp();
 }
