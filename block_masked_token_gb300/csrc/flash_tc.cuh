@@ -49,7 +49,7 @@ struct Smem {
 struct Barriers {
   uint64_t q_full;
   uint64_t k_full[KV_STAGES], k_empty[KV_STAGES], v_full[KV_STAGES], v_empty[KV_STAGES];
-  uint64_t s_full[2], s_free[2];
+  uint64_t s_full[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t o_final, drain;
   uint32_t tmem_base;
@@ -69,7 +69,6 @@ MARS_DEV void init_barriers(Barriers& bar) {
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(&bar.s_full[i], 1);
-    mbar_init(&bar.s_free[i], SOFTMAX_THREADS);
     mbar_init(&bar.p_full[i], SOFTMAX_THREADS);
     mbar_init(&bar.pv_done[i], 1);
   }
@@ -194,8 +193,10 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   };
   for (int j = 0; j < ntiles; ++j) {
     const int st = j % KV_STAGES, sb = j & 1;
+    // S buffer sb was last read by the softmax of tile j-2; that read finished before the
+    // softmax arrived on p_full(j-2), which this thread waited for before issuing PV_{j-2}
+    // in the previous iteration, so no separate wait is needed before overwriting it.
     if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
-    if (!mbar_wait(&bar.s_free[sb], ((j >> 1) & 1) ^ 1, ab, status)) return;
     tc_fence_after();
     const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
 #pragma unroll
@@ -245,8 +246,13 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
   auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(b, parity, ab, status));
   };
+  // tile descriptors are computed one tile ahead (for paged tiles this reads the block
+  // table, whose latency then overlaps the wait for the next S)
+  typename Policy::Tile next_tile = pol.tile(0);
   for (int j = 0; j < ntiles && ok; ++j) {
     const int sb = j & 1, pb = j & 1;
+    const typename Policy::Tile tile = next_tile;
+    if (j + 1 < ntiles) next_tile = pol.tile(j + 1);
     if (!(ok = warp_wait(&bar.s_full[sb], (j >> 1) & 1))) break;
     tc_fence_after();
     const uint32_t s_addr = tmem + S::TMEM_S + sb * BKV + lane_off;
@@ -255,7 +261,6 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     for (int c = 0; c < BKV / 32; ++c)
       tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(r + c * 32));
     tmem_ld_wait();
-    const typename Policy::Tile tile = pol.tile(j);
     if (!rv || !tile.full) {
       // visible columns of this row in this tile: [0, e1) or [s2, e2], on mapped pages
       // (none for a padding row past the end of the query tile)
@@ -324,7 +329,6 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&bar.s_free[sb]);
     mbar_arrive(&bar.p_full[pb]);
   }
   if (!ok) return;
