@@ -195,12 +195,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       flash::load_ring<D>(bar, smem, n_total, a.status, false, issue(&tm_kp, &tm_kb));
     if (!is_v && lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
     if (st_flags && a.status) atomicOr(a.status, st_flags);
-  } else if (warp == 1) {
-    if (lane == 0) {
-      flash::mma_loop<D>(bar, smem, n_total, tmem, a.status);
-      mma_commit(&bar.drain);
-      mbar_wait(&bar.drain, 0, nullptr, a.status);
-    }
+  } else if (warp == 1 || warp == flash::PV_ISSUER_WARP) {
+    if (lane == 0)
+      flash::issuer<D, false>(bar, smem, n_total, tmem, a.status, warp == flash::PV_ISSUER_WARP);
   } else {
     flash::softmax_loop<D>(bar, smem, pol, n_total, tmem, a.scale_log2, a.status);
   }

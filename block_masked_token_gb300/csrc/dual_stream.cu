@@ -158,12 +158,10 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
   } else if (warp == flash::V_LOADER_WARP) {
     flash::load_ring<D>(bar, smem, pol.n_total, a.status, true, issue(&tm_v));
-  } else if (warp == 1) {
-    if (lane == 0) {
-      flash::mma_loop<D>(bar, smem, pol.n_total, tmem, a.status);
-      mma_commit(&bar.drain);
-      mbar_wait(&bar.drain, 0, nullptr, a.status);
-    }
+  } else if (warp == 1 || warp == flash::PV_ISSUER_WARP) {
+    if (lane == 0)
+      flash::issuer<D, true>(bar, smem, pol.n_total, tmem, a.status,
+                             warp == flash::PV_ISSUER_WARP);
   } else {
     flash::softmax_loop<D>(bar, smem, pol, pol.n_total, tmem, a.scale_log2, a.status);
   }

@@ -1,20 +1,21 @@
 // Flash-attention tile engine on tcgen05 shared by the dual-stream and decode kernels.
 //
 // One CTA owns a 128-row query tile held in shared memory and walks a list of 128-key
-// tiles. Roles (224 threads):
+// tiles. Roles (256 threads):
 //   warp 0      Q loader, then K loader: K tiles into a 3-stage ring (TMA, 128-byte
 //               swizzle); warp 6 streams V tiles into their own 3-stage ring, so the two
 //               rings advance independently;
-//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two 128-column fp32
-//               TMEM buffers, then O += P_{j-1} V_{j-1} with O and P in TMEM (P is the
-//               A operand, read from TMEM). A K stage is released as soon as its QK^T
-//               finishes, a V stage after its PV;
+//   warp 1      TMEM owner and QK^T issuer: S_j = Q K_j^T into one of two 128-column
+//               fp32 TMEM buffers; a K stage is released as soon as its QK^T finishes;
+//   warp 7      PV issuer: O += P_j V_j with O and P in TMEM (P is the A operand, read
+//               from TMEM); a V stage is released after its PV;
 //   warps 2..5  softmax: thread = query row. It reads its S_j row (tcgen05.ld) into
 //               registers, takes the row max, and writes P = exp2(S - m) as bf16 pairs
 //               into a TMEM P buffer (tcgen05.st). The running max is raised lazily: O and
 //               l are rescaled (tcgen05.ld / st) only when the max grows by more than 2^8,
 //               which keeps P <= 256 and the result exact up to rounding.
-// S_{j+1} is issued before PV_j so the softmax of one tile overlaps the MMAs of the next.
+// The two issuers run independently, so the softmax of tile j overlaps QK^T of later
+// tiles and the PV of earlier ones.
 #pragma once
 
 #include "sm100.cuh"
@@ -24,8 +25,9 @@ namespace flash {
 
 constexpr int BQ = 128;                    // query rows per CTA tile
 constexpr int BKV = 128;                   // keys per tile
-constexpr int NUM_THREADS = 224;          // 7 warps, roles below
+constexpr int NUM_THREADS = 256;          // 8 warps, roles below
 constexpr int V_LOADER_WARP = 6;
+constexpr int PV_ISSUER_WARP = 7;
 constexpr int SOFTMAX_THREADS = 128;
 constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by > 2^8
 
@@ -51,7 +53,7 @@ struct Barriers {
   uint64_t k_full[KV_STAGES], k_empty[KV_STAGES], v_full[KV_STAGES], v_empty[KV_STAGES];
   uint64_t s_full[2];
   uint64_t p_full[2], pv_done[2];
-  uint64_t o_final, drain;
+  uint64_t o_final, drain, drain_pv;
   uint32_t tmem_base;
   int abort;
 };
@@ -74,6 +76,7 @@ MARS_DEV void init_barriers(Barriers& bar) {
   }
   mbar_init(&bar.o_final, 1);
   mbar_init(&bar.drain, 1);
+  mbar_init(&bar.drain_pv, 1);
   fence_barrier_init();
 }
 
@@ -162,7 +165,72 @@ MARS_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// The MMA issuer (one thread). ntiles >= 1.
+// The MMAs are issued by two threads (tcgen05.mma issue blocks until the tensor pipe
+// accepts the instruction, so a single issuer leaves the pipe idle whenever it waits on a
+// barrier; with two, one thread's waits overlap the other's MMAs). Each commits only its
+// own MMAs. ntiles >= 1 for both.
+
+// QK^T issuer: S_j = Q K_j^T into S buffer j & 1.
+template <int D>
+MARS_DEV void s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
+                       int32_t* status) {
+  using namespace sm100;
+  using S = Smem<D>;
+  const uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);   // S = Q K^T: B K-major
+  const uint32_t q = smem_u32(smem + S::OFF_Q);
+  volatile int* ab = &bar.abort;
+  if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % KV_STAGES, sb = j & 1;
+    if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
+    // S buffer sb was last read by the softmax of tile j-2, which arrives on p_full(j-2)
+    // only after that read completed
+    if (j >= 2 && !mbar_wait(&bar.p_full[sb], ((j - 2) >> 1) & 1, ab, status)) return;
+    tc_fence_after();
+    const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
+      const uint32_t koff = (k >> 2) * (BKV * 128) + (k & 3) * 32;
+      mma_bf16_ss(tmem + S::TMEM_S + sb * BKV, sdesc_sw128(q + off, 16, 1024),
+                  sdesc_sw128(kb + koff, 16, 1024), idesc_s, k != 0);
+    }
+    mma_commit(&bar.s_full[sb]);
+    mma_commit(&bar.k_empty[st]);      // K stage free once this QK^T completes
+  }
+}
+
+// PV issuer: O += P_j V_j (P from TMEM buffer j & 1), then o_final after the last tile.
+template <int D>
+MARS_DEV void pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
+                        int32_t* status) {
+  using namespace sm100;
+  using S = Smem<D>;
+  const uint32_t idesc_o = idesc_bf16_f32(BQ, D, true);      // O = P V: B MN-major
+  volatile int* ab = &bar.abort;
+  for (int j = 0; j < ntiles; ++j) {
+    const int pb = j & 1, st = j % KV_STAGES;
+    if (!mbar_wait(&bar.v_full[st], (j / KV_STAGES) & 1, ab, status)) return;
+    if (!mbar_wait(&bar.p_full[pb], (j >> 1) & 1, ab, status)) return;
+    tc_fence_after();
+    const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
+#pragma unroll
+    for (int k = 0; k < BKV / 16; ++k) {
+      // A = P [128 rows x 128 keys] in TMEM: row = lane, 16 keys = 8 columns per K step
+      const uint32_t a = tmem + S::TMEM_P + pb * (BKV / 2) + k * 8;
+      // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
+      const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
+      mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (j | k) != 0);
+    }
+    mma_commit(&bar.pv_done[pb]);
+    mma_commit(&bar.v_empty[st]);
+  }
+  mma_commit(&bar.o_final);
+}
+
+// Single-thread alternative: one thread issues S_j, then PV_{j-1}, so the QK^T the softmax
+// waits for is never queued behind PV work (used where the softmax is on the critical
+// path). ntiles >= 1.
 template <int D>
 MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
                        int32_t* status) {
@@ -212,6 +280,31 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   }
   if (!issue_pv(ntiles - 1)) return;
   mma_commit(&bar.o_final);
+}
+
+// Run by lane 0 of warps 1 and PV_ISSUER_WARP: the issuer's loop, then a wait (bounded)
+// for its own MMAs so none is in flight when the CTA tears down. With kSplit the two warps
+// issue QK^T and PV separately; otherwise warp 1 runs mma_loop and the PV warp idles.
+template <int D, bool kSplit>
+MARS_DEV void issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem, int32_t* status,
+                     bool pv) {
+  using namespace sm100;
+  if (!kSplit) {
+    if (pv) return;
+    mma_loop<D>(bar, smem, ntiles, tmem, status);
+    mma_commit(&bar.drain);
+    mbar_wait(&bar.drain, 0, nullptr, status);
+    return;
+  }
+  if (pv) {
+    pv_issuer<D>(bar, smem, ntiles, tmem, status);
+    mma_commit(&bar.drain_pv);
+    mbar_wait(&bar.drain_pv, 0, nullptr, status);
+  } else {
+    s_issuer<D>(bar, smem, ntiles, tmem, status);
+    mma_commit(&bar.drain);
+    mbar_wait(&bar.drain, 0, nullptr, status);
+  }
 }
 
 MARS_DEV float ex2_approx(float x) {
