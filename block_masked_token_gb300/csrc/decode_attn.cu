@@ -54,6 +54,7 @@ struct DecodePolicy {
   const int32_t* bt_row;
   float* part;           // [R][D + 4] records of this (sequence, kv head, split)
   int P, start, n_prefix;
+  int s_idx, s_kvh;      // sequence and kv head of this CTA
 
   struct Tile {
     int kp0;             // logical key position of column 0
@@ -93,8 +94,18 @@ struct DecodePolicy {
     c.e2 = -1;
     return c;
   }
-  MARS_DEV void store_chunk(int row, int col, const uint32_t (&r)[32], float, float m,
+  MARS_DEV void store_chunk(int row, int col, const uint32_t (&r)[32], float inv, float m,
                             float l) const {
+    if (a->nsplit == 1) {            // the only split: final output, normalised
+      const int k = row / a->G, h = s_kvh * a->G + row % a->G;
+      float* dst = a->o + (((size_t)s_idx * a->B + k) * a->hq + h) * D + col;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(dst + e) =
+            make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
+                        __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+      return;
+    }
     float* rec = part + (size_t)row * (D + 4);
     if (col == 0) {
       rec[0] = m;
@@ -127,6 +138,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   pol.bt_row = a.block_table + (size_t)s * a.max_pages;
   pol.part = a.ws + ((((size_t)s * a.hkv + kvh) * a.nsplit + sp) * a.R) * (D + 4);
   pol.P = a.seq_lens[s];
+  pol.s_idx = s;
+  pol.s_kvh = kvh;
   pol.start = sp * a.split_len;
   const bool last = sp == a.nsplit - 1;
   const int end = last ? pol.P : min(pol.P, pol.start + a.split_len);
@@ -283,8 +296,10 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* 
   }
   dim3 grid(a.nsplit, a.hkv, batch);
   decode_tc_kernel<D><<<grid, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tkp, tvp, tkb, tvb, a);
-  dim3 cgrid((a.hq * a.B + 7) / 8, batch);
-  decode_combine_kernel<D><<<cgrid, 256, 0, stream>>>(a);
+  if (a.nsplit > 1) {
+    dim3 cgrid((a.hq * a.B + 7) / 8, batch);
+    decode_combine_kernel<D><<<cgrid, 256, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -297,6 +312,9 @@ DecodePlan plan_decode(int batch, int B, int hq, int hkv, int d, int max_len) {
   long long per = (pairs * T + kTargetCtas - 1) / kTargetCtas;
   if (per < 4 * BKV) per = 4 * BKV;
   per = (per + BKV - 1) / BKV * BKV;
+  // With at least two (sequence, kv head) pairs per SM the pairs alone balance the GPU:
+  // one split each, whose CTA writes the normalised output itself (no partials, no merge).
+  if (pairs >= 2LL * kNumSMs) per = (T + BKV - 1) / BKV * BKV;
   p.split_len = (int)per;
   p.nsplit = (int)((T + per - 1) / per);
   if (p.nsplit < 1) p.nsplit = 1;
@@ -317,7 +335,7 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
                scale * 1.4426950408889634f};
   const cudaError_t e = d == 64 ? launch_tc<64>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream)
                                 : launch_tc<128>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream);
-  count_launches(2);
+  count_launches(plan.nsplit > 1 ? 2 : 1);
   return e;
 }
 

@@ -198,6 +198,35 @@ def test_decode_unmapped_page_sets_status():
     assert st & mars.ST_NOPAGE
 
 
+def test_decode_single_split_direct_output():
+    """With at least two (sequence, kv head) pairs per SM the kernel runs one split per
+    pair and writes the normalised output directly (no merge pass)."""
+    cfg = W.DecodeConfig("d6", batch=160, prefix_lo=0, prefix_hi=300, B=4, hq=4, hkv=2, d=64,
+                         hidden=64, vocab=64)
+    inp = _decode_case(cfg, seed=8)
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
+    assert st == 0
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_decode_sustained_config_sampled():
+    """Batch 128, prefixes 2048..8192, B=16, 7B heads: sampled sequences (single-split
+    path, the shape the decode step of the benchmark runs)."""
+    cfg = W.SUSTAINED_DECODE_7B
+    inp = _to_dev(W.make_decode_inputs(cfg, seed=0, device=DEV, steps=1, with_head=False))
+    hint = int(inp.prefix_lens.max()) + cfg.B * cfg.steps
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg, max_len_hint=hint)
+    assert st == 0
+    seqs = [0, 64, 127]
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.cpu().numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size, seqs=seqs)
+    assert_attn_close(o.cpu().numpy()[seqs], ref[seqs], "decode sustained")
+
+
 def test_decode_config_7b_sampled():
     cfg = W.DECODE_7B
     inp = _to_dev(W.make_decode_inputs(cfg, seed=0, device=DEV, with_head=False))
