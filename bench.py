@@ -34,6 +34,13 @@ import torch  # noqa: E402
 from block_masked_token_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TFLOP/s"
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of the kernel as it is now; the summaries and commands are in profiles/. Reset to None
+# whenever the kernel changes, until it is captured again.
+TRAFFIC_HEAD_GEMM = 1124377856         # profiles/head_gemm_sustained_decode_7b_b128_B16.md
+TRAFFIC_DECODE_STEP0 = 1369159896      # profiles/decode_tc_sustained_decode_7b_b128_B16.md
+TRAFFIC_DUAL_STREAM = 332258048        # profiles/dual_stream_tc_dual_stream_7b_b2_2L8192_B16.md
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
 
@@ -343,7 +350,17 @@ def run_gpu(args, rank, world, local):
             "mean_accepted_per_seq_step": tok_local / (K * cfg.batch),
             "decode_attn": {"us_per_call": statistics.mean(t_attn) * 1e6,
                             "hbm_gbs": attn_gbs,
-                            "frac_hbm": attn_gbs / peaks["hbm_gbs"]},
+                            "frac_hbm": attn_gbs / peaks["hbm_gbs"],
+                            "roofline": {"bound": "hbm", "achieved": attn_gbs,
+                                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                         "frac": attn_gbs / peaks["hbm_gbs"],
+                                         "traffic": TRAFFIC_DECODE_STEP0,
+                                         "traffic_note": "step 0 of the workload (prefix "
+                                                         "lengths before any commit)",
+                                         "peak_source": peaks["source"] + " copy bandwidth",
+                                         "algorithmic": "committed K and V rows x hkv x d x "
+                                                        "2 B x 2 + block K/V + Q + O (fp32) "
+                                                        "per call"}},
             "head_accept": {"us_per_call": statistics.mean(t_head) * 1e6,
                             "tflops": head_tflops, "frac_tensor": frac_head},
             "kv_commit": {"us_per_call": statistics.mean(t_commit) * 1e6},
@@ -351,7 +368,7 @@ def run_gpu(args, rank, world, local):
             "roofline": {"kernel": "mars_head_accept (LM head GEMM + fused epilogue)",
                          "bound": "tensor", "achieved": head_tflops,
                          "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                         "frac": frac_head, "traffic": None,
+                         "frac": frac_head, "traffic": TRAFFIC_HEAD_GEMM,
                          "peak_source": peaks["source"] + " bf16 sustained",
                          "algorithmic": f"2*{cfg.batch * cfg.B}*{cfg.hidden}*{cfg.vocab} "
                                         "flop per call"},
@@ -435,7 +452,10 @@ def run_dual(device, peaks, reps=10, warm=3):
     return {"workload": cfg.name, "ms": t * 1e3, "tflops": tf,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
-                         "traffic": None, "peak_source": peaks["source"] + " bf16 burst"},
+                         "traffic": TRAFFIC_DUAL_STREAM,
+                         "peak_source": peaks["source"] + " bf16 burst",
+                         "algorithmic": "4 x d flop per visible (query, key) pair, L(L+1) "
+                                        "pairs per (batch, head)"},
             "l2": "flushed (256 MB write) before each timed launch"}
 
 
