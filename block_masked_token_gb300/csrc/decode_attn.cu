@@ -9,8 +9,10 @@
 // tcgen05 flash engine (flash_tc.cuh) over its split: prefix tiles of 128 keys gathered
 // page by page from the paged pool (8 producer lanes, one 16-token page each, TMA with
 // 128-byte swizzle), and for the last split one more tile with the B block keys (causal:
-// query k sees block keys 0..k). Each split writes an unnormalised partial
-// (m in log2 units, l, O) to the workspace; a second kernel merges the splits.
+// query k sees block keys 0..k). With several splits each writes an unnormalised partial
+// (m in log2 units, l, O) to the workspace and a second kernel merges them; when the
+// (sequence, kv head) pairs alone fill the GPU there is one split per pair and its CTA
+// writes the normalised output directly.
 #include <climits>
 
 #include "common.cuh"

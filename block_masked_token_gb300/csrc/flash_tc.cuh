@@ -15,7 +15,8 @@
 //               l are rescaled (tcgen05.ld / st) only when the max grows by more than 2^8,
 //               which keeps P <= 256 and the result exact up to rounding.
 // The two issuers run independently, so the softmax of tile j overlaps QK^T of later
-// tiles and the PV of earlier ones.
+// tiles and the PV of earlier ones. A kernel may instead let warp 1 issue both (S_j, then
+// PV_{j-1}); the decode kernel does, its tile lists being short.
 #pragma once
 
 #include "sm100.cuh"
