@@ -165,7 +165,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = bar.tmem_base;
+  // read once per warp and broadcast: a warp-uniform TMEM base keeps the MMA operands in
+  // uniform registers, which tcgen05.mma issue depends on for its rate
+  const uint32_t tmem = __shfl_sync(0xffffffffu, bar.tmem_base, 0);
 
   if (warp == 0 || warp == flash::V_LOADER_WARP) {
     // --------------------------------------------- loaders: K ring (warp 0, and Q first),

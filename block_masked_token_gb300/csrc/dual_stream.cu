@@ -136,7 +136,8 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = bar.tmem_base;
+  // read once per warp and broadcast: a warp-uniform TMEM base
+  const uint32_t tmem = __shfl_sync(0xffffffffu, bar.tmem_base, 0);
 
   // one 3D box of 128 rows per 64-column half; rows past the batch read as zeros
   auto issue = [&](const CUtensorMap* tm) {

@@ -314,6 +314,43 @@ MARS_DEV float ex2_approx(float x) {
   return y;
 }
 
+MARS_DEV float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of one row's 128 S values (fp32 bits), scaled to log2 units: 8 independent
+// chains of three-input max, then a short tree.
+MARS_DEV float row_max_log2(const uint32_t (&r)[BKV], float scale_log2) {
+  float pm[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pm[i] = fmaxf(__uint_as_float(r[i]), __uint_as_float(r[8 + i]));
+#pragma unroll
+  for (int k = 2; k < BKV / 8; k += 2)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      pm[i] = max3f(pm[i], __uint_as_float(r[k * 8 + i]), __uint_as_float(r[(k + 1) * 8 + i]));
+  return fmaxf(max3f(pm[0], pm[1], pm[2]), max3f(max3f(pm[3], pm[4], pm[5]), pm[6], pm[7])) *
+         scale_log2;
+}
+
+// P = exp2(S * scale_log2 - m) for 64 S values starting at r[c0], packed as 32 bf16 pairs
+// (even key in the low half); the fp32 values are added to acc (two lanes per float2).
+// The scale-and-shift and the sums run as packed f32x2 operations.
+MARS_DEV void exp2_pack64(const uint32_t (&r)[BKV], int c0, float scale_log2, float neg_m,
+                          uint32_t (&packed)[32], float2 (&acc)[2]) {
+  const float2 sc = make_float2(scale_log2, scale_log2), sh = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const float2 t = __ffma2_rn(make_float2(__uint_as_float(r[c0 + e]), __uint_as_float(r[c0 + e + 1])),
+                                sc, sh);
+    const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    packed[e >> 1] = pack_bf16x2(p.x, p.y);
+    acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], p);
+  }
+}
+
 // Softmax + final normalisation for one query row per thread (threads 64..191).
 // Policy provides: row_valid(row), row_vis(row), tile(j) -> Tile (with .full set when
 // every row sees every key of tile j, so no per-key test runs), cols(vis, tile) ->
@@ -367,17 +404,7 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
           if (!((mk >> e) & 1u)) r[c * 32 + e] = 0xff800000u;
       }
     }
-    // row max of the tile: 8 independent chains, then a tree
-    float pm[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) pm[i] = __uint_as_float(r[i]);
-#pragma unroll
-    for (int k = 1; k < BKV / 8; ++k)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) pm[i] = fmaxf(pm[i], __uint_as_float(r[k * 8 + i]));
-    const float tmax =
-        fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-              fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * scale_log2;
+    const float tmax = row_max_log2(r, scale_log2);
     // lazy rescale of O and l: a row raises its max only when it grows by more than 2^8.
     // Rows whose O already holds keys (m finite) rescale it in TMEM; the TMEM pass runs
     // for the whole warp when any of its rows needs it (alpha = 1 for the others).
@@ -407,23 +434,17 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     // operand of the PV MMA), and the row sum
     const uint32_t p_addr = tmem + S::TMEM_P + pb * (BKV / 2) + lane_off;
     const float neg_m = (m == -INFINITY) ? 0.f : -m;   // no visible key yet: all P are 0
-    float ps[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int h = 0; h < BKV / 64; ++h) {               // 64 keys = 32 columns per store
       uint32_t packed[32];
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(r[h * 64 + e]), scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(r[h * 64 + e + 1]), scale_log2, neg_m));
-        packed[e >> 1] = pack_bf16x2(p0, p1);
-        ps[(e >> 1) & 3] += p0 + p1;
-      }
+      exp2_pack64(r, h * 64, scale_log2, neg_m, packed, acc);
       tmem_st32(p_addr + h * 32, packed);
     }
-    l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&bar.p_full[pb]);
+    mbar_arrive_warp(&bar.p_full[pb]);
   }
   if (!ok) return;
   if (!warp_wait(&bar.o_final, 0)) return;

@@ -77,7 +77,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = tmem_base_s;
+  const uint32_t tmem_base = __shfl_sync(0xffffffffu, tmem_base_s, 0);   // warp-uniform
 
   if (warp == 0) {
     // ------------------------------------------------------------- TMA producer

@@ -81,6 +81,8 @@ def _to_dev(inp):
     (1, 64, 64, 2, 2, 64),        # B = L: masked stream sees no clean key
     (1, 50, 1, 2, 1, 64),         # B = 1
     (1, 33, 40, 2, 1, 128),       # B > L: one block
+    (1, 300, 128, 2, 1, 128),     # B = tile: masked rows use one clean tile fewer
+    (1, 300, 200, 2, 2, 64),      # B > tile, straddling tiles: key tiles only clean rows use
 ])
 def test_dual_stream_small(b, L, B, hq, hkv, d):
     cfg = W.DualStreamConfig("t", b, L, B, hq, hkv, d)
