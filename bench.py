@@ -17,6 +17,7 @@ its GPU; no data crosses ranks except the final max-time / token-sum reduction.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -329,8 +330,17 @@ def run_gpu(args, rank, world, local):
     # ---- end to end through the public API with host buffers (pinned), rank-local
     e2e = run_e2e(runner, inp, cfg, K, Wm, device, dist)
 
+    # ---- the same step as one CUDA graph (launch overhead removed), rank-local
+    graph = run_graph_step(runner, K, Wm)
+
     # ---- dual-stream training-form attention, same run
     dual = run_dual(device, peaks, reps=max(3, min(K, 10)), warm=max(3, Wm))
+
+    # ---- comparison steps on the same sequences: KV-cached AR (B = 1), and the MARS step
+    # at tau = 0 (every block position accepted: the step's ceiling of B tokens)
+    ar = run_step_variant(W.AR_DECODE_7B, device, K, Wm, seed=rank)
+    tau0 = run_step_variant(dataclasses.replace(cfg, name=cfg.name + "_tau0", taus=(0.0,)),
+                            device, K, Wm, seed=rank)
 
     out = None
     if rank == 0:
@@ -364,7 +374,15 @@ def run_gpu(args, rank, world, local):
             "head_accept": {"us_per_call": statistics.mean(t_head) * 1e6,
                             "tflops": head_tflops, "frac_tensor": frac_head},
             "kv_commit": {"us_per_call": statistics.mean(t_commit) * 1e6},
+            "decode_step_graph": graph,
             "dual_stream": dual,
+            "ar_baseline": {**ar, "mars_over_ar": (tokens / seconds) / ar["tok_s"] / world,
+                            "note": "KV-cached AR step (B=1, tau=1.0) over the same "
+                                    "sequences with the same kernels; the MARS/AR ratio "
+                                    "is the synthetic analogue of the pages' wall-clock "
+                                    "table, with random weights (mean N ~ 1)"},
+            "mars_tau0": {**tau0, "mars_over_ar": tau0["tok_s"] / ar["tok_s"],
+                          "note": "coverage run: tau = 0 accepts all B positions"},
             "roofline": {"kernel": "mars_head_accept (LM head GEMM + fused epilogue)",
                          "bound": "tensor", "achieved": head_tflops,
                          "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
@@ -427,6 +445,68 @@ def run_e2e(runner, inp, cfg, K, Wm, device, dist):
     tok, sec = reduce_job(dist, tok, sec, device)
     return {"value": tok / sec, "unit": "accepted tok/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
+
+
+def run_step_variant(cfg, device, K, Wm, seed):
+    """K decode steps of another workload through the same three calls (CUDA events
+    around the whole loop); returns accepted tok/s and the step time."""
+    inp = W.make_decode_inputs(cfg, seed=seed, device=device)
+    runner = DecodeRunner(inp, cfg, device)
+    for i in range(Wm):
+        runner.step(i)
+    torch.cuda.synchronize()
+    runner.reset()
+    a, b = _ev(), _ev()
+    a.record()
+    for i in range(K):
+        runner.step(i)
+    b.record()
+    torch.cuda.synchronize()
+    sec = a.elapsed_time(b) / 1e3
+    tok = float(runner.n_acc[: min(K, cfg.steps)].sum().item())
+    out = {"workload": cfg.name, "tok_s": tok / sec, "ms_per_step": sec / K * 1e3,
+           "mean_accepted_per_seq_step": tok / (K * cfg.batch),
+           "device_status": int(runner.status.item())}
+    del runner, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_graph_step(runner, K, Wm):
+    """One decode step (the three calls) captured as a CUDA graph and replayed K times;
+    each replay repeats step 0's inputs while the sequences keep growing."""
+    from block_masked_token_gb300 import mars
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            runner.step(0)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        n0 = mars.mars_launch_count()
+        with torch.cuda.graph(g):
+            runner.step(0)
+        kernels = mars.mars_launch_count() - n0
+        runner.reset()
+        for _ in range(Wm):
+            g.replay()
+        torch.cuda.synchronize()
+        runner.reset()
+        a, b = _ev(), _ev()
+        a.record()
+        for _ in range(K):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / 1e3 / K * 1e6
+        runner.reset()
+        return {"us_per_step": us, "kernels_per_step": kernels,
+                "device_status": int(runner.status.item())}
+    except RuntimeError as e:                       # capture refused: report, do not fail
+        torch.cuda.synchronize()
+        runner.reset()
+        return {"error": str(e).splitlines()[0][:200]}
 
 
 def run_dual(device, peaks, reps=10, warm=3):

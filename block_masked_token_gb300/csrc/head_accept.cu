@@ -7,7 +7,9 @@
 // of logits into one partial {tile max, sum exp(l - tile max), first argmax} per row; the
 // logits never leave the chip. Kernel 2 merges the partials of each row, writes the token
 // and max-prob = 1 / sum_v exp(l_v - max), and scans each sequence's B positions left to
-// right: N = leading run of max-prob >= tau, at least 1, at most B.
+// right: N = leading run of max-prob >= tau, at least 1, at most B. tau is one value per
+// call, or one per sequence (per request: gist.science explainer, 2.C "Adaptive
+// Throughput"; papernotes.org notes, highlights, third point).
 #include "common.cuh"
 #include "head_gemm_tc.cuh"
 #include "internal.h"
@@ -21,7 +23,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // One CTA per sequence, one warp per block position: merge partials, then the scan.
 __global__ void __launch_bounds__(1024) head_finalize_kernel(
     const float4* __restrict__ part, int rows, int B, int nvt, float tau,
-    int32_t* __restrict__ tokens, float* __restrict__ maxprob, int32_t* __restrict__ n_accept) {
+    const float* __restrict__ taus, int32_t* __restrict__ tokens, float* __restrict__ maxprob,
+    int32_t* __restrict__ n_accept) {
   __shared__ float p_s[32];
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -55,8 +58,9 @@ __global__ void __launch_bounds__(1024) head_finalize_kernel(
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    const float t = taus ? taus[s] : tau;      // a NaN threshold accepts only the floor
     int n = 0;
-    while (n < B && p_s[n] >= tau) ++n;
+    while (n < B && p_s[n] >= t) ++n;
     n_accept[s] = n < 1 ? 1 : n;
   }
 }
@@ -82,9 +86,9 @@ size_t head_workspace_bytes(int batch, int B, int vocab) {
 }
 
 cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, int B,
-                               int hidden, int vocab, float tau, int32_t* tokens,
-                               float* maxprob, int32_t* n_accept, void* workspace,
-                               int32_t* status, cudaStream_t stream) {
+                               int hidden, int vocab, float tau, const float* taus,
+                               int32_t* tokens, float* maxprob, int32_t* n_accept,
+                               void* workspace, int32_t* status, cudaStream_t stream) {
   using namespace head_tc;
   const int rows = batch * B;
   CUtensorMap tm_h, tm_w;
@@ -118,8 +122,8 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   }
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
   head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
-  head_finalize_kernel<<<batch, 32 * B, 0, stream>>>(p.part, rows, B, p.num_n, tau, tokens,
-                                                     maxprob, n_accept);
+  head_finalize_kernel<<<batch, 32 * B, 0, stream>>>(p.part, rows, B, p.num_n, tau, taus,
+                                                     tokens, maxprob, n_accept);
   count_launches(2);
   return cudaGetLastError();
 }

@@ -69,7 +69,7 @@ extern "C" int mars_head_accept_noalloc(const mars_bf16* h, const mars_bf16* w, 
   // Every partial the finalize step reads is written by the GEMM epilogue of the same
   // call, so nothing in the scratch has to start at zero.
   const cudaError_t e =
-      mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, tokens, maxprob, n_accept,
+      mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, nullptr, tokens, maxprob, n_accept,
                                scratch, status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MARS_OK : MARS_ECUDA;
 }

@@ -16,8 +16,8 @@ cudaError_t launch_kv_commit(const uint16_t* k_blk, const uint16_t* v_blk,
                              const int32_t* n_accept, int32_t* seq_lens,
                              const int32_t* block_table, int max_pages, uint16_t* k_pool,
                              uint16_t* v_pool, int num_pages, int32_t* commit_slots,
-                             int batch, int B, int hkv, int d, int32_t* status,
-                             cudaStream_t stream);
+                             int batch, int B, int hkv, int d, bool batch_sync,
+                             int32_t* status, cudaStream_t stream);
 
 // ---- Decode attention: split-KV partials then a combine pass.
 struct DecodePlan {
@@ -38,10 +38,11 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
 
 // ---- LM head + max-prob/argmax + acceptance.
 size_t head_workspace_bytes(int batch, int B, int vocab);
+// taus: one threshold per sequence (device, [batch]), or NULL to use tau for all.
 cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, int B,
-                               int hidden, int vocab, float tau, int32_t* tokens,
-                               float* maxprob, int32_t* n_accept, void* workspace,
-                               int32_t* status, cudaStream_t stream);
+                               int hidden, int vocab, float tau, const float* taus,
+                               int32_t* tokens, float* maxprob, int32_t* n_accept,
+                               void* workspace, int32_t* status, cudaStream_t stream);
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();

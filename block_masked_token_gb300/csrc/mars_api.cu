@@ -90,27 +90,28 @@ int mars_decode_attn(const mars_bf16* q, const mars_bf16* k_blk, const mars_bf16
                                           static_cast<cudaStream_t>(stream)));
 }
 
-int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
-                     int vocab, float tau, int32_t* tokens, float* maxprob,
-                     int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
-                     void* stream) {
+namespace {
+
+int head_accept_checked(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
+                        int vocab, float tau, const float* taus, int32_t* tokens,
+                        float* maxprob, int32_t* n_accept, void* workspace, size_t ws_bytes,
+                        int32_t* status, void* stream) {
   if (batch < 0 || B < 1 || B > 32 || hidden < 8 || vocab < 1) return MARS_EINVAL;
-  if (isnan(tau) || isinf(tau)) return MARS_EINVAL;
   if (hidden % 8) return MARS_EUNSUPPORTED;
   if (batch == 0) return MARS_OK;
   if (!h || !w || !tokens || !maxprob || !n_accept || !workspace) return MARS_EINVAL;
   if (!aligned16(h) || !aligned16(w) || !aligned16(workspace)) return MARS_EALIGN;
   if (ws_bytes < mars::head_workspace_bytes(batch, B, vocab)) return MARS_ENOSPACE;
-  return cuda_rc(mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, tokens,
+  return cuda_rc(mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, taus, tokens,
                                           maxprob, n_accept, workspace, status,
                                           static_cast<cudaStream_t>(stream)));
 }
 
-int mars_kv_commit(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t* n_accept,
-                   int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq,
-                   mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
-                   int32_t* commit_slots, int batch, int B, int hkv, int d, int page_size,
-                   int32_t* status, void* stream) {
+int kv_commit_checked(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t* n_accept,
+                      int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq,
+                      mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
+                      int32_t* commit_slots, int batch, int B, int hkv, int d, int page_size,
+                      bool batch_sync, int32_t* status, void* stream) {
   if (batch < 0 || B < 1 || B > 32 || hkv < 1 || num_pages < 0 || max_pages_per_seq < 0)
     return MARS_EINVAL;
   if (d != 64 && d != 128) return MARS_EUNSUPPORTED;
@@ -122,8 +123,49 @@ int mars_kv_commit(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t
     return MARS_EALIGN;
   return cuda_rc(mars::launch_kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table,
                                         max_pages_per_seq, k_pool, v_pool, num_pages,
-                                        commit_slots, batch, B, hkv, d, status,
+                                        commit_slots, batch, B, hkv, d, batch_sync, status,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
+                     int vocab, float tau, int32_t* tokens, float* maxprob,
+                     int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
+                     void* stream) {
+  if (isnan(tau) || isinf(tau)) return MARS_EINVAL;
+  return head_accept_checked(h, w, batch, B, hidden, vocab, tau, nullptr, tokens, maxprob,
+                             n_accept, workspace, ws_bytes, status, stream);
+}
+
+int mars_head_accept_per_request(const mars_bf16* h, const mars_bf16* w, int batch, int B,
+                                 int hidden, int vocab, const float* taus, int32_t* tokens,
+                                 float* maxprob, int32_t* n_accept, void* workspace,
+                                 size_t ws_bytes, int32_t* status, void* stream) {
+  if (batch > 0 && !taus) return MARS_EINVAL;
+  return head_accept_checked(h, w, batch, B, hidden, vocab, 0.f, taus, tokens, maxprob,
+                             n_accept, workspace, ws_bytes, status, stream);
+}
+
+int mars_kv_commit(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t* n_accept,
+                   int32_t* seq_lens, const int32_t* block_table, int max_pages_per_seq,
+                   mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
+                   int32_t* commit_slots, int batch, int B, int hkv, int d, int page_size,
+                   int32_t* status, void* stream) {
+  return kv_commit_checked(k_blk, v_blk, n_accept, seq_lens, block_table, max_pages_per_seq,
+                           k_pool, v_pool, num_pages, commit_slots, batch, B, hkv, d,
+                           page_size, false, status, stream);
+}
+
+int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
+                              const int32_t* n_accept, int32_t* seq_lens,
+                              const int32_t* block_table, int max_pages_per_seq,
+                              mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
+                              int32_t* commit_slots, int batch, int B, int hkv, int d,
+                              int page_size, int32_t* status, void* stream) {
+  return kv_commit_checked(k_blk, v_blk, n_accept, seq_lens, block_table, max_pages_per_seq,
+                           k_pool, v_pool, num_pages, commit_slots, batch, B, hkv, d,
+                           page_size, true, status, stream);
 }
 
 const char* mars_strerror(int code) {

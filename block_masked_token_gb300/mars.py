@@ -45,8 +45,12 @@ def lib() -> ctypes.CDLL:
                                        P, S, P, P]
         L.mars_head_accept.restype = I
         L.mars_head_accept.argtypes = [P, P, I, I, I, I, F, P, P, P, P, S, P, P]
+        L.mars_head_accept_per_request.restype = I
+        L.mars_head_accept_per_request.argtypes = [P, P, I, I, I, I, P, P, P, P, P, S, P, P]
         L.mars_kv_commit.restype = I
         L.mars_kv_commit.argtypes = [P, P, P, P, P, I, P, P, I, P, I, I, I, I, I, P, P]
+        L.mars_kv_commit_batch_sync.restype = I
+        L.mars_kv_commit_batch_sync.argtypes = L.mars_kv_commit.argtypes
         L.mars_strerror.restype = ctypes.c_char_p
         L.mars_strerror.argtypes = [I]
         L.mars_version.restype = ctypes.c_char_p
@@ -58,8 +62,8 @@ def lib() -> ctypes.CDLL:
 
 
 EXPORTED = ("mars_workspace_bytes", "mars_attn_dual_stream", "mars_decode_attn",
-            "mars_head_accept", "mars_kv_commit", "mars_strerror", "mars_version",
-            "mars_launch_count")
+            "mars_head_accept", "mars_head_accept_per_request", "mars_kv_commit",
+            "mars_kv_commit_batch_sync", "mars_strerror", "mars_version", "mars_launch_count")
 
 
 def mars_strerror(code: int) -> str:
@@ -146,8 +150,7 @@ def mars_decode_attn(q, k_blk, v_blk, k_pool, v_pool, block_table, seq_lens,
                                _ptr(status), _stream(stream)), "mars_decode_attn")
 
 
-def mars_head_accept(h, w, batch: int, B: int, tau: float, tokens, maxprob, n_accept,
-                     workspace, status=None, stream=None):
+def _head_args(h, w, batch, B, tokens, maxprob, n_accept, workspace, status):
     rows, hidden = h.shape
     vocab = w.shape[0]
     _check(h, "h", torch.bfloat16, (batch * B, hidden))
@@ -158,14 +161,31 @@ def mars_head_accept(h, w, batch: int, B: int, tau: float, tokens, maxprob, n_ac
     _check(workspace, "workspace", torch.uint8)
     if status is not None:
         _check(status, "status", torch.int32, (1,))
+    return hidden, vocab
+
+
+def mars_head_accept(h, w, batch: int, B: int, tau: float, tokens, maxprob, n_accept,
+                     workspace, status=None, stream=None):
+    hidden, vocab = _head_args(h, w, batch, B, tokens, maxprob, n_accept, workspace, status)
     _rc(lib().mars_head_accept(_ptr(h), _ptr(w), batch, B, hidden, vocab, float(tau),
                                _ptr(tokens), _ptr(maxprob), _ptr(n_accept), _ptr(workspace),
                                workspace.numel(), _ptr(status), _stream(stream)),
         "mars_head_accept")
 
 
-def mars_kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
-                   commit_slots=None, status=None, stream=None):
+def mars_head_accept_per_request(h, w, batch: int, B: int, taus, tokens, maxprob, n_accept,
+                                 workspace, status=None, stream=None):
+    hidden, vocab = _head_args(h, w, batch, B, tokens, maxprob, n_accept, workspace, status)
+    _check(taus, "taus", torch.float32, (batch,))
+    _rc(lib().mars_head_accept_per_request(_ptr(h), _ptr(w), batch, B, hidden, vocab,
+                                           _ptr(taus), _ptr(tokens), _ptr(maxprob),
+                                           _ptr(n_accept), _ptr(workspace), workspace.numel(),
+                                           _ptr(status), _stream(stream)),
+        "mars_head_accept_per_request")
+
+
+def _kv_commit(fn, name, k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
+               commit_slots, status, stream):
     b, B, hkv, d = k_blk.shape
     num_pages = k_pool.shape[0]
     _check(k_blk, "k_blk", torch.bfloat16)
@@ -179,7 +199,18 @@ def mars_kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool
         _check(commit_slots, "commit_slots", torch.int32, (b, B))
     if status is not None:
         _check(status, "status", torch.int32, (1,))
-    _rc(lib().mars_kv_commit(_ptr(k_blk), _ptr(v_blk), _ptr(n_accept), _ptr(seq_lens),
-                             _ptr(block_table), block_table.shape[1], _ptr(k_pool),
-                             _ptr(v_pool), num_pages, _ptr(commit_slots), b, B, hkv, d,
-                             PAGE_SIZE, _ptr(status), _stream(stream)), "mars_kv_commit")
+    _rc(fn(_ptr(k_blk), _ptr(v_blk), _ptr(n_accept), _ptr(seq_lens), _ptr(block_table),
+           block_table.shape[1], _ptr(k_pool), _ptr(v_pool), num_pages, _ptr(commit_slots), b,
+           B, hkv, d, PAGE_SIZE, _ptr(status), _stream(stream)), name)
+
+
+def mars_kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
+                   commit_slots=None, status=None, stream=None):
+    _kv_commit(lib().mars_kv_commit, "mars_kv_commit", k_blk, v_blk, n_accept, seq_lens,
+               block_table, k_pool, v_pool, commit_slots, status, stream)
+
+
+def mars_kv_commit_batch_sync(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
+                              commit_slots=None, status=None, stream=None):
+    _kv_commit(lib().mars_kv_commit_batch_sync, "mars_kv_commit_batch_sync", k_blk, v_blk,
+               n_accept, seq_lens, block_table, k_pool, v_pool, commit_slots, status, stream)

@@ -72,8 +72,15 @@ SUSTAINED_DECODE_7B = DecodeConfig("sustained_decode_7b_b128_B16_64steps", batch
                                    d=128, hidden=3584, vocab=152064,
                                    taus=(1.0, 0.95, 0.9, 0.8), steps=64, tau_period=16)
 
+# The KV-cached autoregressive step on the same sequences (one query per sequence, one
+# token per step): the same kernels with B = 1 and tau = 1.0. The prefix lengths are the
+# first draw of the generator, so with the same seed they equal the sustained workload's.
+AR_DECODE_7B = DecodeConfig("ar_decode_7b_b128_B1_64steps", batch=128, prefix_lo=2048,
+                            prefix_hi=8192, B=1, hq=28, hkv=4, d=128, hidden=3584,
+                            vocab=152064, taus=(1.0,), steps=64, tau_period=16)
+
 CONFIGS = {c.name: c for c in (TINY_DECODE, DUAL_STREAM_0P5B, DECODE_7B, DUAL_STREAM_7B,
-                               SUSTAINED_DECODE_7B)}
+                               SUSTAINED_DECODE_7B, AR_DECODE_7B)}
 
 
 def _gen(seed: int, device) -> torch.Generator:

@@ -115,6 +115,18 @@ int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, i
                      int32_t* n_accept, void* workspace, size_t ws_bytes, int32_t* status,
                      void* stream);
 
+/* mars_head_accept with one threshold per request ([gist] 2.C "Adaptive Throughput": the
+ * speed is adjusted per request in real time; [notes] highlights, third point: each
+ * request's confidence threshold is tuned online). Sequence s accepts its leading run of
+ * positions with p >= taus[s] (at least 1, at most B); everything else is mars_head_accept.
+ *   taus      [batch] float, device memory, read when the kernels run; a NaN entry
+ *             compares false, so that sequence accepts exactly one token
+ * Returns MARS_EINVAL when taus is NULL (batch > 0). */
+int mars_head_accept_per_request(const mars_bf16* h, const mars_bf16* w, int batch, int B,
+                                 int hidden, int vocab, const float* taus, int32_t* tokens,
+                                 float* maxprob, int32_t* n_accept, void* workspace,
+                                 size_t ws_bytes, int32_t* status, void* stream);
+
 /* Scratch reserved by mars_head_accept_noalloc on every GPU that loads the library. */
 #define MARS_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -156,6 +168,19 @@ int mars_kv_commit(const mars_bf16* k_blk, const mars_bf16* v_blk, const int32_t
                    mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
                    int32_t* commit_slots, int batch, int B, int hkv, int d, int page_size,
                    int32_t* status, void* stream);
+
+/* Batch-synchronised commit ([notes] Key design 4, second paragraph: the batch state
+ * advances by the smallest number of tokens any sample accepted in the step, faster
+ * samples waiting for the others; [gist] 2.D: the cache moves only with what the whole
+ * batch accepted). Exactly mars_kv_commit with every N_s replaced by
+ * N_min = min over the batch of clamp(n_accept[s], 0, B); seq_lens advance by N_min (less
+ * for a sequence stopped by an unmapped page). Same arguments, layouts and errors. */
+int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
+                              const int32_t* n_accept, int32_t* seq_lens,
+                              const int32_t* block_table, int max_pages_per_seq,
+                              mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
+                              int32_t* commit_slots, int batch, int B, int hkv, int d,
+                              int page_size, int32_t* status, void* stream);
 
 /* Human-readable name of a return code. Never NULL. */
 const char* mars_strerror(int code);

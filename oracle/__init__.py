@@ -11,8 +11,10 @@ from .mars_oracle import (  # noqa: F401
     decode_attn,
     gather_prefix,
     head_accept,
+    head_accept_per_request,
     head_logits,
     kv_commit,
+    kv_commit_batch_sync,
     mask_M,
     mask_rows,
     maxprob_argmax,

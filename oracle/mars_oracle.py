@@ -18,7 +18,7 @@ arXiv 2604.07023). Citations name the web page and its section:
   [gist]   the gist.science English explainer, "2. Methodology", part C (Inference
            Mechanism) and part D (Block-Level KV Caching).
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   * indices: M is stated 1-indexed; mask_M keeps that form, arrays are 0-indexed;
   * softmax scale: not stated, 1/sqrt(D);
   * grouped-query attention: not on the pages, query head h uses KV head h // (Hq/Hkv);
@@ -28,7 +28,10 @@ Readings taken where the pages are silent (each also listed in the design doc):
     lowest vocabulary index;
   * acceptance starts at block position 0, ">=" is inclusive, at least one token, at most B;
     tau is a float32 value compared exactly in fp64;
-  * commit: each sequence's own N rows are written every step (per-sequence commit).
+  * commit: each sequence's own N rows are written every step (per-sequence commit);
+    kv_commit_batch_sync gives the batch-synchronised alternative, every sequence
+    committing the smallest N of the batch;
+  * per-request threshold: one float32 tau per sequence (head_accept_per_request).
 
 Every function takes float64 numpy arrays (callers pass bf16-rounded values converted to
 float64) and returns float64 / int64 numpy arrays. Nothing is blocked, fused or reordered
@@ -263,6 +266,19 @@ def head_accept(h, w_vocab_major, batch: int, B: int, tau):
     return tokens, maxprob, n, gap
 
 
+def head_accept_per_request(h, w_vocab_major, batch: int, B: int, taus):
+    """head_accept with a threshold per request: sequence s uses taus[s] ([gist] 2.C
+    "Adaptive Throughput": the speed is adjusted per request in real time; [notes]
+    highlights, third point: the confidence threshold of each request is tuned online).
+    Each taus[s] is taken as a float32 value, as in accept_count."""
+    tokens, maxprob, gap = maxprob_argmax(head_logits(h, w_vocab_major))
+    tokens = tokens.reshape(batch, B)
+    maxprob = maxprob.reshape(batch, B)
+    gap = gap.reshape(batch, B)
+    n = np.array([accept_count(maxprob[s], taus[s]) for s in range(batch)], dtype=np.int64)
+    return tokens, maxprob, n, gap
+
+
 # ---------------------------------------------------------------------------------------
 # Commit into the block-level KV cache ([notes] Key design 4; [gist] 2.D), per sequence.
 # ---------------------------------------------------------------------------------------
@@ -289,3 +305,17 @@ def kv_commit(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
             slots[s, i] = page * page_size + slot
         new_lens[s] = int(seq_lens[s]) + int(n_accept[s])
     return k_pool, v_pool, new_lens, slots
+
+
+def kv_commit_batch_sync(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool,
+                         page_size: int):
+    """Batch-synchronised commit ([notes] Key design 4, second paragraph: the batch
+    advances by the smallest number of tokens any of its samples accepted in the step,
+    the faster samples waiting; [gist] 2.D: the cache moves only with what every sample
+    of the batch accepted). Every sequence commits N_min = min_s N_s rows, N_s clamped to
+    [0, B] first; otherwise exactly kv_commit."""
+    B = k_blk.shape[1]
+    n = [min(max(int(x), 0), B) for x in n_accept]
+    n_min = min(n) if n else 0
+    return kv_commit(k_blk, v_blk, [n_min] * len(n), seq_lens, block_table, k_pool, v_pool,
+                     page_size)

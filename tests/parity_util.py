@@ -37,14 +37,16 @@ def scanned_ambiguous(p_ref_row, tau):
 
 
 def compare_head(tok, p, n, tok_ref, p_ref, n_ref, gap_ref, tau):
-    """tok/p: [b, B]; n: [b]. Returns counts of excluded tokens and sequences."""
+    """tok/p: [b, B]; n: [b]; tau: one threshold, or one per sequence. Returns counts of
+    excluded tokens and sequences."""
     tok, p, n = np.asarray(tok), np.asarray(p, np.float64), np.asarray(n)
+    taus = np.broadcast_to(np.asarray(tau, dtype=np.float64), (len(n),))
     err = np.abs(p - p_ref).max()
     assert err <= MAXPROB_TOL, f"maxprob max-abs error {err:.3e} > {MAXPROB_TOL}"
     tie = gap_ref < GAP_EXCLUDE
     bad = (tok != tok_ref) & ~tie
     assert not bad.any(), f"argmax mismatch at {np.argwhere(bad)[:8].tolist()}"
-    amb = np.array([scanned_ambiguous(p_ref[s], tau) for s in range(len(n))], dtype=bool)
+    amb = np.array([scanned_ambiguous(p_ref[s], taus[s]) for s in range(len(n))], dtype=bool)
     badn = (n != n_ref) & ~amb
     assert not badn.any(), f"N mismatch at {np.flatnonzero(badn)[:8].tolist()}: " \
                            f"{n[badn][:8].tolist()} vs {n_ref[badn][:8].tolist()}"

@@ -81,9 +81,18 @@ def test_host_validation_codes(L):
     bad_b = list(args)
     bad_b[12] = 33
     assert L.mars_decode_attn(*bad_b, 16, 0.0, P, 1 << 30, None, None) == mars.EINVAL
-    # commit: page size, null pool
-    assert L.mars_kv_commit(P, P, P, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 8, None, None) == mars.EUNSUPPORTED
-    assert L.mars_kv_commit(P, P, P, P, P, 4, None, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EINVAL
+    # head, per-request thresholds: null threshold array, then the checks of mars_head_accept
+    assert L.mars_head_accept_per_request(P, P, 1, 4, 256, 512, None, P, P, P, P, 1 << 20, None, None) == mars.EINVAL
+    assert L.mars_head_accept_per_request(P, P, 0, 4, 256, 512, None, P, P, P, P, 1 << 20, None, None) == mars.OK
+    assert L.mars_head_accept_per_request(P, P, 1, 4, 252, 512, P, P, P, P, P, 1 << 20, None, None) == mars.EUNSUPPORTED
+    assert L.mars_head_accept_per_request(P, P, 1, 4, 256, 512, P, P, P, P, P, 16, None, None) == mars.ENOSPACE
+    assert L.mars_head_accept_per_request(P, _p(20), 1, 4, 256, 512, P, P, P, P, P, 1 << 20, None, None) == mars.EALIGN
+    # commit (both policies): page size, null pool, B out of range
+    for fn in (L.mars_kv_commit, L.mars_kv_commit_batch_sync):
+        assert fn(P, P, P, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 8, None, None) == mars.EUNSUPPORTED
+        assert fn(P, P, P, P, P, 4, None, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EINVAL
+        assert fn(P, P, P, P, P, 4, P, P, 10, None, 2, 33, 2, 64, 16, None, None) == mars.EINVAL
+        assert fn(P, P, P, P, P, 4, P, P, 10, None, 0, 4, 2, 64, 16, None, None) == mars.OK
 
 
 def test_binding_rejects_cpu_tensors(L):

@@ -284,6 +284,36 @@ def test_tau_one_gives_one_token_at_7b_vocab():
     assert (n == 1).all() and (p < 1).all()
 
 
+def test_per_request_thresholds_golden_batch():
+    """One batch whose sequences carry different thresholds reproduces the hand-derived N
+    of every row. The max-probs are produced through the head itself: vocabulary 2, hidden
+    1, W = [[0], [1]] and h = logit(p), so that softmax gives exactly p for token 1."""
+    rows = [[x.strip() for x in ln.split("|")] for ln in golden_lines("per_request_tau_cases.txt")]
+    taus = np.array([float(r[0]) for r in rows])
+    probs = np.array([[float(x) for x in r[1].split()] for r in rows])
+    want = np.array([int(r[2]) for r in rows])
+    batch, B = probs.shape
+    h = np.log(probs / (1.0 - probs)).reshape(batch * B, 1)
+    w = np.array([[0.0], [1.0]])
+    tok, p, n, _ = oracle.head_accept_per_request(h, w, batch, B, taus)
+    np.testing.assert_allclose(p, probs, rtol=0, atol=1e-12)
+    assert (tok == 1).all()
+    np.testing.assert_array_equal(n, want)
+    # a single threshold for the whole batch would not give these counts
+    assert any((oracle.head_accept(h, w, batch, B, t)[2] != want).any() for t in taus)
+
+
+def test_per_request_equal_thresholds_reduce_to_per_call():
+    cfg = W.TINY_DECODE
+    inp = W.make_decode_inputs(cfg, seed=0)
+    h, w = W.to_f64(inp.h[0]), W.to_f64(inp.w)
+    for tau in (0.0, 0.3, 0.9, 1.0):
+        a = oracle.head_accept(h, w, cfg.batch, cfg.B, tau)
+        b = oracle.head_accept_per_request(h, w, cfg.batch, cfg.B, [tau] * cfg.batch)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
 # ------------------------------------------------------------------------- commit
 
 def test_commit_golden_case():
@@ -329,6 +359,49 @@ def test_commit_properties():
         np.testing.assert_array_equal(got[:lens[s]], old)        # prefix unchanged
         np.testing.assert_array_equal(got[lens[s]:], kb[s, :n[s]])
         assert (slots[s, n[s]:] == -1).all()
+
+
+def test_commit_batch_sync_golden_case():
+    kv = dict(ln.split(None, 1) for ln in golden_lines("commit_sync_case.txt"))
+    ps, B = int(kv["page_size"]), int(kv["B"])
+    bt = np.array([[int(x) for x in kv["block_table_0"].split()],
+                   [int(x) for x in kv["block_table_1"].split()]])
+    sl = np.array([int(x) for x in kv["seq_len"].split()])
+    n = np.array([int(x) for x in kv["N"].split()])
+    Hkv, D = 2, 3
+    kb = _rand((2, B, Hkv, D), 60)
+    vb = _rand((2, B, Hkv, D), 61)
+    kp = _rand((8, Hkv, ps, D), 62)
+    vp = _rand((8, Hkv, ps, D), 63)
+    kp2, vp2, sl2, slots = oracle.kv_commit_batch_sync(kb, vb, n, sl, bt, kp, vp, ps)
+    np.testing.assert_array_equal(slots[0], [int(x) for x in kv["slots_0"].split()])
+    np.testing.assert_array_equal(slots[1], [int(x) for x in kv["slots_1"].split()])
+    np.testing.assert_array_equal(sl2, [int(x) for x in kv["new_seq_len"].split()])
+    for s in range(2):
+        for i, sl_ in enumerate(slots[s]):
+            if sl_ >= 0:
+                np.testing.assert_array_equal(kp2[sl_ // ps, :, sl_ % ps], kb[s, i])
+                np.testing.assert_array_equal(vp2[sl_ // ps, :, sl_ % ps], vb[s, i])
+
+
+def test_commit_batch_sync_properties():
+    """Every sequence advances by the same amount, the batch minimum; with equal counts it
+    is the per-sequence commit."""
+    ps, Hkv, D, B = 4, 2, 5, 6
+    lens = np.array([0, 3, 7, 12])
+    bt = np.array([[0, 1, -1, -1, -1], [2, 3, -1, -1, -1], [4, 5, 6, -1, -1],
+                   [7, 8, 9, 10, 11]])
+    kb, vb = _rand((4, B, Hkv, D), 70), _rand((4, B, Hkv, D), 71)
+    kp, vp = _rand((13, Hkv, ps, D), 72), _rand((13, Hkv, ps, D), 73)
+    n = np.array([6, 2, 4, 3])
+    _, _, sl2, slots = oracle.kv_commit_batch_sync(kb, vb, n, lens, bt, kp, vp, ps)
+    np.testing.assert_array_equal(sl2, lens + 2)
+    assert ((slots >= 0).sum(axis=1) == 2).all()
+    eq = np.array([3, 3, 3, 3])
+    a = oracle.kv_commit_batch_sync(kb, vb, eq, lens, bt, kp, vp, ps)
+    b = oracle.kv_commit(kb, vb, eq, lens, bt, kp, vp, ps)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
 
 
 # ------------------------------------------- planted mistakes: each must fail some pin

@@ -148,6 +148,9 @@ def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
                    hkv=1, d=128, hidden=64, vocab=64),
     W.DecodeConfig("d4", batch=5, prefix_lo=500, prefix_hi=3000, B=3, hq=8, hkv=2, d=64,
                    hidden=64, vocab=64),
+    # the KV-cached AR step at 7B attention shapes: one query per sequence
+    W.DecodeConfig("d5", batch=4, prefix_lo=2048, prefix_hi=8192, B=1, hq=28, hkv=4, d=128,
+                   hidden=64, vocab=64),
 ])
 def test_decode_small(cfg):
     inp = _decode_case(cfg, seed=1)
@@ -334,6 +337,79 @@ def test_commit_unmapped_page_is_skipped_and_flagged():
     s = slots.cpu().numpy()
     assert s[0, 0] >= 0 and s[0, 1] >= 0 and (s[0, 2:] == -1).all()
     assert sl.cpu().tolist() == [16, 7]
+
+
+# ----------------------------------------------------- per-request thresholds (speed knob)
+
+def run_head_per_request(h, w, batch, B, taus):
+    tokens = torch.empty(batch, B, dtype=torch.int32, device=DEV)
+    maxprob = torch.empty(batch, B, dtype=torch.float32, device=DEV)
+    n = torch.empty(batch, dtype=torch.int32, device=DEV)
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, batch, B, vocab=w.shape[0]))
+    t = torch.tensor(taus, dtype=torch.float32, device=DEV)
+    mars.mars_head_accept_per_request(h, w, batch, B, t, tokens, maxprob, n, ws)
+    torch.cuda.synchronize()
+    return tokens.cpu().numpy(), maxprob.cpu().numpy(), n.cpu().numpy()
+
+
+def test_head_per_request_small():
+    """Eight sequences with eight different thresholds in one call, including 0 (the whole
+    block), 1.0 (one token) and a NaN entry (compares false: one token)."""
+    batch, B = 8, 6
+    cfg = W.DecodeConfig("hr", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
+                         hidden=256, vocab=1000, taus=(0.5,))
+    inp = W.make_decode_inputs(cfg, seed=11)
+    taus = [0.0, 0.05, 0.1, 0.2, 0.3, 0.5, 1.0, float("nan")]
+    tok, p, n = run_head_per_request(inp.h[0].to(DEV), inp.w.to(DEV), batch, B, taus)
+    ref_taus = [t if t == t else 2.0 for t in taus]     # NaN behaves as a threshold > 1
+    rt, rp, rn, gap = oracle.head_accept_per_request(f64(inp.h[0]), f64(inp.w), batch, B,
+                                                     ref_taus)
+    compare_head(tok, p, n, rt, rp, rn, gap, ref_taus)
+    assert n[0] == B and n[6] == 1 and n[7] == 1
+    # the same call with each threshold alone reproduces its sequence
+    for s in (1, 4):
+        _, _, n1 = run_head(inp.h[0].to(DEV), inp.w.to(DEV), batch, B, taus[s])
+        assert n1[s] == n[s]
+
+
+def test_head_per_request_7b_sampled_rows():
+    cfg = W.DECODE_7B
+    inp = W.make_decode_inputs(W.DecodeConfig(**{**cfg.__dict__, "batch": 32}), seed=2,
+                               device=DEV, steps=1)
+    h, w = inp.h[0], inp.w
+    taus = [(0.0, 0.3, 0.5, 0.9)[s % 4] for s in range(cfg.batch)]
+    tok, p, n = run_head_per_request(h, w, cfg.batch, cfg.B, taus)
+    seqs = [0, 1, 2, 3, 17, 30]
+    rows = [s * cfg.B + k for s in seqs for k in range(cfg.B)]
+    rt, rp, rn, gap = oracle.head_accept_per_request(f64(h[rows]), f64(w), len(seqs), cfg.B,
+                                                     [taus[s] for s in seqs])
+    compare_head(tok[seqs], p[seqs], n[seqs], rt, rp, rn, gap, [taus[s] for s in seqs])
+    assert n[0] == cfg.B
+
+
+# ------------------------------------------------------------- batch-synchronised commit
+
+def test_commit_batch_sync_matches_oracle():
+    cfg = W.DecodeConfig("cs", batch=6, prefix_lo=0, prefix_hi=70, B=8, hq=4, hkv=2, d=128,
+                         hidden=64, vocab=64)
+    inp = W.make_decode_inputs(cfg, seed=7, steps=1, with_head=False, extra_pages=4)
+    for n_list in ([5, 8, 3, 7, 6, 4], [8, 8, 8, 8, 8, 8], [2, 9, -1, 4, 4, 4]):
+        n = torch.tensor(n_list, dtype=torch.int32)
+        kp, vp = inp.k_pool.to(DEV), inp.v_pool.to(DEV)
+        sl = inp.prefix_lens.to(DEV)
+        slots = torch.empty(cfg.batch, cfg.B, dtype=torch.int32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        mars.mars_kv_commit_batch_sync(inp.k_blk[0].to(DEV), inp.v_blk[0].to(DEV), n.to(DEV),
+                                       sl, inp.block_table.to(DEV), kp, vp, slots, st)
+        torch.cuda.synchronize()
+        rk, rv, rl, rs = oracle.kv_commit_batch_sync(
+            f64(inp.k_blk[0]), f64(inp.v_blk[0]), n.numpy(), inp.prefix_lens.numpy(),
+            inp.block_table.numpy(), f64(inp.k_pool), f64(inp.v_pool), cfg.page_size)
+        assert int(st.item()) == 0
+        np.testing.assert_array_equal(sl.cpu().numpy(), rl)
+        np.testing.assert_array_equal(slots.cpu().numpy(), rs)
+        np.testing.assert_array_equal(f64(kp.cpu()), rk)
+        np.testing.assert_array_equal(f64(vp.cpu()), rv)
 
 
 # -------------------------------------------------------------- whole decode step chain
