@@ -217,6 +217,41 @@ def dual_flops(cfg):
     return 4.0 * cfg.d * cfg.L * (cfg.L + 1) * cfg.batch * cfg.hq
 
 
+def ce_flops(cfg):
+    return 2.0 * cfg.batch * 2 * cfg.L * cfg.hidden * cfg.vocab
+
+
+def run_ce(device, peaks, reps=5, warm=3):
+    """The dual-stream training loss at the 7B head shape (LM-head GEMM over 2L rows with
+    the cross-entropy fused into its epilogue). W (1.09 GB) and h (117 MB) exceed L2."""
+    from block_masked_token_gb300 import mars
+    cfg = W.CE_LOSS_7B
+    x = W.make_ce_inputs(cfg, seed=0, device=device)
+    loss = torch.empty(3, dtype=torch.float32, device=device)
+    ws = torch.empty(mars.mars_workspace_bytes(mars.OP_CE_LOSS, cfg.batch, 1, vocab=cfg.vocab,
+                                               max_len=cfg.L), dtype=torch.uint8, device=device)
+    for _ in range(warm):
+        mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L, loss, ws)
+    times = []
+    for _ in range(reps):
+        a, b = _ev(), _ev()
+        a.record()
+        mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L, loss, ws)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3)
+    t = statistics.median(times)
+    tf = ce_flops(cfg) / t / 1e12
+    out = {"workload": cfg.name, "ms": t * 1e3, "tflops": tf,
+           "frac_tensor": tf / peaks["bf16_tflops_sustained"],
+           "peak_source": peaks["source"] + " bf16 sustained",
+           "loss": [float(v) for v in loss.cpu()],
+           "l2": "inputs larger than L2 (W 1.09 GB + h 117 MB)"}
+    del x, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -342,6 +377,9 @@ def run_gpu(args, rank, world, local):
     tau0 = run_step_variant(dataclasses.replace(cfg, name=cfg.name + "_tau0", taus=(0.0,)),
                             device, K, Wm, seed=rank)
 
+    # ---- the training-form loss over the dual stream (forward), same run
+    ce = run_ce(device, peaks, reps=max(3, min(K, 5)), warm=max(3, Wm))
+
     out = None
     if rank == 0:
         frac_head = head_tflops / peaks["bf16_tflops_sustained"]
@@ -381,6 +419,7 @@ def run_gpu(args, rank, world, local):
                                     "sequences with the same kernels; the MARS/AR ratio "
                                     "is the synthetic analogue of the pages' wall-clock "
                                     "table, with random weights (mean N ~ 1)"},
+            "ce_loss": ce,
             "mars_tau0": {**tau0, "mars_over_ar": tau0["tok_s"] / ar["tok_s"],
                           "note": "coverage run: tau = 0 accepts all B positions"},
             "roofline": {"kernel": "mars_head_accept (LM head GEMM + fused epilogue)",
@@ -581,7 +620,18 @@ def run_case(args):
     device = torch.device("cuda", 0)
     cfg = W.CONFIGS[args.config]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-    if isinstance(cfg, W.DualStreamConfig):
+    if isinstance(cfg, W.CELossConfig):
+        x = W.make_ce_inputs(cfg, seed=0, device=device)
+        loss = torch.empty(3, dtype=torch.float32, device=device)
+        ws = torch.empty(mars.mars_workspace_bytes(mars.OP_CE_LOSS, cfg.batch, 1,
+                                                   vocab=cfg.vocab, max_len=cfg.L),
+                         dtype=torch.uint8, device=device)
+
+        def call():
+            mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L,
+                                          loss, ws)
+        work = {"flop": ce_flops(cfg)}
+    elif isinstance(cfg, W.DualStreamConfig):
         x = W.make_dual_stream_inputs(cfg, seed=0, device=device)
         o = torch.empty(x["q"].shape, dtype=torch.float32, device=device)
 
@@ -627,7 +677,7 @@ def run_case(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["head", "decode", "dual"], default=None,
+    ap.add_argument("--case", choices=["head", "decode", "dual", "ce"], default=None,
                     help="time one entry point on --config instead of the decode step")
     ap.add_argument("--config", default=None, choices=sorted(W.CONFIGS))
     ap.add_argument("--gpus", type=int, default=1)

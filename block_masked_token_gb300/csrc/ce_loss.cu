@@ -1,0 +1,159 @@
+// Dual-stream training loss L = L_mask + L_AR over the 2L positions of z = [x; x~]
+// (papernotes.org notes of "MARS: Enabling Autoregressive Models Multi-Token Generation",
+// Key design 2: the masked-stream loss plus the clean-stream next-token loss; gist.science
+// explainer, 2.B "Combined Loss").
+//
+// For every row r of h (sequence s, stream position t < 2L) with a target index y_r,
+// ce_r = logsumexp_v(l_rv) - l_{r y_r}, l = h W^T. L_AR is the mean of ce_r over the
+// clean-stream rows (t < L) that carry a target, L_mask the mean over the masked-stream
+// rows (t >= L) that carry one; rows with target -1 are left out. Which positions carry a
+// target (the masked set, the right shift of the clean targets) is the caller's choice.
+//
+// Kernel 1 is the LM-head GEMM of head_gemm_tc.cuh, whose epilogue already reduces each
+// 128 x 256 logit tile to {max, sum exp, argmax} per row and here also keeps the target's
+// logit when it falls in the tile; the logits never reach memory. Kernel 2 merges the
+// partials of each row into ce_r; kernel 3 reduces the rows of each stream in a fixed
+// order (float64 accumulation), so the loss does not depend on scheduling.
+#include "common.cuh"
+#include "head_gemm_tc.cuh"
+#include "internal.h"
+
+namespace mars {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// One warp per row.
+__global__ void __launch_bounds__(256) ce_rows_kernel(const float4* __restrict__ part,
+                                                      const int32_t* __restrict__ targets,
+                                                      int rows, int nvt, int vocab,
+                                                      float* __restrict__ row_ce,
+                                                      int32_t* status) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int t = lane; t < nvt; t += 32) m = fmaxf(m, part[(size_t)t * rows + row].x);
+  m = warp_max(m);
+  float se = 0.f;
+  for (int t = lane; t < nvt; t += 32) {
+    const float4 v = part[(size_t)t * rows + row];
+    se += v.y * exp2f((v.x - m) * kLog2e);
+  }
+  se = warp_sum(se);
+  if (lane == 0) {
+    const int y = targets[row];
+    float ce = 0.f;
+    if (y >= 0 && y < vocab) {
+      const float lse = m + log2f(se) * kLn2;
+      ce = lse - part[(size_t)(y / head_tc::BN) * rows + row].w;
+    } else if (y != -1) {
+      if (status) atomicOr(status, MARS_ST_BADTARGET);
+    }
+    row_ce[row] = ce;
+  }
+}
+
+// One CTA: for each stream (0 clean, 1 masked) the mean of ce over its rows with a valid
+// target, summed in a fixed order in float64. loss = {L_mask, L_AR, L_mask + L_AR}; a
+// stream without any target contributes 0.
+__global__ void __launch_bounds__(256) ce_reduce_kernel(const float* __restrict__ row_ce,
+                                                        const int32_t* __restrict__ targets,
+                                                        int batch, int L, int vocab,
+                                                        float* __restrict__ loss) {
+  __shared__ double s_sum[256];
+  __shared__ int s_cnt[256];
+  float mean[2];
+  const long long n = (long long)batch * L;
+  for (int stream = 0; stream < 2; ++stream) {
+    double sum = 0.0;
+    int cnt = 0;
+    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
+      const long long s = i / L, t = i % L;
+      const long long r = s * 2 * L + (long long)stream * L + t;
+      const int y = targets[r];
+      if (y >= 0 && y < vocab) {
+        sum += (double)row_ce[r];
+        ++cnt;
+      }
+    }
+    s_sum[threadIdx.x] = sum;
+    s_cnt[threadIdx.x] = cnt;
+    __syncthreads();
+    for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+      if (threadIdx.x < o) {
+        s_sum[threadIdx.x] += s_sum[threadIdx.x + o];
+        s_cnt[threadIdx.x] += s_cnt[threadIdx.x + o];
+      }
+      __syncthreads();
+    }
+    mean[stream] = s_cnt[0] ? (float)(s_sum[0] / s_cnt[0]) : 0.f;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    loss[0] = mean[1];
+    loss[1] = mean[0];
+    loss[2] = mean[1] + mean[0];
+  }
+}
+
+}  // namespace
+
+size_t ce_workspace_bytes(int batch, int L, int vocab) {
+  const size_t rows = (size_t)batch * 2 * L;
+  const size_t nvt = (size_t)(vocab + head_tc::BN - 1) / head_tc::BN;
+  const size_t part = rows * nvt * sizeof(float4);
+  return part + ((rows * sizeof(float) + 255) / 256) * 256;
+}
+
+cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* targets,
+                           int batch, int L, int hidden, int vocab, float* loss,
+                           float* row_ce, void* workspace, int32_t* status,
+                           cudaStream_t stream) {
+  using namespace head_tc;
+  const int rows = batch * 2 * L;
+  CUtensorMap tm_h, tm_w;
+  {
+    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)hidden * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)vocab};
+    const uint64_t strides[1] = {(uint64_t)hidden * 2};
+    const uint32_t box[2] = {BK, BN};
+    if (!encode_tmap_bf16(&tm_w, w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  Params p{};
+  p.rows = rows;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.num_m = (rows + BM - 1) / BM;
+  p.num_n = (vocab + BN - 1) / BN;
+  p.num_k = (hidden + BK - 1) / BK;
+  p.num_tiles = p.num_m * p.num_n;
+  p.part = static_cast<float4*>(workspace);
+  p.targets = targets;
+  p.status = status;
+  float* ce = row_ce ? row_ce
+                     : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                (size_t)rows * p.num_n * sizeof(float4));
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_BYTES);
+    attr_set = true;
+  }
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
+  ce_rows_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(p.part, targets, rows, p.num_n, vocab,
+                                                      ce, status);
+  ce_reduce_kernel<<<1, 256, 0, stream>>>(ce, targets, batch, L, vocab, loss);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
+}  // namespace mars

@@ -113,6 +113,7 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   p.num_k = (hidden + BK - 1) / BK;
   p.num_tiles = p.num_m * p.num_n;
   p.part = static_cast<float4*>(workspace);
+  p.targets = nullptr;
   p.status = status;
   static bool attr_set = false;
   if (!attr_set) {

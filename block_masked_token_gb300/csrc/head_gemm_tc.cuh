@@ -2,7 +2,8 @@
 //
 // logits[r, v] = sum_k h[r, k] * W[v, k] for a 128-row x 256-column tile lives only in
 // TMEM; the epilogue reduces it to one partial {tile max, sum exp(l - tile max), first
-// argmax} per (row, vocabulary tile) and the logits never reach global memory.
+// argmax, and the row's target logit when a target index falls in the tile} per (row,
+// vocabulary tile), and the logits never reach global memory.
 //
 // Persistent, warp-specialised CTA (one per SM, 192 threads):
 //   warp 0      TMA producer: h tile [128 x 64] and W tile [256 x 64] per k-block into a
@@ -11,8 +12,11 @@
 //               into one of two 256-column fp32 accumulators;
 //   warps 2..5  epilogue: thread = accumulator row (TMEM lane), 256 columns read with
 //               tcgen05.ld, online max / argmax / sum-exp, one 16-byte store per row.
-// Tiles are ordered with the row block fastest so the CTAs running at the same time
-// share the same W tile through L2: W streams from HBM about once per call.
+// Tiles are ordered in groups of up to 16 row blocks (2048 rows): inside a group the row
+// block is fastest, so the CTAs running at the same time share one W tile through L2, and
+// the group's rows of h (at most 14.7 MB at hidden 3584) stay in L2 while the group sweeps
+// the vocabulary. W therefore streams from HBM once per group (once per call for decode
+// batches), and h once in all.
 #pragma once
 
 #include "sm100.cuh"
@@ -30,14 +34,28 @@ constexpr int TMEM_COLS = 512;                  // 2 accumulators x 256 fp32 col
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;   // + alignment slack
 constexpr float kLog2e = 1.4426950408889634f;
 
+constexpr int GROUP_M = 16;                     // row blocks per tile group
+
 struct Params {
   int rows, hidden, vocab;
   int num_m, num_n, num_k, num_tiles;
-  float4* part;          // [num_n][rows] {max, sumexp, argmax bits, 0}
+  float4* part;          // [num_n][rows] {max, sumexp, argmax bits, target logit or 0}
+  const int32_t* targets;  // [rows] vocabulary index per row, or NULL (no target logits)
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// Row block and vocabulary tile of linear tile index `tile` (see the order above).
+MARS_DEV void tile_coords(int tile, const Params& p, int& mb, int& nb) {
+  const int per_group = GROUP_M * p.num_n;
+  const int g = tile / per_group;
+  const int gm = min(GROUP_M, p.num_m - g * GROUP_M);    // row blocks in this group
+  const int local = tile - g * per_group;
+  mb = g * GROUP_M + local % gm;
+  nb = local / gm;
+}
+
+// static: every translation unit that launches it gets its own copy
+static __global__ void __launch_bounds__(NUM_THREADS, 1)
 head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  Params p) {
   using namespace sm100;
@@ -85,7 +103,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-        const int mb = tile % p.num_m, nb = tile / p.num_m;
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -137,7 +156,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     const int row_in_tile = quad * 32 + lane;
     int t = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++t) {
-      const int mb = tile % p.num_m, nb = tile / p.num_m;
+      int mb, nb;
+      tile_coords(tile, p, mb, nb);
       const int buf = t & 1;
       const uint32_t aph = (t >> 1) & 1;
       // warp-uniform result: the tcgen05.ld below is warp-collective
@@ -146,6 +166,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       const uint32_t taddr = tmem_base + buf * BN + ((uint32_t)(quad * 32) << 16);
       const int col0 = nb * BN;
       const int ncols = min(BN, p.vocab - col0);
+      const int row = mb * BM + row_in_tile;
+      // column of this row's target inside the tile (outside [0, ncols) when elsewhere)
+      const int tcol = (p.targets && row < p.rows) ? p.targets[row] - col0 : -1;
+      float tl = 0.f;
       float m = -INFINITY, ssum = 0.f;
       int am = 0x7fffffff;
 #pragma unroll 1
@@ -153,6 +177,12 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
         uint32_t r[32];
         tmem_ld32(taddr + c * 32, r);
         tmem_ld_wait();
+        const int rel = tcol - c * 32;
+        if (rel >= 0 && rel < 32 && c * 32 + rel < ncols) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == rel) tl = __uint_as_float(r[j]);
+        }
         float cm = -INFINITY;
         int ca = 0x7fffffff;
 #pragma unroll
@@ -178,9 +208,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
-      const int row = mb * BM + row_in_tile;
       if (row < p.rows)
-        p.part[(size_t)nb * p.rows + row] = make_float4(m, ssum, __int_as_float(am), 0.f);
+        p.part[(size_t)nb * p.rows + row] = make_float4(m, ssum, __int_as_float(am), tl);
     }
   }
 

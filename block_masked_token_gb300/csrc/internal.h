@@ -44,6 +44,13 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
                                int32_t* tokens, float* maxprob, int32_t* n_accept,
                                void* workspace, int32_t* status, cudaStream_t stream);
 
+// ---- Dual-stream training loss (L_mask + L_AR) over the 2L rows of each sequence.
+size_t ce_workspace_bytes(int batch, int L, int vocab);
+cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* targets,
+                           int batch, int L, int hidden, int vocab, float* loss,
+                           float* row_ce, void* workspace, int32_t* status,
+                           cudaStream_t stream);
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 

@@ -43,6 +43,10 @@ size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, in
     if (vocab <= 0) return 0;
     return mars::head_workspace_bytes(batch, B, vocab);
   }
+  if (op == MARS_OP_CE_LOSS) {
+    if (vocab <= 0 || max_len < 1) return 0;
+    return mars::ce_workspace_bytes(batch, max_len, vocab);
+  }
   return 0;
 }
 
@@ -166,6 +170,23 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
   return kv_commit_checked(k_blk, v_blk, n_accept, seq_lens, block_table, max_pages_per_seq,
                            k_pool, v_pool, num_pages, commit_slots, batch, B, hkv, d,
                            page_size, true, status, stream);
+}
+
+int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32_t* targets,
+                             int batch, int L, int hidden, int vocab, float* loss,
+                             float* row_ce, void* workspace, size_t ws_bytes,
+                             int32_t* status, void* stream) {
+  if (batch < 0 || L < 1 || hidden < 8 || vocab < 1) return MARS_EINVAL;
+  if (hidden % 8) return MARS_EUNSUPPORTED;
+  if ((long long)batch * 2 * L > 0x7fffffffLL) return MARS_EINVAL;
+  if (!loss) return MARS_EINVAL;
+  if (batch == 0) return cuda_rc(cudaMemsetAsync(loss, 0, 3 * sizeof(float),
+                                                 static_cast<cudaStream_t>(stream)));
+  if (!h || !w || !targets || !workspace) return MARS_EINVAL;
+  if (!aligned16(h) || !aligned16(w) || !aligned16(workspace)) return MARS_EALIGN;
+  if (ws_bytes < mars::ce_workspace_bytes(batch, L, vocab)) return MARS_ENOSPACE;
+  return cuda_rc(mars::launch_ce_loss(h, w, targets, batch, L, hidden, vocab, loss, row_ce,
+                                      workspace, status, static_cast<cudaStream_t>(stream)));
 }
 
 const char* mars_strerror(int code) {

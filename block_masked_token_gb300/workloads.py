@@ -72,6 +72,40 @@ SUSTAINED_DECODE_7B = DecodeConfig("sustained_decode_7b_b128_B16_64steps", batch
                                    d=128, hidden=3584, vocab=152064,
                                    taus=(1.0, 0.95, 0.9, 0.8), steps=64, tau_period=16)
 
+@dataclass(frozen=True)
+class CELossConfig:
+    name: str
+    batch: int
+    L: int
+    hidden: int
+    vocab: int
+
+
+# The training loss over the dual stream at the 7B head shape, with the stream length of
+# the 7B dual-stream attention workload.
+CE_LOSS_7B = CELossConfig("ce_loss_7b_b2_L4096", batch=2, L=4096, hidden=3584, vocab=152064)
+
+
+def make_ce_inputs(cfg: CELossConfig, seed: int = 0, device=None):
+    """Hidden states, head and targets for the dual-stream loss. Draw order: h = s * N(0,1)
+    with s = exp(U[ln 0.5, ln 8]) per row; W ~ N(0, 1/H) [V, H]; targets uniform in
+    [0, V) for every row, then -1 for the last clean row of each sequence (it has no next
+    token). Every masked row carries a target (the masked set is the whole masked stream).
+    Everything bf16 except the int32 targets."""
+    dev = torch.device(device) if device is not None else torch.device("cpu")
+    g = torch.Generator(device=dev).manual_seed(seed)
+    rows = cfg.batch * 2 * cfg.L
+    s = torch.exp(math.log(0.5) + (math.log(8.0) - math.log(0.5)) *
+                  torch.rand(rows, 1, generator=g, device=dev))
+    h = (torch.randn(rows, cfg.hidden, generator=g, device=dev) * s).to(torch.bfloat16)
+    w = (torch.randn(cfg.vocab, cfg.hidden, generator=g, device=dev) /
+         math.sqrt(cfg.hidden)).to(torch.bfloat16)
+    y = torch.randint(0, cfg.vocab, (rows,), generator=g, device=dev, dtype=torch.int64)
+    y = y.to(torch.int32)
+    y.view(cfg.batch, 2 * cfg.L)[:, cfg.L - 1] = -1
+    return {"h": h, "w": w, "targets": y}
+
+
 # The KV-cached autoregressive step on the same sequences (one query per sequence, one
 # token per step): the same kernels with B = 1 and tau = 1.0. The prefix lengths are the
 # first draw of the generator, so with the same seed they equal the sustained workload's.
@@ -80,7 +114,7 @@ AR_DECODE_7B = DecodeConfig("ar_decode_7b_b128_B1_64steps", batch=128, prefix_lo
                             vocab=152064, taus=(1.0,), steps=64, tau_period=16)
 
 CONFIGS = {c.name: c for c in (TINY_DECODE, DUAL_STREAM_0P5B, DECODE_7B, DUAL_STREAM_7B,
-                               SUSTAINED_DECODE_7B, AR_DECODE_7B)}
+                               SUSTAINED_DECODE_7B, AR_DECODE_7B, CE_LOSS_7B)}
 
 
 def _gen(seed: int, device) -> torch.Generator:

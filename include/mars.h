@@ -49,14 +49,17 @@ typedef uint16_t mars_bf16;
 #define MARS_ST_OVERFLOW 2      /* position beyond max_pages_per_seq: write skipped */
 #define MARS_ST_TIMEOUT 4       /* an in-kernel pipeline wait passed its time limit (2 s);
                                    the kernel stopped early and its outputs are invalid */
+#define MARS_ST_BADTARGET 8     /* a loss target outside [-1, vocab): that row is left out */
 
 #define MARS_OP_DECODE_ATTN 1
 #define MARS_OP_HEAD_ACCEPT 2
+#define MARS_OP_CE_LOSS 3
 
 /* Workspace (device scratch, caller-allocated, >= 256-byte aligned) needed by `op`.
  * MARS_OP_DECODE_ATTN uses batch, B, hq, hkv, d, max_len (the max_len_hint of the call);
- * MARS_OP_HEAD_ACCEPT uses batch, B, vocab. Other arguments are ignored. Returns 0 for an
- * unknown op or invalid sizes. */
+ * MARS_OP_HEAD_ACCEPT uses batch, B, vocab; MARS_OP_CE_LOSS uses batch, vocab and max_len
+ * as the stream length L (B must still be in [1, 32]). Other arguments are ignored.
+ * Returns 0 for an unknown op or invalid sizes. */
 size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
                             int vocab, int max_len);
 
@@ -181,6 +184,28 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
                               mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
                               int32_t* commit_slots, int batch, int B, int hkv, int d,
                               int page_size, int32_t* status, void* stream);
+
+/* Dual-stream training loss L = L_mask + L_AR ([notes] Key design 2: the masked-stream
+ * cross-entropy plus the clean-stream next-token cross-entropy; [gist] 2.B "Combined
+ * Loss") for the LM head over the 2L positions of z = [x; x~]. For every row r with a
+ * target y_r: ce_r = log sum_v exp(l_rv) - l_{r y_r}, with l = h W^T computed in fp32 from
+ * bf16 inputs (the logits are never written). L_AR = mean of ce_r over the clean rows
+ * (stream position t < L) with a target, L_mask = mean over the masked rows (t >= L) with
+ * a target; a stream without targets gives 0. The caller chooses which rows carry targets
+ * (the masked set, the right shift of the next-token targets): -1 leaves a row out.
+ *   h         [batch*2L, hidden] bf16   row s*2L + t = sequence s, stream position t
+ *   w         [vocab, hidden] bf16      the LM head, vocabulary-major
+ *   targets   [batch*2L] int32          target word per row, or -1
+ *   loss      [3] float (written)       {L_mask, L_AR, L_mask + L_AR}
+ *   row_ce    [batch*2L] float or NULL  ce_r per row (0 for rows without a target)
+ *   workspace >= mars_workspace_bytes(MARS_OP_CE_LOSS, batch, 1, 0, 0, 0, 0, vocab, L)
+ * hidden % 8 == 0. A target outside [-1, vocab) leaves its row out and flags
+ * MARS_ST_BADTARGET. The sums run in a fixed order (float64), so repeated calls agree
+ * bit for bit. status may be NULL. Forward only: no gradient is produced. */
+int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32_t* targets,
+                             int batch, int L, int hidden, int vocab, float* loss,
+                             float* row_ce, void* workspace, size_t ws_bytes,
+                             int32_t* status, void* stream);
 
 /* Human-readable name of a return code. Never NULL. */
 const char* mars_strerror(int code);

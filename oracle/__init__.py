@@ -8,6 +8,7 @@ from .mars_oracle import (  # noqa: F401
     ar_signal_fraction,
     attn_dual_stream,
     beta,
+    ce_loss_dual,
     decode_attn,
     gather_prefix,
     head_accept,

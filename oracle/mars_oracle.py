@@ -319,3 +319,30 @@ def kv_commit_batch_sync(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, 
     n_min = min(n) if n else 0
     return kv_commit(k_blk, v_blk, [n_min] * len(n), seq_lens, block_table, k_pool, v_pool,
                      page_size)
+
+
+# ---------------------------------------------------------------------------------------
+# Training loss of the dual stream ([notes] Key design 2; [gist] 2.B "Combined Loss").
+# ---------------------------------------------------------------------------------------
+
+def ce_loss_dual(h, w_vocab_major, targets, batch: int, L: int):
+    """L = L_mask + L_AR for hidden states h [batch*2L, H] (row s*2L + t; t < L the clean
+    stream, t >= L the masked stream) and the head W [V, H]. For a row with target y:
+    ce = log sum_v exp(l_v) - l_y, l = h W^T. L_AR is the mean ce over the clean rows with
+    a target, L_mask over the masked rows with one; target -1 leaves a row out; a stream
+    without targets gives 0. Returns (L_mask, L_AR, ce [batch*2L], 0 where no target)."""
+    logits = head_logits(h, w_vocab_major)
+    m = logits.max(axis=1)
+    lse = m + np.log(np.exp(logits - m[:, None]).sum(axis=1))
+    y = np.asarray(targets, dtype=np.int64)
+    V = logits.shape[1]
+    valid = (y >= 0) & (y < V)
+    ce = np.zeros(len(y), dtype=np.float64)
+    rows = np.flatnonzero(valid)
+    ce[rows] = lse[rows] - logits[rows, y[rows]]
+    pos = np.arange(len(y)) % (2 * L)
+    clean = valid & (pos < L)
+    masked = valid & (pos >= L)
+    l_ar = ce[clean].mean() if clean.any() else 0.0
+    l_mask = ce[masked].mean() if masked.any() else 0.0
+    return float(l_mask), float(l_ar), ce

@@ -46,6 +46,13 @@ def test_strerror_and_version(L):
     assert "sm_103a" in mars.mars_version()
 
 
+def test_ce_workspace_size(L):
+    rows, nvt = 2 * 2 * 100, (1000 + 255) // 256
+    want = rows * nvt * 16 + ((rows * 4 + 255) // 256) * 256
+    assert mars.mars_workspace_bytes(mars.OP_CE_LOSS, 2, 1, vocab=1000, max_len=100) == want
+    assert mars.mars_workspace_bytes(mars.OP_CE_LOSS, 2, 1, vocab=1000, max_len=0) == 0
+
+
 def test_workspace_sizes(L):
     assert mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, 2, 4, vocab=512) > 0
     ws = mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, 32, 8, 28, 4, 128, max_len=2048)
@@ -87,6 +94,11 @@ def test_host_validation_codes(L):
     assert L.mars_head_accept_per_request(P, P, 1, 4, 252, 512, P, P, P, P, P, 1 << 20, None, None) == mars.EUNSUPPORTED
     assert L.mars_head_accept_per_request(P, P, 1, 4, 256, 512, P, P, P, P, P, 16, None, None) == mars.ENOSPACE
     assert L.mars_head_accept_per_request(P, _p(20), 1, 4, 256, 512, P, P, P, P, P, 1 << 20, None, None) == mars.EALIGN
+    # loss: null loss pointer, hidden not a multiple of 8, workspace too small, L < 1
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, None, None, P, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 60, 100, P, None, P, 1 << 30, None, None) == mars.EUNSUPPORTED
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, P, None, P, 16, None, None) == mars.ENOSPACE
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 0, 64, 100, P, None, P, 1 << 30, None, None) == mars.EINVAL
     # commit (both policies): page size, null pool, B out of range
     for fn in (L.mars_kv_commit, L.mars_kv_commit_batch_sync):
         assert fn(P, P, P, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 8, None, None) == mars.EUNSUPPORTED

@@ -404,6 +404,51 @@ def test_commit_batch_sync_properties():
         np.testing.assert_array_equal(x, y)
 
 
+# --------------------------------------------------------------- dual-stream loss
+
+def test_ce_loss_hand_worked_case():
+    rows = [[x.strip() for x in ln.split("|")] for ln in golden_lines("ce_loss_case.txt")]
+    y = np.array([int(r[1]) for r in rows])
+    h = np.full((4, 1), math.log(2.0))
+    w = np.array([[0.0], [1.0], [2.0]])
+    l_mask, l_ar, ce = oracle.ce_loss_dual(h, w, y, 1, 2)
+    for (row, tgt, frac), c in zip(rows, ce):
+        if tgt.strip() == "-1":
+            assert c == 0.0
+        else:
+            a, b = (float(v) for v in frac.split("/"))
+            assert abs(c - math.log(a / b)) < 1e-14, (row, c)
+    assert abs(l_ar - math.log(7.0)) < 1e-14
+    assert abs(l_mask - math.log(49.0 / 8.0) / 2) < 1e-14
+
+
+def test_ce_loss_uniform_logits_give_log_vocab():
+    """W = 0 makes every logit equal, so every target costs exactly ln V."""
+    V, H, b, L = 37, 8, 2, 5
+    h = _rand((b * 2 * L, H), 80)
+    y = np.random.default_rng(0).integers(0, V, b * 2 * L)
+    l_mask, l_ar, ce = oracle.ce_loss_dual(h, np.zeros((V, H)), y, b, L)
+    assert np.allclose(ce, math.log(V), rtol=0, atol=1e-14)
+    assert abs(l_mask - math.log(V)) < 1e-14 and abs(l_ar - math.log(V)) < 1e-14
+
+
+def test_ce_loss_against_torch_cross_entropy():
+    V, H, b, L = 300, 24, 3, 7
+    h = _rand((b * 2 * L, H), 81)
+    w = _rand((V, H), 82)
+    y = np.random.default_rng(1).integers(-1, V, b * 2 * L)
+    l_mask, l_ar, ce = oracle.ce_loss_dual(h, w, y, b, L)
+    logits = torch.from_numpy(h @ w.T)
+    yt = torch.from_numpy(y)
+    per = torch.nn.functional.cross_entropy(logits, yt, ignore_index=-1, reduction="none")
+    np.testing.assert_allclose(ce, per.numpy(), rtol=1e-12, atol=1e-12)
+    pos = np.arange(b * 2 * L) % (2 * L)
+    for sel, got in (((pos < L), l_ar), ((pos >= L), l_mask)):
+        ref = torch.nn.functional.cross_entropy(logits[torch.from_numpy(sel)],
+                                                yt[torch.from_numpy(sel)], ignore_index=-1)
+        assert abs(got - float(ref)) < 1e-12
+
+
 # ------------------------------------------- planted mistakes: each must fail some pin
 
 def test_planted_floor_block_index_is_caught(monkeypatch):

@@ -412,6 +412,69 @@ def test_commit_batch_sync_matches_oracle():
         np.testing.assert_array_equal(f64(vp.cpu()), rv)
 
 
+# ------------------------------------------------------------- dual-stream training loss
+
+LOSS_TOL = 2e-4      # fp32 logits of bf16 inputs: |error of lse - l_y| well below 1e-4
+
+
+def run_ce(h, w, y, batch, L, row_ce=True):
+    loss = torch.empty(3, dtype=torch.float32, device=DEV)
+    ce = torch.empty(batch * 2 * L, dtype=torch.float32, device=DEV) if row_ce else None
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_CE_LOSS, batch, 1, vocab=w.shape[0], max_len=L))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mars.mars_dual_stream_ce_loss(h, w, y, batch, L, loss, ws, ce, st)
+    torch.cuda.synchronize()
+    return loss.cpu().numpy(), (ce.cpu().numpy() if row_ce else None), int(st.item())
+
+
+@pytest.mark.parametrize("batch,L,H,V", [(2, 96, 256, 1000), (1, 200, 64, 7), (3, 1, 128, 300)])
+def test_ce_loss_small(batch, L, H, V):
+    cfg = W.CELossConfig("t", batch, L, H, V)
+    x = W.make_ce_inputs(cfg, seed=L + V)
+    y = x["targets"].clone()
+    y[::5] = -1                                   # rows left out of both streams
+    loss, ce, st = run_ce(x["h"].to(DEV), x["w"].to(DEV), y.to(DEV), batch, L)
+    assert st == 0
+    l_mask, l_ar, rce = oracle.ce_loss_dual(f64(x["h"]), f64(x["w"]), y.numpy(), batch, L)
+    np.testing.assert_allclose(ce, rce, rtol=0, atol=LOSS_TOL)
+    assert abs(loss[0] - l_mask) <= LOSS_TOL and abs(loss[1] - l_ar) <= LOSS_TOL
+    assert abs(loss[2] - (l_mask + l_ar)) <= 2 * LOSS_TOL
+    # the loss without the per-row output is the same bits
+    loss2, _, _ = run_ce(x["h"].to(DEV), x["w"].to(DEV), y.to(DEV), batch, L, row_ce=False)
+    np.testing.assert_array_equal(loss, loss2)
+
+
+def test_ce_loss_bad_target_is_flagged_and_left_out():
+    cfg = W.CELossConfig("t", 1, 16, 64, 100)
+    x = W.make_ce_inputs(cfg, seed=3)
+    y = x["targets"].clone()
+    y[20] = 100                                   # == vocab: out of range
+    loss, ce, st = run_ce(x["h"].to(DEV), x["w"].to(DEV), y.to(DEV), 1, 16)
+    assert st & mars.ST_BADTARGET
+    y[20] = -1
+    l_mask, l_ar, _ = oracle.ce_loss_dual(f64(x["h"]), f64(x["w"]), y.numpy(), 1, 16)
+    assert ce[20] == 0.0 and abs(loss[0] - l_mask) <= LOSS_TOL and abs(loss[1] - l_ar) <= LOSS_TOL
+
+
+def test_ce_loss_7b_shapes_sampled_rows():
+    cfg = W.CELossConfig("t7", 1, 512, 3584, 152064)
+    x = W.make_ce_inputs(cfg, seed=0, device=DEV)
+    loss, ce, st = run_ce(x["h"], x["w"], x["targets"], 1, 512)
+    assert st == 0
+    rows = sorted({0, 1, 255, 510, 511, 512, 513, 700, 1023,
+                   *np.random.default_rng(2).integers(0, 1024, 20).tolist()})
+    y = x["targets"].cpu().numpy()
+    h = f64(x["h"][rows])
+    _, _, rce = oracle.ce_loss_dual(h, f64(x["w"]), y[rows], len(rows), 1)
+    # rows were regrouped, so only the per-row values are compared here
+    np.testing.assert_allclose(ce[rows], rce, rtol=0, atol=LOSS_TOL)
+    # the means are those of the per-row values (in float64)
+    pos = np.arange(1024) % 1024
+    ok = y >= 0
+    assert abs(loss[0] - ce[ok & (pos >= 512)].astype(np.float64).mean()) < 1e-5
+    assert abs(loss[1] - ce[ok & (pos < 512)].astype(np.float64).mean()) < 1e-5
+
+
 # -------------------------------------------------------------- whole decode step chain
 
 def test_tiny_decode_step_end_to_end():
