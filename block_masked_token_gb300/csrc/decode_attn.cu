@@ -10,9 +10,10 @@
 // page by page from the paged pool (8 producer lanes, one 16-token page each, TMA with
 // 128-byte swizzle), and for the last split one more tile with the B block keys (causal:
 // query k sees block keys 0..k). With several splits each writes an unnormalised partial
-// (m in log2 units, l, O) to the workspace and a second kernel merges them; when the
-// (sequence, kv head) pairs alone fill the GPU there is one split per pair and its CTA
-// writes the normalised output directly.
+// (m in log2 units, l, O) to the workspace and a second kernel merges them. Splits are
+// used only when there are fewer (sequence, kv head) pairs than SMs and the prefixes are
+// long (each split at least kMinSplitKeys keys); otherwise there is one split per pair and
+// its CTA writes the normalised output directly.
 #include <climits>
 
 #include "common.cuh"
@@ -26,12 +27,11 @@ namespace {
 using flash::BKV;
 using flash::BQ;
 
-// Split-KV sizing: aim for this many CTAs per SM over the host's length bound, so CTAs are
-// short enough to balance across SMs but long enough to amortise their set-up.
-#ifndef MARS_DECODE_CTAS_PER_SM
-#define MARS_DECODE_CTAS_PER_SM 8
-#endif
-constexpr int kTargetCtas = MARS_DECODE_CTAS_PER_SM * kNumSMs;
+// Split-KV sizing. A split costs a partial record and a merge launch, which at 7B shapes
+// outweighs the balance it buys unless a split still streams at least this many keys:
+// with batch 32 and prefixes up to 2048, one split per (sequence, kv head) ran in 33 us
+// against 46-50 us with 2 to 4 splits and the merge.
+constexpr int kMinSplitKeys = 2048;
 constexpr int kPagesPerTile = BKV / kPageSize;   // 8
 
 struct DecodeArgs {
@@ -313,12 +313,19 @@ DecodePlan plan_decode(int batch, int B, int hq, int hkv, int d, int max_len) {
   DecodePlan p{};
   const long long T = (long long)max_len > 0 ? max_len : 1;
   const long long pairs = (long long)batch * hkv;
-  long long per = (pairs * T + kTargetCtas - 1) / kTargetCtas;
-  if (per < 4 * BKV) per = 4 * BKV;
+  const long long sms = num_sms();
+  // one split per (sequence, kv head) when the pairs fill the GPU; otherwise enough splits
+  // for about one wave of CTAs, but only as many as keep every split at least
+  // kMinSplitKeys long (none when the prefixes are shorter than two such splits)
+  long long nsplit = 1;
+  if (pairs < sms) {
+    const long long want = (sms + pairs - 1) / pairs;
+    const long long most = T / kMinSplitKeys;
+    nsplit = want < most ? want : most;
+    if (nsplit < 1) nsplit = 1;
+  }
+  long long per = (T + nsplit - 1) / nsplit;
   per = (per + BKV - 1) / BKV * BKV;
-  // With at least two (sequence, kv head) pairs per SM the pairs alone balance the GPU:
-  // one split each, whose CTA writes the normalised output itself (no partials, no merge).
-  if (pairs >= 2LL * kNumSMs) per = (T + BKV - 1) / BKV * BKV;
   p.split_len = (int)per;
   p.nsplit = (int)((T + per - 1) / per);
   if (p.nsplit < 1) p.nsplit = 1;

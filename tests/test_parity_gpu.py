@@ -204,11 +204,25 @@ def test_decode_unmapped_page_sets_status():
 
 
 def test_decode_single_split_direct_output():
-    """With at least two (sequence, kv head) pairs per SM the kernel runs one split per
-    pair and writes the normalised output directly (no merge pass)."""
+    """With at least as many (sequence, kv head) pairs as SMs the kernel runs one split
+    per pair and writes the normalised output directly (no merge pass)."""
     cfg = W.DecodeConfig("d6", batch=160, prefix_lo=0, prefix_hi=300, B=4, hq=4, hkv=2, d=64,
                          hidden=64, vocab=64)
     inp = _decode_case(cfg, seed=8)
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
+    assert st == 0
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_decode_multi_split_merge():
+    """Few pairs and long prefixes: the keys are split across CTAs (here 5 splits of 2048
+    keys for the longest sequence, some splits past the shorter one's end) and merged."""
+    cfg = W.DecodeConfig("d7", batch=2, prefix_lo=0, prefix_hi=0, prefixes=(9000, 4100), B=8,
+                         hq=7, hkv=1, d=128, hidden=64, vocab=64)
+    inp = _decode_case(cfg, seed=9)
     o, st = run_decode(inp, 0, inp.prefix_lens, cfg)
     assert st == 0
     ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
