@@ -141,12 +141,9 @@ cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* 
   float* ce = row_ce ? row_ce
                      : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                                 (size_t)rows * p.num_n * sizeof(float4));
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)SMEM_BYTES);
-    attr_set = true;
-  }
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_BYTES, attr);
+  if (ea != cudaSuccess) return ea;
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
   head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
   ce_rows_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(p.part, targets, rows, p.num_n, vocab,

@@ -292,12 +292,9 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* 
     if (!encode_tmap_bf16(&tkb, k_blk, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_tmap_bf16(&tvb, v_blk, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(decode_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         S::TOTAL);
-    attr = true;
-  }
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(decode_tc_kernel<D>, S::TOTAL, attr);
+  if (ea != cudaSuccess) return ea;
   dim3 grid(a.nsplit, a.hkv, batch);
   decode_tc_kernel<D><<<grid, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tkp, tvp, tkb, tvb, a);
   if (a.nsplit > 1) {

@@ -196,12 +196,9 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, f
   }
   DualArgs a{o, batch, L, B, hq, hkv, hq / hkv, (L + BQ - 1) / BQ,
              scale * 1.4426950408889634f, status};
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(dual_stream_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         S::TOTAL);
-    attr = true;
-  }
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(dual_stream_tc_kernel<D>, S::TOTAL, attr);
+  if (ea != cudaSuccess) return ea;
   const long long ctas = (long long)a.nqt * 2 * hq * batch;
   dual_stream_tc_kernel<D><<<(unsigned)ctas, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();

@@ -115,12 +115,9 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   p.part = static_cast<float4*>(workspace);
   p.targets = nullptr;
   p.status = status;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)SMEM_BYTES);
-    attr_set = true;
-  }
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_BYTES, attr);
+  if (ea != cudaSuccess) return ea;
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
   head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
   head_finalize_kernel<<<batch, 32 * B, 0, stream>>>(p.part, rows, B, p.num_n, tau, taus,

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -53,6 +55,19 @@ cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* 
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
+
+// Function attributes belong to the device they were set on: raise a kernel's dynamic
+// shared-memory limit once per device (flags indexed by device ordinal).
+template <class Kernel>
+cudaError_t set_smem_limit_once(Kernel* fn, int bytes, std::atomic<int> (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 // ---- Dual-stream attention under mask M.
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -229,11 +229,14 @@ def head_logits(h, w_vocab_major, chunk: int = 16384):
 
 def maxprob_argmax(logits):
     """Per row: token = lowest index attaining the max logit; maxprob = max_v softmax(l)_v
-    = 1 / sum_v exp(l_v - max); gap = max minus the second-largest logit (0 on ties).
+    = 1 / sum_v exp(l_v - max); gap = max minus the second-largest logit (0 on ties;
+    infinite for a one-word vocabulary, which has no second logit).
     Returns (tokens int64 [R], maxprob float64 [R], gap float64 [R])."""
     m = logits.max(axis=1)
     tokens = np.argmax(logits, axis=1)          # first occurrence = lowest index
     maxprob = 1.0 / np.exp(logits - m[:, None]).sum(axis=1)
+    if logits.shape[1] < 2:
+        return tokens.astype(np.int64), maxprob, np.full(len(m), np.inf)
     part = np.partition(logits, -2, axis=1)
     gap = part[:, -1] - part[:, -2]
     return tokens.astype(np.int64), maxprob, gap

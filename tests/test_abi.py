@@ -85,6 +85,9 @@ def test_host_validation_codes(L):
     args = [P, P, P, P, P, 10, P, 4, P, 64, P, 2, 4, 4, 2, 64]
     assert L.mars_decode_attn(*args, 8, 0.0, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_decode_attn(*args, 16, 0.0, P, 16, None, None) == mars.ENOSPACE
+    too_many_rows = list(args)        # 28/4 heads: 7 query rows per kv head per position
+    too_many_rows[13], too_many_rows[14], too_many_rows[12] = 28, 4, 19
+    assert L.mars_decode_attn(*too_many_rows[:15], 128, 16, 0.0, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     bad_b = list(args)
     bad_b[12] = 33
     assert L.mars_decode_attn(*bad_b, 16, 0.0, P, 1 << 30, None, None) == mars.EINVAL

@@ -238,6 +238,15 @@ def test_maxprob_argmax_against_torch():
     assert (p > 1.0 / 1000).all() and (p <= 1.0).all() and (gap >= 0).all()
 
 
+def test_one_word_vocabulary():
+    """V = 1: softmax is 1, so p = 1 >= tau for any tau <= 1 and the whole block is
+    accepted; there is no second logit, so no tie."""
+    h = _rand((6, 8), 90)
+    w = _rand((1, 8), 91)
+    tok, p, n, gap = oracle.head_accept(h, w, 2, 3, 1.0)
+    assert (tok == 0).all() and (p == 1.0).all() and (n == 3).all() and np.isinf(gap).all()
+
+
 def test_head_logits_chunked_equals_matmul():
     h = _rand((6, 40), 30)
     w = _rand((1000, 40), 31)

@@ -83,6 +83,7 @@ def _to_dev(inp):
     (1, 33, 40, 2, 1, 128),       # B > L: one block
     (1, 300, 128, 2, 1, 128),     # B = tile: masked rows use one clean tile fewer
     (1, 300, 200, 2, 2, 64),      # B > tile, straddling tiles: key tiles only clean rows use
+    (3, 257, 5, 3, 3, 128),       # no grouping (hq = hkv), one row past two full tiles
 ])
 def test_dual_stream_small(b, L, B, hq, hkv, d):
     cfg = W.DualStreamConfig("t", b, L, B, hq, hkv, d)
@@ -151,6 +152,12 @@ def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
     # the KV-cached AR step at 7B attention shapes: one query per sequence
     W.DecodeConfig("d5", batch=4, prefix_lo=2048, prefix_hi=8192, B=1, hq=28, hkv=4, d=128,
                    hidden=64, vocab=64),
+    # the largest query tile: G * B = 4 * 32 = 128 rows per kv head
+    W.DecodeConfig("d8", batch=2, prefix_lo=0, prefix_hi=0, prefixes=(129, 1000), B=32, hq=8,
+                   hkv=2, d=128, hidden=64, vocab=64),
+    # empty prefixes: only the block keys
+    W.DecodeConfig("d9", batch=3, prefix_lo=0, prefix_hi=0, prefixes=(0, 0, 0), B=16, hq=4,
+                   hkv=1, d=64, hidden=64, vocab=64),
 ])
 def test_decode_small(cfg):
     inp = _decode_case(cfg, seed=1)
@@ -266,6 +273,7 @@ def test_decode_config_7b_sampled():
     (1, 16, 128, 77, 0.0),          # tau 0: whole block
     (4, 8, 512, 3000, 1.0),         # tau 1: plain AR
     (2, 32, 96, 300, 0.3),
+    (1, 4, 64, 1, 1.0),             # one-word vocabulary: p = 1 >= tau = 1, the whole block
 ])
 def test_head_small(batch, B, hidden, vocab, tau):
     cfg = W.DecodeConfig("h", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
@@ -274,7 +282,7 @@ def test_head_small(batch, B, hidden, vocab, tau):
     tok, p, n = run_head(inp.h[0].to(DEV), inp.w.to(DEV), batch, B, tau)
     rt, rp, rn, gap = oracle.head_accept(f64(inp.h[0]), f64(inp.w), batch, B, tau)
     compare_head(tok, p, n, rt, rp, rn, gap, tau)
-    if tau == 1.0:
+    if tau == 1.0 and vocab > 1:
         assert (n == 1).all()
     if tau == 0.0:
         assert (n == B).all()
