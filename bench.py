@@ -223,31 +223,57 @@ def ce_flops(cfg):
 
 def run_ce(device, peaks, reps=5, warm=3):
     """The dual-stream training loss at the 7B head shape (LM-head GEMM over 2L rows with
-    the cross-entropy fused into its epilogue). W (1.09 GB) and h (117 MB) exceed L2."""
+    the cross-entropy fused into its epilogue), and its gradient (the GEMM again with a
+    dlogits epilogue, then dh and dW as two cuBLAS GEMMs). W (1.09 GB) and h (117 MB)
+    exceed L2."""
     from block_masked_token_gb300 import mars
     cfg = W.CE_LOSS_7B
+    rows = cfg.batch * 2 * cfg.L
     x = W.make_ce_inputs(cfg, seed=0, device=device)
     loss = torch.empty(3, dtype=torch.float32, device=device)
+    lse = torch.empty(rows, dtype=torch.float32, device=device)
     ws = torch.empty(mars.mars_workspace_bytes(mars.OP_CE_LOSS, cfg.batch, 1, vocab=cfg.vocab,
                                                max_len=cfg.L), dtype=torch.uint8, device=device)
-    for _ in range(warm):
-        mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L, loss, ws)
-    times = []
-    for _ in range(reps):
-        a, b = _ev(), _ev()
-        a.record()
-        mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L, loss, ws)
-        b.record()
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b) / 1e3)
-    t = statistics.median(times)
+    wg = torch.empty(mars.mars_workspace_bytes(mars.OP_CE_LOSS_GRAD, cfg.batch, 1,
+                                               vocab=cfg.vocab, max_len=cfg.L),
+                     dtype=torch.uint8, device=device)
+    dh = torch.empty(rows, cfg.hidden, dtype=torch.float32, device=device)
+    dw = torch.empty(cfg.vocab, cfg.hidden, dtype=torch.float32, device=device)
+
+    def fwd():
+        mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L, loss, ws,
+                                      row_lse=lse)
+
+    def bwd():
+        mars.mars_dual_stream_ce_loss_grad(x["h"], x["w"], x["targets"], lse, cfg.batch, cfg.L,
+                                           wg, dh, dw)
+
+    def timed(fn):
+        for _ in range(warm):
+            fn()
+        times = []
+        for _ in range(reps):
+            a, b = _ev(), _ev()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+        return statistics.median(times)
+
+    t = timed(fwd)
+    tg = timed(bwd)
     tf = ce_flops(cfg) / t / 1e12
+    tfg = 3 * ce_flops(cfg) / tg / 1e12
     out = {"workload": cfg.name, "ms": t * 1e3, "tflops": tf,
            "frac_tensor": tf / peaks["bf16_tflops_sustained"],
            "peak_source": peaks["source"] + " bf16 sustained",
            "loss": [float(v) for v in loss.cpu()],
+           "grad_ms": tg * 1e3, "grad_tflops": tfg,
+           "grad_note": "GEMM with dlogits epilogue (bf16 dlogits written, 5 GB) + dh and dW "
+                        "(cuBLAS); 3 x 2*rows*H*V flop",
            "l2": "inputs larger than L2 (W 1.09 GB + h 117 MB)"}
-    del x, ws
+    del x, ws, wg, dh, dw
     torch.cuda.empty_cache()
     return out
 

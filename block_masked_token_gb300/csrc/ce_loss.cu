@@ -14,6 +14,16 @@
 // logit when it falls in the tile; the logits never reach memory. Kernel 2 merges the
 // partials of each row into ce_r; kernel 3 reduces the rows of each stream in a fixed
 // order (float64 accumulation), so the loss does not depend on scheduling.
+//
+// Gradient: dL/dl_rv = (softmax(l_r)_v - [v = y_r]) / N_x for a row of stream x with a
+// target (N_x = that stream's rows with a target), 0 for the others. The head GEMM is run
+// again with an epilogue that writes this dlogits tile in bf16 (using the forward's
+// per-row log-sum-exp), then two plain GEMMs go to cuBLAS: dh = dlogits W and
+// dW = dlogits^T h, both accumulated in fp32.
+#include <cublas_v2.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "head_gemm_tc.cuh"
 #include "internal.h"
@@ -30,6 +40,7 @@ __global__ void __launch_bounds__(256) ce_rows_kernel(const float4* __restrict__
                                                       const int32_t* __restrict__ targets,
                                                       int rows, int nvt, int vocab,
                                                       float* __restrict__ row_ce,
+                                                      float* __restrict__ row_lse,
                                                       int32_t* status) {
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -45,9 +56,10 @@ __global__ void __launch_bounds__(256) ce_rows_kernel(const float4* __restrict__
   se = warp_sum(se);
   if (lane == 0) {
     const int y = targets[row];
+    const float lse = m + log2f(se) * kLn2;
+    if (row_lse) row_lse[row] = lse;
     float ce = 0.f;
     if (y >= 0 && y < vocab) {
-      const float lse = m + log2f(se) * kLn2;
       ce = lse - part[(size_t)(y / head_tc::BN) * rows + row].w;
     } else if (y != -1) {
       if (status) atomicOr(status, MARS_ST_BADTARGET);
@@ -99,7 +111,124 @@ __global__ void __launch_bounds__(256) ce_reduce_kernel(const float* __restrict_
   }
 }
 
+// One CTA: the number of rows with a valid target in each stream; scale = 1 / count (0 for
+// a stream without targets).
+__global__ void __launch_bounds__(256) ce_scale_kernel(const int32_t* __restrict__ targets,
+                                                       int batch, int L, int vocab,
+                                                       float* __restrict__ scale) {
+  __shared__ int s_cnt[2][256];
+  int cnt[2] = {0, 0};
+  const long long rows = (long long)batch * 2 * L;
+  for (long long r = threadIdx.x; r < rows; r += blockDim.x) {
+    const int y = targets[r];
+    if (y >= 0 && y < vocab) ++cnt[(r % (2 * L)) >= L ? 1 : 0];
+  }
+  s_cnt[0][threadIdx.x] = cnt[0];
+  s_cnt[1][threadIdx.x] = cnt[1];
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      s_cnt[0][threadIdx.x] += s_cnt[0][threadIdx.x + o];
+      s_cnt[1][threadIdx.x] += s_cnt[1][threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < 2) scale[threadIdx.x] = s_cnt[threadIdx.x][0] ? 1.f / s_cnt[threadIdx.x][0] : 0.f;
+}
+
+// One cuBLAS handle per device, created on first use; calls are serialised because a
+// handle carries its stream.
+struct Blas {
+  std::mutex mu;
+  cublasHandle_t h[64] = {};
+};
+Blas& blas() {
+  static Blas b;
+  return b;
+}
+
+size_t grad_dlogits_bytes(int batch, int L, int vocab) {
+  const size_t n = (size_t)batch * 2 * L * vocab * sizeof(uint16_t);
+  return (n + 255) / 256 * 256;
+}
+
 }  // namespace
+
+size_t ce_grad_workspace_bytes(int batch, int L, int vocab) {
+  return grad_dlogits_bytes(batch, L, vocab) + 256;
+}
+
+cudaError_t launch_ce_loss_grad(const uint16_t* h, const uint16_t* w, const int32_t* targets,
+                                const float* row_lse, int batch, int L, int hidden, int vocab,
+                                float* dh, float* dw, void* workspace, int32_t* status,
+                                cudaStream_t stream) {
+  using namespace head_tc;
+  const int rows = batch * 2 * L;
+  uint16_t* dlogits = static_cast<uint16_t*>(workspace);
+  float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          grad_dlogits_bytes(batch, L, vocab));
+  CUtensorMap tm_h, tm_w;
+  {
+    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)rows};
+    const uint64_t strides[1] = {(uint64_t)hidden * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)vocab};
+    const uint64_t strides[1] = {(uint64_t)hidden * 2};
+    const uint32_t box[2] = {BK, BN};
+    if (!encode_tmap_bf16(&tm_w, w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  Params p{};
+  p.rows = rows;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.num_m = (rows + BM - 1) / BM;
+  p.num_n = (vocab + BN - 1) / BN;
+  p.num_k = (hidden + BK - 1) / BK;
+  p.num_tiles = p.num_m * p.num_n;
+  p.targets = targets;
+  p.dlogits = dlogits;
+  p.row_lse = row_lse;
+  p.stream_scale = scale;
+  p.two_l = 2 * L;
+  p.status = status;
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_BYTES, attr);
+  if (ea != cudaSuccess) return ea;
+  ce_scale_kernel<<<1, 256, 0, stream>>>(targets, batch, L, vocab, scale);
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
+  count_launches(2);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || (!dh && !dw)) return e;
+
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  Blas& b = blas();
+  std::lock_guard<std::mutex> lock(b.mu);
+  if (!b.h[dev] && cublasCreate(&b.h[dev]) != CUBLAS_STATUS_SUCCESS) {
+    b.h[dev] = nullptr;
+    return cudaErrorInitializationError;
+  }
+  cublasHandle_t hb = b.h[dev];
+  if (cublasSetStream(hb, stream) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
+  const float one = 1.f, zero = 0.f;
+  // row-major C = A B is column-major C^T = B^T A^T
+  if (dh &&  // dh [rows, H] = dlogits [rows, V] . W [V, H]
+      cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_N, hidden, rows, vocab, &one, w, CUDA_R_16BF,
+                   hidden, dlogits, CUDA_R_16BF, vocab, &zero, dh, CUDA_R_32F, hidden,
+                   CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+    return cudaErrorUnknown;
+  if (dw &&  // dW [V, H] = dlogits^T [V, rows] . h [rows, H]
+      cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_T, hidden, vocab, rows, &one, h, CUDA_R_16BF,
+                   hidden, dlogits, CUDA_R_16BF, vocab, &zero, dw, CUDA_R_32F, hidden,
+                   CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+    return cudaErrorUnknown;
+  return cudaSuccess;
+}
 
 size_t ce_workspace_bytes(int batch, int L, int vocab) {
   const size_t rows = (size_t)batch * 2 * L;
@@ -110,7 +239,7 @@ size_t ce_workspace_bytes(int batch, int L, int vocab) {
 
 cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* targets,
                            int batch, int L, int hidden, int vocab, float* loss,
-                           float* row_ce, void* workspace, int32_t* status,
+                           float* row_ce, float* row_lse, void* workspace, int32_t* status,
                            cudaStream_t stream) {
   using namespace head_tc;
   const int rows = batch * 2 * L;
@@ -137,6 +266,7 @@ cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* 
   p.num_tiles = p.num_m * p.num_n;
   p.part = static_cast<float4*>(workspace);
   p.targets = targets;
+  p.dlogits = nullptr;
   p.status = status;
   float* ce = row_ce ? row_ce
                      : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
@@ -147,7 +277,7 @@ cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* 
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
   head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
   ce_rows_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(p.part, targets, rows, p.num_n, vocab,
-                                                      ce, status);
+                                                      ce, row_lse, status);
   ce_reduce_kernel<<<1, 256, 0, stream>>>(ce, targets, batch, L, vocab, loss);
   count_launches(3);
   return cudaGetLastError();

@@ -114,6 +114,7 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   p.num_tiles = p.num_m * p.num_n;
   p.part = static_cast<float4*>(workspace);
   p.targets = nullptr;
+  p.dlogits = nullptr;
   p.status = status;
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_BYTES, attr);

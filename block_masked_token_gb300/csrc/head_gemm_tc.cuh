@@ -19,6 +19,8 @@
 // batches), and h once in all.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "sm100.cuh"
 
 namespace mars {
@@ -41,6 +43,14 @@ struct Params {
   int num_m, num_n, num_k, num_tiles;
   float4* part;          // [num_n][rows] {max, sumexp, argmax bits, target logit or 0}
   const int32_t* targets;  // [rows] vocabulary index per row, or NULL (no target logits)
+  // Gradient mode (dlogits != NULL): instead of the partials, the epilogue writes
+  // dlogits[r, v] = (exp(l_rv - row_lse[r]) - [v == y_r]) * row scale, in bf16, where the
+  // row scale is stream_scale[(r % two_l) >= two_l / 2] for rows with a valid target, 0
+  // otherwise.
+  uint16_t* dlogits;       // [rows, vocab] bf16
+  const float* row_lse;    // [rows]
+  const float* stream_scale;   // [2]: clean rows, masked rows
+  int two_l;
   int32_t* status;
 };
 
@@ -169,6 +179,48 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       const int row = mb * BM + row_in_tile;
       // column of this row's target inside the tile (outside [0, ncols) when elsewhere)
       const int tcol = (p.targets && row < p.rows) ? p.targets[row] - col0 : -1;
+      if (p.dlogits) {
+        // gradient of the mean cross-entropy with respect to this tile of logits
+        float lse = 0.f, scale = 0.f;
+        if (row < p.rows) {
+          const int y = p.targets[row];
+          lse = p.row_lse[row];
+          if (y >= 0 && y < p.vocab)
+            scale = p.stream_scale[(row % p.two_l) >= p.two_l / 2 ? 1 : 0];
+        }
+        const float nl = -lse * kLog2e;
+        uint16_t* drow = p.dlogits + (size_t)(row < p.rows ? row : 0) * p.vocab + col0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_ld_wait();
+          if (row < p.rows && c * 32 < ncols) {
+            uint32_t g2[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float g0 = exp2f(fmaf(__uint_as_float(r[j]), kLog2e, nl));
+              float g1 = exp2f(fmaf(__uint_as_float(r[j + 1]), kLog2e, nl));
+              if (c * 32 + j == tcol) g0 -= 1.f;
+              if (c * 32 + j + 1 == tcol) g1 -= 1.f;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * scale, g1 * scale);
+              g2[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            if (c * 32 + 32 <= ncols && (p.vocab % 8) == 0) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(drow + c * 32 + q * 8) =
+                    make_uint4(g2[4 * q], g2[4 * q + 1], g2[4 * q + 2], g2[4 * q + 3]);
+            } else {
+              for (int j = 0; j < 32 && c * 32 + j < ncols; ++j)
+                drow[c * 32 + j] = (uint16_t)((g2[j >> 1] >> ((j & 1) * 16)) & 0xffffu);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
       float tl = 0.f;
       float m = -INFINITY, ssum = 0.f;
       int am = 0x7fffffff;

@@ -50,8 +50,13 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
 size_t ce_workspace_bytes(int batch, int L, int vocab);
 cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* targets,
                            int batch, int L, int hidden, int vocab, float* loss,
-                           float* row_ce, void* workspace, int32_t* status,
+                           float* row_ce, float* row_lse, void* workspace, int32_t* status,
                            cudaStream_t stream);
+size_t ce_grad_workspace_bytes(int batch, int L, int vocab);
+cudaError_t launch_ce_loss_grad(const uint16_t* h, const uint16_t* w, const int32_t* targets,
+                                const float* row_lse, int batch, int L, int hidden, int vocab,
+                                float* dh, float* dw, void* workspace, int32_t* status,
+                                cudaStream_t stream);
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();

@@ -47,6 +47,10 @@ size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, in
     if (vocab <= 0 || max_len < 1) return 0;
     return mars::ce_workspace_bytes(batch, max_len, vocab);
   }
+  if (op == MARS_OP_CE_LOSS_GRAD) {
+    if (vocab <= 0 || max_len < 1) return 0;
+    return mars::ce_grad_workspace_bytes(batch, max_len, vocab);
+  }
   return 0;
 }
 
@@ -174,7 +178,7 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
 
 int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32_t* targets,
                              int batch, int L, int hidden, int vocab, float* loss,
-                             float* row_ce, void* workspace, size_t ws_bytes,
+                             float* row_ce, float* row_lse, void* workspace, size_t ws_bytes,
                              int32_t* status, void* stream) {
   if (batch < 0 || L < 1 || hidden < 8 || vocab < 1) return MARS_EINVAL;
   if (hidden % 8) return MARS_EUNSUPPORTED;
@@ -186,7 +190,25 @@ int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32
   if (!aligned16(h) || !aligned16(w) || !aligned16(workspace)) return MARS_EALIGN;
   if (ws_bytes < mars::ce_workspace_bytes(batch, L, vocab)) return MARS_ENOSPACE;
   return cuda_rc(mars::launch_ce_loss(h, w, targets, batch, L, hidden, vocab, loss, row_ce,
-                                      workspace, status, static_cast<cudaStream_t>(stream)));
+                                      row_lse, workspace, status,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int mars_dual_stream_ce_loss_grad(const mars_bf16* h, const mars_bf16* w,
+                                  const int32_t* targets, const float* row_lse, int batch,
+                                  int L, int hidden, int vocab, float* dh, float* dw,
+                                  void* workspace, size_t ws_bytes, int32_t* status,
+                                  void* stream) {
+  if (batch < 0 || L < 1 || hidden < 8 || vocab < 1) return MARS_EINVAL;
+  if (hidden % 8 || vocab % 8) return MARS_EUNSUPPORTED;
+  if ((long long)batch * 2 * L > 0x7fffffffLL) return MARS_EINVAL;
+  if (batch == 0) return MARS_OK;
+  if (!h || !w || !targets || !row_lse || !workspace) return MARS_EINVAL;
+  if (!aligned16(h) || !aligned16(w) || !aligned16(workspace)) return MARS_EALIGN;
+  if (ws_bytes < mars::ce_grad_workspace_bytes(batch, L, vocab)) return MARS_ENOSPACE;
+  return cuda_rc(mars::launch_ce_loss_grad(h, w, targets, row_lse, batch, L, hidden, vocab, dh,
+                                           dw, workspace, status,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 const char* mars_strerror(int code) {

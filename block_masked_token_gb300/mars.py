@@ -17,7 +17,7 @@ _lib = None
 
 OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ENOSPACE = 0, -1, -2, -3, -4, -5
 ST_NOPAGE, ST_OVERFLOW, ST_TIMEOUT, ST_BADTARGET = 1, 2, 4, 8
-OP_DECODE_ATTN, OP_HEAD_ACCEPT, OP_CE_LOSS = 1, 2, 3
+OP_DECODE_ATTN, OP_HEAD_ACCEPT, OP_CE_LOSS, OP_CE_LOSS_GRAD = 1, 2, 3, 4
 PAGE_SIZE = 16
 
 
@@ -52,7 +52,9 @@ def lib() -> ctypes.CDLL:
         L.mars_kv_commit_batch_sync.restype = I
         L.mars_kv_commit_batch_sync.argtypes = L.mars_kv_commit.argtypes
         L.mars_dual_stream_ce_loss.restype = I
-        L.mars_dual_stream_ce_loss.argtypes = [P, P, P, I, I, I, I, P, P, P, S, P, P]
+        L.mars_dual_stream_ce_loss.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, P, P]
+        L.mars_dual_stream_ce_loss_grad.restype = I
+        L.mars_dual_stream_ce_loss_grad.argtypes = [P, P, P, P, I, I, I, I, P, P, P, S, P, P]
         L.mars_strerror.restype = ctypes.c_char_p
         L.mars_strerror.argtypes = [I]
         L.mars_version.restype = ctypes.c_char_p
@@ -65,7 +67,8 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("mars_workspace_bytes", "mars_attn_dual_stream", "mars_decode_attn",
             "mars_head_accept", "mars_head_accept_per_request", "mars_kv_commit",
-            "mars_kv_commit_batch_sync", "mars_dual_stream_ce_loss", "mars_strerror",
+            "mars_kv_commit_batch_sync", "mars_dual_stream_ce_loss",
+            "mars_dual_stream_ce_loss_grad", "mars_strerror",
             "mars_version", "mars_launch_count")
 
 
@@ -220,7 +223,7 @@ def mars_kv_commit_batch_sync(k_blk, v_blk, n_accept, seq_lens, block_table, k_p
 
 
 def mars_dual_stream_ce_loss(h, w, targets, batch: int, L: int, loss, workspace, row_ce=None,
-                             status=None, stream=None):
+                             row_lse=None, status=None, stream=None):
     rows, hidden = h.shape
     vocab = w.shape[0]
     _check(h, "h", torch.bfloat16, (batch * 2 * L, hidden))
@@ -228,11 +231,35 @@ def mars_dual_stream_ce_loss(h, w, targets, batch: int, L: int, loss, workspace,
     _check(targets, "targets", torch.int32, (batch * 2 * L,))
     _check(loss, "loss", torch.float32, (3,))
     _check(workspace, "workspace", torch.uint8)
-    if row_ce is not None:
-        _check(row_ce, "row_ce", torch.float32, (batch * 2 * L,))
+    for t, name in ((row_ce, "row_ce"), (row_lse, "row_lse")):
+        if t is not None:
+            _check(t, name, torch.float32, (batch * 2 * L,))
     if status is not None:
         _check(status, "status", torch.int32, (1,))
     _rc(lib().mars_dual_stream_ce_loss(_ptr(h), _ptr(w), _ptr(targets), batch, L, hidden,
-                                       vocab, _ptr(loss), _ptr(row_ce), _ptr(workspace),
-                                       workspace.numel(), _ptr(status), _stream(stream)),
+                                       vocab, _ptr(loss), _ptr(row_ce), _ptr(row_lse),
+                                       _ptr(workspace), workspace.numel(), _ptr(status),
+                                       _stream(stream)),
         "mars_dual_stream_ce_loss")
+
+
+def mars_dual_stream_ce_loss_grad(h, w, targets, row_lse, batch: int, L: int, workspace,
+                                  dh=None, dw=None, status=None, stream=None):
+    rows, hidden = h.shape
+    vocab = w.shape[0]
+    _check(h, "h", torch.bfloat16, (batch * 2 * L, hidden))
+    _check(w, "w", torch.bfloat16, (vocab, hidden))
+    _check(targets, "targets", torch.int32, (batch * 2 * L,))
+    _check(row_lse, "row_lse", torch.float32, (batch * 2 * L,))
+    _check(workspace, "workspace", torch.uint8)
+    if dh is not None:
+        _check(dh, "dh", torch.float32, (batch * 2 * L, hidden))
+    if dw is not None:
+        _check(dw, "dw", torch.float32, (vocab, hidden))
+    if status is not None:
+        _check(status, "status", torch.int32, (1,))
+    _rc(lib().mars_dual_stream_ce_loss_grad(_ptr(h), _ptr(w), _ptr(targets), _ptr(row_lse),
+                                            batch, L, hidden, vocab, _ptr(dh), _ptr(dw),
+                                            _ptr(workspace), workspace.numel(), _ptr(status),
+                                            _stream(stream)),
+        "mars_dual_stream_ce_loss_grad")

@@ -54,11 +54,13 @@ typedef uint16_t mars_bf16;
 #define MARS_OP_DECODE_ATTN 1
 #define MARS_OP_HEAD_ACCEPT 2
 #define MARS_OP_CE_LOSS 3
+#define MARS_OP_CE_LOSS_GRAD 4
 
 /* Workspace (device scratch, caller-allocated, >= 256-byte aligned) needed by `op`.
  * MARS_OP_DECODE_ATTN uses batch, B, hq, hkv, d, max_len (the max_len_hint of the call);
- * MARS_OP_HEAD_ACCEPT uses batch, B, vocab; MARS_OP_CE_LOSS uses batch, vocab and max_len
- * as the stream length L (B must still be in [1, 32]). Other arguments are ignored.
+ * MARS_OP_HEAD_ACCEPT uses batch, B, vocab; MARS_OP_CE_LOSS and MARS_OP_CE_LOSS_GRAD use
+ * batch, vocab and max_len as the stream length L (B must still be in [1, 32]). Other
+ * arguments are ignored.
  * Returns 0 for an unknown op or invalid sizes. */
 size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
                             int vocab, int max_len);
@@ -198,14 +200,34 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
  *   targets   [batch*2L] int32          target word per row, or -1
  *   loss      [3] float (written)       {L_mask, L_AR, L_mask + L_AR}
  *   row_ce    [batch*2L] float or NULL  ce_r per row (0 for rows without a target)
+ *   row_lse   [batch*2L] float or NULL  log sum_v exp(l_rv) per row (every row), the input
+ *                                       of mars_dual_stream_ce_loss_grad
  *   workspace >= mars_workspace_bytes(MARS_OP_CE_LOSS, batch, 1, 0, 0, 0, 0, vocab, L)
  * hidden % 8 == 0. A target outside [-1, vocab) leaves its row out and flags
  * MARS_ST_BADTARGET. The sums run in a fixed order (float64), so repeated calls agree
- * bit for bit. status may be NULL. Forward only: no gradient is produced. */
+ * bit for bit. status may be NULL. The gradient is mars_dual_stream_ce_loss_grad. */
 int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32_t* targets,
                              int batch, int L, int hidden, int vocab, float* loss,
-                             float* row_ce, void* workspace, size_t ws_bytes,
+                             float* row_ce, float* row_lse, void* workspace, size_t ws_bytes,
                              int32_t* status, void* stream);
+
+/* Gradient of L = L_mask + L_AR (as defined for mars_dual_stream_ce_loss) with respect to
+ * h and W: dL/dl_rv = (softmax(l_r)_v - [v = y_r]) / N_x for a row of stream x with a
+ * target (N_x = the rows of that stream with a target) and 0 for the others;
+ * dh = dlogits W, dW = dlogits^T h. The logits are recomputed by the LM-head GEMM, whose
+ * epilogue writes dlogits in bf16 to the workspace using row_lse from the forward call;
+ * the two products are plain cuBLAS GEMMs (bf16 inputs, fp32 accumulate and output).
+ *   row_lse   [batch*2L] float          from mars_dual_stream_ce_loss
+ *   dh        [batch*2L, hidden] float or NULL (written)
+ *   dw        [vocab, hidden] float or NULL    (written)
+ *   workspace >= mars_workspace_bytes(MARS_OP_CE_LOSS_GRAD, batch, 1, 0, 0, 0, 0, vocab, L)
+ *             (about batch*2L*vocab*2 bytes: the bf16 dlogits)
+ * hidden % 8 == 0 and vocab % 8 == 0. */
+int mars_dual_stream_ce_loss_grad(const mars_bf16* h, const mars_bf16* w,
+                                  const int32_t* targets, const float* row_lse, int batch,
+                                  int L, int hidden, int vocab, float* dh, float* dw,
+                                  void* workspace, size_t ws_bytes, int32_t* status,
+                                  void* stream);
 
 /* Human-readable name of a return code. Never NULL. */
 const char* mars_strerror(int code);

@@ -9,6 +9,7 @@ from .mars_oracle import (  # noqa: F401
     attn_dual_stream,
     beta,
     ce_loss_dual,
+    ce_loss_dual_grad,
     decode_attn,
     gather_prefix,
     head_accept,

@@ -349,3 +349,27 @@ def ce_loss_dual(h, w_vocab_major, targets, batch: int, L: int):
     l_ar = ce[clean].mean() if clean.any() else 0.0
     l_mask = ce[masked].mean() if masked.any() else 0.0
     return float(l_mask), float(l_ar), ce
+
+
+def ce_loss_dual_grad(h, w_vocab_major, targets, batch: int, L: int):
+    """Gradient of L = L_mask + L_AR (ce_loss_dual) with respect to the logits, h and W:
+    dL/dl_rv = (softmax(l_r)_v - [v = y_r]) / N_x for a row of stream x with a target
+    (N_x = that stream's rows with a target), 0 for rows without one; dh = dlogits W and
+    dW = dlogits^T h. Returns (dh [R, H], dW [V, H], dlogits [R, V])."""
+    logits = head_logits(h, w_vocab_major)
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    p /= p.sum(axis=1, keepdims=True)
+    y = np.asarray(targets, dtype=np.int64)
+    V = logits.shape[1]
+    valid = (y >= 0) & (y < V)
+    pos = np.arange(len(y)) % (2 * L)
+    n_clean = int((valid & (pos < L)).sum())
+    n_masked = int((valid & (pos >= L)).sum())
+    scale = np.where(pos < L, 1.0 / max(n_clean, 1), 1.0 / max(n_masked, 1))
+    scale = np.where(valid, scale, 0.0)
+    g = p.copy()
+    rows = np.flatnonzero(valid)
+    g[rows, y[rows]] -= 1.0
+    g *= scale[:, None]
+    return g @ w_vocab_major, g.T @ h, g

@@ -98,10 +98,15 @@ def test_host_validation_codes(L):
     assert L.mars_head_accept_per_request(P, P, 1, 4, 256, 512, P, P, P, P, P, 16, None, None) == mars.ENOSPACE
     assert L.mars_head_accept_per_request(P, _p(20), 1, 4, 256, 512, P, P, P, P, P, 1 << 20, None, None) == mars.EALIGN
     # loss: null loss pointer, hidden not a multiple of 8, workspace too small, L < 1
-    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, None, None, P, 1 << 30, None, None) == mars.EINVAL
-    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 60, 100, P, None, P, 1 << 30, None, None) == mars.EUNSUPPORTED
-    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, P, None, P, 16, None, None) == mars.ENOSPACE
-    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 0, 64, 100, P, None, P, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, None, None, None, P, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 60, 100, P, None, None, P, 1 << 30, None, None) == mars.EUNSUPPORTED
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, P, None, None, P, 16, None, None) == mars.ENOSPACE
+    assert L.mars_dual_stream_ce_loss(P, P, P, 1, 0, 64, 100, P, None, None, P, 1 << 30, None, None) == mars.EINVAL
+    # loss gradient: vocabulary not a multiple of 8, null row_lse, workspace too small
+    assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 100, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
+    assert L.mars_dual_stream_ce_loss_grad(P, P, P, None, 1, 4, 64, 96, P, P, P, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 96, P, P, P, 16, None, None) == mars.ENOSPACE
+    assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 0, 4, 64, 96, P, P, P, 16, None, None) == mars.OK
     # commit (both policies): page size, null pool, B out of range
     for fn in (L.mars_kv_commit, L.mars_kv_commit_batch_sync):
         assert fn(P, P, P, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 8, None, None) == mars.EUNSUPPORTED

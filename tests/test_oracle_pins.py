@@ -458,6 +458,50 @@ def test_ce_loss_against_torch_cross_entropy():
         assert abs(got - float(ref)) < 1e-12
 
 
+def test_ce_loss_grad_matches_finite_differences():
+    """Central differences of the oracle's own loss (a property of the mathematics, not of
+    the gradient formula) match dh and dW entry by entry."""
+    V, H, b, L = 11, 5, 2, 3
+    h = _rand((b * 2 * L, H), 83)
+    w = _rand((V, H), 84)
+    y = np.random.default_rng(3).integers(-1, V, b * 2 * L)
+    dh, dw, _ = oracle.ce_loss_dual_grad(h, w, y, b, L)
+    eps = 1e-6
+
+    def total(hh, ww):
+        lm, la, _ = oracle.ce_loss_dual(hh, ww, y, b, L)
+        return lm + la
+
+    for (r, k) in [(0, 0), (3, 4), (7, 2), (11, 1)]:
+        hp, hm = h.copy(), h.copy()
+        hp[r, k] += eps
+        hm[r, k] -= eps
+        assert abs((total(hp, w) - total(hm, w)) / (2 * eps) - dh[r, k]) < 1e-7
+    for (v, k) in [(0, 0), (5, 3), (10, 4)]:
+        wp, wm = w.copy(), w.copy()
+        wp[v, k] += eps
+        wm[v, k] -= eps
+        assert abs((total(h, wp) - total(h, wm)) / (2 * eps) - dw[v, k]) < 1e-7
+
+
+def test_ce_loss_grad_against_torch_autograd():
+    V, H, b, L = 40, 6, 2, 4
+    h = _rand((b * 2 * L, H), 85)
+    w = _rand((V, H), 86)
+    y = np.random.default_rng(4).integers(-1, V, b * 2 * L)
+    dh, dw, _ = oracle.ce_loss_dual_grad(h, w, y, b, L)
+    ht = torch.tensor(h, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    yt = torch.tensor(y)
+    logits = ht @ wt.T
+    pos = torch.arange(b * 2 * L) % (2 * L)
+    loss = (torch.nn.functional.cross_entropy(logits[pos >= L], yt[pos >= L], ignore_index=-1) +
+            torch.nn.functional.cross_entropy(logits[pos < L], yt[pos < L], ignore_index=-1))
+    loss.backward()
+    np.testing.assert_allclose(dh, ht.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
 # ------------------------------------------- planted mistakes: each must fail some pin
 
 def test_planted_floor_block_index_is_caught(monkeypatch):

@@ -444,7 +444,7 @@ def run_ce(h, w, y, batch, L, row_ce=True):
     ce = torch.empty(batch * 2 * L, dtype=torch.float32, device=DEV) if row_ce else None
     ws = _ws(mars.mars_workspace_bytes(mars.OP_CE_LOSS, batch, 1, vocab=w.shape[0], max_len=L))
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    mars.mars_dual_stream_ce_loss(h, w, y, batch, L, loss, ws, ce, st)
+    mars.mars_dual_stream_ce_loss(h, w, y, batch, L, loss, ws, row_ce=ce, status=st)
     torch.cuda.synchronize()
     return loss.cpu().numpy(), (ce.cpu().numpy() if row_ce else None), int(st.item())
 
@@ -495,6 +495,89 @@ def test_ce_loss_7b_shapes_sampled_rows():
     ok = y >= 0
     assert abs(loss[0] - ce[ok & (pos >= 512)].astype(np.float64).mean()) < 1e-5
     assert abs(loss[1] - ce[ok & (pos < 512)].astype(np.float64).mean()) < 1e-5
+
+
+GRAD_TOL = 5e-3      # dlogits rounded to bf16 (2^-9 relative) before the two GEMMs
+
+
+def run_ce_grad(h, w, y, batch, L):
+    rows = batch * 2 * L
+    loss = torch.empty(3, dtype=torch.float32, device=DEV)
+    lse = torch.empty(rows, dtype=torch.float32, device=DEV)
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_CE_LOSS, batch, 1, vocab=w.shape[0], max_len=L))
+    mars.mars_dual_stream_ce_loss(h, w, y, batch, L, loss, ws, row_lse=lse)
+    wg = _ws(mars.mars_workspace_bytes(mars.OP_CE_LOSS_GRAD, batch, 1, vocab=w.shape[0],
+                                       max_len=L))
+    dh = torch.empty(rows, h.shape[1], dtype=torch.float32, device=DEV)
+    dw = torch.empty(w.shape, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mars.mars_dual_stream_ce_loss_grad(h, w, y, lse, batch, L, wg, dh, dw, st)
+    torch.cuda.synchronize()
+    return dh.cpu().numpy(), dw.cpu().numpy(), lse.cpu().numpy(), int(st.item())
+
+
+def _rel(got, ref):
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+@pytest.mark.parametrize("batch,L,H,V", [(2, 96, 256, 1000), (1, 130, 64, 264), (3, 1, 128, 296)])
+def test_ce_loss_grad_small(batch, L, H, V):
+    cfg = W.CELossConfig("g", batch, L, H, V)
+    x = W.make_ce_inputs(cfg, seed=L * 3 + V)
+    y = x["targets"].clone()
+    y[::7] = -1
+    dh, dw, lse, st = run_ce_grad(x["h"].to(DEV), x["w"].to(DEV), y.to(DEV), batch, L)
+    assert st == 0
+    rdh, rdw, _ = oracle.ce_loss_dual_grad(f64(x["h"]), f64(x["w"]), y.numpy(), batch, L)
+    assert _rel(dh, rdh) < GRAD_TOL and _rel(dw, rdw) < GRAD_TOL
+    assert np.abs(dh - rdh).max() <= 4 * GRAD_TOL * np.abs(rdh).max()
+    assert np.abs(dw - rdw).max() <= 4 * GRAD_TOL * np.abs(rdw).max()
+    logits = f64(x["h"]) @ f64(x["w"]).T
+    m = logits.max(axis=1)
+    rlse = m + np.log(np.exp(logits - m[:, None]).sum(axis=1))
+    np.testing.assert_allclose(lse, rlse, rtol=0, atol=LOSS_TOL)
+
+
+def test_ce_loss_grad_7b_shapes_sampled():
+    """Hidden 3584, vocabulary 152064, 512 rows: dh on sampled rows, dW on sampled words
+    (the reference still needs every row's log-sum-exp, computed here in chunks)."""
+    cfg = W.CELossConfig("g7", 1, 256, 3584, 152064)
+    x = W.make_ce_inputs(cfg, seed=1, device=DEV)
+    dh, dw, lse, st = run_ce_grad(x["h"], x["w"], x["targets"], 1, 256)
+    assert st == 0
+    h, w = f64(x["h"]), f64(x["w"])
+    y = x["targets"].cpu().numpy()
+    rows = sorted({0, 1, 255, 256, 257, 511, *np.random.default_rng(5).integers(0, 512, 10).tolist()})
+    words = sorted({0, 1, 152063, *y[y >= 0][:6].tolist(),
+                    *np.random.default_rng(6).integers(0, 152064, 6).tolist()})
+    # exact log-sum-exp of every row (chunked over the vocabulary), then the gradient
+    lse_ref = np.empty(512)
+    for r0 in range(0, 512, 64):
+        lg = h[r0:r0 + 64] @ w.T
+        m = lg.max(axis=1)
+        lse_ref[r0:r0 + 64] = m + np.log(np.exp(lg - m[:, None]).sum(axis=1))
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=LOSS_TOL)
+    valid = y >= 0
+    pos = np.arange(512) % 512
+    scale = np.where(pos < 256, 1.0 / (valid & (pos < 256)).sum(), 1.0 / (valid & (pos >= 256)).sum())
+    scale = np.where(valid, scale, 0.0)
+
+    def grad_rows(rr):
+        g = np.exp(h[rr] @ w.T - lse_ref[rr][:, None])
+        for i, r in enumerate(rr):
+            if valid[r]:
+                g[i, y[r]] -= 1.0
+        return g * scale[rr][:, None]
+
+    rdh = grad_rows(rows) @ w
+    assert _rel(dh[rows], rdh) < GRAD_TOL
+    lg = h @ w[words].T                                   # [512, words]
+    g = np.exp(lg - lse_ref[:, None])
+    for j, v in enumerate(words):
+        g[(y == v) & valid, j] -= 1.0
+    g *= scale[:, None]
+    rdw = g.T @ h
+    assert _rel(dw[words], rdw) < GRAD_TOL
 
 
 # -------------------------------------------------------------- whole decode step chain
