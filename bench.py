@@ -594,7 +594,34 @@ def run_dual(device, peaks, reps=10, warm=3):
     t = statistics.median(times)
     fl = dual_flops(cfg)
     tf = fl / t / 1e12
-    return {"workload": cfg.name, "ms": t * 1e3, "tflops": tf,
+    # the gradient of the same attention (training step), upstream gradient ~ N(0, 1)
+    d_o = torch.randn(o.shape, device=device)
+    ws = torch.empty(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, cfg.batch, 1, cfg.hq,
+                                               cfg.hkv, cfg.d, max_len=cfg.L),
+                     dtype=torch.uint8, device=device)
+    dq = torch.empty(o.shape, dtype=torch.float32, device=device)
+    dk = torch.empty(x["k"].shape, dtype=torch.float32, device=device)
+    dv = torch.empty(x["v"].shape, dtype=torch.float32, device=device)
+    for _ in range(warm):
+        mars.mars_attn_dual_stream_grad(x["q"], x["k"], x["v"], o, d_o, cfg.L, cfg.B, dq, dk,
+                                        dv, ws)
+    gt = []
+    for _ in range(max(3, reps // 2)):
+        a, b = _ev(), _ev()
+        a.record()
+        mars.mars_attn_dual_stream_grad(x["q"], x["k"], x["v"], o, d_o, cfg.L, cfg.B, dq, dk,
+                                        dv, ws)
+        b.record()
+        torch.cuda.synchronize()
+        gt.append(a.elapsed_time(b) / 1e3)
+    tg = statistics.median(gt)
+    del ws, dq, dk, dv, d_o
+    torch.cuda.empty_cache()
+    grad = {"ms": tg * 1e3, "tflops": 2.5 * fl / tg / 1e12,
+            "frac_tensor": 2.5 * fl / tg / 1e12 / peaks["bf16_tflops"],
+            "note": "10 d flop per visible pair (S again, dP, dV, dK, dQ); products are cuBLAS "
+                    "GEMMs over the dense 2L x 2L matrices of each kv group"}
+    return {"workload": cfg.name, "ms": t * 1e3, "tflops": tf, "grad": grad,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
                          "traffic": TRAFFIC_DUAL_STREAM,

@@ -16,7 +16,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmars.so")
 
 SOURCES = ["mars_api.cu", "kv_commit.cu", "decode_attn.cu", "head_accept.cu", "dual_stream.cu",
-           "tmap.cu", "head_accept_noalloc.cu", "ce_loss.cu"]
+           "tmap.cu", "head_accept_noalloc.cu", "ce_loss.cu", "dual_stream_grad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

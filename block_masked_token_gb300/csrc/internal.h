@@ -46,6 +46,13 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
                                int32_t* tokens, float* maxprob, int32_t* n_accept,
                                void* workspace, int32_t* status, cudaStream_t stream);
 
+// ---- Gradient of the dual-stream attention (cuBLAS products, materialised per kv group).
+size_t dual_grad_workspace_bytes(int batch, int L, int hq, int hkv, int d);
+cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const float* o, const float* d_o, int batch, int L, int B,
+                                    int hq, int hkv, int d, float scale, float* dq, float* dk,
+                                    float* dv, void* workspace, cudaStream_t stream);
+
 // ---- Dual-stream training loss (L_mask + L_AR) over the 2L rows of each sequence.
 size_t ce_workspace_bytes(int batch, int L, int vocab);
 cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* targets,

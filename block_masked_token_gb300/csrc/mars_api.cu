@@ -47,6 +47,10 @@ size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, in
     if (vocab <= 0 || max_len < 1) return 0;
     return mars::ce_workspace_bytes(batch, max_len, vocab);
   }
+  if (op == MARS_OP_DUAL_GRAD) {
+    if (check_heads(hq, hkv, d) != MARS_OK || max_len < 1) return 0;
+    return mars::dual_grad_workspace_bytes(batch, max_len, hq, hkv, d);
+  }
   if (op == MARS_OP_CE_LOSS_GRAD) {
     if (vocab <= 0 || max_len < 1) return 0;
     return mars::ce_grad_workspace_bytes(batch, max_len, vocab);
@@ -174,6 +178,28 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
   return kv_commit_checked(k_blk, v_blk, n_accept, seq_lens, block_table, max_pages_per_seq,
                            k_pool, v_pool, num_pages, commit_slots, batch, B, hkv, d,
                            page_size, true, status, stream);
+}
+
+int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                               const float* o, const float* d_o, int batch, int L, int B,
+                               int hq, int hkv, int d, float scale, float* dq, float* dk,
+                               float* dv, void* workspace, size_t ws_bytes, int32_t* status,
+                               void* stream) {
+  (void)status;
+  if (batch < 0 || L < 1 || B < 1) return MARS_EINVAL;
+  int rc = check_heads(hq, hkv, d);
+  if (rc) return rc;
+  if (batch == 0) return MARS_OK;
+  if (!q || !k || !v || !o || !d_o || !dq || !dk || !dv || !workspace) return MARS_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return MARS_EALIGN;
+  if (ws_bytes < mars::dual_grad_workspace_bytes(batch, L, hq, hkv, d)) return MARS_ENOSPACE;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+  if (isinf(scale)) return MARS_EINVAL;
+  return cuda_rc(mars::launch_dual_stream_grad(q, k, v, o, d_o, batch, L, B, hq, hkv, d, scale,
+                                               dq, dk, dv, workspace,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32_t* targets,

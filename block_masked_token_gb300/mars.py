@@ -17,7 +17,7 @@ _lib = None
 
 OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ENOSPACE = 0, -1, -2, -3, -4, -5
 ST_NOPAGE, ST_OVERFLOW, ST_TIMEOUT, ST_BADTARGET = 1, 2, 4, 8
-OP_DECODE_ATTN, OP_HEAD_ACCEPT, OP_CE_LOSS, OP_CE_LOSS_GRAD = 1, 2, 3, 4
+OP_DECODE_ATTN, OP_HEAD_ACCEPT, OP_CE_LOSS, OP_CE_LOSS_GRAD, OP_DUAL_GRAD = 1, 2, 3, 4, 5
 PAGE_SIZE = 16
 
 
@@ -53,6 +53,9 @@ def lib() -> ctypes.CDLL:
         L.mars_kv_commit_batch_sync.argtypes = L.mars_kv_commit.argtypes
         L.mars_dual_stream_ce_loss.restype = I
         L.mars_dual_stream_ce_loss.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, P, P]
+        L.mars_attn_dual_stream_grad.restype = I
+        L.mars_attn_dual_stream_grad.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P,
+                                                 S, P, P]
         L.mars_dual_stream_ce_loss_grad.restype = I
         L.mars_dual_stream_ce_loss_grad.argtypes = [P, P, P, P, I, I, I, I, P, P, P, S, P, P]
         L.mars_strerror.restype = ctypes.c_char_p
@@ -68,7 +71,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("mars_workspace_bytes", "mars_attn_dual_stream", "mars_decode_attn",
             "mars_head_accept", "mars_head_accept_per_request", "mars_kv_commit",
             "mars_kv_commit_batch_sync", "mars_dual_stream_ce_loss",
-            "mars_dual_stream_ce_loss_grad", "mars_strerror",
+            "mars_dual_stream_ce_loss_grad", "mars_attn_dual_stream_grad", "mars_strerror",
             "mars_version", "mars_launch_count")
 
 
@@ -263,3 +266,23 @@ def mars_dual_stream_ce_loss_grad(h, w, targets, row_lse, batch: int, L: int, wo
                                             _ptr(workspace), workspace.numel(), _ptr(status),
                                             _stream(stream)),
         "mars_dual_stream_ce_loss_grad")
+
+
+def mars_attn_dual_stream_grad(q, k, v, o, d_o, L: int, B: int, dq, dk, dv, workspace,
+                               scale: float = 0.0, status=None, stream=None):
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    _check(q, "q", torch.bfloat16, (b, 2 * L, hq, d))
+    _check(k, "k", torch.bfloat16, (b, 2 * L, hkv, d))
+    _check(v, "v", torch.bfloat16, (b, 2 * L, hkv, d))
+    _check(o, "o", torch.float32, (b, 2 * L, hq, d))
+    _check(d_o, "d_o", torch.float32, (b, 2 * L, hq, d))
+    _check(dq, "dq", torch.float32, (b, 2 * L, hq, d))
+    _check(dk, "dk", torch.float32, (b, 2 * L, hkv, d))
+    _check(dv, "dv", torch.float32, (b, 2 * L, hkv, d))
+    _check(workspace, "workspace", torch.uint8)
+    _rc(lib().mars_attn_dual_stream_grad(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), b, L,
+                                         B, hq, hkv, d, float(scale), _ptr(dq), _ptr(dk),
+                                         _ptr(dv), _ptr(workspace), workspace.numel(),
+                                         _ptr(status), _stream(stream)),
+        "mars_attn_dual_stream_grad")

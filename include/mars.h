@@ -55,11 +55,13 @@ typedef uint16_t mars_bf16;
 #define MARS_OP_HEAD_ACCEPT 2
 #define MARS_OP_CE_LOSS 3
 #define MARS_OP_CE_LOSS_GRAD 4
+#define MARS_OP_DUAL_GRAD 5
 
 /* Workspace (device scratch, caller-allocated, >= 256-byte aligned) needed by `op`.
  * MARS_OP_DECODE_ATTN uses batch, B, hq, hkv, d, max_len (the max_len_hint of the call);
  * MARS_OP_HEAD_ACCEPT uses batch, B, vocab; MARS_OP_CE_LOSS and MARS_OP_CE_LOSS_GRAD use
- * batch, vocab and max_len as the stream length L (B must still be in [1, 32]). Other
+ * batch, vocab and max_len as the stream length L; MARS_OP_DUAL_GRAD uses batch, hq, hkv,
+ * d and max_len as L (for these three, pass B = 1: it must still be in [1, 32]). Other
  * arguments are ignored.
  * Returns 0 for an unknown op or invalid sizes. */
 size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
@@ -186,6 +188,25 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
                               mars_bf16* k_pool, mars_bf16* v_pool, int num_pages,
                               int32_t* commit_slots, int batch, int B, int hkv, int d,
                               int page_size, int32_t* status, void* stream);
+
+/* Gradient of mars_attn_dual_stream (the training step's backward of the attention under
+ * M, [notes] Key design 1 and overall framework): for upstream gradient dO, per (batch,
+ * query head) with P = softmax(scale Q K^T + M): dQ = scale dS K, and per kv head
+ * dK = scale sum dS^T Q, dV = sum P^T dO over its query heads, where dS = P * (dP - D),
+ * dP = dO V^T, D_i = sum_c dO_ic O_ic.
+ *   q [b, 2L, hq, d], k, v [b, 2L, hkv, d] bf16   the forward's inputs
+ *   o, d_o [b, 2L, hq, d] float                   the forward's output and its gradient
+ *   dq [b, 2L, hq, d], dk, dv [b, 2L, hkv, d] float (written)
+ *   workspace >= mars_workspace_bytes(MARS_OP_DUAL_GRAD, b, 1, hq, hkv, d, 0, 0, L) bytes:
+ *             one kv group's 2L x 2L scores (fp32) and probabilities (bf16), dO in bf16
+ * The products are cuBLAS GEMMs (bf16 inputs, fp32 accumulate); the masked softmax and
+ * dS are libmars kernels. P and dS are rounded to bf16 before their products.
+ * scale <= 0 means 1/sqrt(d). status may be NULL (no device-side checks). */
+int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                               const float* o, const float* d_o, int batch, int L, int B,
+                               int hq, int hkv, int d, float scale, float* dq, float* dk,
+                               float* dv, void* workspace, size_t ws_bytes, int32_t* status,
+                               void* stream);
 
 /* Dual-stream training loss L = L_mask + L_AR ([notes] Key design 2: the masked-stream
  * cross-entropy plus the clean-stream next-token cross-entropy; [gist] 2.B "Combined

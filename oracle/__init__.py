@@ -7,6 +7,7 @@ from .mars_oracle import (  # noqa: F401
     accept_count,
     ar_signal_fraction,
     attn_dual_stream,
+    attn_dual_stream_grad,
     beta,
     ce_loss_dual,
     ce_loss_dual_grad,

@@ -165,6 +165,34 @@ def attn_dual_stream(q, k, v, L: int, B: int, scale: float | None = None, rows=N
     return out
 
 
+def attn_dual_stream_grad(q, k, v, do, L: int, B: int, scale: float | None = None):
+    """Gradient of the dual-stream attention (attn_dual_stream) for an upstream gradient
+    dO [b, 2L, Hq, D]: per (batch, query head h), with kv head h // (Hq/Hkv),
+    P = masked softmax of S = scale Q K^T, dP = dO V^T, dS = P * (dP - rowsum(P * dP)),
+    dQ = scale dS K, and summed over the query heads of a kv head dK = scale dS^T Q,
+    dV = P^T dO. Returns (dq [b, 2L, Hq, D], dk [b, 2L, Hkv, D], dv [b, 2L, Hkv, D])."""
+    b, n, Hq, D = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    vis = mask_M(L, B)
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for bi in range(b):
+        for h in range(Hq):
+            hk = h // g
+            Q, K, V, dO = q[bi, :, h, :], k[bi, :, hk, :], v[bi, :, hk, :], do[bi, :, h, :]
+            P = _masked_softmax_rows(scale * (Q @ K.T), vis)
+            dP = dO @ V.T
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dq[bi, :, h, :] = scale * (dS @ K)
+            dk[bi, :, hk, :] += scale * (dS.T @ Q)
+            dv[bi, :, hk, :] += P.T @ dO
+    return dq, dk, dv
+
+
 # ---------------------------------------------------------------------------------------
 # Decode form ([gist] 2.C, 2.D; [notes] Key design 3, Key design 4): B [MASK] queries per
 # sequence over the committed prefix in a paged cache, causal inside the block.

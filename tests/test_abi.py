@@ -102,6 +102,11 @@ def test_host_validation_codes(L):
     assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 60, 100, P, None, None, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_dual_stream_ce_loss(P, P, P, 1, 4, 64, 100, P, None, None, P, 16, None, None) == mars.ENOSPACE
     assert L.mars_dual_stream_ce_loss(P, P, P, 1, 0, 64, 100, P, None, None, P, 1 << 30, None, None) == mars.EINVAL
+    # attention gradient: unsupported head dim, null output, workspace too small
+    ga = [P, P, P, P, P, 1, 8, 2, 4, 2]
+    assert L.mars_attn_dual_stream_grad(*ga, 96, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
+    assert L.mars_attn_dual_stream_grad(*ga, 64, 0.0, None, P, P, P, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream_grad(*ga, 64, 0.0, P, P, P, P, 16, None, None) == mars.ENOSPACE
     # loss gradient: vocabulary not a multiple of 8, null row_lse, workspace too small
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 100, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, None, 1, 4, 64, 96, P, P, P, 1 << 30, None, None) == mars.EINVAL

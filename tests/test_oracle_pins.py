@@ -502,6 +502,51 @@ def test_ce_loss_grad_against_torch_autograd():
     np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_dual_stream_grad_matches_finite_differences():
+    """Central differences of <O, dO> computed by the forward oracle match dQ, dK, dV."""
+    b, L, B, Hq, Hkv, D = 1, 5, 2, 4, 2, 3
+    q = _rand((b, 2 * L, Hq, D), 87)
+    k = _rand((b, 2 * L, Hkv, D), 88)
+    v = _rand((b, 2 * L, Hkv, D), 89)
+    do = _rand((b, 2 * L, Hq, D), 90)
+    dq, dk, dv = oracle.attn_dual_stream_grad(q, k, v, do, L, B)
+    eps = 1e-6
+
+    def f(qq, kk, vv):
+        return float((oracle.attn_dual_stream(qq, kk, vv, L, B) * do).sum())
+
+    for arr, grad, idx in ((q, dq, [(0, 0, 0, 0), (0, 7, 3, 2), (0, 9, 1, 1)]),
+                           (k, dk, [(0, 1, 0, 0), (0, 6, 1, 2), (0, 9, 1, 1)]),
+                           (v, dv, [(0, 0, 0, 1), (0, 5, 1, 0), (0, 8, 0, 2)])):
+        for ix in idx:
+            p_, m_ = arr.copy(), arr.copy()
+            p_[ix] += eps
+            m_[ix] -= eps
+            args_p = [p_ if a is arr else a for a in (q, k, v)]
+            args_m = [m_ if a is arr else a for a in (q, k, v)]
+            fd = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert abs(fd - grad[ix]) < 1e-7, (ix, fd, grad[ix])
+
+
+def test_dual_stream_grad_against_torch_autograd():
+    b, L, B, Hq, Hkv, D = 2, 6, 4, 4, 2, 8
+    q = _rand((b, 2 * L, Hq, D), 91)
+    k = _rand((b, 2 * L, Hkv, D), 92)
+    v = _rand((b, 2 * L, Hkv, D), 93)
+    do = _rand((b, 2 * L, Hq, D), 94)
+    dq, dk, dv = oracle.attn_dual_stream_grad(q, k, v, do, L, B)
+    qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    mask = torch.tensor(oracle.mask_M(L, B))
+    rep = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt.transpose(1, 2), kt.repeat_interleave(rep, dim=2).transpose(1, 2),
+        vt.repeat_interleave(rep, dim=2).transpose(1, 2), attn_mask=mask).transpose(1, 2)
+    (o * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
 # ------------------------------------------- planted mistakes: each must fail some pin
 
 def test_planted_floor_block_index_is_caught(monkeypatch):

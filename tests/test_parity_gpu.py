@@ -131,6 +131,58 @@ def test_dual_stream_divergent_rescale():
     assert_attn_close(o.cpu().numpy(), ref)
 
 
+# Attention gradient: P and dS are rounded to bf16 before their products (2^-9 relative
+# each), and D = rowsum(dO * O) uses the forward kernel's fp32 output.
+ATTN_GRAD_TOL = 2e-2
+
+
+def run_dual_grad(x, L, B):
+    q, k, v = x["q"], x["k"], x["v"]
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    o = run_dual(q, k, v, L, B)
+    g = torch.Generator(device=q.device).manual_seed(17)
+    d_o = torch.randn(o.shape, generator=g, device=q.device)
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, b, 1, hq, hkv, d, max_len=L))
+    dq = torch.empty(o.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    mars.mars_attn_dual_stream_grad(q, k, v, o, d_o, L, B, dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    return d_o, dq, dk, dv
+
+
+@pytest.mark.parametrize("b,L,B,hq,hkv,d", [
+    (1, 8, 2, 2, 1, 64),
+    (2, 37, 4, 4, 2, 64),          # L not a multiple of B
+    (1, 130, 16, 7, 1, 128),       # GQA 7, ragged
+    (1, 64, 64, 2, 2, 128),        # B = L
+])
+def test_dual_stream_grad_small(b, L, B, hq, hkv, d):
+    cfg = W.DualStreamConfig("g", b, L, B, hq, hkv, d)
+    x = W.make_dual_stream_inputs(cfg, seed=L + B)
+    xd = {kk: vv.to(DEV) for kk, vv in x.items()}
+    d_o, dq, dk, dv = run_dual_grad(xd, L, B)
+    rq, rk, rv = oracle.attn_dual_stream_grad(f64(x["q"]), f64(x["k"]), f64(x["v"]),
+                                              d_o.cpu().double().numpy(), L, B)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        err = _rel(got.cpu().numpy(), ref)
+        assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
+
+
+def test_dual_stream_grad_7b_heads_2l2048():
+    """7B head shapes (one kv group of 7 query heads, d 128), 2L = 2048, B = 16."""
+    cfg = W.DualStreamConfig("g7", 1, 1024, 16, 7, 1, 128)
+    x = W.make_dual_stream_inputs(cfg, seed=3)
+    xd = {kk: vv.to(DEV) for kk, vv in x.items()}
+    d_o, dq, dk, dv = run_dual_grad(xd, 1024, 16)
+    rq, rk, rv = oracle.attn_dual_stream_grad(f64(x["q"]), f64(x["k"]), f64(x["v"]),
+                                              d_o.cpu().double().numpy(), 1024, 16)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        err = _rel(got.cpu().numpy(), ref)
+        assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
+
+
 # ------------------------------------------------------------------------ decode attention
 
 def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
