@@ -596,7 +596,7 @@ def run_dual(device, peaks, reps=10, warm=3):
     tf = fl / t / 1e12
     # the gradient of the same attention (training step), upstream gradient ~ N(0, 1)
     d_o = torch.randn(o.shape, device=device)
-    ws = torch.empty(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, cfg.batch, 1, cfg.hq,
+    ws = torch.empty(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, cfg.batch, cfg.B, cfg.hq,
                                                cfg.hkv, cfg.d, max_len=cfg.L),
                      dtype=torch.uint8, device=device)
     dq = torch.empty(o.shape, dtype=torch.float32, device=device)
@@ -620,7 +620,8 @@ def run_dual(device, peaks, reps=10, warm=3):
     grad = {"ms": tg * 1e3, "tflops": 2.5 * fl / tg / 1e12,
             "frac_tensor": 2.5 * fl / tg / 1e12 / peaks["bf16_tflops"],
             "note": "10 d flop per visible pair (S again, dP, dV, dK, dQ); products are cuBLAS "
-                    "GEMMs over the dense 2L x 2L matrices of each kv group"}
+                    "GEMMs over the clean-key block (2L x L) and the masked blocks of each "
+                    "kv group"}
     return {"workload": cfg.name, "ms": t * 1e3, "tflops": tf, "grad": grad,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],

@@ -47,7 +47,7 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
                                void* workspace, int32_t* status, cudaStream_t stream);
 
 // ---- Gradient of the dual-stream attention (cuBLAS products, materialised per kv group).
-size_t dual_grad_workspace_bytes(int batch, int L, int hq, int hkv, int d);
+size_t dual_grad_workspace_bytes(int batch, int L, int B, int hq, int hkv, int d);
 cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                     const float* o, const float* d_o, int batch, int L, int B,
                                     int hq, int hkv, int d, float scale, float* dq, float* dk,

@@ -34,7 +34,12 @@ extern "C" {
 size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
                             int vocab, int max_len) {
   (void)hidden;
-  if (batch <= 0 || B < 1 || B > 32) return 0;
+  if (batch <= 0 || B < 1) return 0;
+  if (op == MARS_OP_DUAL_GRAD) {                 // B is the block size of mask M here
+    if (check_heads(hq, hkv, d) != MARS_OK || max_len < 1) return 0;
+    return mars::dual_grad_workspace_bytes(batch, max_len, B, hq, hkv, d);
+  }
+  if (B > 32) return 0;
   if (op == MARS_OP_DECODE_ATTN) {
     if (check_heads(hq, hkv, d) != MARS_OK || max_len < 0) return 0;
     return mars::plan_decode(batch, B, hq, hkv, d, max_len).ws_bytes;
@@ -46,10 +51,6 @@ size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, in
   if (op == MARS_OP_CE_LOSS) {
     if (vocab <= 0 || max_len < 1) return 0;
     return mars::ce_workspace_bytes(batch, max_len, vocab);
-  }
-  if (op == MARS_OP_DUAL_GRAD) {
-    if (check_heads(hq, hkv, d) != MARS_OK || max_len < 1) return 0;
-    return mars::dual_grad_workspace_bytes(batch, max_len, hq, hkv, d);
   }
   if (op == MARS_OP_CE_LOSS_GRAD) {
     if (vocab <= 0 || max_len < 1) return 0;
@@ -194,7 +195,7 @@ int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mar
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return MARS_EALIGN;
-  if (ws_bytes < mars::dual_grad_workspace_bytes(batch, L, hq, hkv, d)) return MARS_ENOSPACE;
+  if (ws_bytes < mars::dual_grad_workspace_bytes(batch, L, B, hq, hkv, d)) return MARS_ENOSPACE;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
   if (isinf(scale)) return MARS_EINVAL;
   return cuda_rc(mars::launch_dual_stream_grad(q, k, v, o, d_o, batch, L, B, hq, hkv, d, scale,

@@ -60,9 +60,9 @@ typedef uint16_t mars_bf16;
 /* Workspace (device scratch, caller-allocated, >= 256-byte aligned) needed by `op`.
  * MARS_OP_DECODE_ATTN uses batch, B, hq, hkv, d, max_len (the max_len_hint of the call);
  * MARS_OP_HEAD_ACCEPT uses batch, B, vocab; MARS_OP_CE_LOSS and MARS_OP_CE_LOSS_GRAD use
- * batch, vocab and max_len as the stream length L; MARS_OP_DUAL_GRAD uses batch, hq, hkv,
- * d and max_len as L (for these three, pass B = 1: it must still be in [1, 32]). Other
- * arguments are ignored.
+ * batch, vocab and max_len as the stream length L (pass B = 1 for these two);
+ * MARS_OP_DUAL_GRAD uses batch, B (the block size of mask M, any value >= 1), hq, hkv, d
+ * and max_len as L. Other arguments are ignored.
  * Returns 0 for an unknown op or invalid sizes. */
 size_t mars_workspace_bytes(int op, int batch, int B, int hq, int hkv, int d, int hidden,
                             int vocab, int max_len);
@@ -197,8 +197,9 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
  *   q [b, 2L, hq, d], k, v [b, 2L, hkv, d] bf16   the forward's inputs
  *   o, d_o [b, 2L, hq, d] float                   the forward's output and its gradient
  *   dq [b, 2L, hq, d], dk, dv [b, 2L, hkv, d] float (written)
- *   workspace >= mars_workspace_bytes(MARS_OP_DUAL_GRAD, b, 1, hq, hkv, d, 0, 0, L) bytes:
- *             one kv group's 2L x 2L scores (fp32) and probabilities (bf16), dO in bf16
+ *   workspace >= mars_workspace_bytes(MARS_OP_DUAL_GRAD, b, B, hq, hkv, d, 0, 0, L) bytes:
+ *             for one kv group the scores against the clean keys (2L x L) and inside
+ *             the masked blocks (fp32), their probabilities (bf16), and dO in bf16
  * The products are cuBLAS GEMMs (bf16 inputs, fp32 accumulate); the masked softmax and
  * dS are libmars kernels. P and dS are rounded to bf16 before their products.
  * scale <= 0 means 1/sqrt(d). status may be NULL (no device-side checks). */

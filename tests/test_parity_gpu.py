@@ -143,7 +143,7 @@ def run_dual_grad(x, L, B):
     o = run_dual(q, k, v, L, B)
     g = torch.Generator(device=q.device).manual_seed(17)
     d_o = torch.randn(o.shape, generator=g, device=q.device)
-    ws = _ws(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, b, 1, hq, hkv, d, max_len=L))
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, b, B, hq, hkv, d, max_len=L))
     dq = torch.empty(o.shape, dtype=torch.float32, device=q.device)
     dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
     dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
@@ -157,6 +157,8 @@ def run_dual_grad(x, L, B):
     (2, 37, 4, 4, 2, 64),          # L not a multiple of B
     (1, 130, 16, 7, 1, 128),       # GQA 7, ragged
     (1, 64, 64, 2, 2, 128),        # B = L
+    (1, 20, 1, 2, 1, 64),          # B = 1: masked rows see only themselves among masked keys
+    (1, 33, 40, 2, 2, 128),        # B > L: one block
 ])
 def test_dual_stream_grad_small(b, L, B, hq, hkv, d):
     cfg = W.DualStreamConfig("g", b, L, B, hq, hkv, d)
