@@ -471,45 +471,69 @@ def run_gpu(args, rank, world, local):
 
 def run_e2e(runner, inp, cfg, K, Wm, device, dist):
     """Same metric, end to end: every step copies its inputs (q, k_blk, v_blk, h) from
-    pinned host memory to the device and reads tokens, max-probs and N back."""
+    pinned host memory to the device and reads tokens, max-probs and N back. The input
+    copy of step i+1 runs on a second stream while step i computes (two device input
+    buffers), as a serving loop would overlap them; every copy is inside the timed
+    region."""
     nbuf = min(cfg.steps, 4)
     host = []
     for s in range(nbuf):
         host.append([t.cpu().pin_memory() for t in (inp.q[s], inp.k_blk[s], inp.v_blk[s],
                                                      inp.h[s])])
-    dq = [torch.empty_like(t, device=device) for t in host[0]]
+    dbuf = [[torch.empty_like(t, device=device) for t in host[0]] for _ in range(2)]
     out_tok = torch.empty(cfg.batch, cfg.B, dtype=torch.int32).pin_memory()
     out_p = torch.empty(cfg.batch, cfg.B, dtype=torch.float32).pin_memory()
     out_n = torch.empty(cfg.batch, dtype=torch.int32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host[0])
     d2h = sum(t.numel() * t.element_size() for t in (out_tok, out_p, out_n))
+    main = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device=device)
 
-    def one(i):
-        src = host[i % nbuf]
-        for d_, h_ in zip(dq, src):
-            d_.copy_(h_, non_blocking=True)
-        runner.step(i, q=dq[0], kb=dq[1], vb=dq[2], h=dq[3])
-        out_tok.copy_(runner.tokens, non_blocking=True)
-        out_p.copy_(runner.maxprob, non_blocking=True)
-        out_n.copy_(runner.n_acc[i % cfg.steps], non_blocking=True)
+    def loop(n, start=None):
+        copied = [torch.cuda.Event() for _ in range(2)]
+        free = [torch.cuda.Event() for _ in range(2)]
+        used = [False, False]
 
-    for i in range(Wm):
-        one(i)
+        def copy_in(i):
+            b = i % 2
+            with torch.cuda.stream(side):
+                if start is not None and i == 0:
+                    side.wait_event(start)
+                if used[b]:
+                    side.wait_event(free[b])       # the step that last read this buffer
+                for d_, h_ in zip(dbuf[b], host[i % nbuf]):
+                    d_.copy_(h_, non_blocking=True)
+                copied[b].record(side)
+
+        copy_in(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                copy_in(i + 1)
+            main.wait_event(copied[b])
+            runner.step(i, q=dbuf[b][0], kb=dbuf[b][1], vb=dbuf[b][2], h=dbuf[b][3])
+            free[b].record(main)
+            used[b] = True
+            out_tok.copy_(runner.tokens, non_blocking=True)
+            out_p.copy_(runner.maxprob, non_blocking=True)
+            out_n.copy_(runner.n_acc[i % cfg.steps], non_blocking=True)
+
+    loop(Wm)
     torch.cuda.synchronize()
     runner.reset()
     barrier(dist, device)
     start, stop = _ev(), _ev()
     torch.cuda.synchronize()
     start.record()
-    for i in range(K):
-        one(i)
+    loop(K, start)
     stop.record()
     torch.cuda.synchronize()
     sec = start.elapsed_time(stop) / 1e3
     tok = float(runner.n_acc[: min(K, cfg.steps)].sum().item())
     tok, sec = reduce_job(dist, tok, sec, device)
     return {"value": tok / sec, "unit": "accepted tok/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "overlap": "input copy of step i+1 on a second stream during step i"}
 
 
 def run_step_variant(cfg, device, K, Wm, seed):
