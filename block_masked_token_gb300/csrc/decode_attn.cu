@@ -13,7 +13,8 @@
 // (m in log2 units, l, O) to the workspace and a second kernel merges them. Splits are
 // used only when there are fewer (sequence, kv head) pairs than SMs and the prefixes are
 // long (each split at least kMinSplitKeys keys); otherwise there is one split per pair and
-// its CTA writes the normalised output directly.
+// its CTA writes the normalised output directly. When the CTAs take more than one wave, a
+// small kernel first orders the sequences by length so that the longest start first.
 #include <climits>
 
 #include "common.cuh"
@@ -32,11 +33,15 @@ using flash::BQ;
 // with batch 32 and prefixes up to 2048, one split per (sequence, kv head) ran in 33 us
 // against 46-50 us with 2 to 4 splits and the merge.
 constexpr int kMinSplitKeys = 2048;
+// Largest batch whose CTAs are ordered by sequence length (the order is built in shared
+// memory by one CTA); larger batches run in index order.
+constexpr int kMaxOrderBatch = 4096;
 constexpr int kPagesPerTile = BKV / kPageSize;   // 8
 
 struct DecodeArgs {
   const int32_t* block_table;
   const int32_t* seq_lens;
+  const int32_t* order;  // sequences by decreasing length (CTA z -> sequence), or NULL
   float* ws;
   float* o;
   int32_t* status;
@@ -133,7 +138,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   extern __shared__ uint8_t smem_raw[];
   __shared__ flash::Barriers bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sp = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int sp = blockIdx.x, kvh = blockIdx.y;
+  const int s = a.order ? a.order[blockIdx.z] : (int)blockIdx.z;
 
   DecodePolicy<D> pol;
   pol.a = &a;
@@ -259,6 +265,26 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs a) {
   for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = acc[i] * inv;
 }
 
+// Longest sequences first: CTAs start in blockIdx order, so this keeps the long pairs out
+// of the last wave, which otherwise leaves SMs idle while a few long CTAs finish. One CTA;
+// rank_i = #{j : len_j > len_i, or len_j == len_i and j < i}; order[rank_i] = i.
+__global__ void __launch_bounds__(1024) decode_order_kernel(const int32_t* __restrict__ seq_lens,
+                                                            int batch,
+                                                            int32_t* __restrict__ order) {
+  __shared__ int lens[kMaxOrderBatch];
+  for (int i = threadIdx.x; i < batch; i += blockDim.x) lens[i] = seq_lens[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < batch; i += blockDim.x) {
+    const int li = lens[i];
+    int rank = 0;
+    for (int j = 0; j < batch; ++j) {
+      const int lj = lens[j];
+      rank += (lj > li) || (lj == li && j < i);
+    }
+    order[rank] = i;
+  }
+}
+
 template <int D>
 cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
                       const uint16_t* k_pool, const uint16_t* v_pool, DecodeArgs& a, int batch,
@@ -327,7 +353,10 @@ DecodePlan plan_decode(int batch, int B, int hq, int hkv, int d, int max_len) {
   p.nsplit = (int)((T + per - 1) / per);
   if (p.nsplit < 1) p.nsplit = 1;
   p.rows = (hq / hkv) * B;
-  p.ws_bytes = (size_t)batch * hkv * p.nsplit * p.rows * (d + 4) * sizeof(float);
+  // more than one wave of CTAs: order the sequences by length (see decode_order_kernel)
+  p.ordered = pairs * p.nsplit > sms && batch > 1 && batch <= kMaxOrderBatch;
+  p.order_bytes = p.ordered ? ((size_t)batch * sizeof(int32_t) + 255) / 256 * 256 : 0;
+  p.ws_bytes = p.order_bytes + (size_t)batch * hkv * p.nsplit * p.rows * (d + 4) * sizeof(float);
   return p;
 }
 
@@ -338,8 +367,14 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
                                const int32_t* seq_lens, const DecodePlan& plan, float* o,
                                int batch, int B, int hq, int hkv, int d, float scale,
                                void* workspace, int32_t* status, cudaStream_t stream) {
-  DecodeArgs a{block_table, seq_lens, static_cast<float*>(workspace), o, status, num_pages,
-               max_pages, B, hq, hkv, hq / hkv, plan.rows, plan.split_len, plan.nsplit,
+  int32_t* order = plan.ordered ? static_cast<int32_t*>(workspace) : nullptr;
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.order_bytes);
+  if (order) {
+    decode_order_kernel<<<1, 1024, 0, stream>>>(seq_lens, batch, order);
+    count_launches(1);
+  }
+  DecodeArgs a{block_table, seq_lens, order, part, o, status, num_pages, max_pages, B, hq,
+               hkv, hq / hkv, plan.rows, plan.split_len, plan.nsplit,
                scale * 1.4426950408889634f};
   const cudaError_t e = d == 64 ? launch_tc<64>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream)
                                 : launch_tc<128>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream);

@@ -26,6 +26,8 @@ struct DecodePlan {
   int split_len;   // keys per split (multiple of 128)
   int nsplit;      // splits per (sequence, kv head)
   int rows;        // query rows per (sequence, kv head) = (hq / hkv) * B
+  bool ordered;    // CTAs take the sequences longest first (order array in the workspace)
+  size_t order_bytes;
   size_t ws_bytes;
 };
 DecodePlan plan_decode(int batch, int B, int hq, int hkv, int d, int max_len);
