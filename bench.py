@@ -40,7 +40,7 @@ METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TF
 # of the kernel as it is now; the summaries and commands are in profiles/. Reset to None
 # whenever the kernel changes, until it is captured again.
 TRAFFIC_HEAD_GEMM = 1124588416         # profiles/head_gemm_sustained_decode_7b_b128_B16.md
-TRAFFIC_DECODE_STEP0 = None           # re-capture pending after the longest-first order
+TRAFFIC_DECODE_STEP0 = 1365895680      # profiles/decode_tc_sustained_decode_7b_b128_B16.md
 TRAFFIC_DUAL_STREAM = 330587136        # profiles/dual_stream_tc_dual_stream_7b_b2_2L8192_B16.md
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
