@@ -5,13 +5,13 @@
 //   warp 0      Q loader, then K loader: K tiles into a 3-stage ring (TMA, 128-byte
 //               swizzle); warp 6 streams V tiles into their own 3-stage ring, so the two
 //               rings advance independently;
-//   warp 1      TMEM owner and QK^T issuer: S_j = Q K_j^T into one of two 128-column
+//   warp 1      TMEM owner and QK^T issuer: S_j = Q K_j^T into one of three 128-column
 //               fp32 TMEM buffers; a K stage is released as soon as its QK^T finishes;
 //   warp 7      PV issuer: O += P_j V_j with O and P in TMEM (P is the A operand, read
 //               from TMEM); a V stage is released after its PV;
 //   warps 2..5  softmax: thread = query row. It reads its S_j row (tcgen05.ld) into
 //               registers, takes the row max, and writes P = exp2(S - m) as bf16 pairs
-//               into a TMEM P buffer (tcgen05.st). The running max is raised lazily: O and
+//               over the upper half of that S buffer (tcgen05.st). The running max is raised lazily: O and
 //               l are rescaled (tcgen05.ld / st) only when the max grows by more than 2^8,
 //               which keeps P <= 256 and the result exact up to rounding.
 // The two issuers run independently, so the softmax of tile j overlaps QK^T of later
@@ -33,6 +33,7 @@ constexpr int SOFTMAX_THREADS = 128;
 constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by > 2^8
 
 constexpr int KV_STAGES = 3;               // depth of the K ring and of the V ring
+constexpr int NBUF = 3;                    // S/P buffers in TMEM
 
 template <int D>
 struct Smem {
@@ -42,18 +43,20 @@ struct Smem {
   static constexpr int OFF_K = Q_BYTES;                          // K ring
   static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;     // V ring
   static constexpr int TOTAL = OFF_V + KV_STAGES * KV_BYTES + 1024;   // + alignment slack
-  // TMEM columns: S double buffer (fp32), O (fp32), P double buffer (bf16 pairs)
-  static constexpr int TMEM_S = 0;                   // S buffers at columns 0 and 128
-  static constexpr int TMEM_O = 2 * BKV;             // O at column 256 (D columns)
-  static constexpr int TMEM_P = 2 * BKV + 128;       // P buffers at 384 and 448 (64 each)
+  // TMEM columns: three S buffers (fp32) at 0, 128, 256 and O (fp32) at 384. P of a tile
+  // (bf16 pairs, 64 columns) is written over the upper half of that tile's S buffer once
+  // the softmax has read S; PV reads it from there.
+  static constexpr int TMEM_S = 0;
+  static constexpr int TMEM_O = NBUF * BKV;
+  static constexpr int P_OFF = BKV / 2;              // P inside an S buffer
   static constexpr int TMEM_COLS = 512;
 };
 
 struct Barriers {
   uint64_t q_full;
   uint64_t k_full[KV_STAGES], k_empty[KV_STAGES], v_full[KV_STAGES], v_empty[KV_STAGES];
-  uint64_t s_full[2];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t s_full[NBUF];
+  uint64_t p_full[NBUF], pv_done[NBUF];
   uint64_t o_final, drain, drain_pv;
   uint32_t tmem_base;
   int abort;
@@ -70,7 +73,7 @@ MARS_DEV void init_barriers(Barriers& bar) {
     mbar_init(&bar.v_full[i], 1);
     mbar_init(&bar.v_empty[i], 1);
   }
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < NBUF; ++i) {
     mbar_init(&bar.s_full[i], 1);
     mbar_init(&bar.p_full[i], SOFTMAX_THREADS);
     mbar_init(&bar.pv_done[i], 1);
@@ -171,7 +174,7 @@ MARS_DEV uint32_t pack_bf16x2(float lo, float hi) {
 // barrier; with two, one thread's waits overlap the other's MMAs). Each commits only its
 // own MMAs. ntiles >= 1 for both.
 
-// QK^T issuer: S_j = Q K_j^T into S buffer j & 1.
+// QK^T issuer: S_j = Q K_j^T into S buffer j % NBUF.
 template <int D>
 MARS_DEV void s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
                        int32_t* status) {
@@ -182,11 +185,10 @@ MARS_DEV void s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   volatile int* ab = &bar.abort;
   if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
   for (int j = 0; j < ntiles; ++j) {
-    const int st = j % KV_STAGES, sb = j & 1;
+    const int st = j % KV_STAGES, sb = j % NBUF;
     if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
-    // S buffer sb was last read by the softmax of tile j-2, which arrives on p_full(j-2)
-    // only after that read completed
-    if (j >= 2 && !mbar_wait(&bar.p_full[sb], ((j - 2) >> 1) & 1, ab, status)) return;
+    // S buffer sb last held tile j-NBUF, whose P the PV of that tile read from it
+    if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status)) return;
     tc_fence_after();
     const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
 #pragma unroll
@@ -201,7 +203,7 @@ MARS_DEV void s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   }
 }
 
-// PV issuer: O += P_j V_j (P from TMEM buffer j & 1), then o_final after the last tile.
+// PV issuer: O += P_j V_j (P from the upper half of S buffer j % NBUF), then o_final.
 template <int D>
 MARS_DEV void pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
                         int32_t* status) {
@@ -210,15 +212,15 @@ MARS_DEV void pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   const uint32_t idesc_o = idesc_bf16_f32(BQ, D, true);      // O = P V: B MN-major
   volatile int* ab = &bar.abort;
   for (int j = 0; j < ntiles; ++j) {
-    const int pb = j & 1, st = j % KV_STAGES;
+    const int pb = j % NBUF, st = j % KV_STAGES;
     if (!mbar_wait(&bar.v_full[st], (j / KV_STAGES) & 1, ab, status)) return;
-    if (!mbar_wait(&bar.p_full[pb], (j >> 1) & 1, ab, status)) return;
+    if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return;
     tc_fence_after();
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
     for (int k = 0; k < BKV / 16; ++k) {
       // A = P [128 rows x 128 keys] in TMEM: row = lane, 16 keys = 8 columns per K step
-      const uint32_t a = tmem + S::TMEM_P + pb * (BKV / 2) + k * 8;
+      const uint32_t a = tmem + S::TMEM_S + pb * BKV + S::P_OFF + k * 8;
       // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
       const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
       mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (j | k) != 0);
@@ -243,15 +245,15 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   volatile int* ab = &bar.abort;
   if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
   auto issue_pv = [&](int j) -> bool {
-    const int pb = j & 1, st = j % KV_STAGES;
+    const int pb = j % NBUF, st = j % KV_STAGES;
     if (!mbar_wait(&bar.v_full[st], (j / KV_STAGES) & 1, ab, status)) return false;
-    if (!mbar_wait(&bar.p_full[pb], (j >> 1) & 1, ab, status)) return false;
+    if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return false;
     tc_fence_after();
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
     for (int k = 0; k < BKV / 16; ++k) {
       // A = P [128 rows x 128 keys] in TMEM: row = lane, 16 keys = 8 columns per K step
-      const uint32_t a = tmem + S::TMEM_P + pb * (BKV / 2) + k * 8;
+      const uint32_t a = tmem + S::TMEM_S + pb * BKV + S::P_OFF + k * 8;
       // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
       const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
       mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (j | k) != 0);
@@ -261,11 +263,10 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     return true;
   };
   for (int j = 0; j < ntiles; ++j) {
-    const int st = j % KV_STAGES, sb = j & 1;
-    // S buffer sb was last read by the softmax of tile j-2; that read finished before the
-    // softmax arrived on p_full(j-2), which this thread waited for before issuing PV_{j-2}
-    // in the previous iteration, so no separate wait is needed before overwriting it.
+    const int st = j % KV_STAGES, sb = j % NBUF;
     if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
+    // S buffer sb last held tile j-NBUF, whose P the PV of that tile read from it
+    if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status)) return;
     tc_fence_after();
     const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
 #pragma unroll
@@ -381,10 +382,10 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
   // table, whose latency then overlaps the wait for the next S)
   typename Policy::Tile next_tile = pol.tile(0);
   for (int j = 0; j < ntiles && ok; ++j) {
-    const int sb = j & 1, pb = j & 1;
+    const int sb = j % NBUF;
     const typename Policy::Tile tile = next_tile;
     if (j + 1 < ntiles) next_tile = pol.tile(j + 1);
-    if (!(ok = warp_wait(&bar.s_full[sb], (j >> 1) & 1))) break;
+    if (!(ok = warp_wait(&bar.s_full[sb], (j / NBUF) & 1))) break;
     tc_fence_after();
     const uint32_t s_addr = tmem + S::TMEM_S + sb * BKV + lane_off;
     uint32_t r[BKV];
@@ -412,7 +413,7 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     const bool rescale_o = raise && m != -INFINITY;
     if (__any_sync(0xffffffffu, rescale_o)) {
       // PV of the previous tile must have landed in O before O is rescaled
-      if (!(ok = warp_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
+      if (!(ok = warp_wait(&bar.pv_done[(j - 1) % NBUF], ((j - 1) / NBUF) & 1))) break;
       tc_fence_after();
       const float alpha = rescale_o ? ex2_approx(m - tmax) : 1.f;
       l *= alpha;
@@ -428,11 +429,9 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
       tmem_st_wait();
     }
     if (raise) m = tmax;
-    // P buffer pb was read by PV of tile j-2
-    if (!(ok = warp_wait(&bar.pv_done[pb], ((j >> 1) & 1) ^ 1))) break;
-    // P = exp2(S*scale - m) -> bf16 pairs into the TMEM P buffer (row = lane, the A
-    // operand of the PV MMA), and the row sum
-    const uint32_t p_addr = tmem + S::TMEM_P + pb * (BKV / 2) + lane_off;
+    // P = exp2(S*scale - m) -> bf16 pairs over the upper half of this tile's S buffer (S is
+    // in registers now; row = lane, the A operand of the PV MMA), and the row sum
+    const uint32_t p_addr = tmem + S::TMEM_S + sb * BKV + S::P_OFF + lane_off;
     const float neg_m = (m == -INFINITY) ? 0.f : -m;   // no visible key yet: all P are 0
     float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -444,7 +443,7 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive_warp(&bar.p_full[pb]);
+    mbar_arrive_warp(&bar.p_full[sb]);
   }
   if (!ok) return;
   if (!warp_wait(&bar.o_final, 0)) return;
