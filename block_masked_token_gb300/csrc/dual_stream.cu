@@ -27,8 +27,9 @@ using flash::BQ;
 
 template <int D>
 struct DualPolicy {
-  float* o;
-  int L, B, hq, two_l;
+  static constexpr bool kStagedStore = true;
+  const CUtensorMap* tm_o;   // O as [2*batch][L][hq][D] fp32, box [1][128][1][32]
+  int L, B, hq;
   int b, h, stream, r0;
   int n_clean, n_total, mstart, full_limit;
 
@@ -61,19 +62,16 @@ struct DualPolicy {
     c.pmask = 0xffu;
     return c;
   }
-  MARS_DEV void store_chunk(int row, int col, const uint32_t (&r)[32], float inv, float,
-                            float) const {
-    float* dst = o + (((size_t)b * two_l + (size_t)stream * L + r0 + row) * hq + h) * D + col;
+  // rows past L (a partial last query tile) fall outside the map's L extent and are not
+  // written
+  MARS_DEV void store_tile(const uint8_t* stage) const {
 #pragma unroll
-    for (int e = 0; e < 32; e += 4)
-      *reinterpret_cast<float4*>(dst + e) =
-          make_float4(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv,
-                      __uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+    for (int c = 0; c < D / 32; ++c)
+      sm100::tma_store_4d(tm_o, stage + c * (BQ * 128), c * 32, h, r0, b * 2 + stream);
   }
 };
 
 struct DualArgs {
-  float* o;
   int batch, L, B, hq, hkv, G, nqt;
   float scale_log2;
   int32_t* status;
@@ -83,7 +81,8 @@ template <int D>
 __global__ void __launch_bounds__(flash::NUM_THREADS, 1)
 dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, DualArgs a) {
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, DualArgs a) {
   using namespace sm100;
   using S = flash::Smem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -102,11 +101,10 @@ dual_stream_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int qt = a.nqt - 1 - (id >> 1);
 
   DualPolicy<D> pol;
-  pol.o = a.o;
+  pol.tm_o = &tm_o;
   pol.L = a.L;
   pol.B = a.B;
   pol.hq = a.hq;
-  pol.two_l = 2 * a.L;
   pol.b = b;
   pol.h = h;
   pol.stream = stream;
@@ -179,7 +177,7 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, f
                       int batch, int L, int B, int hq, int hkv, float scale,
                       int32_t* status, cudaStream_t stream) {
   using S = flash::Smem<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t rows = (uint64_t)batch * 2 * L;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hq, rows};
@@ -194,13 +192,19 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, f
     if (!encode_tmap_bf16(&tk, k, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_tmap_bf16(&tv, v, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  DualArgs a{o, batch, L, B, hq, hkv, hq / hkv, (L + BQ - 1) / BQ,
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)hq, (uint64_t)L, (uint64_t)batch * 2};
+    const uint64_t str[3] = {(uint64_t)D * 4, (uint64_t)hq * D * 4, (uint64_t)L * hq * D * 4};
+    const uint32_t box[4] = {32, 1, BQ, 1};
+    if (!encode_tmap_f32(&to, o, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  DualArgs a{batch, L, B, hq, hkv, hq / hkv, (L + BQ - 1) / BQ,
              scale * 1.4426950408889634f, status};
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(dual_stream_tc_kernel<D>, S::TOTAL, attr);
   if (ea != cudaSuccess) return ea;
   const long long ctas = (long long)a.nqt * 2 * hq * batch;
-  dual_stream_tc_kernel<D><<<(unsigned)ctas, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tk, tv, a);
+  dual_stream_tc_kernel<D><<<(unsigned)ctas, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,7 @@ struct Barriers {
   uint64_t s_full[NBUF];
   uint64_t p_full[NBUF], pv_done[NBUF];
   uint64_t o_final, drain, drain_pv;
+  uint64_t o_staged;      // softmax threads have written O to shared memory (staged store)
   uint32_t tmem_base;
   int abort;
 };
@@ -78,6 +79,7 @@ MARS_DEV void init_barriers(Barriers& bar) {
     mbar_init(&bar.p_full[i], SOFTMAX_THREADS);
     mbar_init(&bar.pv_done[i], 1);
   }
+  mbar_init(&bar.o_staged, SOFTMAX_THREADS);
   mbar_init(&bar.o_final, 1);
   mbar_init(&bar.drain, 1);
   mbar_init(&bar.drain_pv, 1);
@@ -356,7 +358,8 @@ MARS_DEV void exp2_pack64(const uint32_t (&r)[BKV], int c0, float scale_log2, fl
 // Policy provides: row_valid(row), row_vis(row), tile(j) -> Tile (with .full set when
 // every row sees every key of tile j, so no per-key test runs), cols(vis, tile) ->
 // ColRange (the columns of tile j visible to the row; a tile must admit only keys it
-// owns, so no key is counted twice), store_chunk(row, col, 32 fp32 of O, 1/l, m, l).
+// owns, so no key is counted twice), and either store_chunk(row, col, 32 fp32 of O, 1/l,
+// m, l) or, with kStagedStore, store_tile(staging) which issues the TMA stores of O/l.
 // Each tile's S row is read from TMEM once (4 loads, one wait) into registers.
 template <int D, class Policy>
 MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int ntiles,
@@ -449,12 +452,40 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
   if (!warp_wait(&bar.o_final, 0)) return;
   tc_fence_after();
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  if constexpr (Policy::kStagedStore) {
+    // O / l goes to shared memory as D/32 boxes of [128 rows][32 fp32] in the 128-byte
+    // swizzled layout (a quarter-warp's 16-byte stores then hit distinct banks), and one
+    // thread writes the boxes out with TMA stores. The K ring is idle once o_final has
+    // completed: every QK^T that read it is done.
+    static_assert(D / 32 * BQ * 128 <= KV_STAGES * S::KV_BYTES, "staging fits the K ring");
+    uint8_t* stage = smem + S::OFF_K;
 #pragma unroll 1
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, o);
-    tmem_ld_wait();
-    if (rv) pol.store_chunk(row, c * 32, o, inv, m, l);
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, o);
+      tmem_ld_wait();
+      uint8_t* box = stage + c * (BQ * 128);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(box + sw_off(row, q)) =
+            make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                        __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive_warp(&bar.o_staged);
+    if (threadIdx.x == 2 * 32 && mbar_wait(&bar.o_staged, 0, ab, status)) {
+      pol.store_tile(stage);
+      bulk_commit();
+      bulk_wait_read_all();     // the CTA may exit once the stores have read shared memory
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, o);
+      tmem_ld_wait();
+      if (rv) pol.store_chunk(row, c * 32, o, inv, m, l);
+    }
   }
 }
 

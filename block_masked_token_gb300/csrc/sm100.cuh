@@ -112,6 +112,24 @@ MARS_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int 
       : "memory");
 }
 
+// Tiled 4D store from shared memory (bulk async-group). The source must have been written
+// by the generic proxy and published with fence_proxy_async_smem(); out-of-range box
+// elements are not written.
+MARS_DEV void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y, int z,
+                           int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+MARS_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+MARS_DEV void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 MARS_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -243,9 +261,11 @@ MARS_DEV uint32_t sw128(uint32_t byte_off) { return byte_off ^ ((byte_off >> 3) 
 
 // ---------------------------------------------------------------- host: tensor maps
 
-// Encode a 2D/3D bf16 tensor map with 128-byte swizzle. dims/strides innermost first;
-// strides in bytes for dims 1..rank-1. Returns false on failure.
+// Encode a bf16 (or fp32) tensor map of rank 1..5 with 128-byte swizzle. dims/strides
+// innermost first; strides in bytes for dims 1..rank-1. Returns false on failure.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
+bool encode_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box);
 
 }  // namespace mars

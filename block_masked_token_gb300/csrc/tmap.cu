@@ -24,10 +24,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box) {
+namespace {
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || rank < 1 || rank > 5) return false;
   cuuint64_t gdim[5], gstride[4];
   cuuint32_t bdim[5], estride[5];
   for (int i = 0; i < rank; ++i) {
@@ -36,11 +38,22 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
     estride[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides_bytes[i];
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
-                  const_cast<void*>(base), gdim, gstride, bdim, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, type, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, bdim,
+                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box);
+}
+
+bool encode_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides_bytes, box);
 }
 
 }  // namespace mars
