@@ -459,17 +459,21 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     // completed: every QK^T that read it is done.
     static_assert(D / 32 * BQ * 128 <= KV_STAGES * S::KV_BYTES, "staging fits the K ring");
     uint8_t* stage = smem + S::OFF_K;
-#pragma unroll 1
+    uint32_t o[D];                                   // the whole O row: one TMEM wait
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c)
+      tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+    tmem_ld_wait();
+#pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, o);
-      tmem_ld_wait();
       uint8_t* box = stage + c * (BQ * 128);
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t* v = o + c * 32 + 4 * q;
         *reinterpret_cast<float4*>(box + sw_off(row, q)) =
-            make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                        __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+            make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
+                        __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+      }
     }
     fence_proxy_async_smem();
     mbar_arrive_warp(&bar.o_staged);
