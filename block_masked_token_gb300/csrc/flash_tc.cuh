@@ -32,17 +32,27 @@ constexpr int PV_ISSUER_WARP = 7;
 constexpr int SOFTMAX_THREADS = 128;
 constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by > 2^8
 
-constexpr int KV_STAGES = 3;               // depth of the K ring and of the V ring
+// Ring depths of the K and V tile rings (with Q and a 32 KB O staging area they fill the
+// 227 KB of shared memory).
+#ifndef MARS_K_STAGES
+#define MARS_K_STAGES 3
+#endif
+#ifndef MARS_V_STAGES
+#define MARS_V_STAGES 2
+#endif
+constexpr int K_STAGES = MARS_K_STAGES;
+constexpr int V_STAGES = MARS_V_STAGES;
 constexpr int NBUF = 3;                    // S/P buffers in TMEM
 
-template <int D>
+template <int D, int STAGE_BOXES = 0>
 struct Smem {
   static constexpr int Q_BYTES = BQ * D * 2;         // D/64 swizzled regions of [128][64]
   static constexpr int KV_BYTES = BKV * D * 2;       // one K or V tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;                          // K ring
-  static constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;     // V ring
-  static constexpr int TOTAL = OFF_V + KV_STAGES * KV_BYTES + 1024;   // + alignment slack
+  static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;      // V ring
+  static constexpr int OFF_STAGE = OFF_V + V_STAGES * KV_BYTES;  // O staging (optional)
+  static constexpr int TOTAL = OFF_STAGE + STAGE_BOXES * BQ * 128 + 1024;   // + alignment slack
   // TMEM columns: three S buffers (fp32) at 0, 128, 256 and O (fp32) at 384. P of a tile
   // (bf16 pairs, 64 columns) is written over the upper half of that tile's S buffer once
   // the softmax has read S; PV reads it from there.
@@ -54,11 +64,13 @@ struct Smem {
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[KV_STAGES], k_empty[KV_STAGES], v_full[KV_STAGES], v_empty[KV_STAGES];
+  uint64_t k_full[K_STAGES], k_empty[K_STAGES], v_full[V_STAGES], v_empty[V_STAGES];
   uint64_t s_full[NBUF];
   uint64_t p_full[NBUF], pv_done[NBUF];
   uint64_t o_final, drain, drain_pv;
   uint64_t o_staged;      // softmax threads have written O to shared memory (staged store)
+  uint64_t stage_free;    // the stores of the previous staging round have read it
+  uint64_t q_empty;       // the QK^T MMAs of an item have completed (Q may be replaced)
   uint32_t tmem_base;
   int abort;
 };
@@ -68,9 +80,11 @@ MARS_DEV void init_barriers(Barriers& bar) {
   using namespace sm100;
   bar.abort = 0;
   mbar_init(&bar.q_full, 1);
-  for (int i = 0; i < KV_STAGES; ++i) {
+  for (int i = 0; i < K_STAGES; ++i) {
     mbar_init(&bar.k_full[i], 1);
     mbar_init(&bar.k_empty[i], 1);
+  }
+  for (int i = 0; i < V_STAGES; ++i) {
     mbar_init(&bar.v_full[i], 1);
     mbar_init(&bar.v_empty[i], 1);
   }
@@ -80,6 +94,8 @@ MARS_DEV void init_barriers(Barriers& bar) {
     mbar_init(&bar.pv_done[i], 1);
   }
   mbar_init(&bar.o_staged, SOFTMAX_THREADS);
+  mbar_init(&bar.stage_free, 1);
+  mbar_init(&bar.q_empty, 1);
   mbar_init(&bar.o_final, 1);
   mbar_init(&bar.drain, 1);
   mbar_init(&bar.drain_pv, 1);
@@ -92,34 +108,64 @@ MARS_DEV void init_barriers(Barriers& bar) {
 // calls `issue(j, dst, bar)` (the kernel decides which lanes issue the TMA copies of tile
 // j into dst, completing on bar). Returns after waiting (bounded) for every copy it
 // issued, so the CTA never exits with copies in flight.
-template <int D, class Issue>
-MARS_DEV void load_ring(Barriers& bar, uint8_t* smem, int ntiles, int32_t* status, bool is_v,
-                        Issue issue) {
+// j0: ring position of tile 0 (tiles of earlier work items of a persistent CTA); last[st]
+// keeps the ring position of the latest copy into each stage, across calls, for the final
+// drain (drain = true on the last call).
+template <int D, int NST, class Issue>
+MARS_DEV bool load_ring_n(Barriers& bar, uint64_t* full, uint64_t* empty, uint8_t* ring,
+                          int ntiles, int j0, int (&last)[NST], bool drain, int32_t* status,
+                          Issue& issue) {
   using namespace sm100;
   using S = Smem<D>;
   const int lane = threadIdx.x & 31;
   volatile int* ab = &bar.abort;
-  uint64_t* full = is_v ? bar.v_full : bar.k_full;
-  uint64_t* empty = is_v ? bar.v_empty : bar.k_empty;
-  uint8_t* ring = smem + (is_v ? S::OFF_V : S::OFF_K);
-  int last[KV_STAGES];
-  for (int i = 0; i < KV_STAGES; ++i) last[i] = -1;
+  bool good = true;
   for (int j = 0; j < ntiles; ++j) {
-    const int st = j % KV_STAGES;
+    const int jg = j0 + j;
+    const int st = jg % NST;
     int ok = 1;
     if (lane == 0) {
-      ok = mbar_wait(&empty[st], ((j / KV_STAGES) & 1) ^ 1, ab, status);
+      ok = mbar_wait(&empty[st], ((jg / NST) & 1) ^ 1, ab, status);
       if (ok) mbar_arrive_expect_tx(&full[st], S::KV_BYTES);
     }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+      good = false;
+      break;
+    }
     issue(j, ring + st * S::KV_BYTES, &full[st]);
-    last[st] = j;
+    last[st] = jg;
   }
-  if (lane == 0) {
-    for (int st = 0; st < KV_STAGES; ++st)
-      if (last[st] >= 0) mbar_wait(&full[st], (last[st] / KV_STAGES) & 1, nullptr, status);
+  if ((drain || !good) && lane == 0) {
+    for (int st = 0; st < NST; ++st)
+      if (last[st] >= 0) mbar_wait(&full[st], (last[st] / NST) & 1, nullptr, status);
   }
   __syncwarp();
+  return good;
+}
+
+// One work item's K (or V) tiles into its ring; see load_ring_n. Returns false on abort.
+template <int D, int NST, class Issue>
+MARS_DEV bool load_ring_item(Barriers& bar, uint8_t* smem, int ntiles, int j0, int (&last)[NST],
+                             bool drain, int32_t* status, bool is_v, Issue issue) {
+  using S = Smem<D>;
+  return is_v ? load_ring_n<D, NST>(bar, bar.v_full, bar.v_empty, smem + S::OFF_V, ntiles, j0,
+                                    last, drain, status, issue)
+              : load_ring_n<D, NST>(bar, bar.k_full, bar.k_empty, smem + S::OFF_K, ntiles, j0,
+                                    last, drain, status, issue);
+}
+
+template <int D, class Issue>
+MARS_DEV void load_ring(Barriers& bar, uint8_t* smem, int ntiles, int32_t* status, bool is_v,
+                        Issue issue) {
+  if (is_v) {
+    int last[V_STAGES];
+    for (int i = 0; i < V_STAGES; ++i) last[i] = -1;
+    load_ring_item<D, V_STAGES>(bar, smem, ntiles, 0, last, true, status, true, issue);
+  } else {
+    int last[K_STAGES];
+    for (int i = 0; i < K_STAGES; ++i) last[i] = -1;
+    load_ring_item<D, K_STAGES>(bar, smem, ntiles, 0, last, true, status, false, issue);
+  }
 }
 
 // Row-visibility of a query row: keys jg (in the kernel's key index space) with
@@ -177,20 +223,24 @@ MARS_DEV uint32_t pack_bf16x2(float lo, float hi) {
 // own MMAs. ntiles >= 1 for both.
 
 // QK^T issuer: S_j = Q K_j^T into S buffer j % NBUF.
+// j0: global position of tile 0 in the rings and S buffers; q_parity: phase of q_full
+// holding this item's Q. Returns false on abort.
 template <int D>
-MARS_DEV void s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
-                       int32_t* status) {
+MARS_DEV bool s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
+                       int32_t* status, int j0 = 0, uint32_t q_parity = 0) {
   using namespace sm100;
   using S = Smem<D>;
   const uint32_t idesc_s = idesc_bf16_f32(BQ, BKV, false);   // S = Q K^T: B K-major
   const uint32_t q = smem_u32(smem + S::OFF_Q);
   volatile int* ab = &bar.abort;
-  if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
-  for (int j = 0; j < ntiles; ++j) {
-    const int st = j % KV_STAGES, sb = j % NBUF;
-    if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
+  if (!mbar_wait(&bar.q_full, q_parity, ab, status)) return false;
+  for (int jl = 0; jl < ntiles; ++jl) {
+    const int j = j0 + jl;
+    const int st = j % K_STAGES, sb = j % NBUF;
+    if (!mbar_wait(&bar.k_full[st], (j / K_STAGES) & 1, ab, status)) return false;
     // S buffer sb last held tile j-NBUF, whose P the PV of that tile read from it
-    if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status)) return;
+    if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status))
+      return false;
     tc_fence_after();
     const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
 #pragma unroll
@@ -203,20 +253,22 @@ MARS_DEV void s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     mma_commit(&bar.s_full[sb]);
     mma_commit(&bar.k_empty[st]);      // K stage free once this QK^T completes
   }
+  return true;
 }
 
 // PV issuer: O += P_j V_j (P from the upper half of S buffer j % NBUF), then o_final.
 template <int D>
-MARS_DEV void pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
-                        int32_t* status) {
+MARS_DEV bool pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
+                        int32_t* status, int j0 = 0) {
   using namespace sm100;
   using S = Smem<D>;
   const uint32_t idesc_o = idesc_bf16_f32(BQ, D, true);      // O = P V: B MN-major
   volatile int* ab = &bar.abort;
-  for (int j = 0; j < ntiles; ++j) {
-    const int pb = j % NBUF, st = j % KV_STAGES;
-    if (!mbar_wait(&bar.v_full[st], (j / KV_STAGES) & 1, ab, status)) return;
-    if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return;
+  for (int jl = 0; jl < ntiles; ++jl) {
+    const int j = j0 + jl;
+    const int pb = j % NBUF, st = j % V_STAGES;
+    if (!mbar_wait(&bar.v_full[st], (j / V_STAGES) & 1, ab, status)) return false;
+    if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return false;
     tc_fence_after();
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
@@ -225,12 +277,13 @@ MARS_DEV void pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
       const uint32_t a = tmem + S::TMEM_S + pb * BKV + S::P_OFF + k * 8;
       // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
       const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
-      mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (j | k) != 0);
+      mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (jl | k) != 0);
     }
     mma_commit(&bar.pv_done[pb]);
     mma_commit(&bar.v_empty[st]);
   }
   mma_commit(&bar.o_final);
+  return true;
 }
 
 // Single-thread alternative: one thread issues S_j, then PV_{j-1}, so the QK^T the softmax
@@ -247,8 +300,8 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   volatile int* ab = &bar.abort;
   if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
   auto issue_pv = [&](int j) -> bool {
-    const int pb = j % NBUF, st = j % KV_STAGES;
-    if (!mbar_wait(&bar.v_full[st], (j / KV_STAGES) & 1, ab, status)) return false;
+    const int pb = j % NBUF, st = j % V_STAGES;
+    if (!mbar_wait(&bar.v_full[st], (j / V_STAGES) & 1, ab, status)) return false;
     if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return false;
     tc_fence_after();
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
@@ -265,8 +318,8 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     return true;
   };
   for (int j = 0; j < ntiles; ++j) {
-    const int st = j % KV_STAGES, sb = j % NBUF;
-    if (!mbar_wait(&bar.k_full[st], (j / KV_STAGES) & 1, ab, status)) return;
+    const int st = j % K_STAGES, sb = j % NBUF;
+    if (!mbar_wait(&bar.k_full[st], (j / K_STAGES) & 1, ab, status)) return;
     // S buffer sb last held tile j-NBUF, whose P the PV of that tile read from it
     if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status)) return;
     tc_fence_after();
@@ -359,11 +412,17 @@ MARS_DEV void exp2_pack64(const uint32_t (&r)[BKV], int c0, float scale_log2, fl
 // every row sees every key of tile j, so no per-key test runs), cols(vis, tile) ->
 // ColRange (the columns of tile j visible to the row; a tile must admit only keys it
 // owns, so no key is counted twice), and either store_chunk(row, col, 32 fp32 of O, 1/l,
-// m, l) or, with kStagedStore, store_tile(staging) which issues the TMA stores of O/l.
+// m, l) or, with kStagedStore, kStageBoxes, stage(smem) (the staging area) and
+// store_boxes(staging, first box, boxes), which issues the TMA stores of O/l.
 // Each tile's S row is read from TMEM once (4 loads, one wait) into registers.
+//
+// A persistent kernel calls it once per work item with j0 (global position of the item's
+// first tile), o_parity (phase of o_final for the item) and epi_round (staging rounds done
+// so far, kept across items); it then makes the final bulk-store wait itself.
 template <int D, class Policy>
-MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int ntiles,
-                           uint32_t tmem, float scale_log2, int32_t* status) {
+MARS_DEV bool softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int ntiles,
+                           uint32_t tmem, float scale_log2, int32_t* status, int j0 = 0,
+                           uint32_t o_parity = 0, int* epi_round = nullptr) {
   using namespace sm100;
   using S = Smem<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -385,10 +444,11 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
   // table, whose latency then overlaps the wait for the next S)
   typename Policy::Tile next_tile = pol.tile(0);
   for (int j = 0; j < ntiles && ok; ++j) {
-    const int sb = j % NBUF;
+    const int jg = j0 + j;
+    const int sb = jg % NBUF;
     const typename Policy::Tile tile = next_tile;
     if (j + 1 < ntiles) next_tile = pol.tile(j + 1);
-    if (!(ok = warp_wait(&bar.s_full[sb], (j / NBUF) & 1))) break;
+    if (!(ok = warp_wait(&bar.s_full[sb], (jg / NBUF) & 1))) break;
     tc_fence_after();
     const uint32_t s_addr = tmem + S::TMEM_S + sb * BKV + lane_off;
     uint32_t r[BKV];
@@ -416,7 +476,7 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     const bool rescale_o = raise && m != -INFINITY;
     if (__any_sync(0xffffffffu, rescale_o)) {
       // PV of the previous tile must have landed in O before O is rescaled
-      if (!(ok = warp_wait(&bar.pv_done[(j - 1) % NBUF], ((j - 1) / NBUF) & 1))) break;
+      if (!(ok = warp_wait(&bar.pv_done[(jg - 1) % NBUF], ((jg - 1) / NBUF) & 1))) break;
       tc_fence_after();
       const float alpha = rescale_o ? ex2_approx(m - tmax) : 1.f;
       l *= alpha;
@@ -448,40 +508,64 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     tc_fence_before();
     mbar_arrive_warp(&bar.p_full[sb]);
   }
-  if (!ok) return;
-  if (!warp_wait(&bar.o_final, 0)) return;
+  if (!ok) return false;
+  if (!warp_wait(&bar.o_final, o_parity)) return false;
   tc_fence_after();
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
   if constexpr (Policy::kStagedStore) {
-    // O / l goes to shared memory as D/32 boxes of [128 rows][32 fp32] in the 128-byte
+    // O / l goes to shared memory as 32-column boxes of [128 rows][32 fp32] in the 128-byte
     // swizzled layout (a quarter-warp's 16-byte stores then hit distinct banks), and one
-    // thread writes the boxes out with TMA stores. The K ring is idle once o_final has
-    // completed: every QK^T that read it is done.
-    static_assert(D / 32 * BQ * 128 <= KV_STAGES * S::KV_BYTES, "staging fits the K ring");
-    uint8_t* stage = smem + S::OFF_K;
+    // thread writes them out with TMA stores, kStageBoxes boxes per round. Before a round
+    // overwrites the staging, that thread waits until the previous round's stores have
+    // read it and releases the others through stage_free.
+    constexpr int NBOX = D / 32;
+    constexpr int PER = Policy::kStageBoxes;
+    static_assert(NBOX % PER == 0, "rounds cover O");
+    constexpr int kStoreThread = 2 * 32;
+    uint8_t* stage = pol.stage(smem);
     uint32_t o[D];                                   // the whole O row: one TMEM wait
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c)
+    for (int c = 0; c < NBOX; ++c)
       tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
     tmem_ld_wait();
+    int local_round = 0;
+    int& er = epi_round ? *epi_round : local_round;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint8_t* box = stage + c * (BQ * 128);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t* v = o + c * 32 + 4 * q;
-        *reinterpret_cast<float4*>(box + sw_off(row, q)) =
-            make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
-                        __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+    for (int b0 = 0; b0 < NBOX; b0 += PER) {
+      if (er > 0) {
+        if (threadIdx.x == kStoreThread) {
+          bulk_wait_read_all();
+          mbar_arrive(&bar.stage_free);
+        }
+        if (!warp_wait(&bar.stage_free, (er - 1) & 1)) return false;
       }
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        uint8_t* box = stage + c * (BQ * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* v = o + (b0 + c) * 32 + 4 * q;
+          *reinterpret_cast<float4*>(box + sw_off(row, q)) =
+              make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
+                          __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive_warp(&bar.o_staged);
+      bool st_ok = true;
+      if (threadIdx.x == kStoreThread) {
+        st_ok = mbar_wait(&bar.o_staged, er & 1, ab, status);
+        if (st_ok) {
+          pol.store_boxes(stage, b0, PER);
+          bulk_commit();
+        }
+      }
+      if (!__all_sync(0xffffffffu, st_ok)) return false;
+      ++er;
     }
-    fence_proxy_async_smem();
-    mbar_arrive_warp(&bar.o_staged);
-    if (threadIdx.x == 2 * 32 && mbar_wait(&bar.o_staged, 0, ab, status)) {
-      pol.store_tile(stage);
-      bulk_commit();
-      bulk_wait_read_all();     // the CTA may exit once the stores have read shared memory
-    }
+    // a single-item call drains its stores here (the CTA may exit once they have read
+    // shared memory); a persistent kernel drains after its last item
+    if (!epi_round && threadIdx.x == kStoreThread) bulk_wait_read_all();
   } else {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
@@ -491,6 +575,7 @@ MARS_DEV void softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
       if (rv) pol.store_chunk(row, c * 32, o, inv, m, l);
     }
   }
+  return true;
 }
 
 }  // namespace flash

@@ -62,14 +62,20 @@ MARS_DEV void mbar_arrive_warp(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], 32;" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One wait attempt. With the suspend-time hint the thread sleeps until the phase
+// completes (or the hint's time passes) instead of returning at once, so a waiting issuer
+// or loader thread does not take issue slots from the softmax warps that share its SM
+// sub-partition.
+constexpr uint32_t kSuspendHintNs = 1000000;    // 1 ms
+
 MARS_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -80,15 +86,13 @@ MARS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                         int32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (abort && *abort) return false;
-      if (globaltimer() - t0 > kWaitNs) {
-        if (abort) *abort = 1;
-        if (status) atomicOr(status, MARS_ST_TIMEOUT);
-        return false;
-      }
+    if (abort && *abort) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      if (abort) *abort = 1;
+      if (status) atomicOr(status, MARS_ST_TIMEOUT);
+      return false;
     }
   }
 }

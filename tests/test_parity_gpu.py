@@ -115,6 +115,17 @@ def test_dual_stream_config_7b_sampled():
         assert_attn_close(got, ref[bb, :, h], f"dual 7B b{bb} h{h}")
 
 
+def test_dual_stream_many_items_per_cta():
+    """More work items than SMs at d = 64 with a ragged last query tile and an odd block
+    size: each persistent CTA runs several items, so the rings, S buffers, O staging and
+    barrier phases carry over from item to item."""
+    cfg = W.DualStreamConfig("t", 3, 700, 7, 12, 3, 64)
+    x = W.make_dual_stream_inputs(cfg, seed=11)
+    o = run_dual(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), cfg.L, cfg.B)
+    ref = oracle.attn_dual_stream(f64(x["q"]), f64(x["k"]), f64(x["v"]), cfg.L, cfg.B)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
 def test_dual_stream_divergent_rescale():
     """One query row meets a key scoring far above its earlier maximum in a later key tile
     while the other rows of its warp do not: the per-row running maximum is raised for
