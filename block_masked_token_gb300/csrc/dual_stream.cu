@@ -31,8 +31,11 @@ using flash::BQ;
 template <int D>
 struct DualPolicy {
   static constexpr bool kStagedStore = true;
+  static constexpr bool kRowStats = true;
   static constexpr int kStageBoxes = D / 32 < 2 ? D / 32 : 2;
   const CUtensorMap* tm_o;   // O as [2*batch][L][hq][D] fp32, box [1][128][1][32]
+  float* lse;                // optional: [batch][hq][2L] row log-sum-exp (log2 units)
+  int store_o;               // 0: O is not written (a statistics-only run)
   int L, B, hq;
   int b, h, stream, r0;
   int n_clean, n_total, mstart, full_limit;
@@ -70,9 +73,15 @@ struct DualPolicy {
   MARS_DEV uint8_t* stage(uint8_t* smem) const {
     return smem + flash::Smem<D, kStageBoxes>::OFF_STAGE;
   }
+  // log2 of the row's softmax denominator in units of scale*log2(e)*score: m + log2(l)
+  MARS_DEV void row_stats(int row, float m, float l) const {
+    if (lse && row_valid(row))
+      lse[((size_t)b * hq + h) * 2 * L + (size_t)stream * L + r0 + row] = m + log2f(l);
+  }
   // rows past L (a partial last query tile) fall outside the map's L extent and are not
   // written
   MARS_DEV void store_boxes(const uint8_t* stage, int b0, int n) const {
+    if (!store_o) return;
     for (int c = 0; c < n; ++c)
       sm100::tma_store_4d(tm_o, stage + c * (BQ * 128), (b0 + c) * 32, h, r0, b * 2 + stream);
   }
@@ -82,6 +91,8 @@ struct DualArgs {
   int batch, L, B, hq, hkv, G, nqt;
   float scale_log2;
   int32_t* status;
+  float* lse;
+  int store_o;
 };
 
 // Work item id -> (batch, head, stream, query tile) and the key tiles it visits. Ids run
@@ -96,6 +107,8 @@ MARS_DEV DualPolicy<D> make_item(const DualArgs& a, int id, const CUtensorMap* t
   const int stream = id & 1;
   const int qt = a.nqt - 1 - (id >> 1);
   pol.tm_o = tm_o;
+  pol.lse = a.lse;
+  pol.store_o = a.store_o;
   pol.L = a.L;
   pol.B = a.B;
   pol.hq = a.hq;
@@ -271,7 +284,7 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
 template <int D>
 cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
                       int batch, int L, int B, int hq, int hkv, float scale,
-                      int32_t* status, cudaStream_t stream) {
+                      int32_t* status, float* lse, cudaStream_t stream) {
   using S = flash::Smem<D>;
   CUtensorMap tq, tk, tv, to;
   const uint64_t rows = (uint64_t)batch * 2 * L;
@@ -292,10 +305,12 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, f
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)hq, (uint64_t)L, (uint64_t)batch * 2};
     const uint64_t str[3] = {(uint64_t)D * 4, (uint64_t)hq * D * 4, (uint64_t)L * hq * D * 4};
     const uint32_t box[4] = {32, 1, BQ, 1};
-    if (!encode_tmap_f32(&to, o, 4, dims, str, box)) return cudaErrorInvalidValue;
+    // without O (a statistics-only run) the map is encoded over lse and never used
+    const void* base = o ? static_cast<const void*>(o) : static_cast<const void*>(lse);
+    if (!encode_tmap_f32(&to, base, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
   DualArgs a{batch, L, B, hq, hkv, hq / hkv, (L + BQ - 1) / BQ,
-             scale * 1.4426950408889634f, status};
+             scale * 1.4426950408889634f, status, lse, o != nullptr};
   const long long items = (long long)a.nqt * 2 * hq * batch;
   using SP = flash::Smem<D, DualPolicy<D>::kStageBoxes>;
   static_assert(SP::TOTAL + sizeof(flash::Barriers) <= 227 * 1024,
@@ -313,9 +328,11 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, f
 
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* o, int batch, int L, int B, int hq, int hkv, int d,
-                               float scale, int32_t* status, cudaStream_t stream) {
-  cudaError_t e = d == 64 ? launch_tc<64>(q, k, v, o, batch, L, B, hq, hkv, scale, status, stream)
-                          : launch_tc<128>(q, k, v, o, batch, L, B, hq, hkv, scale, status, stream);
+                               float scale, int32_t* status, cudaStream_t stream, float* lse) {
+  if (!o && !lse) return cudaErrorInvalidValue;
+  cudaError_t e =
+      d == 64 ? launch_tc<64>(q, k, v, o, batch, L, B, hq, hkv, scale, status, lse, stream)
+              : launch_tc<128>(q, k, v, o, batch, L, B, hq, hkv, scale, status, lse, stream);
   count_launches(1);
   return e;
 }

@@ -2,42 +2,48 @@
 // "MARS: Enabling Autoregressive Models Multi-Token Generation", Key design 1, eq. M; the
 // training step of the overall framework runs the backward of this forward).
 //
-// Only two blocks of the 2L x 2L score matrix hold visible keys: every row against the
-// clean keys (S_c, 2L x L: causal for clean rows, keys before the block start for masked
-// rows) and each masked row against the keys of its own block (S_m, one Bb x Bb block per
-// block of the masked stream, Bb = min(B, L)); clean rows never see masked keys. For each
-// (batch, kv head) the G query heads that share it are handled together:
-//   S_g  = Q_g K^T on those blocks       (cuBLAS; batched over g, and over blocks for S_m)
-//   P_g  = softmax(scale S_g + M)        (here: one CTA per row, visible keys only)
-//   dP_g = dO_g V^T on the same blocks   (cuBLAS, into the S buffers)
-//   dV  += P_g^T dO_g                    (cuBLAS, accumulated over g)
-//   dS_g = P_g * (dP_g - D)              (here, in place over P; D_i = rowsum(dO_i * O_i))
-//   dK  += scale dS_g^T Q_g              (cuBLAS, accumulated over g)
-//   dQ_g = scale dS_g K                  (cuBLAS)
-// The blocks of one kv group are materialised in the workspace (scores fp32, P and dS
-// bf16, masked entries exactly 0). This is the plain formulation with library GEMMs; a
-// fused tile kernel in the manner of the forward would never store the blocks.
-#include <cublas_v2.h>
+// With P = softmax(scale * S + M), S = Q K^T, and D_i = rowsum(dO_i * O_i):
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dK = scale dS^T Q,   dQ = scale dS K.
+// One fused tcgen05 kernel, never storing a score block:
+//   - a work item is (batch, kv head, 128-key tile of one stream); one persistent CTA per
+//     SM runs items heaviest first;
+//   - the item visits every (query head of the kv group, 128-row query tile) pair that sees
+//     one of its keys under M, and per pair runs five MMAs with TMEM accumulators:
+//       S^T = K Q^T, dP^T = V dO^T            (keys on TMEM lanes, queries on columns)
+//       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM)
+//       dQ_pair = dS K                        (A = dS from shared memory, MN-major)
+//     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by one thread per key row;
+//   - dK and dV stay in TMEM over all of the item's pairs and are written once; each pair's
+//     dQ part is added to dQ (fp32 vector atomics), so dQ is zeroed first.
+// lse (log2 of each query row's softmax denominator) comes from a statistics-only run of
+// the forward kernel; P and dS are rounded to bf16 as MMA operands.
 #include <cuda_bf16.h>
 
-#include <mutex>
+#include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace mars {
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
+using namespace sm100;
 
-// dO (fp32) -> bf16 copy, and D[b, i, h] = sum_d dO[b, i, h, d] * O[b, i, h, d]. One warp
+constexpr int GT = 128;                // keys per key tile, query rows per query tile
+constexpr int GRAD_THREADS = 192;      // warp 0 loads, warp 1 TMEM + MMAs, warps 2..5 math
+constexpr int MATH_THREADS = 128;
+constexpr int NSTAGE = 2;              // Q / dO ring depth
+
+// dO (fp32) -> bf16 copy, and D[b][h][i] = sum_d dO[b, i, h, d] * O[b, i, h, d]. One warp
 // per (b, i, h) row.
 __global__ void __launch_bounds__(256) grad_prep_kernel(const float* __restrict__ o,
                                                         const float* __restrict__ d_o,
                                                         __nv_bfloat16* __restrict__ do_bf,
                                                         float* __restrict__ drow,
-                                                        long long nrows, int d) {
+                                                        long long nrows, int n, int hq, int d) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= nrows) return;
@@ -50,154 +56,498 @@ __global__ void __launch_bounds__(256) grad_prep_kernel(const float* __restrict_
     do_bf[row * d + c] = __float2bfloat16_rn(x);
   }
   acc = warp_sum(acc);
-  if (lane == 0) drow[row] = acc;
+  const long long h = row % hq, bi = row / hq, i = bi % n, b = bi / n;
+  if (lane == 0) drow[(b * hq + h) * n + i] = acc;
 }
 
-// Geometry of the two score blocks of one head (see the header).
-struct Blocks {
-  int L, B, Bb, nb;   // stream length, block size, block width in S_m, blocks in S_m
+template <int D>
+struct GSmem {
+  static constexpr int T_BYTES = GT * D * 2;                 // one [128][D] bf16 tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = T_BYTES;
+  static constexpr int OFF_RING = 2 * T_BYTES;
+  // a stage: Q [128][D], dO [128][D] (dS [128 keys][128 queries] later, MN-major), lse and
+  // D of its 128 query rows; 1024-byte aligned
+  static constexpr int DO_BYTES = GT * GT * 2 > T_BYTES ? GT * GT * 2 : T_BYTES;
+  static constexpr int ST_Q = 0, ST_DO = T_BYTES, ST_LSE = T_BYTES + DO_BYTES,
+                       ST_D = ST_LSE + GT * 4;
+  static constexpr int STAGE = (ST_D + GT * 4 + 1023) / 1024 * 1024;
+  static constexpr int TOTAL = OFF_RING + NSTAGE * STAGE + 1024;   // + alignment slack
+  // TMEM columns
+  static constexpr int TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TM_COLS = 512;
 };
 
-MARS_DEV Blocks blocks_of(int L, int B) {
-  Blocks g;
-  g.L = L;
-  g.B = B;
-  g.Bb = B < L ? B : L;
-  g.nb = (L + g.Bb - 1) / g.Bb;
-  return g;
-}
+struct GBar {
+  uint64_t kv_full, kv_empty;
+  uint64_t full[NSTAGE], empty[NSTAGE];
+  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, dv_done, dk_done;
+  uint64_t acc_full, acc_free, drain;
+  uint32_t tmem_base;
+  int abort;
+};
 
-// Row i of head g (one CTA): the visible keys are S_c[i][0 .. e1) and, for a masked row
-// t = i - L, S_m[t][0 .. cm] (cm = t - block start); P is written in full (0 elsewhere).
-// S_c: [G][2L][L], S_m: [G][nb * Bb][Bb] fp32; P_c, P_m: same shapes, bf16.
-__global__ void __launch_bounds__(256) grad_softmax_kernel(const float* __restrict__ s_c,
-                                                           const float* __restrict__ s_m,
-                                                           __nv_bfloat16* __restrict__ p_c,
-                                                           __nv_bfloat16* __restrict__ p_m,
-                                                           int L, int B, float scale_log2) {
-  __shared__ float red_m[8], red_s[8];
-  const Blocks geo = blocks_of(L, B);
-  const int n = 2 * L;
-  const long long grow = blockIdx.x;                   // g * 2L + i
-  const int g = (int)(grow / n), i = (int)(grow % n);
-  const float* crow = s_c + grow * L;
-  __nv_bfloat16* pcrow = p_c + grow * L;
-  int e1, cm;                                           // clean keys [0, e1); block keys [0, cm]
-  const float* mrow = nullptr;
-  __nv_bfloat16* pmrow = nullptr;
-  if (i < L) {
-    e1 = i + 1;
-    cm = -1;
+struct GArgs {
+  int batch, L, B, hq, hkv, G, nt;
+  float scale, scale_log2;
+  const float* lse;        // [batch][hq][2L]
+  const float* drow;       // [batch][hq][2L]
+  float* dq;               // [batch][2L][hq][D], zeroed
+  float* dk;               // [batch][2L][hkv][D]
+  float* dv;
+  int32_t* status;
+};
+
+// Work item: keys [128 jt, 128 jt + 128) of stream ks (0 clean, 1 masked) of (b, kvh).
+// Ids run over clean key tiles from the first (seen by most query tiles) to the last, then
+// over the masked key tiles.
+struct GItem {
+  int b, kvh, ks, jt;
+  int nc, mlo, npg;        // clean keys: clean query tiles [jt, nt), masked [mlo, nt)
+};
+
+MARS_DEV GItem grad_item(const GArgs& a, int id) {
+  GItem it;
+  const int per = a.batch * a.hkv;
+  const int kt = id / per, bk = id % per;
+  it.b = bk % a.batch;
+  it.kvh = bk / a.batch;
+  if (kt < a.nt) {
+    it.ks = 0;
+    it.jt = kt;
+    it.nc = a.nt - kt;
+    // masked row t sees clean key k iff its block start (t/B)*B > k: t >= (k/B + 1) B
+    const int tmin = (GT * kt / a.B + 1) * a.B;
+    it.mlo = tmin <= a.L - 1 ? tmin / GT : a.nt;
+    it.npg = it.nc + (a.nt - it.mlo);
   } else {
-    const int t = i - L, bs = (t / B) * B;
-    e1 = bs;
-    cm = t - bs;
-    const long long mr = (long long)g * geo.nb * geo.Bb + t;
-    mrow = s_m + mr * geo.Bb;
-    pmrow = p_m + mr * geo.Bb;
+    it.ks = 1;
+    it.jt = kt - a.nt;
+    // masked key u is seen by masked rows t in [u, end of u's block)
+    const int umax = min(GT * it.jt + GT - 1, a.L - 1);
+    const int tmax = min(a.L, (umax / a.B + 1) * a.B) - 1;
+    it.nc = 0;
+    it.mlo = it.jt;
+    it.npg = tmax / GT - it.jt + 1;
   }
-  const int nvis = e1 + cm + 1;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float m = -INFINITY, sum = 0.f;                       // in log2 units
-  for (int t = threadIdx.x; t < nvis; t += blockDim.x) {
-    const float x = (t < e1 ? crow[t] : mrow[t - e1]) * scale_log2;
-    if (x > m) {
-      sum = sum * exp2f(m - x) + 1.f;
-      m = x;
-    } else {
-      sum += exp2f(x - m);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2v = __shfl_xor_sync(0xffffffffu, sum, o);
-    const float mm = fmaxf(m, m2);
-    sum = (m == -INFINITY ? 0.f : sum * exp2f(m - mm)) +
-          (m2 == -INFINITY ? 0.f : s2v * exp2f(m2 - mm));
-    m = mm;
-  }
-  if (lane == 0) {
-    red_m[warp] = m;
-    red_s[warp] = sum;
-  }
-  __syncthreads();
-  float mt = red_m[0];
-  for (int w = 1; w < 8; ++w) mt = fmaxf(mt, red_m[w]);
-  float st = 0.f;
-  for (int w = 0; w < 8; ++w)
-    if (red_m[w] != -INFINITY) st += red_s[w] * exp2f(red_m[w] - mt);
-  const float inv = 1.f / st;                           // the diagonal is always visible
-  for (int j = threadIdx.x; j < L; j += blockDim.x)
-    pcrow[j] = __float2bfloat16_rn(j < e1 ? exp2f(crow[j] * scale_log2 - mt) * inv : 0.f);
-  if (pmrow)
-    for (int c = threadIdx.x; c < geo.Bb; c += blockDim.x)
-      pmrow[c] = __float2bfloat16_rn(c <= cm ? exp2f(mrow[c] * scale_log2 - mt) * inv : 0.f);
+  return it;
 }
 
-// dS = P * (dP - D_i), in place over P (bf16), on the visible keys of row i of head g (P,
-// hence dS, is 0 on the others). dP in the S buffers; D of query head h0 + g at row i:
-// drow[((b * 2L + i) * hq) + h0 + g].
-__global__ void __launch_bounds__(256) grad_ds_kernel(__nv_bfloat16* __restrict__ p_c,
-                                                      __nv_bfloat16* __restrict__ p_m,
-                                                      const float* __restrict__ dp_c,
-                                                      const float* __restrict__ dp_m,
-                                                      const float* __restrict__ drow,
-                                                      int L, int B, int hq, int h0, int b) {
-  const Blocks geo = blocks_of(L, B);
-  const int n = 2 * L;
-  const long long grow = blockIdx.x;
-  const int g = (int)(grow / n), i = (int)(grow % n);
-  const float dv = drow[((long long)b * n + i) * hq + h0 + g];
-  int e1 = i + 1, cm = -1;
-  long long mr = 0;
-  if (i >= L) {
-    const int t = i - L, bs = (t / B) * B;
-    e1 = bs;
-    cm = t - bs;
-    mr = ((long long)g * geo.nb * geo.Bb + t) * geo.Bb;
-  }
-  for (int t = threadIdx.x; t < e1 + cm + 1; t += blockDim.x) {
-    if (t < e1) {
-      const long long x = grow * L + t;
-      p_c[x] = __float2bfloat16_rn(__bfloat162float(p_c[x]) * (dp_c[x] - dv));
-    } else {
-      const long long x = mr + (t - e1);
-      p_m[x] = __float2bfloat16_rn(__bfloat162float(p_m[x]) * (dp_m[x] - dv));
-    }
-  }
-}
-
-struct Blas {
-  std::mutex mu;
-  cublasHandle_t h[64] = {};
+// Pair p of an item: query head g of the group, query stream qs, query tile qi.
+struct GPair {
+  int g, qs, qi;
 };
-Blas& blas() {
-  static Blas b;
-  return b;
+
+MARS_DEV GPair grad_pair(const GItem& it, int p) {
+  GPair q;
+  q.g = p / it.npg;
+  const int r = p % it.npg;
+  if (r < it.nc) {
+    q.qs = 0;
+    q.qi = it.jt + r;
+  } else {
+    q.qs = 1;
+    q.qi = it.mlo + (r - it.nc);
+  }
+  return q;
+}
+
+// Query columns [lo, hi] of a pair's tile that key kk (index within its stream) is visible
+// to; empty (lo > hi) for a key past L.
+MARS_DEV void visible_cols(const GArgs& a, const GItem& it, const GPair& pr, int kk, int& lo,
+                           int& hi) {
+  const int q0 = GT * pr.qi;
+  lo = 1;
+  hi = 0;
+  if (kk >= a.L) return;
+  int tlo, thi;                              // visible query rows of stream qs
+  if (it.ks == 0 && pr.qs == 0) {            // clean key, clean rows: t >= kk
+    tlo = kk;
+    thi = a.L - 1;
+  } else if (it.ks == 0) {                   // clean key, masked rows: block start > kk
+    tlo = (kk / a.B + 1) * a.B;
+    thi = a.L - 1;
+  } else {                                   // masked key, masked rows of its block, t >= kk
+    tlo = kk;
+    thi = min(a.L, (kk / a.B + 1) * a.B) - 1;
+  }
+  lo = max(tlo - q0, 0);
+  hi = min(thi - q0, GT - 1);
+}
+
+MARS_DEV uint32_t bits(int lo, int hi) {     // bits [lo, hi) of a 32-bit word, clamped
+  lo = max(0, min(32, lo));
+  hi = max(0, min(32, hi));
+  if (hi <= lo) return 0u;
+  return (hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u)) & ~((1u << lo) - 1u);
+}
+
+MARS_DEV uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+MARS_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Swizzled byte offset of 16-byte chunk c (0..7) of 128-byte row r (the TMA 128-byte
+// swizzle layout, which is also the MMA's canonical one).
+MARS_DEV uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Instruction descriptor with A and B majorness (bit 15: A MN-major, bit 16: B MN-major).
+MARS_DEV uint32_t idesc_ab(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
+}
+
+template <int D>
+__global__ void __launch_bounds__(GRAD_THREADS, 1)
+dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, GArgs a) {
+  using S = GSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ GBar bar;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* ab = &bar.abort;
+
+  if (threadIdx.x == 0) {
+    bar.abort = 0;
+    mbar_init(&bar.kv_full, 1);
+    mbar_init(&bar.kv_empty, 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&bar.full[i], 1);
+      mbar_init(&bar.empty[i], 1);
+    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.dp_full, 1);
+    mbar_init(&bar.p_full, MATH_THREADS);
+    mbar_init(&bar.ds_full, MATH_THREADS);
+    mbar_init(&bar.dq_full, 1);
+    mbar_init(&bar.dq_free, MATH_THREADS);
+    mbar_init(&bar.dv_done, 1);
+    mbar_init(&bar.dk_done, 1);
+    mbar_init(&bar.acc_full, 1);
+    mbar_init(&bar.acc_free, MATH_THREADS);
+    mbar_init(&bar.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar.tmem_base, S::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = __shfl_sync(0xffffffffu, bar.tmem_base, 0);
+
+  const int total = a.batch * a.hkv * 2 * a.nt;
+  const int G = gridDim.x, c = blockIdx.x;
+  auto item_id = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
+  const int rounds = (total + G - 1) / G;
+  const int n2 = 2 * a.L;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- loads
+    int gp = 0, ii = 0, nkv = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int id = item_id(r);
+      if (id >= total) continue;
+      const GItem it = grad_item(a, id);
+      if (lane == 0) {
+        if (ii > 0) ok = mbar_wait(&bar.kv_empty, (ii - 1) & 1, ab, a.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&bar.kv_full, 2 * S::T_BYTES);
+          const int z = it.b * n2 + it.ks * a.L + GT * it.jt;
+          for (int x = 0; x < D / 64; ++x) {
+            tma_load_3d(smem + S::OFF_K + x * (GT * 128), &tm_k, &bar.kv_full, x * 64, it.kvh, z);
+            tma_load_3d(smem + S::OFF_V + x * (GT * 128), &tm_v, &bar.kv_full, x * 64, it.kvh, z);
+          }
+          ++nkv;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      const int np = a.G * it.npg;
+      for (int p = 0; p < np && ok; ++p, ++gp) {
+        const GPair pr = grad_pair(it, p);
+        const int st = gp % NSTAGE;
+        uint8_t* stage = smem + S::OFF_RING + st * S::STAGE;
+        if (lane == 0) ok = mbar_wait(&bar.empty[st], ((gp / NSTAGE) & 1) ^ 1, ab, a.status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        // lse and D of the tile's rows (0 past L); published by the arrive below
+        const int h = it.kvh * a.G + pr.g;
+        const size_t rb = ((size_t)it.b * a.hq + h) * n2 + (size_t)pr.qs * a.L;
+        float* ls = reinterpret_cast<float*>(stage + S::ST_LSE);
+        float* ds = reinterpret_cast<float*>(stage + S::ST_D);
+        for (int i = lane; i < GT; i += 32) {
+          const int t = GT * pr.qi + i;
+          ls[i] = t < a.L ? a.lse[rb + t] : 0.f;
+          ds[i] = t < a.L ? a.drow[rb + t] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar.full[st], 2 * S::T_BYTES);
+          const int z = it.b * n2 + pr.qs * a.L + GT * pr.qi;
+          for (int x = 0; x < D / 64; ++x) {
+            tma_load_3d(stage + S::ST_Q + x * (GT * 128), &tm_q, &bar.full[st], x * 64, h, z);
+            tma_load_3d(stage + S::ST_DO + x * (GT * 128), &tm_do, &bar.full[st], x * 64, h, z);
+          }
+        }
+      }
+      ++ii;
+    }
+    // wait (bounded) for the copies still in flight
+    if (lane == 0) {
+      if (nkv > 0) mbar_wait(&bar.kv_full, (nkv - 1) & 1, nullptr, a.status);
+      for (int k = 1; k <= NSTAGE && gp - k >= 0; ++k)
+        mbar_wait(&bar.full[(gp - k) % NSTAGE], ((gp - k) / NSTAGE) & 1, nullptr, a.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_ab(GT, GT, false, false);   // S^T, dP^T: K-major A, B
+      const uint32_t id_acc = idesc_ab(GT, D, false, true);    // dV, dK: TMEM A, MN-major B
+      const uint32_t id_dq = idesc_ab(GT, D, true, true);      // dQ: MN-major A and B
+      const uint32_t kb = smem_u32(smem + S::OFF_K), vb = smem_u32(smem + S::OFF_V);
+      int gp = 0, ii = 0;
+      bool ok = true;
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int id = item_id(r);
+        if (id >= total) continue;
+        const GItem it = grad_item(a, id);
+        ok = mbar_wait(&bar.kv_full, ii & 1, ab, a.status);
+        if (ok && ii > 0) ok = mbar_wait(&bar.acc_free, (ii - 1) & 1, ab, a.status);
+        const int np = a.G * it.npg;
+        for (int p = 0; p < np && ok; ++p, ++gp) {
+          const int st = gp % NSTAGE;
+          const uint32_t sb = smem_u32(smem + S::OFF_RING + st * S::STAGE);
+          const uint32_t qb = sb + S::ST_Q, dob = sb + S::ST_DO;
+          if (!(ok = mbar_wait(&bar.full[st], (gp / NSTAGE) & 1, ab, a.status))) break;
+          // the S buffer holds the previous pair's dQ part until the math threads read it
+          if (gp > 0 && !(ok = mbar_wait(&bar.dq_free, (gp - 1) & 1, ab, a.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {               // S^T = K Q^T
+            const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
+            mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(kb + off, 16, 1024),
+                        sdesc_sw128(qb + off, 16, 1024), id_qk, k != 0);
+          }
+          mma_commit(&bar.s_full);
+          // the dP buffer holds the previous pair's dS^T until its dK MMA has read it
+          if (gp > 0 && !(ok = mbar_wait(&bar.dk_done, (gp - 1) & 1, ab, a.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {               // dP^T = V dO^T
+            const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
+            mma_bf16_ss(tmem + S::TM_DP, sdesc_sw128(vb + off, 16, 1024),
+                        sdesc_sw128(dob + off, 16, 1024), id_qk, k != 0);
+          }
+          mma_commit(&bar.dp_full);
+          if (!(ok = mbar_wait(&bar.p_full, gp & 1, ab, a.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < GT / 16; ++k)                // dV += P^T dO
+            mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + 64 + k * 8,
+                        sdesc_sw128(dob + k * 2048, GT * 128, 1024), id_acc, (p | k) != 0);
+          mma_commit(&bar.dv_done);
+          if (!(ok = mbar_wait(&bar.ds_full, gp & 1, ab, a.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < GT / 16; ++k)                // dK += dS^T Q
+            mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + 64 + k * 8,
+                        sdesc_sw128(qb + k * 2048, GT * 128, 1024), id_acc, (p | k) != 0);
+          mma_commit(&bar.dk_done);
+          // dQ overwrites the S buffer, whose upper half (P^T) the dV MMA reads
+          if (!(ok = mbar_wait(&bar.dv_done, gp & 1, ab, a.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < GT / 16; ++k)                // dQ part = dS K (dS over dO)
+            mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(dob + k * 2048, GT * 128, 1024),
+                        sdesc_sw128(kb + k * 2048, GT * 128, 1024), id_dq, k != 0);
+          mma_commit(&bar.dq_full);
+          mma_commit(&bar.empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bar.kv_empty);
+        mma_commit(&bar.acc_full);
+        ++ii;
+      }
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0, nullptr, a.status);
+    }
+  } else {
+    // ---------------------------------------------------------------- math (warps 2..5)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;                  // TMEM lane: key row, then query row
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(b, parity, ab, a.status));
+    };
+    int gp = 0, ii = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int id = item_id(r);
+      if (id >= total) continue;
+      const GItem it = grad_item(a, id);
+      const int kk = GT * it.jt + row;                 // this thread's key (within stream ks)
+      const int np = a.G * it.npg;
+      for (int p = 0; p < np && ok; ++p, ++gp) {
+        const GPair pr = grad_pair(it, p);
+        const int st = gp % NSTAGE;
+        uint8_t* stage = smem + S::OFF_RING + st * S::STAGE;
+        const float* ls = reinterpret_cast<const float*>(stage + S::ST_LSE);
+        const float* dsv = reinterpret_cast<const float*>(stage + S::ST_D);
+        int lo, hi;
+        visible_cols(a, it, pr, kk, lo, hi);
+        // P^T row: exp2(scale log2e S - lse) on the visible query columns, 0 elsewhere
+        if (!(ok = warp_wait(&bar.s_full, gp & 1))) break;
+        tc_fence_after();
+        uint32_t v[GT];
+#pragma unroll
+        for (int q = 0; q < GT / 32; ++q)
+          tmem_ld32(tmem + S::TM_S + q * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+        tmem_ld_wait();
+        uint32_t pp[GT / 2];
+#pragma unroll
+        for (int q = 0; q < GT / 32; ++q) {
+          const uint32_t mk = bits(lo - 32 * q, hi + 1 - 32 * q);
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(ls + 32 * q + e);
+            const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+            float pv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              pv[u] = ((mk >> (e + u)) & 1u)
+                          ? ex2(__uint_as_float(v[32 * q + e + u]) * a.scale_log2 - l[u])
+                          : 0.f;
+            pp[16 * q + e / 2] = pack2(pv[0], pv[1]);
+            pp[16 * q + e / 2 + 1] = pack2(pv[2], pv[3]);
+          }
+        }
+        tmem_st32(tmem + S::TM_S + 64 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
+        tmem_st32(tmem + S::TM_S + 96 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&bar.p_full);
+        // dS^T row = P^T * (dP^T - D): to TMEM (dK) and, MN-major, over dO (dQ)
+        if (!(ok = warp_wait(&bar.dp_full, gp & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < GT / 32; ++q)
+          tmem_ld32(tmem + S::TM_DP + q * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+        tmem_ld_wait();
+        uint32_t* sp = pp;                             // dS over P, pair by pair
+#pragma unroll
+        for (int e = 0; e < GT; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dsv + e);
+          const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2]);
+          const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2 + 1]);
+          const float s0 = __low2float(p01) * (__uint_as_float(v[e]) - d4.x);
+          const float s1 = __high2float(p01) * (__uint_as_float(v[e + 1]) - d4.y);
+          const float s2 = __low2float(p23) * (__uint_as_float(v[e + 2]) - d4.z);
+          const float s3 = __high2float(p23) * (__uint_as_float(v[e + 3]) - d4.w);
+          sp[e / 2] = pack2(s0, s1);
+          sp[e / 2 + 1] = pack2(s2, s3);
+        }
+        tmem_st32(tmem + S::TM_DP + 64 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(sp));
+        tmem_st32(tmem + S::TM_DP + 96 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(sp + 32));
+        // dO may be overwritten once the dV MMA that reads it has completed
+        if (!(ok = warp_wait(&bar.dv_done, gp & 1))) break;
+        {
+          uint8_t* dsm = stage + S::ST_DO;               // [keys][queries], two 64-query atoms
+#pragma unroll
+          for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<uint4*>(dsm + x * (GT * 128) + swz(row, cc)) =
+                  make_uint4(sp[32 * x + 4 * cc], sp[32 * x + 4 * cc + 1],
+                             sp[32 * x + 4 * cc + 2], sp[32 * x + 4 * cc + 3]);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive_warp(&bar.ds_full);
+        // dQ part: this thread's query row
+        if (!(ok = warp_wait(&bar.dq_full, gp & 1))) break;
+        tc_fence_after();
+        uint32_t dqr[D];
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q)
+          tmem_ld32(tmem + S::TM_S + q * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(dqr + q * 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&bar.dq_free);
+        const int t = GT * pr.qi + row;
+        if (t < a.L) {
+          const int h = it.kvh * a.G + pr.g;
+          float* dst = a.dq + (((size_t)it.b * n2 + (size_t)pr.qs * a.L + t) * a.hq + h) * D;
+#pragma unroll
+          for (int e = 0; e < D; e += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + e),
+                      make_float4(__uint_as_float(dqr[e]) * a.scale,
+                                  __uint_as_float(dqr[e + 1]) * a.scale,
+                                  __uint_as_float(dqr[e + 2]) * a.scale,
+                                  __uint_as_float(dqr[e + 3]) * a.scale));
+        }
+      }
+      if (!ok) break;
+      // the item's dV and dK rows
+      if (!(ok = warp_wait(&bar.acc_full, ii & 1))) break;
+      tc_fence_after();
+      const size_t o = (((size_t)it.b * n2 + (size_t)it.ks * a.L + kk) * a.hkv + it.kvh) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {        // dV, then dK (scaled)
+        uint32_t acc[D];
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q)
+          tmem_ld32(tmem + (which ? S::TM_DK : S::TM_DV) + q * 32 + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(acc + q * 32));
+        tmem_ld_wait();
+        if (which) {
+          tc_fence_before();
+          mbar_arrive_warp(&bar.acc_free);
+        }
+        if (kk < a.L) {
+          float* dst = (which ? a.dk : a.dv) + o;
+          const float f = which ? a.scale : 1.f;
+#pragma unroll
+          for (int e = 0; e < D; e += 4)
+            *reinterpret_cast<float4*>(dst + e) =
+                make_float4(__uint_as_float(acc[e]) * f, __uint_as_float(acc[e + 1]) * f,
+                            __uint_as_float(acc[e + 2]) * f, __uint_as_float(acc[e + 3]) * f);
+        }
+      }
+      ++ii;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::TM_COLS);
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-}  // namespace
-
-namespace {
-
 struct GradBuffers {
-  float* s_c;               // [G][2L][L]   scores against the clean keys, then dP
-  float* s_m;               // [G][nb*Bb][Bb] scores inside the masked blocks, then dP
-  __nv_bfloat16* p_c;       // P, then dS (same shapes)
-  __nv_bfloat16* p_m;
   __nv_bfloat16* do_bf;     // dO in bf16, [b, 2L, hq, d]
-  float* drow;              // D, [b, 2L, hq]
+  float* drow;              // D, [b][hq][2L]
+  float* lse;               // [b][hq][2L]
   size_t bytes;
 };
 
-GradBuffers carve(void* base, int batch, int L, int B, int hq, int hkv, int d) {
+GradBuffers carve(void* base, int batch, int L, int hq, int d) {
   const size_t n = 2 * (size_t)L;
-  const size_t G = (size_t)(hq / hkv);
-  const size_t Bb = (size_t)(B < L ? B : L);
-  const size_t nb = ((size_t)L + Bb - 1) / Bb;
   GradBuffers g{};
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -206,149 +556,78 @@ GradBuffers carve(void* base, int batch, int L, int B, int hq, int hkv, int d) {
     off += align256(bytes);
     return at;
   };
-  g.s_c = reinterpret_cast<float*>(take(G * n * L * sizeof(float)));
-  g.s_m = reinterpret_cast<float*>(take(G * nb * Bb * Bb * sizeof(float)));
-  g.p_c = reinterpret_cast<__nv_bfloat16*>(take(G * n * L * sizeof(uint16_t)));
-  g.p_m = reinterpret_cast<__nv_bfloat16*>(take(G * nb * Bb * Bb * sizeof(uint16_t)));
   g.do_bf = reinterpret_cast<__nv_bfloat16*>(take((size_t)batch * n * hq * d * sizeof(uint16_t)));
   g.drow = reinterpret_cast<float*>(take((size_t)batch * n * hq * sizeof(float)));
+  g.lse = reinterpret_cast<float*>(take((size_t)batch * n * hq * sizeof(float)));
   g.bytes = off;
   return g;
+}
+
+template <int D>
+cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const GradBuffers& w, int batch, int L, int B, int hq, int hkv,
+                           float scale, float* dq, float* dk, float* dv, int32_t* status,
+                           cudaStream_t stream) {
+  using S = GSmem<D>;
+  static_assert(S::TOTAL + sizeof(GBar) <= 227 * 1024, "gradient layout fits shared memory");
+  CUtensorMap tq, tdo, tk, tv;
+  const uint64_t rows = (uint64_t)batch * 2 * L;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hq, rows};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)hq * D * 2};
+    const uint32_t box[3] = {64, 1, GT};
+    if (!encode_tmap_bf16(&tq, q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tdo, w.do_bf, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hkv, rows};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)hkv * D * 2};
+    const uint32_t box[3] = {64, 1, GT};
+    if (!encode_tmap_bf16(&tk, k, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tv, v, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  GArgs a{batch, L, B, hq, hkv, hq / hkv, (L + GT - 1) / GT, scale, scale * 1.4426950408889634f,
+          w.lse, w.drow, dq, dk, dv, status};
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(dual_grad_kernel<D>, S::TOTAL, attr);
+  if (ea != cudaSuccess) return ea;
+  const long long items = (long long)batch * hkv * 2 * a.nt;
+  const long long ctas = std::min<long long>(items, num_sms());
+  dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t dual_grad_workspace_bytes(int batch, int L, int B, int hq, int hkv, int d) {
-  return carve(nullptr, batch, L, B, hq, hkv, d).bytes;
+  (void)B;
+  (void)hkv;
+  return carve(nullptr, batch, L, hq, d).bytes;
 }
 
 cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                     const float* o, const float* d_o, int batch, int L, int B,
                                     int hq, int hkv, int d, float scale, float* dq, float* dk,
-                                    float* dv, void* workspace, cudaStream_t stream) {
+                                    float* dv, void* workspace, int32_t* status,
+                                    cudaStream_t stream) {
   const long long n = 2LL * L;
-  const int G = hq / hkv;
-  const GradBuffers w = carve(workspace, batch, L, B, hq, hkv, d);
-  const int Bb = B < L ? B : L;
-  const int nb = (L + Bb - 1) / Bb;
-  const int nfull = L / Bb, rem = L % Bb;
-
+  const GradBuffers w = carve(workspace, batch, L, hq, d);
+  cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)batch * n * hq * d * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  // row statistics: the forward without its O store
+  if ((e = launch_dual_stream(q, k, v, nullptr, batch, L, B, hq, hkv, d, scale, status, stream,
+                              w.lse)) != cudaSuccess)
+    return e;
   const long long nrows = (long long)batch * n * hq;
   grad_prep_kernel<<<(unsigned)((nrows + 7) / 8), 256, 0, stream>>>(o, d_o, w.do_bf, w.drow,
-                                                                    nrows, d);
-  count_launches(1);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  Blas& bl = blas();
-  std::lock_guard<std::mutex> lock(bl.mu);
-  if (!bl.h[dev] && cublasCreate(&bl.h[dev]) != CUBLAS_STATUS_SUCCESS) {
-    bl.h[dev] = nullptr;
-    return cudaErrorInitializationError;
-  }
-  cublasHandle_t hb = bl.h[dev];
-  if (cublasSetStream(hb, stream) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  const float one = 1.f, zero = 0.f;
-  const int ldq = hq * d, ldk = hkv * d, nn = (int)n;
-  const long long strideC = n * L;                      // one head's S_c
-  const long long strideM = (long long)nb * Bb * Bb;    // one head's S_m
-  const long long blkM = (long long)Bb * Bb;            // one block of S_m
-  const float scale_log2 = scale * kLog2e;
-  const unsigned grows = (unsigned)(G * n);
-  bool good = true;
-  auto ok = [&](cublasStatus_t st) { good = good && st == CUBLAS_STATUS_SUCCESS; };
-  const cublasOperation_t N_ = CUBLAS_OP_N, T_ = CUBLAS_OP_T;
-  const cudaDataType_t BF = CUDA_R_16BF, F32 = CUDA_R_32F;
-  const cublasComputeType_t CT = CUBLAS_COMPUTE_32F;
-
-  // S = X Y^T on the two blocks (X: query-side rows, Y: key-side rows; both bf16), into
-  // (c, m): the batch over g for the clean-key block, and per g the batch over masked
-  // blocks plus the short last block.
-  auto scores = [&](const void* X0, int ldx, const void* Y, float* c, float* m) {
-    // clean keys: c_g[i][j] = sum X_g[i] Y[j], i < 2L, j < L  (column-major C^T = Y X_g^T)
-    ok(cublasGemmStridedBatchedEx(hb, T_, N_, L, nn, d, &one, Y, BF, ldk, 0, X0, BF, ldx, d,
-                                  &zero, c, F32, L, strideC, G, CT, CUBLAS_GEMM_DEFAULT));
-    for (int g = 0; g < G; ++g) {
-      const uint16_t* Xg = static_cast<const uint16_t*>(X0) + g * d + (size_t)L * ldx;
-      const uint16_t* Ym = static_cast<const uint16_t*>(Y) + (size_t)L * ldk;
-      float* mg = m + g * strideM;
-      if (nfull)
-        ok(cublasGemmStridedBatchedEx(hb, T_, N_, Bb, Bb, d, &one, Ym, BF, ldk,
-                                      (long long)Bb * ldk, Xg, BF, ldx, (long long)Bb * ldx,
-                                      &zero, mg, F32, Bb, blkM, nfull, CT, CUBLAS_GEMM_DEFAULT));
-      if (rem)
-        ok(cublasGemmEx(hb, T_, N_, rem, rem, d, &one, Ym + (size_t)nfull * Bb * ldk, BF, ldk,
-                        Xg + (size_t)nfull * Bb * ldx, BF, ldx, &zero, mg + nfull * blkM, F32,
-                        Bb, CT, CUBLAS_GEMM_DEFAULT));
-    }
-  };
-  // R += alpha sum_g P_g^T X_g for the key-side rows R (dV with P, X = dO; dK with dS,
-  // X = Q): the clean keys from the clean block, the masked keys block by block.
-  auto key_side = [&](const __nv_bfloat16* pc, const __nv_bfloat16* pm, const void* X0,
-                      int ldx, float alpha, float* R) {
-    for (int g = 0; g < G; ++g) {
-      const float* beta = g ? &one : &zero;
-      const uint16_t* Xg = static_cast<const uint16_t*>(X0) + g * d;
-      // R[0:L]^T (d x L) = X_g^T (d x 2L) . P_c (2L x L)
-      ok(cublasGemmEx(hb, N_, T_, d, L, nn, &alpha, Xg, BF, ldx, pc + g * strideC, BF, L, beta,
-                      R, F32, ldk, CT, CUBLAS_GEMM_DEFAULT));
-      const uint16_t* Xm = Xg + (size_t)L * ldx;
-      float* Rm = R + (size_t)L * ldk;
-      if (nfull)
-        ok(cublasGemmStridedBatchedEx(hb, N_, T_, d, Bb, Bb, &alpha, Xm, BF, ldx,
-                                      (long long)Bb * ldx, pm + g * strideM, BF, Bb, blkM, beta,
-                                      Rm, F32, ldk, (long long)Bb * ldk, nfull, CT,
-                                      CUBLAS_GEMM_DEFAULT));
-      if (rem)
-        ok(cublasGemmEx(hb, N_, T_, d, rem, rem, &alpha, Xm + (size_t)nfull * Bb * ldx, BF, ldx,
-                        pm + g * strideM + nfull * blkM, BF, Bb, beta,
-                        Rm + (size_t)nfull * Bb * ldk, F32, ldk, CT, CUBLAS_GEMM_DEFAULT));
-    }
-  };
-
-  for (int b = 0; b < batch && good; ++b) {
-    for (int hk = 0; hk < hkv && good; ++hk) {
-      const int h0 = hk * G;
-      const uint16_t* Q0 = q + ((size_t)b * n * hq + h0) * d;
-      const __nv_bfloat16* dO0 = w.do_bf + ((size_t)b * n * hq + h0) * d;
-      const uint16_t* K = k + ((size_t)b * n * hkv + hk) * d;
-      const uint16_t* V = v + ((size_t)b * n * hkv + hk) * d;
-      float* dQ0 = dq + ((size_t)b * n * hq + h0) * d;
-      float* dK = dk + ((size_t)b * n * hkv + hk) * d;
-      float* dV = dv + ((size_t)b * n * hkv + hk) * d;
-      scores(Q0, ldq, K, w.s_c, w.s_m);
-      grad_softmax_kernel<<<grows, 256, 0, stream>>>(w.s_c, w.s_m, w.p_c, w.p_m, L, B,
-                                                     scale_log2);
-      scores(dO0, ldq, V, w.s_c, w.s_m);                  // dP
-      key_side(w.p_c, w.p_m, dO0, ldq, 1.f, dV);
-      grad_ds_kernel<<<grows, 256, 0, stream>>>(w.p_c, w.p_m, w.s_c, w.s_m, w.drow, L, B, hq,
-                                                h0, b);
-      key_side(w.p_c, w.p_m, Q0, ldq, scale, dK);
-      // dQ_g = scale (dS_c K_c + dS_m K_m)   (column-major: dQ_g^T = K^T dS_g^T)
-      ok(cublasGemmStridedBatchedEx(hb, N_, N_, d, nn, L, &scale, K, BF, ldk, 0, w.p_c, BF, L,
-                                    strideC, &zero, dQ0, F32, ldq, d, G, CT,
-                                    CUBLAS_GEMM_DEFAULT));
-      for (int g = 0; g < G; ++g) {
-        const uint16_t* Km = K + (size_t)L * ldk;
-        float* dQm = dQ0 + g * d + (size_t)L * ldq;
-        if (nfull)
-          ok(cublasGemmStridedBatchedEx(hb, N_, N_, d, Bb, Bb, &scale, Km, BF, ldk,
-                                        (long long)Bb * ldk, w.p_m + g * strideM, BF, Bb, blkM,
-                                        &one, dQm, F32, ldq, (long long)Bb * ldq, nfull, CT,
-                                        CUBLAS_GEMM_DEFAULT));
-        if (rem)
-          ok(cublasGemmEx(hb, N_, N_, d, rem, rem, &scale, Km + (size_t)nfull * Bb * ldk, BF,
-                          ldk, w.p_m + g * strideM + nfull * blkM, BF, Bb, &one,
-                          dQm + (size_t)nfull * Bb * ldq, F32, ldq, CT, CUBLAS_GEMM_DEFAULT));
-      }
-      count_launches(2);
-    }
-  }
-  if (!good) return cudaErrorUnknown;
-  return cudaGetLastError();
+                                                                    nrows, (int)n, hq, d);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = d == 64 ? launch_grad_tc<64>(q, k, v, w, batch, L, B, hq, hkv, scale, dq, dk, dv, status,
+                                   stream)
+              : launch_grad_tc<128>(q, k, v, w, batch, L, B, hq, hkv, scale, dq, dk, dv, status,
+                                    stream);
+  count_launches(2);
+  return e;
 }
 
 }  // namespace mars

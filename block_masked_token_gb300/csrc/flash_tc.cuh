@@ -411,7 +411,8 @@ MARS_DEV void exp2_pack64(const uint32_t (&r)[BKV], int c0, float scale_log2, fl
 // Policy provides: row_valid(row), row_vis(row), tile(j) -> Tile (with .full set when
 // every row sees every key of tile j, so no per-key test runs), cols(vis, tile) ->
 // ColRange (the columns of tile j visible to the row; a tile must admit only keys it
-// owns, so no key is counted twice), and either store_chunk(row, col, 32 fp32 of O, 1/l,
+// owns, so no key is counted twice), with kRowStats row_stats(row, m, l) once the row is
+// done, and either store_chunk(row, col, 32 fp32 of O, 1/l,
 // m, l) or, with kStagedStore, kStageBoxes, stage(smem) (the staging area) and
 // store_boxes(staging, first box, boxes), which issues the TMA stores of O/l.
 // Each tile's S row is read from TMEM once (4 loads, one wait) into registers.
@@ -509,6 +510,7 @@ MARS_DEV bool softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
     mbar_arrive_warp(&bar.p_full[sb]);
   }
   if (!ok) return false;
+  if constexpr (Policy::kRowStats) pol.row_stats(row, m, l);
   if (!warp_wait(&bar.o_final, o_parity)) return false;
   tc_fence_after();
   const float inv = (l > 0.f) ? 1.f / l : 0.f;

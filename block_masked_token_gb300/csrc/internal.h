@@ -53,7 +53,8 @@ size_t dual_grad_workspace_bytes(int batch, int L, int B, int hq, int hkv, int d
 cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                     const float* o, const float* d_o, int batch, int L, int B,
                                     int hq, int hkv, int d, float scale, float* dq, float* dk,
-                                    float* dv, void* workspace, cudaStream_t stream);
+                                    float* dv, void* workspace, int32_t* status,
+                                    cudaStream_t stream);
 
 // ---- Dual-stream training loss (L_mask + L_AR) over the 2L rows of each sequence.
 size_t ce_workspace_bytes(int batch, int L, int vocab);
@@ -83,9 +84,12 @@ cudaError_t set_smem_limit_once(Kernel* fn, int bytes, std::atomic<int> (&done)[
   return e;
 }
 
-// ---- Dual-stream attention under mask M.
+// ---- Dual-stream attention under mask M. o may be null when lse is given (the row
+// statistics alone: lse[b][h][row] = log2 of the softmax denominator, in units of
+// scale*log2(e)*score).
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* o, int batch, int L, int B, int hq, int hkv, int d,
-                               float scale, int32_t* status, cudaStream_t stream);
+                               float scale, int32_t* status, cudaStream_t stream,
+                               float* lse = nullptr);
 
 }  // namespace mars

@@ -186,7 +186,6 @@ int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mar
                                int hq, int hkv, int d, float scale, float* dq, float* dk,
                                float* dv, void* workspace, size_t ws_bytes, int32_t* status,
                                void* stream) {
-  (void)status;
   if (batch < 0 || L < 1 || B < 1) return MARS_EINVAL;
   int rc = check_heads(hq, hkv, d);
   if (rc) return rc;
@@ -199,7 +198,7 @@ int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mar
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
   if (isinf(scale)) return MARS_EINVAL;
   return cuda_rc(mars::launch_dual_stream_grad(q, k, v, o, d_o, batch, L, B, hq, hkv, d, scale,
-                                               dq, dk, dv, workspace,
+                                               dq, dk, dv, workspace, status,
                                                static_cast<cudaStream_t>(stream)));
 }
 

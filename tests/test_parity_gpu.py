@@ -170,6 +170,7 @@ def run_dual_grad(x, L, B):
     (1, 64, 64, 2, 2, 128),        # B = L
     (1, 20, 1, 2, 1, 64),          # B = 1: masked rows see only themselves among masked keys
     (1, 33, 40, 2, 2, 128),        # B > L: one block
+    (1, 300, 48, 4, 2, 64),        # blocks straddle 128-key tiles; three key tiles a stream
 ])
 def test_dual_stream_grad_small(b, L, B, hq, hkv, d):
     cfg = W.DualStreamConfig("g", b, L, B, hq, hkv, d)
@@ -178,6 +179,21 @@ def test_dual_stream_grad_small(b, L, B, hq, hkv, d):
     d_o, dq, dk, dv = run_dual_grad(xd, L, B)
     rq, rk, rv = oracle.attn_dual_stream_grad(f64(x["q"]), f64(x["k"]), f64(x["v"]),
                                               d_o.cpu().double().numpy(), L, B)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        err = _rel(got.cpu().numpy(), ref)
+        assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
+
+
+def test_dual_stream_grad_many_items_per_cta():
+    """More (batch, kv head, key tile) work items than SMs, so persistent CTAs carry the
+    rings, TMEM accumulators and barrier phases from item to item; ragged L, odd-sized
+    blocks that straddle key tiles."""
+    cfg = W.DualStreamConfig("gm", 3, 1100, 24, 6, 3, 64)
+    x = W.make_dual_stream_inputs(cfg, seed=5)
+    xd = {kk: vv.to(DEV) for kk, vv in x.items()}
+    d_o, dq, dk, dv = run_dual_grad(xd, cfg.L, cfg.B)
+    rq, rk, rv = oracle.attn_dual_stream_grad(f64(x["q"]), f64(x["k"]), f64(x["v"]),
+                                              d_o.cpu().double().numpy(), cfg.L, cfg.B)
     for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
         err = _rel(got.cpu().numpy(), ref)
         assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
