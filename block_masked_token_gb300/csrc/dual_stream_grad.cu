@@ -5,16 +5,20 @@
 // With P = softmax(scale * S + M), S = Q K^T, and D_i = rowsum(dO_i * O_i):
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dK = scale dS^T Q,   dQ = scale dS K.
 // One fused tcgen05 kernel, never storing a score block:
-//   - a work item is (batch, kv head, 128-key tile of one stream); one persistent CTA per
-//     SM runs items heaviest first;
-//   - the item visits every (query head of the kv group, 128-row query tile) pair that sees
-//     one of its keys under M, and per pair runs five MMAs with TMEM accumulators:
+//   - a work item is (batch, query head, 128-key tile of one stream); one persistent CTA
+//     per SM runs items heaviest first;
+//   - the item visits every 128-row query tile that sees one of its keys under M, and per
+//     (key tile, query tile) pair runs five MMAs with TMEM accumulators:
 //       S^T = K Q^T, dP^T = V dO^T            (keys on TMEM lanes, queries on columns)
-//       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM)
+//       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM, bf16 over the
+//                                              fp32 columns they were formed from)
 //       dQ_pair = dS K                        (A = dS from shared memory, MN-major)
-//     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by one thread per key row;
-//   - dK and dV stay in TMEM over all of the item's pairs and are written once; each pair's
-//     dQ part is added to dQ (fp32 vector atomics), so dQ is zeroed first.
+//     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by two threads per key row
+//     (64 query columns each: with lse known, no row-wide exchange is needed);
+//   - dK and dV stay in TMEM over the item's pairs; at the end of the item they are added
+//     to dK and dV, and each pair's dQ part to dQ (fp32 vector atomics), so all three are
+//     zeroed first. Splitting the G query heads of a kv group into separate items keeps
+//     the work items small enough to balance across the SMs.
 // lse (log2 of each query row's softmax denominator) comes from a statistics-only run of
 // the forward kernel; P and dS are rounded to bf16 as MMA operands.
 #include <cuda_bf16.h>
@@ -33,8 +37,9 @@ namespace {
 using namespace sm100;
 
 constexpr int GT = 128;                // keys per key tile, query rows per query tile
-constexpr int GRAD_THREADS = 192;      // warp 0 loads, warp 1 TMEM + MMAs, warps 2..5 math
-constexpr int MATH_THREADS = 128;
+constexpr int MATH_WARPS = 8;          // two per TMEM lane quadrant, 64 query columns each
+constexpr int GRAD_THREADS = 64 + 32 * MATH_WARPS;   // warp 0 loads, warp 1 TMEM + MMAs
+constexpr int MATH_THREADS = 32 * MATH_WARPS;
 constexpr int NSTAGE = 2;              // Q / dO ring depth
 
 // dO (fp32) -> bf16 copy, and D[b][h][i] = sum_d dO[b, i, h, d] * O[b, i, h, d]. One warp
@@ -97,18 +102,21 @@ struct GArgs {
   int32_t* status;
 };
 
-// Work item: keys [128 jt, 128 jt + 128) of stream ks (0 clean, 1 masked) of (b, kvh).
-// Ids run over clean key tiles from the first (seen by most query tiles) to the last, then
-// over the masked key tiles.
+// Work item: keys [128 jt, 128 jt + 128) of stream ks (0 clean, 1 masked) of (b, kvh),
+// against query head kvh*G + g. Ids run over clean key tiles from the first (seen by most
+// query tiles) to the last, then over the masked key tiles.
 struct GItem {
-  int b, kvh, ks, jt;
+  int b, kvh, g, ks, jt;
   int nc, mlo, npg;        // clean keys: clean query tiles [jt, nt), masked [mlo, nt)
 };
 
 MARS_DEV GItem grad_item(const GArgs& a, int id) {
   GItem it;
-  const int per = a.batch * a.hkv;
-  const int kt = id / per, bk = id % per;
+  const int per = a.batch * a.hkv * a.G;
+  const int kt = id / per;
+  int bk = id % per;
+  it.g = bk % a.G;
+  bk /= a.G;
   it.b = bk % a.batch;
   it.kvh = bk / a.batch;
   if (kt < a.nt) {
@@ -132,15 +140,14 @@ MARS_DEV GItem grad_item(const GArgs& a, int id) {
   return it;
 }
 
-// Pair p of an item: query head g of the group, query stream qs, query tile qi.
+// Pair p of an item: query stream qs, query tile qi.
 struct GPair {
-  int g, qs, qi;
+  int qs, qi;
 };
 
 MARS_DEV GPair grad_pair(const GItem& it, int p) {
   GPair q;
-  q.g = p / it.npg;
-  const int r = p % it.npg;
+  const int r = p;
   if (r < it.nc) {
     q.qs = 0;
     q.qi = it.jt + r;
@@ -197,6 +204,11 @@ MARS_DEV float ex2(float x) {
 // swizzle layout, which is also the MMA's canonical one).
 MARS_DEV uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
+// TMEM column of K-step k (16 queries) of P^T or dS^T in its buffer: queries [0, 64) are
+// packed over columns [0, 32) and queries [64, 128) over [64, 96), the first half of each
+// half's own fp32 columns.
+MARS_DEV uint32_t p_col(int k) { return (uint32_t)(8 * k + (k >= 4 ? 32 : 0)); }
+
 // Instruction descriptor with A and B majorness (bit 15: A MN-major, bit 16: B MN-major).
 MARS_DEV uint32_t idesc_ab(int M, int N, bool a_mn, bool b_mn) {
   return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
@@ -246,7 +258,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = __shfl_sync(0xffffffffu, bar.tmem_base, 0);
 
-  const int total = a.batch * a.hkv * 2 * a.nt;
+  const int total = a.batch * a.hkv * a.G * 2 * a.nt;
   const int G = gridDim.x, c = blockIdx.x;
   auto item_id = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
   const int rounds = (total + G - 1) / G;
@@ -273,7 +285,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      const int np = a.G * it.npg;
+      const int np = it.npg;
       for (int p = 0; p < np && ok; ++p, ++gp) {
         const GPair pr = grad_pair(it, p);
         const int st = gp % NSTAGE;
@@ -282,7 +294,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // lse and D of the tile's rows (0 past L); published by the arrive below
-        const int h = it.kvh * a.G + pr.g;
+        const int h = it.kvh * a.G + it.g;
         const size_t rb = ((size_t)it.b * a.hq + h) * n2 + (size_t)pr.qs * a.L;
         float* ls = reinterpret_cast<float*>(stage + S::ST_LSE);
         float* ds = reinterpret_cast<float*>(stage + S::ST_D);
@@ -325,7 +337,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         const GItem it = grad_item(a, id);
         ok = mbar_wait(&bar.kv_full, ii & 1, ab, a.status);
         if (ok && ii > 0) ok = mbar_wait(&bar.acc_free, (ii - 1) & 1, ab, a.status);
-        const int np = a.G * it.npg;
+        const int np = it.npg;
         for (int p = 0; p < np && ok; ++p, ++gp) {
           const int st = gp % NSTAGE;
           const uint32_t sb = smem_u32(smem + S::OFF_RING + st * S::STAGE);
@@ -355,17 +367,17 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < GT / 16; ++k)                // dV += P^T dO
-            mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + 64 + k * 8,
+            mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + p_col(k),
                         sdesc_sw128(dob + k * 2048, GT * 128, 1024), id_acc, (p | k) != 0);
           mma_commit(&bar.dv_done);
           if (!(ok = mbar_wait(&bar.ds_full, gp & 1, ab, a.status))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < GT / 16; ++k)                // dK += dS^T Q
-            mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + 64 + k * 8,
+            mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + p_col(k),
                         sdesc_sw128(qb + k * 2048, GT * 128, 1024), id_acc, (p | k) != 0);
           mma_commit(&bar.dk_done);
-          // dQ overwrites the S buffer, whose upper half (P^T) the dV MMA reads
+          // dQ overwrites the S buffer, whose P^T columns the dV MMA reads
           if (!(ok = mbar_wait(&bar.dv_done, gp & 1, ab, a.status))) break;
           tc_fence_after();
 #pragma unroll
@@ -384,10 +396,13 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_wait(&bar.drain, 0, nullptr, a.status);
     }
   } else {
-    // ---------------------------------------------------------------- math (warps 2..5)
+    // ------------------------------------------------- math (warps 2..9, two per quadrant)
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;                  // query columns [64 half, 64 half + 64)
     const int row = quad * 32 + lane;                  // TMEM lane: key row, then query row
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    constexpr int HC = GT / 2;                         // columns per thread
+    constexpr int HD = D / 2;                          // accumulator columns per thread
     auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, ab, a.status));
     };
@@ -398,26 +413,30 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (id >= total) continue;
       const GItem it = grad_item(a, id);
       const int kk = GT * it.jt + row;                 // this thread's key (within stream ks)
-      const int np = a.G * it.npg;
+      const int h = it.kvh * a.G + it.g;
+      const int np = it.npg;
       for (int p = 0; p < np && ok; ++p, ++gp) {
         const GPair pr = grad_pair(it, p);
         const int st = gp % NSTAGE;
         uint8_t* stage = smem + S::OFF_RING + st * S::STAGE;
-        const float* ls = reinterpret_cast<const float*>(stage + S::ST_LSE);
-        const float* dsv = reinterpret_cast<const float*>(stage + S::ST_D);
+        const float* ls = reinterpret_cast<const float*>(stage + S::ST_LSE) + HC * half;
+        const float* dsv = reinterpret_cast<const float*>(stage + S::ST_D) + HC * half;
         int lo, hi;
         visible_cols(a, it, pr, kk, lo, hi);
-        // P^T row: exp2(scale log2e S - lse) on the visible query columns, 0 elsewhere
+        lo -= HC * half;
+        hi -= HC * half;
+        // P^T: exp2(scale log2e S - lse) on the visible query columns, 0 elsewhere
         if (!(ok = warp_wait(&bar.s_full, gp & 1))) break;
         tc_fence_after();
-        uint32_t v[GT];
+        uint32_t v[HC];
 #pragma unroll
-        for (int q = 0; q < GT / 32; ++q)
-          tmem_ld32(tmem + S::TM_S + q * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+        for (int q = 0; q < HC / 32; ++q)
+          tmem_ld32(tmem + S::TM_S + HC * half + q * 32 + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
         tmem_ld_wait();
-        uint32_t pp[GT / 2];
+        uint32_t pp[HC / 2];
 #pragma unroll
-        for (int q = 0; q < GT / 32; ++q) {
+        for (int q = 0; q < HC / 32; ++q) {
           const uint32_t mk = bits(lo - 32 * q, hi + 1 - 32 * q);
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
@@ -433,21 +452,21 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
             pp[16 * q + e / 2 + 1] = pack2(pv[2], pv[3]);
           }
         }
-        tmem_st32(tmem + S::TM_S + 64 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
-        tmem_st32(tmem + S::TM_S + 96 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp + 32));
+        // over this half's own S^T columns (the other half may still be reading its own)
+        tmem_st32(tmem + S::TM_S + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive_warp(&bar.p_full);
-        // dS^T row = P^T * (dP^T - D): to TMEM (dK) and, MN-major, over dO (dQ)
+        // dS^T = P^T * (dP^T - D): to TMEM (dK) and, MN-major, over dO (dQ)
         if (!(ok = warp_wait(&bar.dp_full, gp & 1))) break;
         tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < GT / 32; ++q)
-          tmem_ld32(tmem + S::TM_DP + q * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
+        for (int q = 0; q < HC / 32; ++q)
+          tmem_ld32(tmem + S::TM_DP + HC * half + q * 32 + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
         tmem_ld_wait();
-        uint32_t* sp = pp;                             // dS over P, pair by pair
 #pragma unroll
-        for (int e = 0; e < GT; e += 4) {
+        for (int e = 0; e < HC; e += 4) {                // dS over P, pair by pair
           const float4 d4 = *reinterpret_cast<const float4*>(dsv + e);
           const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2]);
           const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2 + 1]);
@@ -455,43 +474,41 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
           const float s1 = __high2float(p01) * (__uint_as_float(v[e + 1]) - d4.y);
           const float s2 = __low2float(p23) * (__uint_as_float(v[e + 2]) - d4.z);
           const float s3 = __high2float(p23) * (__uint_as_float(v[e + 3]) - d4.w);
-          sp[e / 2] = pack2(s0, s1);
-          sp[e / 2 + 1] = pack2(s2, s3);
+          pp[e / 2] = pack2(s0, s1);
+          pp[e / 2 + 1] = pack2(s2, s3);
         }
-        tmem_st32(tmem + S::TM_DP + 64 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(sp));
-        tmem_st32(tmem + S::TM_DP + 96 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(sp + 32));
+        tmem_st32(tmem + S::TM_DP + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
         // dO may be overwritten once the dV MMA that reads it has completed
         if (!(ok = warp_wait(&bar.dv_done, gp & 1))) break;
         {
-          uint8_t* dsm = stage + S::ST_DO;               // [keys][queries], two 64-query atoms
+          // [keys][queries] in two 64-query atoms: this thread's half is atom `half`
+          uint8_t* dsm = stage + S::ST_DO + half * (GT * 128);
 #pragma unroll
-          for (int x = 0; x < 2; ++x)
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-              *reinterpret_cast<uint4*>(dsm + x * (GT * 128) + swz(row, cc)) =
-                  make_uint4(sp[32 * x + 4 * cc], sp[32 * x + 4 * cc + 1],
-                             sp[32 * x + 4 * cc + 2], sp[32 * x + 4 * cc + 3]);
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4*>(dsm + swz(row, cc)) =
+                make_uint4(pp[4 * cc], pp[4 * cc + 1], pp[4 * cc + 2], pp[4 * cc + 3]);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive_warp(&bar.ds_full);
-        // dQ part: this thread's query row
+        // dQ part: this thread's query row, columns [HD half, HD half + HD)
         if (!(ok = warp_wait(&bar.dq_full, gp & 1))) break;
         tc_fence_after();
-        uint32_t dqr[D];
+        uint32_t dqr[HD];
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q)
-          tmem_ld32(tmem + S::TM_S + q * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(dqr + q * 32));
+        for (int q = 0; q < HD / 32; ++q)
+          tmem_ld32(tmem + S::TM_S + HD * half + q * 32 + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(dqr + q * 32));
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive_warp(&bar.dq_free);
         const int t = GT * pr.qi + row;
         if (t < a.L) {
-          const int h = it.kvh * a.G + pr.g;
-          float* dst = a.dq + (((size_t)it.b * n2 + (size_t)pr.qs * a.L + t) * a.hq + h) * D;
+          float* dst = a.dq + (((size_t)it.b * n2 + (size_t)pr.qs * a.L + t) * a.hq + h) * D +
+                       HD * half;
 #pragma unroll
-          for (int e = 0; e < D; e += 4)
+          for (int e = 0; e < HD; e += 4)
             atomicAdd(reinterpret_cast<float4*>(dst + e),
                       make_float4(__uint_as_float(dqr[e]) * a.scale,
                                   __uint_as_float(dqr[e + 1]) * a.scale,
@@ -500,30 +517,33 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
       if (!ok) break;
-      // the item's dV and dK rows
+      // the item's dV and dK rows (this thread's half of the columns), added to dV and dK
       if (!(ok = warp_wait(&bar.acc_full, ii & 1))) break;
       tc_fence_after();
-      const size_t o = (((size_t)it.b * n2 + (size_t)it.ks * a.L + kk) * a.hkv + it.kvh) * D;
+      uint32_t dvr[HD], dkr[HD];
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {        // dV, then dK (scaled)
-        uint32_t acc[D];
+      for (int q = 0; q < HD / 32; ++q) {
+        tmem_ld32(tmem + S::TM_DV + HD * half + q * 32 + lane_off,
+                  *reinterpret_cast<uint32_t(*)[32]>(dvr + q * 32));
+        tmem_ld32(tmem + S::TM_DK + HD * half + q * 32 + lane_off,
+                  *reinterpret_cast<uint32_t(*)[32]>(dkr + q * 32));
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&bar.acc_free);
+      if (kk < a.L) {
+        const size_t o =
+            (((size_t)it.b * n2 + (size_t)it.ks * a.L + kk) * a.hkv + it.kvh) * D + HD * half;
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q)
-          tmem_ld32(tmem + (which ? S::TM_DK : S::TM_DV) + q * 32 + lane_off,
-                    *reinterpret_cast<uint32_t(*)[32]>(acc + q * 32));
-        tmem_ld_wait();
-        if (which) {
-          tc_fence_before();
-          mbar_arrive_warp(&bar.acc_free);
-        }
-        if (kk < a.L) {
-          float* dst = (which ? a.dk : a.dv) + o;
-          const float f = which ? a.scale : 1.f;
-#pragma unroll
-          for (int e = 0; e < D; e += 4)
-            *reinterpret_cast<float4*>(dst + e) =
-                make_float4(__uint_as_float(acc[e]) * f, __uint_as_float(acc[e + 1]) * f,
-                            __uint_as_float(acc[e + 2]) * f, __uint_as_float(acc[e + 3]) * f);
+        for (int e = 0; e < HD; e += 4) {
+          atomicAdd(reinterpret_cast<float4*>(a.dv + o + e),
+                    make_float4(__uint_as_float(dvr[e]), __uint_as_float(dvr[e + 1]),
+                                __uint_as_float(dvr[e + 2]), __uint_as_float(dvr[e + 3])));
+          atomicAdd(reinterpret_cast<float4*>(a.dk + o + e),
+                    make_float4(__uint_as_float(dkr[e]) * a.scale,
+                                __uint_as_float(dkr[e + 1]) * a.scale,
+                                __uint_as_float(dkr[e + 2]) * a.scale,
+                                __uint_as_float(dkr[e + 3]) * a.scale));
         }
       }
       ++ii;
@@ -591,7 +611,7 @@ cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t*
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(dual_grad_kernel<D>, S::TOTAL, attr);
   if (ea != cudaSuccess) return ea;
-  const long long items = (long long)batch * hkv * 2 * a.nt;
+  const long long items = (long long)batch * hq * 2 * a.nt;
   const long long ctas = std::min<long long>(items, num_sms());
   dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();
@@ -613,6 +633,10 @@ cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const 
   const long long n = 2LL * L;
   const GradBuffers w = carve(workspace, batch, L, hq, d);
   cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)batch * n * hq * d * sizeof(float), stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(dk, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(dv, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   // row statistics: the forward without its O store
   if ((e = launch_dual_stream(q, k, v, nullptr, batch, L, B, hq, hkv, d, scale, status, stream,
