@@ -16,8 +16,8 @@
 //     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by two threads per key row
 //     (64 query columns each: with lse known, no row-wide exchange is needed);
 //   - dK and dV stay in TMEM over the item's pairs; at the end of the item they are added
-//     to dK and dV, and each pair's dQ part to dQ (fp32 vector atomics), so all three are
-//     zeroed first. Splitting the G query heads of a kv group into separate items keeps
+//     to dK and dV (fp32 vector atomics); each pair's dQ part is staged in shared memory
+//     and added to dQ by a TMA bulk reduce-add. All three are zeroed first. Splitting the G query heads of a kv group into separate items keeps
 //     the work items small enough to balance across the SMs.
 // lse (log2 of each query row's softmax denominator) comes from a statistics-only run of
 // the forward kernel; P and dS are rounded to bf16 as MMA operands.
@@ -84,7 +84,7 @@ struct GSmem {
 
 struct GBar {
   uint64_t kv_full, kv_empty;
-  uint64_t full[NSTAGE], empty[NSTAGE];
+  uint64_t full[NSTAGE], dq_staged[NSTAGE];
   uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, dv_done, dk_done;
   uint64_t acc_full, acc_free, drain;
   uint32_t tmem_base;
@@ -96,7 +96,6 @@ struct GArgs {
   float scale, scale_log2;
   const float* lse;        // [batch][hq][2L]
   const float* drow;       // [batch][hq][2L]
-  float* dq;               // [batch][2L][hq][D], zeroed
   float* dk;               // [batch][2L][hkv][D]
   float* dv;
   int32_t* status;
@@ -219,7 +218,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_do,
                  const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, GArgs a) {
+                 const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_dq, GArgs a) {
   using S = GSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ GBar bar;
@@ -234,7 +234,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&bar.kv_empty, 1);
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&bar.full[i], 1);
-      mbar_init(&bar.empty[i], 1);
+      mbar_init(&bar.dq_staged[i], MATH_THREADS);
     }
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.dp_full, 1);
@@ -268,6 +268,21 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---------------------------------------------------------------- loads
     int gp = 0, ii = 0, nkv = 0;
     bool ok = true;
+    // coordinates in dQ (head, row, 2 batch + stream) of the pair each stage last held
+    int hist_h[NSTAGE], hist_t[NSTAGE], hist_w[NSTAGE];
+    // lane 0: add pair g2's dQ part, staged over its stage by the math warps, into dQ;
+    // returns once the bulk reduction has read the stage
+    auto flush = [&](int g2) -> bool {
+      const int s2 = g2 % NSTAGE;
+      if (!mbar_wait(&bar.dq_staged[s2], (g2 / NSTAGE) & 1, ab, a.status)) return false;
+      const uint8_t* stg = smem + S::OFF_RING + s2 * S::STAGE;
+      for (int c2 = 0; c2 < D / 32; ++c2)
+        tma_reduce_add_4d(&tm_dq, stg + c2 * (GT * 128), c2 * 32, hist_h[s2], hist_t[s2],
+                          hist_w[s2]);
+      bulk_commit();
+      bulk_wait_read_all();
+      return true;
+    };
     for (int r = 0; r < rounds && ok; ++r) {
       const int id = item_id(r);
       if (id >= total) continue;
@@ -290,7 +305,8 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         const GPair pr = grad_pair(it, p);
         const int st = gp % NSTAGE;
         uint8_t* stage = smem + S::OFF_RING + st * S::STAGE;
-        if (lane == 0) ok = mbar_wait(&bar.empty[st], ((gp / NSTAGE) & 1) ^ 1, ab, a.status);
+        // the stage's previous pair is done once its dQ part has been reduced out of it
+        if (lane == 0 && gp >= NSTAGE) ok = flush(gp - NSTAGE);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // lse and D of the tile's rows (0 past L); published by the arrive below
@@ -305,6 +321,9 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         __syncwarp();
         if (lane == 0) {
+          hist_h[st] = h;
+          hist_t[st] = GT * pr.qi;
+          hist_w[st] = it.b * 2 + pr.qs;
           mbar_arrive_expect_tx(&bar.full[st], 2 * S::T_BYTES);
           const int z = it.b * n2 + pr.qs * a.L + GT * pr.qi;
           for (int x = 0; x < D / 64; ++x) {
@@ -315,8 +334,9 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       ++ii;
     }
-    // wait (bounded) for the copies still in flight
+    // the last pairs' dQ parts; then wait (bounded) for the copies still in flight
     if (lane == 0) {
+      for (int g2 = gp - NSTAGE < 0 ? 0 : gp - NSTAGE; ok && g2 < gp; ++g2) ok = flush(g2);
       if (nkv > 0) mbar_wait(&bar.kv_full, (nkv - 1) & 1, nullptr, a.status);
       for (int k = 1; k <= NSTAGE && gp - k >= 0; ++k)
         mbar_wait(&bar.full[(gp - k) % NSTAGE], ((gp - k) / NSTAGE) & 1, nullptr, a.status);
@@ -385,7 +405,6 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
             mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(dob + k * 2048, GT * 128, 1024),
                         sdesc_sw128(kb + k * 2048, GT * 128, 1024), id_dq, k != 0);
           mma_commit(&bar.dq_full);
-          mma_commit(&bar.empty[st]);
         }
         if (!ok) break;
         mma_commit(&bar.kv_empty);
@@ -413,7 +432,6 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (id >= total) continue;
       const GItem it = grad_item(a, id);
       const int kk = GT * it.jt + row;                 // this thread's key (within stream ks)
-      const int h = it.kvh * a.G + it.g;
       const int np = it.npg;
       for (int p = 0; p < np && ok; ++p, ++gp) {
         const GPair pr = grad_pair(it, p);
@@ -503,18 +521,23 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive_warp(&bar.dq_free);
-        const int t = GT * pr.qi + row;
-        if (t < a.L) {
-          float* dst = a.dq + (((size_t)it.b * n2 + (size_t)pr.qs * a.L + t) * a.hq + h) * D +
-                       HD * half;
+        {
+          // scaled, over the pair's stage (every MMA that read it is done) as 32-column
+          // boxes of [128 rows][128 B], 128-byte swizzled, for the loader's reduce-add
 #pragma unroll
-          for (int e = 0; e < HD; e += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + e),
-                      make_float4(__uint_as_float(dqr[e]) * a.scale,
-                                  __uint_as_float(dqr[e + 1]) * a.scale,
-                                  __uint_as_float(dqr[e + 2]) * a.scale,
-                                  __uint_as_float(dqr[e + 3]) * a.scale));
+          for (int bx = 0; bx < HD / 32; ++bx) {
+            uint8_t* box = stage + (HD * half / 32 + bx) * (GT * 128);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              const uint32_t* w4 = dqr + 32 * bx + 4 * cc;
+              *reinterpret_cast<float4*>(box + swz(row, cc)) =
+                  make_float4(__uint_as_float(w4[0]) * a.scale, __uint_as_float(w4[1]) * a.scale,
+                              __uint_as_float(w4[2]) * a.scale, __uint_as_float(w4[3]) * a.scale);
+            }
+          }
         }
+        fence_proxy_async_smem();
+        mbar_arrive_warp(&bar.dq_staged[st]);
       }
       if (!ok) break;
       // the item's dV and dK rows (this thread's half of the columns), added to dV and dK
@@ -590,7 +613,7 @@ cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t*
                            cudaStream_t stream) {
   using S = GSmem<D>;
   static_assert(S::TOTAL + sizeof(GBar) <= 227 * 1024, "gradient layout fits shared memory");
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, tdq;
   const uint64_t rows = (uint64_t)batch * 2 * L;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hq, rows};
@@ -606,14 +629,21 @@ cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t*
     if (!encode_tmap_bf16(&tk, k, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_tmap_bf16(&tv, v, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
+  {
+    // dQ as [2 batch][L][hq][D] fp32: rows past L of a partial query tile are not touched
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)hq, (uint64_t)L, (uint64_t)batch * 2};
+    const uint64_t str[3] = {(uint64_t)D * 4, (uint64_t)hq * D * 4, (uint64_t)L * hq * D * 4};
+    const uint32_t box[4] = {32, 1, GT, 1};
+    if (!encode_tmap_f32(&tdq, dq, 4, dims, str, box)) return cudaErrorInvalidValue;
+  }
   GArgs a{batch, L, B, hq, hkv, hq / hkv, (L + GT - 1) / GT, scale, scale * 1.4426950408889634f,
-          w.lse, w.drow, dq, dk, dv, status};
+          w.lse, w.drow, dk, dv, status};
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(dual_grad_kernel<D>, S::TOTAL, attr);
   if (ea != cudaSuccess) return ea;
   const long long items = (long long)batch * hq * 2 * a.nt;
   const long long ctas = std::min<long long>(items, num_sms());
-  dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, a);
+  dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, tdq, a);
   return cudaGetLastError();
 }
 

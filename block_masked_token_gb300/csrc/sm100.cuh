@@ -127,6 +127,17 @@ MARS_DEV void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y
       : "memory");
 }
 
+// Tiled 4D reduce-add from shared memory into global (bulk async-group; the element type
+// and the add come from the tensor map). Out-of-range box elements are skipped.
+MARS_DEV void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int x, int y, int z,
+                                int w) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 MARS_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until every committed bulk store of this thread has finished reading shared memory.
