@@ -34,7 +34,9 @@ struct DualPolicy {
   static constexpr bool kRowStats = true;
   static constexpr int kStageBoxes = D / 32 < 2 ? D / 32 : 2;
   const CUtensorMap* tm_o;   // O as [2*batch][L][hq][D] fp32, box [1][128][1][32]
-  float* lse;                // optional: [batch][hq][2L] row log-sum-exp (log2 units)
+  float* lse;                // optional: [batch][hq][2][Lp] row log-sum-exp (log2 units),
+                             // Lp = L rounded up to 128 (the pad is not written)
+  int lp;
   int store_o;               // 0: O is not written (a statistics-only run)
   int L, B, hq;
   int b, h, stream, r0;
@@ -76,7 +78,7 @@ struct DualPolicy {
   // log2 of the row's softmax denominator in units of scale*log2(e)*score: m + log2(l)
   MARS_DEV void row_stats(int row, float m, float l) const {
     if (lse && row_valid(row))
-      lse[((size_t)b * hq + h) * 2 * L + (size_t)stream * L + r0 + row] = m + log2f(l);
+      lse[(((size_t)b * hq + h) * 2 + stream) * lp + r0 + row] = m + log2f(l);
   }
   // rows past L (a partial last query tile) fall outside the map's L extent and are not
   // written
@@ -108,6 +110,7 @@ MARS_DEV DualPolicy<D> make_item(const DualArgs& a, int id, const CUtensorMap* t
   const int qt = a.nqt - 1 - (id >> 1);
   pol.tm_o = tm_o;
   pol.lse = a.lse;
+  pol.lp = a.nqt * BQ;
   pol.store_o = a.store_o;
   pol.L = a.L;
   pol.B = a.B;
@@ -281,6 +284,309 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
   cta_teardown(tmem, warp);
 }
 
+// ------------------------------------------------------------------ dQ of the gradient
+
+// dQ = scale * sum over visible key tiles j of dS_j K_j, dS = P * (dP - D), P =
+// exp2(scale log2(e) S - lse), S = Q K_j^T, dP = dO V_j^T: the row-parallel half of the
+// attention gradient. Work items, their key tiles and the masks are the forward's; per key
+// tile three MMAs (S, dP, dQ += dS K) with dQ accumulated in TMEM and written once per row.
+// TMEM: S in two buffers (columns 0 and 128), dP at 256, dQ at 384. Warps: 0 K loader,
+// 1 TMEM owner and MMA issuer (it also loads each item's Q and dO), 2..9 math (two per
+// TMEM lane quadrant, 64 key columns each), 10 V loader.
+constexpr int DQ_MATH_WARPS = 8;
+constexpr int DQ_THREADS = 32 * (3 + DQ_MATH_WARPS);
+constexpr int DQ_V_WARP = 2 + DQ_MATH_WARPS;
+
+struct DQBar {
+  uint64_t s_full[2], dq_done[2];
+  uint64_t dp_full, dp_free, ds_full, acc_free;
+};
+
+struct DQArgs {
+  DualArgs f;              // shape, scale_log2, status
+  float scale;
+  const float* lse;        // [batch][hq][2][Lp], Lp = L rounded up to 128
+  const float* drow;       // same layout
+  float* dq;               // [batch][2L][hq][D]
+};
+
+// K-step k (16 keys) of dS in its S buffer: keys [0, 64) over columns [0, 32), keys
+// [64, 128) over [64, 96) (each math warp packs its bf16 values over fp32 columns it has
+// itself already read).
+MARS_DEV uint32_t ds_col(int k) { return (uint32_t)(8 * k + (k >= 4 ? 32 : 0)); }
+
+template <int D>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, DQArgs da) {
+  using namespace sm100;
+  using Pol = DualPolicy<D>;
+  using S = flash::Smem<D, Pol::kStageBoxes>;     // Q, K ring, V ring; dO over the staging
+  static_assert(D * BQ * 2 <= Pol::kStageBoxes * BQ * 128, "dO tile fits the staging area");
+  constexpr int TM_DP = 256, TM_DQ = 384;
+  const DualArgs& a = da.f;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ flash::Barriers bar;
+  __shared__ DQBar qb;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qb.s_full[i], 1);
+      mbar_init(&qb.dq_done[i], 1);
+    }
+    mbar_init(&qb.dp_full, 1);
+    mbar_init(&qb.dp_free, 32 * DQ_MATH_WARPS);
+    mbar_init(&qb.ds_full, 32 * DQ_MATH_WARPS);
+    mbar_init(&qb.acc_free, 32 * DQ_MATH_WARPS);
+  }
+  const uint32_t tmem = cta_setup(bar, warp);     // also initialises bar (thread 0)
+  volatile int* ab = &bar.abort;
+  const int total = a.nqt * 2 * a.hq * a.batch;
+  const int G = gridDim.x, c = blockIdx.x;
+  auto item_id = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
+  const int rounds = (total + G - 1) / G;
+
+  if (warp == 0 || warp == DQ_V_WARP) {
+    const bool is_v = warp != 0;
+    int last_k[flash::K_STAGES], last_v[flash::V_STAGES];
+    for (int i = 0; i < flash::K_STAGES; ++i) last_k[i] = -1;
+    for (int i = 0; i < flash::V_STAGES; ++i) last_v[i] = -1;
+    int j0 = 0;
+    for (int r = 0; r < rounds; ++r) {
+      const int id = item_id(r);
+      if (id >= total) continue;
+      const Pol pol = make_item<D>(a, id, nullptr);
+      const bool ok = is_v ? flash::load_ring_item<D, flash::V_STAGES>(
+                                 bar, smem, pol.n_total, j0, last_v, false, a.status, true,
+                                 KVIssue<D, Pol>{&pol, &tm_v})
+                           : flash::load_ring_item<D, flash::K_STAGES>(
+                                 bar, smem, pol.n_total, j0, last_k, false, a.status, false,
+                                 KVIssue<D, Pol>{&pol, &tm_k});
+      if (!ok) break;
+      j0 += pol.n_total;
+    }
+    const Pol none{};
+    if (is_v)
+      flash::load_ring_item<D, flash::V_STAGES>(bar, smem, 0, j0, last_v, true, a.status, true,
+                                                KVIssue<D, Pol>{&none, &tm_v});
+    else
+      flash::load_ring_item<D, flash::K_STAGES>(bar, smem, 0, j0, last_k, true, a.status, false,
+                                                KVIssue<D, Pol>{&none, &tm_k});
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(BQ, BKV, false);   // S, dP: K-major A and B
+      const uint32_t id_q = idesc_bf16_f32(BQ, D, true);      // dQ: TMEM A, MN-major B
+      const uint32_t qa = smem_u32(smem + S::OFF_Q), da_ = smem_u32(smem + S::OFF_STAGE);
+      int jg0 = 0, i = 0, nq = 0;
+      bool ok = true;
+      auto issue_s = [&](int jg) -> bool {                // S_jg = Q K^T into buffer jg % 2
+        const int st = jg % flash::K_STAGES, sb = jg & 1;
+        if (!mbar_wait(&bar.k_full[st], (jg / flash::K_STAGES) & 1, ab, a.status)) return false;
+        if (jg >= 2 && !mbar_wait(&qb.dq_done[sb], ((jg >> 1) - 1) & 1, ab, a.status)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
+          mma_bf16_ss(tmem + sb * BKV, sdesc_sw128(qa + off, 16, 1024),
+                      sdesc_sw128(kb + off, 16, 1024), id_s, k != 0);
+        }
+        mma_commit(&qb.s_full[sb]);
+        return true;
+      };
+      auto issue_dp = [&](int jg) -> bool {               // dP_jg = dO V^T
+        const int st = jg % flash::V_STAGES;
+        if (!mbar_wait(&bar.v_full[st], (jg / flash::V_STAGES) & 1, ab, a.status)) return false;
+        if (jg >= 1 && !mbar_wait(&qb.dp_free, (jg - 1) & 1, ab, a.status)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
+          mma_bf16_ss(tmem + TM_DP, sdesc_sw128(da_ + off, 16, 1024),
+                      sdesc_sw128(vb + off, 16, 1024), id_s, k != 0);
+        }
+        mma_commit(&qb.dp_full);
+        mma_commit(&bar.v_empty[st]);
+        return true;
+      };
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int id = item_id(r);
+        if (id >= total) continue;
+        const Pol pol = make_item<D>(a, id, nullptr);
+        // Q and dO are replaced once the previous item's S and dP MMAs have completed
+        if (i > 0 && !(ok = mbar_wait(&bar.q_empty, (i - 1) & 1, ab, a.status))) break;
+        mbar_arrive_expect_tx(&bar.q_full, 2 * S::Q_BYTES);
+        for (int x = 0; x < D / 64; ++x) {
+          const int z = pol.zb + pol.stream * a.L + pol.r0;
+          tma_load_3d(smem + S::OFF_Q + x * (BQ * 128), &tm_q, &bar.q_full, x * 64, pol.h, z);
+          tma_load_3d(smem + S::OFF_STAGE + x * (BQ * 128), &tm_do, &bar.q_full, x * 64, pol.h, z);
+        }
+        ++nq;
+        if (!(ok = mbar_wait(&bar.q_full, i & 1, ab, a.status))) break;
+        const int n = pol.n_total;
+        if (!(ok = issue_s(jg0) && issue_dp(jg0))) break;
+        for (int jl = 0; jl < n && ok; ++jl) {
+          const int jg = jg0 + jl, sb = jg & 1;
+          // the next tile's S and dP go ahead of this tile's dQ
+          if (jl + 1 < n && !(ok = issue_s(jg + 1) && issue_dp(jg + 1))) break;
+          if (jl == 0 && i > 0 && !(ok = mbar_wait(&qb.acc_free, (i - 1) & 1, ab, a.status)))
+            break;
+          if (!(ok = mbar_wait(&qb.ds_full, jg & 1, ab, a.status))) break;
+          tc_fence_after();
+          const int st = jg % flash::K_STAGES;
+          const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k)             // dQ += dS K (K tile MN-major)
+            mma_bf16_ts(tmem + TM_DQ, tmem + sb * BKV + ds_col(k),
+                        sdesc_sw128(kb + k * 2048, BKV * 128, 1024), id_q, (jl | k) != 0);
+          mma_commit(&qb.dq_done[sb]);
+          mma_commit(&bar.k_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bar.q_empty);
+        mma_commit(&bar.o_final);
+        jg0 += n;
+        ++i;
+      }
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0, nullptr, a.status);
+      if (nq > 0) mbar_wait(&bar.q_full, (nq - 1) & 1, nullptr, a.status);
+    }
+  } else {
+    // math: thread = query row (TMEM lane), 64 key columns per warp
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(b, parity, ab, a.status));
+    };
+    int jg0 = 0, i = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int id = item_id(r);
+      if (id >= total) continue;
+      const Pol pol = make_item<D>(a, id, nullptr);
+      const bool rv = pol.row_valid(row);
+      const flash::RowVis vis = pol.row_vis(row);
+      const size_t srow = (((size_t)pol.b * a.hq + pol.h) * 2 + pol.stream) * (a.nqt * BQ) +
+                          pol.r0 + row;
+      const float lse = rv ? da.lse[srow] : 0.f;
+      const float dd = rv ? da.drow[srow] : 0.f;
+      const int n = pol.n_total;
+      for (int jl = 0; jl < n && ok; ++jl) {
+        const int jg = jg0 + jl, sb = jg & 1;
+        const typename Pol::Tile tile = pol.tile(jl);
+        const flash::ColRange cr = rv ? pol.cols(vis, tile) : flash::ColRange{0, 0, -1, 0u};
+        if (!(ok = warp_wait(&qb.s_full[sb], (jg >> 1) & 1))) break;
+        if (!(ok = warp_wait(&qb.dp_full, jg & 1))) break;
+        tc_fence_after();
+        uint32_t sv[64], pv[64];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          tmem_ld32(tmem + sb * BKV + 64 * half + 32 * q + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q));
+          tmem_ld32(tmem + TM_DP + 64 * half + 32 * q + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(pv + 32 * q));
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&qb.dp_free);
+        uint32_t ds[32];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t mk = rv ? flash::chunk_mask(cr, 2 * half + q) : 0u;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float x[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int cidx = 32 * q + e + u;
+              const float p = ((mk >> (e + u)) & 1u)
+                                  ? flash::ex2_approx(__uint_as_float(sv[cidx]) * a.scale_log2 - lse)
+                                  : 0.f;
+              // P rounded to bf16 as in the key-tile kernel's dV and dS
+              const float pb = __bfloat162float(__float2bfloat16_rn(p));
+              x[u] = pb * (__uint_as_float(pv[cidx]) - dd);
+            }
+            ds[16 * q + e / 2] = flash::pack_bf16x2(x[0], x[1]);
+          }
+        }
+        tmem_st32(tmem + sb * BKV + 64 * half + lane_off, ds);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&qb.ds_full);
+      }
+      if (!ok) break;
+      // dQ row, this warp's half of the columns
+      if (!(ok = warp_wait(&bar.o_final, i & 1))) break;
+      tc_fence_after();
+      constexpr int HD = D / 2;
+      uint32_t o[HD];
+#pragma unroll
+      for (int q = 0; q < HD / 32; ++q)
+        tmem_ld32(tmem + TM_DQ + HD * half + 32 * q + lane_off,
+                  *reinterpret_cast<uint32_t(*)[32]>(o + 32 * q));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&qb.acc_free);
+      if (rv) {
+        float* dst = da.dq + ((((size_t)pol.b * 2 * a.L + (size_t)pol.stream * a.L + pol.r0 + row) *
+                                   a.hq + pol.h) * D) + HD * half;
+#pragma unroll
+        for (int e = 0; e < HD; e += 4)
+          *reinterpret_cast<float4*>(dst + e) =
+              make_float4(__uint_as_float(o[e]) * da.scale, __uint_as_float(o[e + 1]) * da.scale,
+                          __uint_as_float(o[e + 2]) * da.scale, __uint_as_float(o[e + 3]) * da.scale);
+      }
+      jg0 += n;
+      ++i;
+    }
+  }
+  cta_teardown(tmem, warp);
+}
+
+template <int D>
+cudaError_t launch_dq_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const uint16_t* do_bf, const float* lse, const float* drow, float* dq,
+                         int batch, int L, int B, int hq, int hkv, float scale, int32_t* status,
+                         cudaStream_t stream) {
+  using SP = flash::Smem<D, DualPolicy<D>::kStageBoxes>;
+  static_assert(SP::TOTAL + sizeof(flash::Barriers) + sizeof(DQBar) <= 227 * 1024,
+                "dQ layout fits shared memory");
+  CUtensorMap tq, tdo, tk, tv;
+  const uint64_t rows = (uint64_t)batch * 2 * L;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hq, rows};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)hq * D * 2};
+    const uint32_t box[3] = {64, 1, BQ};
+    if (!encode_tmap_bf16(&tq, q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tdo, do_bf, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hkv, rows};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)hkv * D * 2};
+    const uint32_t box[3] = {64, 1, BKV};
+    if (!encode_tmap_bf16(&tk, k, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tv, v, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  DQArgs da{{batch, L, B, hq, hkv, hq / hkv, (L + BQ - 1) / BQ, scale * 1.4426950408889634f,
+             status, nullptr, 0},
+            scale, lse, drow, dq};
+  const long long items = (long long)da.f.nqt * 2 * hq * batch;
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(dual_dq_kernel<D>, SP::TOTAL, attr);
+  if (ea != cudaSuccess) return ea;
+  const long long ctas = std::min<long long>(items, num_sms());
+  dual_dq_kernel<D><<<(unsigned)ctas, DQ_THREADS, SP::TOTAL, stream>>>(tq, tdo, tk, tv, da);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
                       int batch, int L, int B, int hq, int hkv, float scale,
@@ -333,6 +639,18 @@ cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint1
   cudaError_t e =
       d == 64 ? launch_tc<64>(q, k, v, o, batch, L, B, hq, hkv, scale, status, lse, stream)
               : launch_tc<128>(q, k, v, o, batch, L, B, hq, hkv, scale, status, lse, stream);
+  count_launches(1);
+  return e;
+}
+
+cudaError_t launch_dual_stream_dq(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  const uint16_t* do_bf, const float* lse, const float* drow,
+                                  float* dq, int batch, int L, int B, int hq, int hkv, int d,
+                                  float scale, int32_t* status, cudaStream_t stream) {
+  cudaError_t e = d == 64 ? launch_dq_tc<64>(q, k, v, do_bf, lse, drow, dq, batch, L, B, hq, hkv,
+                                             scale, status, stream)
+                          : launch_dq_tc<128>(q, k, v, do_bf, lse, drow, dq, batch, L, B, hq,
+                                              hkv, scale, status, stream);
   count_launches(1);
   return e;
 }

@@ -4,23 +4,23 @@
 //
 // With P = softmax(scale * S + M), S = Q K^T, and D_i = rowsum(dO_i * O_i):
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dK = scale dS^T Q,   dQ = scale dS K.
-// One fused tcgen05 kernel, never storing a score block:
-//   - a work item is (batch, query head, 128-key tile of one stream); one persistent CTA
-//     per SM runs items heaviest first;
-//   - the item visits every 128-row query tile that sees one of its keys under M, and per
-//     (key tile, query tile) pair runs five MMAs with TMEM accumulators:
+// Two tcgen05 kernels, neither storing a score block:
+//   - dual_grad_kernel (here): a work item is (batch, query head, 128-key tile of one
+//     stream); one persistent CTA per SM runs items heaviest first. The item visits every
+//     128-row query tile that sees one of its keys under M, and per (key tile, query tile)
+//     pair runs four MMAs with TMEM accumulators:
 //       S^T = K Q^T, dP^T = V dO^T            (keys on TMEM lanes, queries on columns)
 //       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM, bf16 over the
 //                                              fp32 columns they were formed from)
-//       dQ_pair = dS K                        (A = dS from shared memory, MN-major)
 //     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by two threads per key row
-//     (64 query columns each: with lse known, no row-wide exchange is needed);
-//   - dK and dV stay in TMEM over the item's pairs; at the end of the item they are added
-//     to dK and dV (fp32 vector atomics); each pair's dQ part is staged in shared memory
-//     and added to dQ by a TMA bulk reduce-add. All three are zeroed first. Splitting the G query heads of a kv group into separate items keeps
-//     the work items small enough to balance across the SMs.
-// lse (log2 of each query row's softmax denominator) comes from a statistics-only run of
-// the forward kernel; P and dS are rounded to bf16 as MMA operands.
+//     (64 query columns each: with lse known, no row-wide exchange is needed). S^T of the
+//     next pair is issued as soon as dV has read P^T, so it runs under this pair's dS.
+//     dK and dV stay in TMEM over the item's pairs and are then added to dK and dV (fp32
+//     vector atomics; the G query heads of a kv group add into the same rows).
+//   - the dQ kernel (with the forward, whose work items and masks it shares): per query
+//     tile, dQ accumulates dS K over the visible key tiles in TMEM and is written once.
+// The row statistics (lse: log2 of each query row's softmax denominator) come from a
+// statistics-only run of the forward kernel; P and dS are rounded to bf16 as MMA operands.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -42,13 +42,14 @@ constexpr int GRAD_THREADS = 64 + 32 * MATH_WARPS;   // warp 0 loads, warp 1 TME
 constexpr int MATH_THREADS = 32 * MATH_WARPS;
 constexpr int NSTAGE = 2;              // Q / dO ring depth
 
-// dO (fp32) -> bf16 copy, and D[b][h][i] = sum_d dO[b, i, h, d] * O[b, i, h, d]. One warp
-// per (b, i, h) row.
+// dO (fp32) -> bf16 copy, and D[b][h][stream][t] = sum_d dO[b, i, h, d] * O[b, i, h, d]
+// (i = stream * L + t; rows padded to lp per stream). One warp per (b, i, h) row.
 __global__ void __launch_bounds__(256) grad_prep_kernel(const float* __restrict__ o,
                                                         const float* __restrict__ d_o,
                                                         __nv_bfloat16* __restrict__ do_bf,
                                                         float* __restrict__ drow,
-                                                        long long nrows, int n, int hq, int d) {
+                                                        long long nrows, int n, int hq, int d,
+                                                        int lp) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= nrows) return;
@@ -62,7 +63,8 @@ __global__ void __launch_bounds__(256) grad_prep_kernel(const float* __restrict_
   }
   acc = warp_sum(acc);
   const long long h = row % hq, bi = row / hq, i = bi % n, b = bi / n;
-  if (lane == 0) drow[(b * hq + h) * n + i] = acc;
+  const long long L = n / 2, stream = i / L, t = i % L;
+  if (lane == 0) drow[((b * hq + h) * 2 + stream) * lp + t] = acc;
 }
 
 template <int D>
@@ -71,9 +73,8 @@ struct GSmem {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = T_BYTES;
   static constexpr int OFF_RING = 2 * T_BYTES;
-  // a stage: Q [128][D], dO [128][D] (dS [128 keys][128 queries] later, MN-major), lse and
-  // D of its 128 query rows; 1024-byte aligned
-  static constexpr int DO_BYTES = GT * GT * 2 > T_BYTES ? GT * GT * 2 : T_BYTES;
+  // a stage: Q [128][D], dO [128][D], lse and D of its 128 query rows; 1024-byte aligned
+  static constexpr int DO_BYTES = T_BYTES;
   static constexpr int ST_Q = 0, ST_DO = T_BYTES, ST_LSE = T_BYTES + DO_BYTES,
                        ST_D = ST_LSE + GT * 4;
   static constexpr int STAGE = (ST_D + GT * 4 + 1023) / 1024 * 1024;
@@ -84,8 +85,8 @@ struct GSmem {
 
 struct GBar {
   uint64_t kv_full, kv_empty;
-  uint64_t full[NSTAGE], dq_staged[NSTAGE];
-  uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free, dv_done, dk_done;
+  uint64_t full[NSTAGE], empty[NSTAGE];
+  uint64_t s_full, dp_full, p_full, ds_full, dv_done, dk_done;
   uint64_t acc_full, acc_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -94,8 +95,8 @@ struct GBar {
 struct GArgs {
   int batch, L, B, hq, hkv, G, nt;
   float scale, scale_log2;
-  const float* lse;        // [batch][hq][2L]
-  const float* drow;       // [batch][hq][2L]
+  const float* lse;        // [batch][hq][2][Lp], Lp = 128 nt (pad rows zero)
+  const float* drow;       // same layout
   float* dk;               // [batch][2L][hkv][D]
   float* dv;
   int32_t* status;
@@ -199,10 +200,6 @@ MARS_DEV float ex2(float x) {
   return y;
 }
 
-// Swizzled byte offset of 16-byte chunk c (0..7) of 128-byte row r (the TMA 128-byte
-// swizzle layout, which is also the MMA's canonical one).
-MARS_DEV uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
 // TMEM column of K-step k (16 queries) of P^T or dS^T in its buffer: queries [0, 64) are
 // packed over columns [0, 32) and queries [64, 128) over [64, 96), the first half of each
 // half's own fp32 columns.
@@ -218,8 +215,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_do,
                  const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_dq, GArgs a) {
+                 const __grid_constant__ CUtensorMap tm_v, GArgs a) {
   using S = GSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ GBar bar;
@@ -234,14 +230,12 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&bar.kv_empty, 1);
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&bar.full[i], 1);
-      mbar_init(&bar.dq_staged[i], MATH_THREADS);
+      mbar_init(&bar.empty[i], 1);
     }
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.dp_full, 1);
     mbar_init(&bar.p_full, MATH_THREADS);
     mbar_init(&bar.ds_full, MATH_THREADS);
-    mbar_init(&bar.dq_full, 1);
-    mbar_init(&bar.dq_free, MATH_THREADS);
     mbar_init(&bar.dv_done, 1);
     mbar_init(&bar.dk_done, 1);
     mbar_init(&bar.acc_full, 1);
@@ -268,21 +262,6 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---------------------------------------------------------------- loads
     int gp = 0, ii = 0, nkv = 0;
     bool ok = true;
-    // coordinates in dQ (head, row, 2 batch + stream) of the pair each stage last held
-    int hist_h[NSTAGE], hist_t[NSTAGE], hist_w[NSTAGE];
-    // lane 0: add pair g2's dQ part, staged over its stage by the math warps, into dQ;
-    // returns once the bulk reduction has read the stage
-    auto flush = [&](int g2) -> bool {
-      const int s2 = g2 % NSTAGE;
-      if (!mbar_wait(&bar.dq_staged[s2], (g2 / NSTAGE) & 1, ab, a.status)) return false;
-      const uint8_t* stg = smem + S::OFF_RING + s2 * S::STAGE;
-      for (int c2 = 0; c2 < D / 32; ++c2)
-        tma_reduce_add_4d(&tm_dq, stg + c2 * (GT * 128), c2 * 32, hist_h[s2], hist_t[s2],
-                          hist_w[s2]);
-      bulk_commit();
-      bulk_wait_read_all();
-      return true;
-    };
     for (int r = 0; r < rounds && ok; ++r) {
       const int id = item_id(r);
       if (id >= total) continue;
@@ -305,26 +284,17 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         const GPair pr = grad_pair(it, p);
         const int st = gp % NSTAGE;
         uint8_t* stage = smem + S::OFF_RING + st * S::STAGE;
-        // the stage's previous pair is done once its dQ part has been reduced out of it
-        if (lane == 0 && gp >= NSTAGE) ok = flush(gp - NSTAGE);
+        if (lane == 0) ok = mbar_wait(&bar.empty[st], ((gp / NSTAGE) & 1) ^ 1, ab, a.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        // lse and D of the tile's rows (0 past L); published by the arrive below
         const int h = it.kvh * a.G + it.g;
-        const size_t rb = ((size_t)it.b * a.hq + h) * n2 + (size_t)pr.qs * a.L;
-        float* ls = reinterpret_cast<float*>(stage + S::ST_LSE);
-        float* ds = reinterpret_cast<float*>(stage + S::ST_D);
-        for (int i = lane; i < GT; i += 32) {
-          const int t = GT * pr.qi + i;
-          ls[i] = t < a.L ? a.lse[rb + t] : 0.f;
-          ds[i] = t < a.L ? a.drow[rb + t] : 0.f;
-        }
-        __syncwarp();
         if (lane == 0) {
-          hist_h[st] = h;
-          hist_t[st] = GT * pr.qi;
-          hist_w[st] = it.b * 2 + pr.qs;
-          mbar_arrive_expect_tx(&bar.full[st], 2 * S::T_BYTES);
+          // lse and D of the tile's 128 rows (one padded row block each), then Q and dO
+          const size_t rb = (((size_t)it.b * a.hq + h) * 2 + pr.qs) * (size_t)(GT * a.nt) +
+                            (size_t)GT * pr.qi;
+          mbar_arrive_expect_tx(&bar.full[st], 2 * S::T_BYTES + 2 * GT * 4);
+          bulk_load(stage + S::ST_LSE, a.lse + rb, GT * 4, &bar.full[st]);
+          bulk_load(stage + S::ST_D, a.drow + rb, GT * 4, &bar.full[st]);
           const int z = it.b * n2 + pr.qs * a.L + GT * pr.qi;
           for (int x = 0; x < D / 64; ++x) {
             tma_load_3d(stage + S::ST_Q + x * (GT * 128), &tm_q, &bar.full[st], x * 64, h, z);
@@ -334,9 +304,8 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       ++ii;
     }
-    // the last pairs' dQ parts; then wait (bounded) for the copies still in flight
+    // wait (bounded) for the copies still in flight
     if (lane == 0) {
-      for (int g2 = gp - NSTAGE < 0 ? 0 : gp - NSTAGE; ok && g2 < gp; ++g2) ok = flush(g2);
       if (nkv > 0) mbar_wait(&bar.kv_full, (nkv - 1) & 1, nullptr, a.status);
       for (int k = 1; k <= NSTAGE && gp - k >= 0; ++k)
         mbar_wait(&bar.full[(gp - k) % NSTAGE], ((gp - k) / NSTAGE) & 1, nullptr, a.status);
@@ -347,64 +316,77 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0) {
       const uint32_t id_qk = idesc_ab(GT, GT, false, false);   // S^T, dP^T: K-major A, B
       const uint32_t id_acc = idesc_ab(GT, D, false, true);    // dV, dK: TMEM A, MN-major B
-      const uint32_t id_dq = idesc_ab(GT, D, true, true);      // dQ: MN-major A and B
       const uint32_t kb = smem_u32(smem + S::OFF_K), vb = smem_u32(smem + S::OFF_V);
+      auto stage_of = [&](int g2) { return smem_u32(smem + S::OFF_RING + (g2 % NSTAGE) * S::STAGE); };
+      auto issue_st = [&](int g2) -> bool {            // S^T = K Q^T of pair g2
+        if (!mbar_wait(&bar.full[g2 % NSTAGE], (g2 / NSTAGE) & 1, ab, a.status)) return false;
+        // the S buffer holds P^T of the previous pair until its dV MMA has read it
+        if (g2 > 0 && !mbar_wait(&bar.dv_done, (g2 - 1) & 1, ab, a.status)) return false;
+        tc_fence_after();
+        const uint32_t qb = stage_of(g2) + S::ST_Q;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
+          mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(kb + off, 16, 1024),
+                      sdesc_sw128(qb + off, 16, 1024), id_qk, k != 0);
+        }
+        mma_commit(&bar.s_full);
+        return true;
+      };
+      auto issue_dp = [&](int g2) -> bool {            // dP^T = V dO^T of pair g2
+        // the dP buffer holds dS^T of the previous pair until its dK MMA has read it
+        if (g2 > 0 && !mbar_wait(&bar.dk_done, (g2 - 1) & 1, ab, a.status)) return false;
+        tc_fence_after();
+        const uint32_t dob = stage_of(g2) + S::ST_DO;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
+          mma_bf16_ss(tmem + S::TM_DP, sdesc_sw128(vb + off, 16, 1024),
+                      sdesc_sw128(dob + off, 16, 1024), id_qk, k != 0);
+        }
+        mma_commit(&bar.dp_full);
+        return true;
+      };
       int gp = 0, ii = 0;
       bool ok = true;
       for (int r = 0; r < rounds && ok; ++r) {
         const int id = item_id(r);
         if (id >= total) continue;
         const GItem it = grad_item(a, id);
-        ok = mbar_wait(&bar.kv_full, ii & 1, ab, a.status);
-        if (ok && ii > 0) ok = mbar_wait(&bar.acc_free, (ii - 1) & 1, ab, a.status);
+        if (!(ok = mbar_wait(&bar.kv_full, ii & 1, ab, a.status))) break;
         const int np = it.npg;
+        if (!(ok = issue_st(gp) && issue_dp(gp))) break;
         for (int p = 0; p < np && ok; ++p, ++gp) {
-          const int st = gp % NSTAGE;
-          const uint32_t sb = smem_u32(smem + S::OFF_RING + st * S::STAGE);
-          const uint32_t qb = sb + S::ST_Q, dob = sb + S::ST_DO;
-          if (!(ok = mbar_wait(&bar.full[st], (gp / NSTAGE) & 1, ab, a.status))) break;
-          // the S buffer holds the previous pair's dQ part until the math threads read it
-          if (gp > 0 && !(ok = mbar_wait(&bar.dq_free, (gp - 1) & 1, ab, a.status))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {               // S^T = K Q^T
-            const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
-            mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(kb + off, 16, 1024),
-                        sdesc_sw128(qb + off, 16, 1024), id_qk, k != 0);
-          }
-          mma_commit(&bar.s_full);
-          // the dP buffer holds the previous pair's dS^T until its dK MMA has read it
-          if (gp > 0 && !(ok = mbar_wait(&bar.dk_done, (gp - 1) & 1, ab, a.status))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {               // dP^T = V dO^T
-            const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
-            mma_bf16_ss(tmem + S::TM_DP, sdesc_sw128(vb + off, 16, 1024),
-                        sdesc_sw128(dob + off, 16, 1024), id_qk, k != 0);
-          }
-          mma_commit(&bar.dp_full);
+          const uint32_t sb = stage_of(gp);
           if (!(ok = mbar_wait(&bar.p_full, gp & 1, ab, a.status))) break;
+          // dV of the item starts from zero: the previous item's dV and dK must be read
+          if (p == 0 && ii > 0 && !(ok = mbar_wait(&bar.acc_free, (ii - 1) & 1, ab, a.status)))
+            break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < GT / 16; ++k)                // dV += P^T dO
             mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + p_col(k),
-                        sdesc_sw128(dob + k * 2048, GT * 128, 1024), id_acc, (p | k) != 0);
+                        sdesc_sw128(sb + S::ST_DO + k * 2048, GT * 128, 1024), id_acc,
+                        (p | k) != 0);
           mma_commit(&bar.dv_done);
+          // the next pair's S^T runs under this pair's dS when its Q has already landed;
+          // dK (which frees this pair's stage) never waits for the next pair's loads
+          bool next_s = false;
+          if (p + 1 < np && mbar_try_wait(&bar.full[(gp + 1) % NSTAGE], ((gp + 1) / NSTAGE) & 1)) {
+            if (!(ok = issue_st(gp + 1))) break;
+            next_s = true;
+          }
           if (!(ok = mbar_wait(&bar.ds_full, gp & 1, ab, a.status))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < GT / 16; ++k)                // dK += dS^T Q
             mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + p_col(k),
-                        sdesc_sw128(qb + k * 2048, GT * 128, 1024), id_acc, (p | k) != 0);
+                        sdesc_sw128(sb + S::ST_Q + k * 2048, GT * 128, 1024), id_acc,
+                        (p | k) != 0);
           mma_commit(&bar.dk_done);
-          // dQ overwrites the S buffer, whose P^T columns the dV MMA reads
-          if (!(ok = mbar_wait(&bar.dv_done, gp & 1, ab, a.status))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < GT / 16; ++k)                // dQ part = dS K (dS over dO)
-            mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(dob + k * 2048, GT * 128, 1024),
-                        sdesc_sw128(kb + k * 2048, GT * 128, 1024), id_dq, k != 0);
-          mma_commit(&bar.dq_full);
+          mma_commit(&bar.empty[gp % NSTAGE]);
+          if (p + 1 < np && !next_s && !(ok = issue_st(gp + 1))) break;
+          if (p + 1 < np && !(ok = issue_dp(gp + 1))) break;
         }
         if (!ok) break;
         mma_commit(&bar.kv_empty);
@@ -475,7 +457,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive_warp(&bar.p_full);
-        // dS^T = P^T * (dP^T - D): to TMEM (dK) and, MN-major, over dO (dQ)
+        // dS^T = P^T * (dP^T - D), over this half's own dP^T columns (the dK MMA's A)
         if (!(ok = warp_wait(&bar.dp_full, gp & 1))) break;
         tc_fence_after();
 #pragma unroll
@@ -496,48 +478,9 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
           pp[e / 2 + 1] = pack2(s2, s3);
         }
         tmem_st32(tmem + S::TM_DP + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
-        // dO may be overwritten once the dV MMA that reads it has completed
-        if (!(ok = warp_wait(&bar.dv_done, gp & 1))) break;
-        {
-          // [keys][queries] in two 64-query atoms: this thread's half is atom `half`
-          uint8_t* dsm = stage + S::ST_DO + half * (GT * 128);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<uint4*>(dsm + swz(row, cc)) =
-                make_uint4(pp[4 * cc], pp[4 * cc + 1], pp[4 * cc + 2], pp[4 * cc + 3]);
-        }
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive_warp(&bar.ds_full);
-        // dQ part: this thread's query row, columns [HD half, HD half + HD)
-        if (!(ok = warp_wait(&bar.dq_full, gp & 1))) break;
-        tc_fence_after();
-        uint32_t dqr[HD];
-#pragma unroll
-        for (int q = 0; q < HD / 32; ++q)
-          tmem_ld32(tmem + S::TM_S + HD * half + q * 32 + lane_off,
-                    *reinterpret_cast<uint32_t(*)[32]>(dqr + q * 32));
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive_warp(&bar.dq_free);
-        {
-          // scaled, over the pair's stage (every MMA that read it is done) as 32-column
-          // boxes of [128 rows][128 B], 128-byte swizzled, for the loader's reduce-add
-#pragma unroll
-          for (int bx = 0; bx < HD / 32; ++bx) {
-            uint8_t* box = stage + (HD * half / 32 + bx) * (GT * 128);
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              const uint32_t* w4 = dqr + 32 * bx + 4 * cc;
-              *reinterpret_cast<float4*>(box + swz(row, cc)) =
-                  make_float4(__uint_as_float(w4[0]) * a.scale, __uint_as_float(w4[1]) * a.scale,
-                              __uint_as_float(w4[2]) * a.scale, __uint_as_float(w4[3]) * a.scale);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive_warp(&bar.dq_staged[st]);
       }
       if (!ok) break;
       // the item's dV and dK rows (this thread's half of the columns), added to dV and dK
@@ -584,13 +527,14 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct GradBuffers {
   __nv_bfloat16* do_bf;     // dO in bf16, [b, 2L, hq, d]
-  float* drow;              // D, [b][hq][2L]
-  float* lse;               // [b][hq][2L]
+  float* drow;              // D, [b][hq][2][Lp], Lp = L rounded up to 128
+  float* lse;               // same layout
   size_t bytes;
 };
 
 GradBuffers carve(void* base, int batch, int L, int hq, int d) {
   const size_t n = 2 * (size_t)L;
+  const size_t np = 2 * (size_t)((L + GT - 1) / GT * GT);     // both streams, padded rows
   GradBuffers g{};
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -600,8 +544,8 @@ GradBuffers carve(void* base, int batch, int L, int hq, int d) {
     return at;
   };
   g.do_bf = reinterpret_cast<__nv_bfloat16*>(take((size_t)batch * n * hq * d * sizeof(uint16_t)));
-  g.drow = reinterpret_cast<float*>(take((size_t)batch * n * hq * sizeof(float)));
-  g.lse = reinterpret_cast<float*>(take((size_t)batch * n * hq * sizeof(float)));
+  g.drow = reinterpret_cast<float*>(take((size_t)batch * np * hq * sizeof(float)));
+  g.lse = reinterpret_cast<float*>(take((size_t)batch * np * hq * sizeof(float)));
   g.bytes = off;
   return g;
 }
@@ -609,11 +553,11 @@ GradBuffers carve(void* base, int batch, int L, int hq, int d) {
 template <int D>
 cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                            const GradBuffers& w, int batch, int L, int B, int hq, int hkv,
-                           float scale, float* dq, float* dk, float* dv, int32_t* status,
+                           float scale, float* dk, float* dv, int32_t* status,
                            cudaStream_t stream) {
   using S = GSmem<D>;
   static_assert(S::TOTAL + sizeof(GBar) <= 227 * 1024, "gradient layout fits shared memory");
-  CUtensorMap tq, tdo, tk, tv, tdq;
+  CUtensorMap tq, tdo, tk, tv;
   const uint64_t rows = (uint64_t)batch * 2 * L;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)hq, rows};
@@ -629,13 +573,6 @@ cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t*
     if (!encode_tmap_bf16(&tk, k, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_tmap_bf16(&tv, v, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  {
-    // dQ as [2 batch][L][hq][D] fp32: rows past L of a partial query tile are not touched
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)hq, (uint64_t)L, (uint64_t)batch * 2};
-    const uint64_t str[3] = {(uint64_t)D * 4, (uint64_t)hq * D * 4, (uint64_t)L * hq * D * 4};
-    const uint32_t box[4] = {32, 1, GT, 1};
-    if (!encode_tmap_f32(&tdq, dq, 4, dims, str, box)) return cudaErrorInvalidValue;
-  }
   GArgs a{batch, L, B, hq, hkv, hq / hkv, (L + GT - 1) / GT, scale, scale * 1.4426950408889634f,
           w.lse, w.drow, dk, dv, status};
   static std::atomic<int> attr[64];
@@ -643,7 +580,7 @@ cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t*
   if (ea != cudaSuccess) return ea;
   const long long items = (long long)batch * hq * 2 * a.nt;
   const long long ctas = std::min<long long>(items, num_sms());
-  dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, tdq, a);
+  dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -662,9 +599,13 @@ cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const 
                                     cudaStream_t stream) {
   const long long n = 2LL * L;
   const GradBuffers w = carve(workspace, batch, L, hq, d);
-  cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)batch * n * hq * d * sizeof(float), stream);
+  const int lp = (L + GT - 1) / GT * GT;
+  cudaError_t e = cudaMemsetAsync(dk, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
+  // lse and D rows past L (the pads of a partial last tile) must read as finite zeros
   if (e == cudaSuccess)
-    e = cudaMemsetAsync(dk, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
+    e = cudaMemsetAsync(w.drow, 0, (size_t)batch * hq * 2 * lp * sizeof(float), stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(w.lse, 0, (size_t)batch * hq * 2 * lp * sizeof(float), stream);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(dv, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
   if (e != cudaSuccess) return e;
@@ -674,14 +615,16 @@ cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const 
     return e;
   const long long nrows = (long long)batch * n * hq;
   grad_prep_kernel<<<(unsigned)((nrows + 7) / 8), 256, 0, stream>>>(o, d_o, w.do_bf, w.drow,
-                                                                    nrows, (int)n, hq, d);
+                                                                    nrows, (int)n, hq, d, lp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = d == 64 ? launch_grad_tc<64>(q, k, v, w, batch, L, B, hq, hkv, scale, dq, dk, dv, status,
+  e = d == 64 ? launch_grad_tc<64>(q, k, v, w, batch, L, B, hq, hkv, scale, dk, dv, status,
                                    stream)
-              : launch_grad_tc<128>(q, k, v, w, batch, L, B, hq, hkv, scale, dq, dk, dv, status,
+              : launch_grad_tc<128>(q, k, v, w, batch, L, B, hq, hkv, scale, dk, dv, status,
                                     stream);
   count_launches(2);
-  return e;
+  if (e != cudaSuccess) return e;
+  return launch_dual_stream_dq(q, k, v, reinterpret_cast<const uint16_t*>(w.do_bf), w.lse,
+                               w.drow, dq, batch, L, B, hq, hkv, d, scale, status, stream);
 }
 
 }  // namespace mars

@@ -85,11 +85,18 @@ cudaError_t set_smem_limit_once(Kernel* fn, int bytes, std::atomic<int> (&done)[
 }
 
 // ---- Dual-stream attention under mask M. o may be null when lse is given (the row
-// statistics alone: lse[b][h][row] = log2 of the softmax denominator, in units of
-// scale*log2(e)*score).
+// statistics alone: lse[b][h][stream][t], t < Lp = L rounded up to 128, = log2 of the
+// softmax denominator in units of scale*log2(e)*score; the pad is not written).
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* o, int batch, int L, int B, int hq, int hkv, int d,
                                float scale, int32_t* status, cudaStream_t stream,
                                float* lse = nullptr);
+
+// dQ of the dual-stream attention gradient from the forward's row statistics: lse and
+// D = rowsum(dO * O) as [b][hq][2][Lp] fp32, dO in bf16 like q. Writes every row of dq.
+cudaError_t launch_dual_stream_dq(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  const uint16_t* do_bf, const float* lse, const float* drow,
+                                  float* dq, int batch, int L, int B, int hq, int hkv, int d,
+                                  float scale, int32_t* status, cudaStream_t stream);
 
 }  // namespace mars
