@@ -643,9 +643,9 @@ def run_dual(device, peaks, reps=10, warm=3):
     torch.cuda.empty_cache()
     grad = {"ms": tg * 1e3, "tflops": 2.5 * fl / tg / 1e12,
             "frac_tensor": 2.5 * fl / tg / 1e12 / peaks["bf16_tflops"],
-            "note": "10 d flop per visible pair (S again, dP, dV, dK, dQ); one fused tcgen05 "
-                    "kernel over (batch, kv head, key tile) items after a statistics-only "
-                    "forward run; dQ by fp32 atomics"}
+            "note": "10 d flop per visible pair (S again, dP, dV, dK, dQ); a statistics-only "
+                    "forward run, then a tcgen05 dK/dV kernel over (batch, head, key tile) "
+                    "items and a row-parallel tcgen05 dQ kernel"}
     return {"workload": cfg.name, "ms": t * 1e3, "tflops": tf, "grad": grad,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
