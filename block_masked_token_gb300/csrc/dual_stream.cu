@@ -12,6 +12,9 @@
 // holding its own blocks. Fully masked tiles are never loaded; tiles every row sees in
 // full skip the per-key test. One persistent CTA per SM runs many items back to back. The
 // tile engine (flash_tc.cuh) runs QK^T and PV on tcgen05 with S and O in TMEM.
+//
+// The same items drive the dQ half of the attention gradient (dual_dq_kernel below); a
+// statistics-only run of the forward (no O store) gives the gradient its row log-sum-exp.
 #include <algorithm>
 #include <climits>
 

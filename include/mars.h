@@ -198,11 +198,14 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
  *   o, d_o [b, 2L, hq, d] float                   the forward's output and its gradient
  *   dq [b, 2L, hq, d], dk, dv [b, 2L, hkv, d] float (written)
  *   workspace >= mars_workspace_bytes(MARS_OP_DUAL_GRAD, b, B, hq, hkv, d, 0, 0, L) bytes:
- *             for one kv group the scores against the clean keys (2L x L) and inside
- *             the masked blocks (fp32), their probabilities (bf16), and dO in bf16
- * The products are cuBLAS GEMMs (bf16 inputs, fp32 accumulate); the masked softmax and
- * dS are libmars kernels. P and dS are rounded to bf16 before their products.
- * scale <= 0 means 1/sqrt(d). status may be NULL (no device-side checks). */
+ *             dO in bf16 and, per query row, the softmax log-sum-exp and D (fp32)
+ * The call recomputes the row statistics with the forward kernel, then runs a tcgen05
+ * kernel per (batch, query head, key tile) for dK and dV and a row-parallel one for dQ;
+ * no score block is stored. P and dS are rounded to bf16 before their products (fp32
+ * accumulate). dK and dV are sums over the kv group's query heads in an order that
+ * depends on scheduling (fp32 atomics), so they may differ in the last bits from run to
+ * run. scale <= 0 means 1/sqrt(d). status: as for mars_attn_dual_stream (a pipeline wait
+ * that ran out sets MARS_ST_TIMEOUT); may be NULL. */
 int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
                                const float* o, const float* d_o, int batch, int L, int B,
                                int hq, int hkv, int d, float scale, float* dq, float* dk,
