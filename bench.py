@@ -712,10 +712,25 @@ def run_case(args):
     elif isinstance(cfg, W.DualStreamConfig):
         x = W.make_dual_stream_inputs(cfg, seed=0, device=device)
         o = torch.empty(x["q"].shape, dtype=torch.float32, device=device)
-
-        def call():
+        if args.case == "dual_grad":
             mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
-        work = {"flop": dual_flops(cfg)}
+            d_o = torch.randn(o.shape, device=device)
+            b_, _, hq_, d_ = x["q"].shape
+            ws = torch.empty(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, b_, cfg.B, hq_,
+                                                       x["k"].shape[2], d_, max_len=cfg.L),
+                             dtype=torch.uint8, device=device)
+            dq = torch.empty(o.shape, dtype=torch.float32, device=device)
+            dk = torch.empty(x["k"].shape, dtype=torch.float32, device=device)
+            dv = torch.empty(x["v"].shape, dtype=torch.float32, device=device)
+
+            def call():
+                mars.mars_attn_dual_stream_grad(x["q"], x["k"], x["v"], o, d_o, cfg.L, cfg.B,
+                                                dq, dk, dv, ws)
+            work = {"flop": 2.5 * dual_flops(cfg)}
+        else:
+            def call():
+                mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
+            work = {"flop": dual_flops(cfg)}
     else:
         inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1,
                                    with_head=args.case == "head")
@@ -755,7 +770,7 @@ def run_case(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["head", "decode", "dual", "ce"], default=None,
+    ap.add_argument("--case", choices=["head", "decode", "dual", "dual_grad", "ce"], default=None,
                     help="time one entry point on --config instead of the decode step")
     ap.add_argument("--config", default=None, choices=sorted(W.CONFIGS))
     ap.add_argument("--gpus", type=int, default=1)

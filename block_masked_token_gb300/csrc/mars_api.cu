@@ -251,6 +251,6 @@ const char* mars_strerror(int code) {
 
 uint64_t mars_launch_count(void) { return mars::g_launches.load(std::memory_order_relaxed); }
 
-const char* mars_version(void) { return "libmars sm_103a v1 (cuda-core reference kernels)"; }
+const char* mars_version(void) { return "libmars sm_103a v2 (tcgen05/TMA kernels)"; }
 
 }  // extern "C"
