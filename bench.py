@@ -639,10 +639,27 @@ def run_dual(device, peaks, reps=10, warm=3):
         torch.cuda.synchronize()
         gt.append(a.elapsed_time(b) / 1e3)
     tg = statistics.median(gt)
-    del ws, dq, dk, dv, d_o
+    # the training step's form: the forward keeps its row statistics, the gradient reuses them
+    lse = torch.empty(mars.dual_lse_shape(cfg.batch, cfg.hq, cfg.L), device=device)
+    mars.mars_attn_dual_stream_lse(x["q"], x["k"], x["v"], o, lse, L=cfg.L, B=cfg.B)
+    for _ in range(warm):
+        mars.mars_attn_dual_stream_grad_lse(x["q"], x["k"], x["v"], o, d_o, lse, cfg.L, cfg.B,
+                                            dq, dk, dv, ws)
+    gl = []
+    for _ in range(max(3, reps // 2)):
+        a, b = _ev(), _ev()
+        a.record()
+        mars.mars_attn_dual_stream_grad_lse(x["q"], x["k"], x["v"], o, d_o, lse, cfg.L, cfg.B,
+                                            dq, dk, dv, ws)
+        b.record()
+        torch.cuda.synchronize()
+        gl.append(a.elapsed_time(b) / 1e3)
+    tgl = statistics.median(gl)
+    del ws, dq, dk, dv, d_o, lse
     torch.cuda.empty_cache()
     grad = {"ms": tg * 1e3, "tflops": 2.5 * fl / tg / 1e12,
             "frac_tensor": 2.5 * fl / tg / 1e12 / peaks["bf16_tflops"],
+            "from_forward_lse_ms": tgl * 1e3,
             "note": "10 d flop per visible pair (S again, dP, dV, dK, dQ); a statistics-only "
                     "forward run, then a tcgen05 dK/dV kernel over (batch, head, key tile) "
                     "items and a row-parallel tcgen05 dQ kernel"}

@@ -38,7 +38,7 @@ struct DualPolicy {
   static constexpr int kStageBoxes = D / 32 < 2 ? D / 32 : 2;
   const CUtensorMap* tm_o;   // O as [2*batch][L][hq][D] fp32, box [1][128][1][32]
   float* lse;                // optional: [batch][hq][2][Lp] row log-sum-exp (log2 units),
-                             // Lp = L rounded up to 128 (the pad is not written)
+                             // Lp = L rounded up to 128 (pad rows written as 0)
   int lp;
   int store_o;               // 0: O is not written (a statistics-only run)
   int L, B, hq;
@@ -78,10 +78,12 @@ struct DualPolicy {
   MARS_DEV uint8_t* stage(uint8_t* smem) const {
     return smem + flash::Smem<D, kStageBoxes>::OFF_STAGE;
   }
-  // log2 of the row's softmax denominator in units of scale*log2(e)*score: m + log2(l)
+  // log2 of the row's softmax denominator in units of scale*log2(e)*score: m + log2(l);
+  // the pad rows of a partial last tile get 0
   MARS_DEV void row_stats(int row, float m, float l) const {
-    if (lse && row_valid(row))
-      lse[(((size_t)b * hq + h) * 2 + stream) * lp + r0 + row] = m + log2f(l);
+    if (lse)
+      lse[(((size_t)b * hq + h) * 2 + stream) * lp + r0 + row] =
+          row_valid(row) ? m + log2f(l) : 0.f;
   }
   // rows past L (a partial last query tile) fall outside the map's L extent and are not
   // written

@@ -596,23 +596,24 @@ cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const 
                                     const float* o, const float* d_o, int batch, int L, int B,
                                     int hq, int hkv, int d, float scale, float* dq, float* dk,
                                     float* dv, void* workspace, int32_t* status,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, const float* lse_in) {
   const long long n = 2LL * L;
-  const GradBuffers w = carve(workspace, batch, L, hq, d);
+  GradBuffers w = carve(workspace, batch, L, hq, d);
   const int lp = (L + GT - 1) / GT * GT;
   cudaError_t e = cudaMemsetAsync(dk, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
-  // lse and D rows past L (the pads of a partial last tile) must read as finite zeros
+  // D rows past L (the pads of a partial last tile) must read as finite zeros; the
+  // forward writes the lse pads itself
   if (e == cudaSuccess)
     e = cudaMemsetAsync(w.drow, 0, (size_t)batch * hq * 2 * lp * sizeof(float), stream);
   if (e == cudaSuccess)
-    e = cudaMemsetAsync(w.lse, 0, (size_t)batch * hq * 2 * lp * sizeof(float), stream);
-  if (e == cudaSuccess)
     e = cudaMemsetAsync(dv, 0, (size_t)batch * n * hkv * d * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  // row statistics: the forward without its O store
-  if ((e = launch_dual_stream(q, k, v, nullptr, batch, L, B, hq, hkv, d, scale, status, stream,
-                              w.lse)) != cudaSuccess)
-    return e;
+  if (lse_in) {
+    w.lse = const_cast<float*>(lse_in);              // the forward's, read only
+  } else if ((e = launch_dual_stream(q, k, v, nullptr, batch, L, B, hq, hkv, d, scale, status,
+                                     stream, w.lse)) != cudaSuccess) {
+    return e;                                        // row statistics: forward without O
+  }
   const long long nrows = (long long)batch * n * hq;
   grad_prep_kernel<<<(unsigned)((nrows + 7) / 8), 256, 0, stream>>>(o, d_o, w.do_bf, w.drow,
                                                                     nrows, (int)n, hq, d, lp);

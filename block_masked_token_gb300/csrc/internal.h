@@ -54,7 +54,7 @@ cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const 
                                     const float* o, const float* d_o, int batch, int L, int B,
                                     int hq, int hkv, int d, float scale, float* dq, float* dk,
                                     float* dv, void* workspace, int32_t* status,
-                                    cudaStream_t stream);
+                                    cudaStream_t stream, const float* lse = nullptr);
 
 // ---- Dual-stream training loss (L_mask + L_AR) over the 2L rows of each sequence.
 size_t ce_workspace_bytes(int batch, int L, int vocab);
@@ -86,7 +86,7 @@ cudaError_t set_smem_limit_once(Kernel* fn, int bytes, std::atomic<int> (&done)[
 
 // ---- Dual-stream attention under mask M. o may be null when lse is given (the row
 // statistics alone: lse[b][h][stream][t], t < Lp = L rounded up to 128, = log2 of the
-// softmax denominator in units of scale*log2(e)*score; the pad is not written).
+// softmax denominator in units of scale*log2(e)*score; pad rows are written as 0).
 cudaError_t launch_dual_stream(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                float* o, int batch, int L, int B, int hq, int hkv, int d,
                                float scale, int32_t* status, cudaStream_t stream,

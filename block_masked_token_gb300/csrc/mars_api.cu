@@ -74,6 +74,22 @@ int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf1
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int mars_attn_dual_stream_lse(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                              float* o, float* lse, int batch, int L, int B, int hq, int hkv,
+                              int d, float scale, int32_t* status, void* stream) {
+  if (batch < 0 || L < 1 || B < 1) return MARS_EINVAL;
+  int rc = check_heads(hq, hkv, d);
+  if (rc) return rc;
+  if (batch == 0) return MARS_OK;
+  if (!q || !k || !v || !o || !lse) return MARS_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return MARS_EALIGN;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+  if (isinf(scale)) return MARS_EINVAL;
+  return cuda_rc(mars::launch_dual_stream(q, k, v, o, batch, L, B, hq, hkv, d, scale, status,
+                                          static_cast<cudaStream_t>(stream), lse));
+}
+
 int mars_decode_attn(const mars_bf16* q, const mars_bf16* k_blk, const mars_bf16* v_blk,
                      const mars_bf16* k_pool, const mars_bf16* v_pool, int num_pages,
                      const int32_t* block_table, int max_pages_per_seq,
@@ -181,16 +197,19 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
                            page_size, true, status, stream);
 }
 
-int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
-                               const float* o, const float* d_o, int batch, int L, int B,
-                               int hq, int hkv, int d, float scale, float* dq, float* dk,
-                               float* dv, void* workspace, size_t ws_bytes, int32_t* status,
-                               void* stream) {
+namespace {
+
+int dual_grad_checked(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                      const float* o, const float* d_o, const float* lse, int batch, int L,
+                      int B, int hq, int hkv, int d, float scale, float* dq, float* dk,
+                      float* dv, void* workspace, size_t ws_bytes, int32_t* status,
+                      void* stream) {
   if (batch < 0 || L < 1 || B < 1) return MARS_EINVAL;
   int rc = check_heads(hq, hkv, d);
   if (rc) return rc;
   if (batch == 0) return MARS_OK;
   if (!q || !k || !v || !o || !d_o || !dq || !dk || !dv || !workspace) return MARS_EINVAL;
+  if (lse && !aligned16(lse)) return MARS_EALIGN;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
     return MARS_EALIGN;
@@ -199,7 +218,28 @@ int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mar
   if (isinf(scale)) return MARS_EINVAL;
   return cuda_rc(mars::launch_dual_stream_grad(q, k, v, o, d_o, batch, L, B, hq, hkv, d, scale,
                                                dq, dk, dv, workspace, status,
-                                               static_cast<cudaStream_t>(stream)));
+                                               static_cast<cudaStream_t>(stream), lse));
+}
+
+}  // namespace
+
+int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                               const float* o, const float* d_o, int batch, int L, int B,
+                               int hq, int hkv, int d, float scale, float* dq, float* dk,
+                               float* dv, void* workspace, size_t ws_bytes, int32_t* status,
+                               void* stream) {
+  return dual_grad_checked(q, k, v, o, d_o, nullptr, batch, L, B, hq, hkv, d, scale, dq, dk, dv,
+                           workspace, ws_bytes, status, stream);
+}
+
+int mars_attn_dual_stream_grad_lse(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                                   const float* o, const float* d_o, const float* lse,
+                                   int batch, int L, int B, int hq, int hkv, int d, float scale,
+                                   float* dq, float* dk, float* dv, void* workspace,
+                                   size_t ws_bytes, int32_t* status, void* stream) {
+  if (batch > 0 && !lse) return MARS_EINVAL;
+  return dual_grad_checked(q, k, v, o, d_o, lse, batch, L, B, hq, hkv, d, scale, dq, dk, dv,
+                           workspace, ws_bytes, status, stream);
 }
 
 int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32_t* targets,

@@ -56,6 +56,11 @@ def lib() -> ctypes.CDLL:
         L.mars_attn_dual_stream_grad.restype = I
         L.mars_attn_dual_stream_grad.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P,
                                                  S, P, P]
+        L.mars_attn_dual_stream_lse.restype = I
+        L.mars_attn_dual_stream_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+        L.mars_attn_dual_stream_grad_lse.restype = I
+        L.mars_attn_dual_stream_grad_lse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P,
+                                                     P, P, S, P, P]
         L.mars_dual_stream_ce_loss_grad.restype = I
         L.mars_dual_stream_ce_loss_grad.argtypes = [P, P, P, P, I, I, I, I, P, P, P, S, P, P]
         L.mars_strerror.restype = ctypes.c_char_p
@@ -71,7 +76,8 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("mars_workspace_bytes", "mars_attn_dual_stream", "mars_decode_attn",
             "mars_head_accept", "mars_head_accept_per_request", "mars_kv_commit",
             "mars_kv_commit_batch_sync", "mars_dual_stream_ce_loss",
-            "mars_dual_stream_ce_loss_grad", "mars_attn_dual_stream_grad", "mars_strerror",
+            "mars_dual_stream_ce_loss_grad", "mars_attn_dual_stream_grad",
+            "mars_attn_dual_stream_lse", "mars_attn_dual_stream_grad_lse", "mars_strerror",
             "mars_version", "mars_launch_count")
 
 
@@ -266,6 +272,52 @@ def mars_dual_stream_ce_loss_grad(h, w, targets, row_lse, batch: int, L: int, wo
                                             _ptr(workspace), workspace.numel(), _ptr(status),
                                             _stream(stream)),
         "mars_dual_stream_ce_loss_grad")
+
+
+def dual_lse_shape(b: int, hq: int, L: int):
+    """Shape of the row statistics mars_attn_dual_stream_lse writes: [b, hq, 2, Lp], Lp = L
+    rounded up to a multiple of 128."""
+    return (b, hq, 2, (L + 127) // 128 * 128)
+
+
+def mars_attn_dual_stream_lse(q, k, v, o, lse, L: int, B: int, scale: float = 0.0, status=None,
+                              stream=None):
+    """mars_attn_dual_stream that also writes each row's softmax log-sum-exp (log2) into
+    lse [b, hq, 2, Lp] float32 (see include/mars.h)."""
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    _check(q, "q", torch.bfloat16, (b, 2 * L, hq, d))
+    _check(k, "k", torch.bfloat16, (b, 2 * L, hkv, d))
+    _check(v, "v", torch.bfloat16, (b, 2 * L, hkv, d))
+    _check(o, "o", torch.float32, (b, 2 * L, hq, d))
+    _check(lse, "lse", torch.float32, dual_lse_shape(b, hq, L))
+    if status is not None:
+        _check(status, "status", torch.int32, (1,))
+    _rc(lib().mars_attn_dual_stream_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), b, L, B,
+                                        hq, hkv, d, float(scale), _ptr(status), _stream(stream)),
+        "mars_attn_dual_stream_lse")
+
+
+def mars_attn_dual_stream_grad_lse(q, k, v, o, d_o, lse, L: int, B: int, dq, dk, dv, workspace,
+                                   scale: float = 0.0, status=None, stream=None):
+    """mars_attn_dual_stream_grad from the forward's lse (mars_attn_dual_stream_lse)."""
+    b, n, hq, d = q.shape
+    hkv = k.shape[2]
+    _check(q, "q", torch.bfloat16, (b, 2 * L, hq, d))
+    _check(k, "k", torch.bfloat16, (b, 2 * L, hkv, d))
+    _check(v, "v", torch.bfloat16, (b, 2 * L, hkv, d))
+    _check(o, "o", torch.float32, (b, 2 * L, hq, d))
+    _check(d_o, "d_o", torch.float32, (b, 2 * L, hq, d))
+    _check(lse, "lse", torch.float32, dual_lse_shape(b, hq, L))
+    _check(dq, "dq", torch.float32, (b, 2 * L, hq, d))
+    _check(dk, "dk", torch.float32, (b, 2 * L, hkv, d))
+    _check(dv, "dv", torch.float32, (b, 2 * L, hkv, d))
+    _check(workspace, "workspace", torch.uint8)
+    _rc(lib().mars_attn_dual_stream_grad_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o),
+                                             _ptr(lse), b, L, B, hq, hkv, d, float(scale),
+                                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                             workspace.numel(), _ptr(status), _stream(stream)),
+        "mars_attn_dual_stream_grad_lse")
 
 
 def mars_attn_dual_stream_grad(q, k, v, o, d_o, L: int, B: int, dq, dk, dv, workspace,

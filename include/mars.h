@@ -82,6 +82,17 @@ int mars_attn_dual_stream(const mars_bf16* q, const mars_bf16* k, const mars_bf1
                           float* o, int batch, int L, int B, int hq, int hkv, int d,
                           float scale, int32_t* status, void* stream);
 
+/* mars_attn_dual_stream that also writes each query row's softmax log-sum-exp, the
+ * statistic its gradient needs (the training step's forward keeps it for the backward):
+ *   lse [batch, hq, 2, Lp] float (written), Lp = L rounded up to a multiple of 128;
+ *       lse[b][h][s][t] = log2 of sum over the keys visible to row s*L + t of
+ *       exp2(scale * log2(e) * q.k), for t < L; rows L <= t < Lp are written as 0.
+ * lse is 16-byte aligned. Other arguments, layouts and errors as mars_attn_dual_stream;
+ * o is written identically. */
+int mars_attn_dual_stream_lse(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                              float* o, float* lse, int batch, int L, int B, int hq, int hkv,
+                              int d, float scale, int32_t* status, void* stream);
+
 /* Decode-form attention ([gist] 2.C sliding window; [notes] Key design 3 and 4): each
  * sequence s appends B [MASK] queries after its committed prefix of P_s = seq_lens[s]
  * tokens held in a paged cache; block query k sees all P_s prefix keys and block keys
@@ -211,6 +222,16 @@ int mars_attn_dual_stream_grad(const mars_bf16* q, const mars_bf16* k, const mar
                                int hq, int hkv, int d, float scale, float* dq, float* dk,
                                float* dv, void* workspace, size_t ws_bytes, int32_t* status,
                                void* stream);
+
+/* mars_attn_dual_stream_grad from the forward's row statistics: lse as written by
+ * mars_attn_dual_stream_lse with the same q, k, v, L, B and scale (read only), which
+ * saves the forward pass the plain entry point runs to recompute it. Other arguments,
+ * workspace, layouts and errors as mars_attn_dual_stream_grad. */
+int mars_attn_dual_stream_grad_lse(const mars_bf16* q, const mars_bf16* k, const mars_bf16* v,
+                                   const float* o, const float* d_o, const float* lse,
+                                   int batch, int L, int B, int hq, int hkv, int d, float scale,
+                                   float* dq, float* dk, float* dv, void* workspace,
+                                   size_t ws_bytes, int32_t* status, void* stream);
 
 /* Dual-stream training loss L = L_mask + L_AR ([notes] Key design 2: the masked-stream
  * cross-entropy plus the clean-stream next-token cross-entropy; [gist] 2.B "Combined

@@ -165,6 +165,26 @@ def attn_dual_stream(q, k, v, L: int, B: int, scale: float | None = None, rows=N
     return out
 
 
+def attn_dual_stream_lse(q, k, L: int, B: int, scale: float | None = None):
+    """Per query row, log2 of the softmax denominator of attn_dual_stream: lse[b, h, i] =
+    log2 sum over the keys j visible to row i under M of exp(scale * q_i . k_j)
+    ([notes] Key design 1, eq. M; the statistic the backward pass of that softmax reuses).
+    q: [b, 2L, Hq, D], k: [b, 2L, Hkv, D] (float64). Returns [b, Hq, 2L] float64."""
+    b, n, Hq, D = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    vis = mask_rows(L, B, np.arange(n))
+    out = np.empty((b, Hq, n))
+    for bi in range(b):
+        for h in range(Hq):
+            S = np.where(vis, scale * (q[bi, :, h, :] @ k[bi, :, h // g, :].T), NEG_INF)
+            m = S.max(axis=1)
+            out[bi, h] = (m + np.log(np.exp(S - m[:, None]).sum(axis=1))) / math.log(2.0)
+    return out
+
+
 def attn_dual_stream_grad(q, k, v, do, L: int, B: int, scale: float | None = None):
     """Gradient of the dual-stream attention (attn_dual_stream) for an upstream gradient
     dO [b, 2L, Hq, D]: per (batch, query head h), with kv head h // (Hq/Hkv),

@@ -107,7 +107,17 @@ def test_host_validation_codes(L):
     assert L.mars_attn_dual_stream_grad(*ga, 96, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_attn_dual_stream_grad(*ga, 64, 0.0, None, P, P, P, 1 << 30, None, None) == mars.EINVAL
     assert L.mars_attn_dual_stream_grad(*ga, 64, 0.0, P, P, P, P, 16, None, None) == mars.ENOSPACE
-    # loss gradient: vocabulary not a multiple of 8, null row_lse, workspace too small
+    # forward with row statistics: null lse, misaligned lse, unsupported head dim
+    assert L.mars_attn_dual_stream_lse(P, P, P, P, None, 1, 8, 2, 4, 2, 64, 0.0, None, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream_lse(P, P, P, P, _p(20), 1, 8, 2, 4, 2, 64, 0.0, None, None) == mars.EALIGN
+    assert L.mars_attn_dual_stream_lse(P, P, P, P, P, 1, 8, 2, 4, 2, 96, 0.0, None, None) == mars.EUNSUPPORTED
+    assert L.mars_attn_dual_stream_lse(P, P, P, P, None, 0, 8, 2, 4, 2, 64, 0.0, None, None) == mars.OK
+    # gradient from those statistics: null lse, misaligned lse, workspace too small
+    gl = [P, P, P, P, P]
+    assert L.mars_attn_dual_stream_grad_lse(*gl, None, 1, 8, 2, 4, 2, 64, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_attn_dual_stream_grad_lse(*gl, _p(20), 1, 8, 2, 4, 2, 64, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EALIGN
+    assert L.mars_attn_dual_stream_grad_lse(*gl, P, 1, 8, 2, 4, 2, 64, 0.0, P, P, P, P, 16, None, None) == mars.ENOSPACE
+        # loss gradient: vocabulary not a multiple of 8, null row_lse, workspace too small
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 100, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, None, 1, 4, 64, 96, P, P, P, 1 << 30, None, None) == mars.EINVAL
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 96, P, P, P, 16, None, None) == mars.ENOSPACE

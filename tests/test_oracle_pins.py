@@ -164,6 +164,37 @@ def test_dual_stream_row_sampling_matches_full():
     np.testing.assert_allclose(part[1][:, [1, 3]], full[1][rows][:, [1, 3]], rtol=0, atol=0)
 
 
+def test_dual_stream_lse_zero_queries_counts_visible_keys():
+    """With q = 0 every visible score is 0, so the denominator is the number of visible
+    keys: t + 1 for row t of either stream (clean row t sees keys 0..t; masked row t sees
+    the clean keys before its block start bs and its own block's keys bs..t)."""
+    L, B = 23, 5
+    q = np.zeros((1, 2 * L, 2, 8))
+    k = _rand((1, 2 * L, 1, 8), 3)
+    lse = oracle.attn_dual_stream_lse(q, k, L, B)
+    t = np.arange(L)
+    want = np.log2(np.concatenate([t + 1, t + 1]).astype(np.float64))
+    np.testing.assert_allclose(lse[0, 0], want, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 1], want, rtol=0, atol=1e-12)
+
+
+def test_dual_stream_lse_reproduces_attention_probabilities():
+    """The probabilities attn_dual_stream applies are exp2(scale log2(e) s - lse): with V
+    the identity (one value column per key), O itself is the probability matrix."""
+    L, B = 9, 2
+    n = 2 * L
+    q = _rand((1, n, 2, n), 11) * 0.5                # head dim 2L, the width of V = I
+    k = _rand((1, n, 1, n), 12)
+    v = np.eye(n)[None, :, None, :]                  # [1, 2L, 1, 2L]
+    o = oracle.attn_dual_stream(q, k, v, L, B, scale=0.4)
+    lse = oracle.attn_dual_stream_lse(q, k, L, B, scale=0.4)
+    vis = oracle.mask_rows(L, B, np.arange(n))
+    for h in range(2):
+        s = 0.4 * q[0, :, h] @ k[0, :, 0].T
+        p = np.where(vis, np.exp2(s / math.log(2.0) - lse[0, h][:, None]), 0.0)
+        np.testing.assert_allclose(o[0, :, h], p, rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------------- decode form
 
 def _paged_from_logical(logical, page_size, perm, Hkv, D):

@@ -184,6 +184,48 @@ def test_dual_stream_grad_small(b, L, B, hq, hkv, d):
         assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
 
 
+def test_dual_stream_lse_matches_oracle():
+    """The forward with row statistics writes the same O as the plain forward and, per row,
+    the log2 softmax denominator of the oracle; the pad rows of the last tile are 0."""
+    cfg = W.DualStreamConfig("lse", 2, 200, 16, 4, 2, 128)
+    x = W.make_dual_stream_inputs(cfg, seed=21)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o = run_dual(q, k, v, cfg.L, cfg.B)
+    o2 = torch.empty_like(o)
+    lse = torch.full(mars.dual_lse_shape(2, 4, cfg.L), float("nan"), device=DEV)
+    mars.mars_attn_dual_stream_lse(q, k, v, o2, lse, cfg.L, cfg.B)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+    ref = oracle.attn_dual_stream_lse(f64(x["q"]), f64(x["k"]), cfg.L, cfg.B)
+    got = lse.cpu().double().numpy()
+    for s_ in range(2):
+        err = np.abs(got[:, :, s_, :cfg.L] - ref[:, :, s_ * cfg.L:(s_ + 1) * cfg.L]).max()
+        assert err < 1e-3, f"stream {s_}: lse max-abs error {err:.2e}"
+    assert (got[:, :, :, cfg.L:] == 0).all()
+
+
+def test_dual_stream_grad_from_lse_matches_plain_grad():
+    """The gradient from the forward's statistics equals the plain gradient (which
+    recomputes them with the same kernel): dQ bit for bit, dK/dV up to the order of their
+    fp32 atomic sums."""
+    cfg = W.DualStreamConfig("glse", 1, 300, 48, 4, 2, 64)
+    x = W.make_dual_stream_inputs(cfg, seed=8)
+    xd = {kk: vv.to(DEV) for kk, vv in x.items()}
+    d_o, dq, dk, dv = run_dual_grad(xd, cfg.L, cfg.B)
+    q, k, v = xd["q"], xd["k"], xd["v"]
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    lse = torch.empty(mars.dual_lse_shape(1, 4, cfg.L), device=DEV)
+    mars.mars_attn_dual_stream_lse(q, k, v, o, lse, cfg.L, cfg.B)
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, 1, cfg.B, 4, 2, 64, max_len=cfg.L))
+    dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    mars.mars_attn_dual_stream_grad_lse(q, k, v, o, d_o, lse, cfg.L, cfg.B, dq2, dk2, dv2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2)
+    for a_, b_, name in ((dk, dk2, "dk"), (dv, dv2, "dv")):
+        err = _rel(a_.cpu().numpy(), b_.cpu().numpy())
+        assert err < 1e-5, f"{name} relative difference {err:.2e}"
+
+
 def test_dual_stream_grad_many_items_per_cta():
     """More (batch, kv head, key tile) work items than SMs, so persistent CTAs carry the
     rings, TMEM accumulators and barrier phases from item to item; ragged L, odd-sized
