@@ -502,25 +502,30 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive_warp(&qb.dp_free);
-        uint32_t ds[32];
+        // masked keys become -inf (exp2 gives 0) where the tile is not fully visible
+        if (!rv || !tile.full) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t mk = rv ? flash::chunk_mask(cr, 2 * half + q) : 0u;
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t mk = rv ? flash::chunk_mask(cr, 2 * half + q) : 0u;
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float x[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cidx = 32 * q + e + u;
-              const float p = ((mk >> (e + u)) & 1u)
-                                  ? flash::ex2_approx(__uint_as_float(sv[cidx]) * a.scale_log2 - lse)
-                                  : 0.f;
-              // P rounded to bf16 as in the key-tile kernel's dV and dS
-              const float pb = __bfloat162float(__float2bfloat16_rn(p));
-              x[u] = pb * (__uint_as_float(pv[cidx]) - dd);
-            }
-            ds[16 * q + e / 2] = flash::pack_bf16x2(x[0], x[1]);
+            for (int e = 0; e < 32; ++e)
+              if (!((mk >> e) & 1u)) sv[32 * q + e] = 0xff800000u;
           }
+        }
+        // P = exp2(scale log2e S - lse) rounded to bf16 (as the key-tile kernel's P),
+        // dS = P * (dP - D), in packed f32x2 operations
+        uint32_t ds[32];
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nl2 = make_float2(-lse, -lse), nd2 = make_float2(-dd, -dd);
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float2 t = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                      sc2, nl2);
+          const uint32_t pb = flash::pack_bf16x2(flash::ex2_approx(t.x), flash::ex2_approx(t.y));
+          const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb));
+          const float2 x = __fmul2_rn(pf, __fadd2_rn(make_float2(__uint_as_float(pv[e]),
+                                                                 __uint_as_float(pv[e + 1])), nd2));
+          ds[e / 2] = flash::pack_bf16x2(x.x, x.y);
         }
         tmem_st32(tmem + sb * BKV + 64 * half + lane_off, ds);
         tmem_st_wait();

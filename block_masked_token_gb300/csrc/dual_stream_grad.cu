@@ -434,23 +434,28 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
           tmem_ld32(tmem + S::TM_S + HC * half + q * 32 + lane_off,
                     *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
         tmem_ld_wait();
-        uint32_t pp[HC / 2];
+        // masked columns become -inf (exp2 gives 0) only where this row's range does not
+        // cover the whole half; the scale-and-shift runs as packed f32x2 FMAs
+        if (!(lo <= 0 && hi >= HC - 1)) {
 #pragma unroll
-        for (int q = 0; q < HC / 32; ++q) {
-          const uint32_t mk = bits(lo - 32 * q, hi + 1 - 32 * q);
+          for (int q = 0; q < HC / 32; ++q) {
+            const uint32_t mk = bits(lo - 32 * q, hi + 1 - 32 * q);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(ls + 32 * q + e);
-            const float l[4] = {l4.x, l4.y, l4.z, l4.w};
-            float pv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              pv[u] = ((mk >> (e + u)) & 1u)
-                          ? ex2(__uint_as_float(v[32 * q + e + u]) * a.scale_log2 - l[u])
-                          : 0.f;
-            pp[16 * q + e / 2] = pack2(pv[0], pv[1]);
-            pp[16 * q + e / 2 + 1] = pack2(pv[2], pv[3]);
+            for (int e = 0; e < 32; ++e)
+              if (!((mk >> e) & 1u)) v[32 * q + e] = 0xff800000u;
           }
+        }
+        uint32_t pp[HC / 2];
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+#pragma unroll
+        for (int e = 0; e < HC; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(ls + e);
+          const float2 t01 = __ffma2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                                        sc2, make_float2(-l4.x, -l4.y));
+          const float2 t23 = __ffma2_rn(make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+                                        sc2, make_float2(-l4.z, -l4.w));
+          pp[e / 2] = pack2(ex2(t01.x), ex2(t01.y));
+          pp[e / 2 + 1] = pack2(ex2(t23.x), ex2(t23.y));
         }
         // over this half's own S^T columns (the other half may still be reading its own)
         tmem_st32(tmem + S::TM_S + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
@@ -466,16 +471,18 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
                     *reinterpret_cast<uint32_t(*)[32]>(v + q * 32));
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < HC; e += 4) {                // dS over P, pair by pair
+        for (int e = 0; e < HC; e += 4) {                // dS over P, packed f32x2
           const float4 d4 = *reinterpret_cast<const float4*>(dsv + e);
-          const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2]);
-          const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2 + 1]);
-          const float s0 = __low2float(p01) * (__uint_as_float(v[e]) - d4.x);
-          const float s1 = __high2float(p01) * (__uint_as_float(v[e + 1]) - d4.y);
-          const float s2 = __low2float(p23) * (__uint_as_float(v[e + 2]) - d4.z);
-          const float s3 = __high2float(p23) * (__uint_as_float(v[e + 3]) - d4.w);
-          pp[e / 2] = pack2(s0, s1);
-          pp[e / 2 + 1] = pack2(s2, s3);
+          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2]));
+          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[e / 2 + 1]));
+          const float2 s01 = __fmul2_rn(p01, __fadd2_rn(make_float2(__uint_as_float(v[e]),
+                                                                    __uint_as_float(v[e + 1])),
+                                                        make_float2(-d4.x, -d4.y)));
+          const float2 s23 = __fmul2_rn(p23, __fadd2_rn(make_float2(__uint_as_float(v[e + 2]),
+                                                                    __uint_as_float(v[e + 3])),
+                                                        make_float2(-d4.z, -d4.w)));
+          pp[e / 2] = pack2(s01.x, s01.y);
+          pp[e / 2 + 1] = pack2(s23.x, s23.y);
         }
         tmem_st32(tmem + S::TM_DP + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
         tmem_st_wait();
