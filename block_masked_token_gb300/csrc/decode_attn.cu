@@ -57,7 +57,7 @@ MARS_DEV bool page_ok(const DecodeArgs& a, const int32_t* bt_row, int lp) {
 
 template <int D>
 struct DecodePolicy {
-  static constexpr bool kStagedStore = false;
+  static constexpr bool kHandOff = false;
   static constexpr bool kRowStats = false;
   const DecodeArgs* a;
   const int32_t* bt_row;

@@ -33,7 +33,7 @@ using flash::BQ;
 // round) while the K/V rings already stream the next item.
 template <int D>
 struct DualPolicy {
-  static constexpr bool kStagedStore = true;
+  static constexpr bool kHandOff = true;
   static constexpr bool kRowStats = true;
   static constexpr int kStageBoxes = D / 32 < 2 ? D / 32 : 2;
   const CUtensorMap* tm_o;   // O as [2*batch][L][hq][D] fp32, box [1][128][1][32]
@@ -75,6 +75,9 @@ struct DualPolicy {
     c.pmask = 0xffu;
     return c;
   }
+  float* inv_slot;           // 1/l of the item's 128 rows for the epilogue warps
+  int item;                  // index of this item among the CTA's items
+  MARS_DEV void hand_off(int row, float inv) const { inv_slot[row] = inv; }
   MARS_DEV uint8_t* stage(uint8_t* smem) const {
     return smem + flash::Smem<D, kStageBoxes>::OFF_STAGE;
   }
@@ -192,13 +195,26 @@ MARS_DEV void cta_teardown(uint32_t tmem, int warp) {
   }
 }
 
-// One CTA per SM runs work items r*G + c (even rounds r) and
-// r*G + G-1-c (odd rounds), G = gridDim.x, c = blockIdx.x, so heavy and light items even
-// out. The rings, S buffers and barrier phases run on across items; the next item's Q is
-// loaded as soon as the current item's last QK^T has completed, and its first K/V tiles
-// stream in while the softmax warps write out the current item's O.
+// One CTA per SM runs work items r*G + c (even rounds r) and r*G + G-1-c (odd rounds),
+// G = gridDim.x, c = blockIdx.x, so heavy and light items even out. The rings, S buffers
+// and barrier phases run on across items; the next item's Q is loaded as soon as the
+// current item's last QK^T has completed. Three warpgroups: warps 0..3 K loader, QK^T
+// issuer (TMEM owner), V loader, PV issuer; 4..7 softmax; 8..11 epilogue. The softmax
+// warps hand each item's 1/l to the epilogue warps and go straight on to the next item,
+// while those read O out of TMEM and write it back with TMA stores; the next item's
+// first PV waits until O has been read.
+constexpr int DUAL_THREADS = 384;
+constexpr int DUAL_WG0_REGS = 88, DUAL_SOFTMAX_REGS = 232, DUAL_EPI_REGS = 160;
+static_assert(128 * (DUAL_WG0_REGS + DUAL_SOFTMAX_REGS + DUAL_EPI_REGS) <=
+                  DUAL_THREADS * (65536 / DUAL_THREADS / 8 * 8),
+              "the register split fits the launch's register pool");
+
+struct DualEpi {
+  float inv[2][BQ];        // 1/l per row, by item parity
+};
+
 template <int D>
-__global__ void __launch_bounds__(flash::NUM_THREADS, 1)
+__global__ void __launch_bounds__(DUAL_THREADS, 1)
 dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
                               const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v,
@@ -207,6 +223,7 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
   using Pol = DualPolicy<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ flash::Barriers bar;
+  __shared__ DualEpi epi;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -216,44 +233,48 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int G = gridDim.x, c = blockIdx.x;
   auto item_id = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
   const int rounds = (total + G - 1) / G;
+  const int wg = warp >> 2;
 
-  if (warp == 0 || warp == flash::V_LOADER_WARP) {
-    const bool is_v = warp != 0;
-    int last_k[flash::K_STAGES], last_v[flash::V_STAGES];
-    for (int i = 0; i < flash::K_STAGES; ++i) last_k[i] = -1;
-    for (int i = 0; i < flash::V_STAGES; ++i) last_v[i] = -1;
-    int j0 = 0;
-    for (int r = 0; r < rounds; ++r) {
-      const int id = item_id(r);
-      if (id >= total) continue;
-      const Pol pol = make_item<D>(a, id, &tm_o);
-      const bool ok = is_v ? flash::load_ring_item<D, flash::V_STAGES>(
-                                 bar, smem, pol.n_total, j0, last_v, false, a.status, true,
-                                 KVIssue<D, Pol>{&pol, &tm_v})
-                           : flash::load_ring_item<D, flash::K_STAGES>(
-                                 bar, smem, pol.n_total, j0, last_k, false, a.status, false,
-                                 KVIssue<D, Pol>{&pol, &tm_k});
-      if (!ok) break;
-      j0 += pol.n_total;
-    }
-    // wait (bounded) for every copy still in flight
-    const Pol none{};
-    if (is_v)
-      flash::load_ring_item<D, flash::V_STAGES>(bar, smem, 0, j0, last_v, true, a.status, true,
-                                                KVIssue<D, Pol>{&none, &tm_v});
-    else
-      flash::load_ring_item<D, flash::K_STAGES>(bar, smem, 0, j0, last_k, true, a.status, false,
-                                                KVIssue<D, Pol>{&none, &tm_k});
-  } else if (warp == 1 || warp == flash::PV_ISSUER_WARP) {
-    if (lane == 0) {
-      const bool pv = warp == flash::PV_ISSUER_WARP;
+  if (wg == 0) {
+    regs_lower<DUAL_WG0_REGS>();
+    if (warp == 0 || warp == 2) {
+      const bool is_v = warp == 2;
+      int last_k[flash::K_STAGES], last_v[flash::V_STAGES];
+      for (int i = 0; i < flash::K_STAGES; ++i) last_k[i] = -1;
+      for (int i = 0; i < flash::V_STAGES; ++i) last_v[i] = -1;
+      int j0 = 0;
+      for (int r = 0; r < rounds; ++r) {
+        const int id = item_id(r);
+        if (id >= total) continue;
+        const Pol pol = make_item<D>(a, id, &tm_o);
+        const bool ok = is_v ? flash::load_ring_item<D, flash::V_STAGES>(
+                                   bar, smem, pol.n_total, j0, last_v, false, a.status, true,
+                                   KVIssue<D, Pol>{&pol, &tm_v})
+                             : flash::load_ring_item<D, flash::K_STAGES>(
+                                   bar, smem, pol.n_total, j0, last_k, false, a.status, false,
+                                   KVIssue<D, Pol>{&pol, &tm_k});
+        if (!ok) break;
+        j0 += pol.n_total;
+      }
+      // wait (bounded) for every copy still in flight
+      const Pol none{};
+      if (is_v)
+        flash::load_ring_item<D, flash::V_STAGES>(bar, smem, 0, j0, last_v, true, a.status, true,
+                                                  KVIssue<D, Pol>{&none, &tm_v});
+      else
+        flash::load_ring_item<D, flash::K_STAGES>(bar, smem, 0, j0, last_k, true, a.status, false,
+                                                  KVIssue<D, Pol>{&none, &tm_k});
+    } else if (lane == 0) {
+      const bool pv = warp == 3;
       int j0 = 0, i = 0, nq = 0;
       for (int r = 0; r < rounds; ++r) {
         const int id = item_id(r);
         if (id >= total) continue;
         const Pol pol = make_item<D>(a, id, &tm_o);
         if (pv) {
-          if (!flash::pv_issuer<D>(bar, smem, pol.n_total, tmem, a.status, j0)) break;
+          if (!flash::pv_issuer<D>(bar, smem, pol.n_total, tmem, a.status, j0,
+                                   i > 0 ? (i - 1) & 1 : -1))
+            break;
         } else {
           // Q is replaced once the previous item's QK^T MMAs have completed
           if (i > 0 && !mbar_wait(&bar.q_empty, (i - 1) & 1, ab, a.status)) break;
@@ -272,19 +293,40 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
       // and for the last Q copy (in flight still if the item was abandoned)
       if (!pv && nq > 0) mbar_wait(&bar.q_full, (nq - 1) & 1, nullptr, a.status);
     }
-  } else {
-    int j0 = 0, i = 0, er = 0;
+  } else if (wg == 1) {
+    regs_raise<DUAL_SOFTMAX_REGS>();
+    int j0 = 0, i = 0;
     for (int r = 0; r < rounds; ++r) {
       const int id = item_id(r);
       if (id >= total) continue;
-      const Pol pol = make_item<D>(a, id, &tm_o);
-      if (!flash::softmax_loop<D>(bar, smem, pol, pol.n_total, tmem, a.scale_log2, a.status, j0,
-                                  i & 1, &er))
+      Pol pol = make_item<D>(a, id, &tm_o);
+      pol.inv_slot = epi.inv[i & 1];
+      pol.item = i;
+      if (!flash::softmax_loop<D>(bar, smem, pol, pol.n_total, tmem, a.scale_log2, a.status, j0))
         break;
       j0 += pol.n_total;
       ++i;
     }
-    if (threadIdx.x == 2 * 32) bulk_wait_read_all();   // last stores have read the staging
+  } else {
+    regs_lower<DUAL_EPI_REGS>();
+    const int store_thread = 8 * 32;
+    const int row = (warp & 3) * 32 + lane;
+    volatile int* abv = ab;
+    int i = 0, er = 0;
+    for (int r = 0; r < rounds; ++r) {
+      const int id = item_id(r);
+      if (id >= total) continue;
+      const Pol pol = make_item<D>(a, id, &tm_o);
+      // 1/l of this thread's row, handed over by the softmax warps
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.epi_ready, i & 1, abv, a.status))) break;
+      const float inv = epi.inv[i & 1][row];
+      mbar_arrive_warp(&bar.epi_taken);
+      if (!flash::staged_epilogue<D>(bar, smem, pol, tmem, i & 1, inv, er, store_thread,
+                                     a.status))
+        break;
+      ++i;
+    }
+    if ((int)threadIdx.x == store_thread) bulk_wait_read_all();   // stores have read staging
   }
   cta_teardown(tmem, warp);
 }
@@ -629,13 +671,13 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, f
              scale * 1.4426950408889634f, status, lse, o != nullptr};
   const long long items = (long long)a.nqt * 2 * hq * batch;
   using SP = flash::Smem<D, DualPolicy<D>::kStageBoxes>;
-  static_assert(SP::TOTAL + sizeof(flash::Barriers) <= 227 * 1024,
+  static_assert(SP::TOTAL + sizeof(flash::Barriers) + sizeof(DualEpi) <= 227 * 1024,
                 "persistent layout: Q, both rings and the staging fit shared memory");
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(dual_stream_persistent_kernel<D>, SP::TOTAL, attr);
   if (ea != cudaSuccess) return ea;
   const long long ctas = std::min<long long>(items, num_sms());
-  dual_stream_persistent_kernel<D><<<(unsigned)ctas, flash::NUM_THREADS, SP::TOTAL, stream>>>(
+  dual_stream_persistent_kernel<D><<<(unsigned)ctas, DUAL_THREADS, SP::TOTAL, stream>>>(
       tq, tk, tv, to, a);
   return cudaGetLastError();
 }

@@ -71,6 +71,9 @@ struct Barriers {
   uint64_t o_staged;      // softmax threads have written O to shared memory (staged store)
   uint64_t stage_free;    // the stores of the previous staging round have read it
   uint64_t q_empty;       // the QK^T MMAs of an item have completed (Q may be replaced)
+  uint64_t epi_ready;     // softmax threads have handed over 1/l of their rows (hand-off)
+  uint64_t epi_taken;     // epilogue threads have taken that hand-off (hand-off)
+  uint64_t o_free;        // epilogue threads have read O out of TMEM (hand-off)
   uint32_t tmem_base;
   int abort;
 };
@@ -96,6 +99,9 @@ MARS_DEV void init_barriers(Barriers& bar) {
   mbar_init(&bar.o_staged, SOFTMAX_THREADS);
   mbar_init(&bar.stage_free, 1);
   mbar_init(&bar.q_empty, 1);
+  mbar_init(&bar.epi_ready, SOFTMAX_THREADS);
+  mbar_init(&bar.epi_taken, SOFTMAX_THREADS);
+  mbar_init(&bar.o_free, SOFTMAX_THREADS);
   mbar_init(&bar.o_final, 1);
   mbar_init(&bar.drain, 1);
   mbar_init(&bar.drain_pv, 1);
@@ -257,9 +263,11 @@ MARS_DEV bool s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
 }
 
 // PV issuer: O += P_j V_j (P from the upper half of S buffer j % NBUF), then o_final.
+// With o_free_parity >= 0 the first PV (which overwrites O) waits until the epilogue
+// warps have read the previous item's O (the hand-off form).
 template <int D>
 MARS_DEV bool pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
-                        int32_t* status, int j0 = 0) {
+                        int32_t* status, int j0 = 0, int o_free_parity = -1) {
   using namespace sm100;
   using S = Smem<D>;
   const uint32_t idesc_o = idesc_bf16_f32(BQ, D, true);      // O = P V: B MN-major
@@ -269,6 +277,9 @@ MARS_DEV bool pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     const int pb = j % NBUF, st = j % V_STAGES;
     if (!mbar_wait(&bar.v_full[st], (j / V_STAGES) & 1, ab, status)) return false;
     if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return false;
+    if (jl == 0 && o_free_parity >= 0 &&
+        !mbar_wait(&bar.o_free, (uint32_t)o_free_parity, ab, status))
+      return false;
     tc_fence_after();
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
@@ -412,18 +423,16 @@ MARS_DEV void exp2_pack64(const uint32_t (&r)[BKV], int c0, float scale_log2, fl
 // every row sees every key of tile j, so no per-key test runs), cols(vis, tile) ->
 // ColRange (the columns of tile j visible to the row; a tile must admit only keys it
 // owns, so no key is counted twice), with kRowStats row_stats(row, m, l) once the row is
-// done, and either store_chunk(row, col, 32 fp32 of O, 1/l,
-// m, l) or, with kStagedStore, kStageBoxes, stage(smem) (the staging area) and
-// store_boxes(staging, first box, boxes), which issues the TMA stores of O/l.
+// done, and either store_chunk(row, col, 32 fp32 of O, 1/l, m, l) or, with kHandOff,
+// hand_off(row, 1/l) for the epilogue warps (staged_epilogue below).
 // Each tile's S row is read from TMEM once (4 loads, one wait) into registers.
 //
 // A persistent kernel calls it once per work item with j0 (global position of the item's
-// first tile), o_parity (phase of o_final for the item) and epi_round (staging rounds done
-// so far, kept across items); it then makes the final bulk-store wait itself.
+// first tile) and o_parity (phase of o_final for the item, used without hand-off).
 template <int D, class Policy>
 MARS_DEV bool softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int ntiles,
                            uint32_t tmem, float scale_log2, int32_t* status, int j0 = 0,
-                           uint32_t o_parity = 0, int* epi_round = nullptr) {
+                           uint32_t o_parity = 0) {
   using namespace sm100;
   using S = Smem<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -511,64 +520,19 @@ MARS_DEV bool softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
   }
   if (!ok) return false;
   if constexpr (Policy::kRowStats) pol.row_stats(row, m, l);
-  if (!warp_wait(&bar.o_final, o_parity)) return false;
-  tc_fence_after();
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
-  if constexpr (Policy::kStagedStore) {
-    // O / l goes to shared memory as 32-column boxes of [128 rows][32 fp32] in the 128-byte
-    // swizzled layout (a quarter-warp's 16-byte stores then hit distinct banks), and one
-    // thread writes them out with TMA stores, kStageBoxes boxes per round. Before a round
-    // overwrites the staging, that thread waits until the previous round's stores have
-    // read it and releases the others through stage_free.
-    constexpr int NBOX = D / 32;
-    constexpr int PER = Policy::kStageBoxes;
-    static_assert(NBOX % PER == 0, "rounds cover O");
-    constexpr int kStoreThread = 2 * 32;
-    uint8_t* stage = pol.stage(smem);
-    uint32_t o[D];                                   // the whole O row: one TMEM wait
-#pragma unroll
-    for (int c = 0; c < NBOX; ++c)
-      tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
-    tmem_ld_wait();
-    int local_round = 0;
-    int& er = epi_round ? *epi_round : local_round;
-#pragma unroll
-    for (int b0 = 0; b0 < NBOX; b0 += PER) {
-      if (er > 0) {
-        if (threadIdx.x == kStoreThread) {
-          bulk_wait_read_all();
-          mbar_arrive(&bar.stage_free);
-        }
-        if (!warp_wait(&bar.stage_free, (er - 1) & 1)) return false;
-      }
-#pragma unroll
-      for (int c = 0; c < PER; ++c) {
-        uint8_t* box = stage + c * (BQ * 128);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t* v = o + (b0 + c) * 32 + 4 * q;
-          *reinterpret_cast<float4*>(box + sw_off(row, q)) =
-              make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
-                          __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive_warp(&bar.o_staged);
-      bool st_ok = true;
-      if (threadIdx.x == kStoreThread) {
-        st_ok = mbar_wait(&bar.o_staged, er & 1, ab, status);
-        if (st_ok) {
-          pol.store_boxes(stage, b0, PER);
-          bulk_commit();
-        }
-      }
-      if (!__all_sync(0xffffffffu, st_ok)) return false;
-      ++er;
-    }
-    // a single-item call drains its stores here (the CTA may exit once they have read
-    // shared memory); a persistent kernel drains after its last item
-    if (!epi_round && threadIdx.x == kStoreThread) bulk_wait_read_all();
+  if constexpr (Policy::kHandOff) {
+    // the epilogue warps read O and store it; these threads go on to the next item. A
+    // short item can finish here before the epilogue has got to the previous one: hand
+    // over only once that one's hand-off has been taken, so epi_ready never runs two
+    // phases ahead of its waiter.
+    if (pol.item > 0 && !warp_wait(&bar.epi_taken, (uint32_t)(pol.item - 1) & 1)) return false;
+    pol.hand_off(row, inv);
+    mbar_arrive_warp(&bar.epi_ready);
+    return true;
   } else {
+    if (!warp_wait(&bar.o_final, o_parity)) return false;
+    tc_fence_after();
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -576,6 +540,77 @@ MARS_DEV bool softmax_loop(Barriers& bar, uint8_t* smem, const Policy& pol, int 
       tmem_ld_wait();
       if (rv) pol.store_chunk(row, c * 32, o, inv, m, l);
     }
+    return true;
+  }
+}
+
+// Epilogue warps of the hand-off form (one warp per TMEM lane quadrant, thread = row): per
+// work item, once the softmax threads have handed over 1/l (epi_ready) and the last PV has
+// completed (o_final), read O out of TMEM, release it to the next item's first PV
+// (o_free), and write O/l to shared memory as 32-column boxes of [128 rows][32 fp32] in the
+// 128-byte swizzled layout (a quarter-warp's 16-byte stores then hit distinct banks). One
+// thread (store_thread) writes them out with TMA stores, kStageBoxes boxes per round;
+// before a round overwrites the staging it waits until the previous round's stores have
+// read it and releases the others through stage_free. er counts rounds across items; the
+// caller drains the last stores (bulk_wait_read_all on store_thread) before exiting.
+template <int D, class Policy>
+MARS_DEV bool staged_epilogue(Barriers& bar, uint8_t* smem, const Policy& pol, uint32_t tmem,
+                              uint32_t parity, float inv, int& er, int store_thread,
+                              int32_t* status) {
+  using namespace sm100;
+  using S = Smem<D>;
+  const int lane = threadIdx.x & 31;
+  const int row = ((threadIdx.x >> 5) & 3) * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(row & ~31) << 16;
+  volatile int* ab = &bar.abort;
+  auto warp_wait = [&](uint64_t* b, uint32_t par) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(b, par, ab, status));
+  };
+  constexpr int NBOX = D / 32;
+  constexpr int PER = Policy::kStageBoxes;
+  static_assert(NBOX % PER == 0, "rounds cover O");
+  if (!warp_wait(&bar.o_final, parity)) return false;
+  tc_fence_after();
+  uint32_t o[D];                                     // the whole O row: one TMEM wait
+#pragma unroll
+  for (int c = 0; c < NBOX; ++c)
+    tmem_ld32(tmem + S::TMEM_O + c * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+  tmem_ld_wait();
+  tc_fence_before();
+  mbar_arrive_warp(&bar.o_free);
+  uint8_t* stage = pol.stage(smem);
+#pragma unroll
+  for (int b0 = 0; b0 < NBOX; b0 += PER) {
+    if (er > 0) {
+      if ((int)threadIdx.x == store_thread) {
+        bulk_wait_read_all();
+        mbar_arrive(&bar.stage_free);
+      }
+      if (!warp_wait(&bar.stage_free, (er - 1) & 1)) return false;
+    }
+#pragma unroll
+    for (int c = 0; c < PER; ++c) {
+      uint8_t* box = stage + c * (BQ * 128);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t* v = o + (b0 + c) * 32 + 4 * q;
+        *reinterpret_cast<float4*>(box + sw_off(row, q)) =
+            make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv,
+                        __uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive_warp(&bar.o_staged);
+    bool st_ok = true;
+    if ((int)threadIdx.x == store_thread) {
+      st_ok = mbar_wait(&bar.o_staged, er & 1, ab, status);
+      if (st_ok) {
+        pol.store_boxes(stage, b0, PER);
+        bulk_commit();
+      }
+    }
+    if (!__all_sync(0xffffffffu, st_ok)) return false;
+    ++er;
   }
   return true;
 }

@@ -154,6 +154,21 @@ MARS_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* ba
       : "memory");
 }
 
+// Per-thread register count of the calling warpgroup (all 128 threads, warp-uniform):
+// raise to or lower to N (a multiple of 8 in [24, 256]). Raises draw on the registers the
+// block was launched with (threads x registers per thread), which the lowered warpgroups
+// give back; the sum over the warpgroups must fit that pool.
+template <uint32_t N>
+MARS_DEV void regs_raise() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+MARS_DEV void regs_lower() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 MARS_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
