@@ -41,7 +41,7 @@ METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TF
 # whenever the kernel changes, until it is captured again.
 TRAFFIC_HEAD_GEMM = 1124735872         # profiles/head_gemm_sustained_decode_7b_b128_B16.md
 TRAFFIC_DECODE_STEP0 = 1365705088      # profiles/decode_tc_sustained_decode_7b_b128_B16.md
-TRAFFIC_DUAL_STREAM = 329225472        # profiles/dual_stream_persistent_dual_stream_7b_b2_2L8192_B16.md
+TRAFFIC_DUAL_STREAM = 330413824        # profiles/dual_stream_persistent_dual_stream_7b_b2_2L8192_B16.md
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
 
