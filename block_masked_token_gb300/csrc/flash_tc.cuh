@@ -1,9 +1,9 @@
 // Flash-attention tile engine on tcgen05 shared by the dual-stream and decode kernels.
 //
-// One CTA owns a 128-row query tile held in shared memory and walks a list of 128-key
-// tiles. Roles (256 threads):
+// A CTA runs a 128-row query tile held in shared memory over a list of 128-key tiles.
+// Roles, as the decode kernel lays them out (256 threads):
 //   warp 0      Q loader, then K loader: K tiles into a 3-stage ring (TMA, 128-byte
-//               swizzle); warp 6 streams V tiles into their own 3-stage ring, so the two
+//               swizzle); warp 6 streams V tiles into their own 2-stage ring, so the two
 //               rings advance independently;
 //   warp 1      TMEM owner and QK^T issuer: S_j = Q K_j^T into one of three 128-column
 //               fp32 TMEM buffers; a K stage is released as soon as its QK^T finishes;
@@ -11,12 +11,16 @@
 //               from TMEM); a V stage is released after its PV;
 //   warps 2..5  softmax: thread = query row. It reads its S_j row (tcgen05.ld) into
 //               registers, takes the row max, and writes P = exp2(S - m) as bf16 pairs
-//               over the upper half of that S buffer (tcgen05.st). The running max is raised lazily: O and
-//               l are rescaled (tcgen05.ld / st) only when the max grows by more than 2^8,
-//               which keeps P <= 256 and the result exact up to rounding.
+//               over the upper half of that S buffer (tcgen05.st). The running max is
+//               raised lazily: O and l are rescaled (tcgen05.ld / st) only when the max
+//               grows by more than 2^8, which keeps P <= 256 and the result exact up to
+//               rounding.
 // The two issuers run independently, so the softmax of tile j overlaps QK^T of later
 // tiles and the PV of earlier ones. A kernel may instead let warp 1 issue both (S_j, then
-// PV_{j-1}); the decode kernel does, its tile lists being short.
+// PV_{j-1}); the decode kernel does, its tile lists being short. The functions take warp
+// roles from their caller, and the softmax derives its TMEM lane quadrant from warp & 3,
+// so a kernel may place the roles differently: the persistent dual-stream kernel runs
+// them as warpgroups and adds epilogue warps (staged_epilogue).
 #pragma once
 
 #include "sm100.cuh"
