@@ -84,6 +84,9 @@ cudaError_t set_smem_limit_once(Kernel* fn, int bytes, std::atomic<int> (&done)[
   return e;
 }
 
+// ---- One CTA waiting on an mbarrier that nothing completes (the wait-limit self-check).
+cudaError_t launch_wait_timeout_check(int32_t* status, cudaStream_t stream);
+
 // ---- Dual-stream attention under mask M. o may be null when lse is given (the row
 // statistics alone: lse[b][h][stream][t], t < Lp = L rounded up to 128, = log2 of the
 // softmax denominator in units of scale*log2(e)*score; pad rows are written as 0).

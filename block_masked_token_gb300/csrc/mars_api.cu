@@ -6,8 +6,29 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace mars {
+
+namespace {
+
+// Thread 0 waits on a fresh mbarrier whose phase nothing completes.
+__global__ void wait_timeout_check_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(&bar, 1);
+    sm100::fence_barrier_init();
+    sm100::mbar_wait(&bar, 0, nullptr, status);   // gives up after the wait limit
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_check(int32_t* status, cudaStream_t stream) {
+  wait_timeout_check_kernel<<<1, 32, 0, stream>>>(status);
+  count_launches(1);
+  return cudaGetLastError();
+}
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 }  // namespace mars
@@ -287,6 +308,11 @@ const char* mars_strerror(int code) {
     case MARS_ENOSPACE: return "workspace too small";
     default: return "unknown error";
   }
+}
+
+int mars_check_wait_timeout(int32_t* status, void* stream) {
+  if (!status) return MARS_EINVAL;
+  return cuda_rc(mars::launch_wait_timeout_check(status, static_cast<cudaStream_t>(stream)));
 }
 
 uint64_t mars_launch_count(void) { return mars::g_launches.load(std::memory_order_relaxed); }

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
                                                      P, P, S, P, P]
         L.mars_dual_stream_ce_loss_grad.restype = I
         L.mars_dual_stream_ce_loss_grad.argtypes = [P, P, P, P, I, I, I, I, P, P, P, S, P, P]
+        L.mars_check_wait_timeout.restype = I
+        L.mars_check_wait_timeout.argtypes = [P, P]
         L.mars_strerror.restype = ctypes.c_char_p
         L.mars_strerror.argtypes = [I]
         L.mars_version.restype = ctypes.c_char_p
@@ -77,8 +79,15 @@ EXPORTED = ("mars_workspace_bytes", "mars_attn_dual_stream", "mars_decode_attn",
             "mars_head_accept", "mars_head_accept_per_request", "mars_kv_commit",
             "mars_kv_commit_batch_sync", "mars_dual_stream_ce_loss",
             "mars_dual_stream_ce_loss_grad", "mars_attn_dual_stream_grad",
-            "mars_attn_dual_stream_lse", "mars_attn_dual_stream_grad_lse", "mars_strerror",
+            "mars_attn_dual_stream_lse", "mars_attn_dual_stream_grad_lse",
+            "mars_check_wait_timeout", "mars_strerror",
             "mars_version", "mars_launch_count")
+
+
+def mars_check_wait_timeout(status, stream=None):
+    """Enqueue the wait-limit self-check: sets ST_TIMEOUT in status after about 2 s."""
+    _check(status, "status", torch.int32, (1,))
+    _rc(lib().mars_check_wait_timeout(_ptr(status), _stream(stream)), "mars_check_wait_timeout")
 
 
 def mars_strerror(code: int) -> str:

@@ -275,6 +275,13 @@ int mars_dual_stream_ce_loss_grad(const mars_bf16* h, const mars_bf16* w,
                                   void* workspace, size_t ws_bytes, int32_t* status,
                                   void* stream);
 
+/* Self-check of the in-kernel wait limit every pipeline relies on: enqueues one small
+ * kernel that waits on an mbarrier nothing completes. The wait gives up after its time
+ * limit (about 2 s) and ORs MARS_ST_TIMEOUT into *status (device int32, zeroed by the
+ * caller, required); the kernel then exits normally and the context stays usable.
+ * Asynchronous like the other calls. */
+int mars_check_wait_timeout(int32_t* status, void* stream);
+
 /* Human-readable name of a return code. Never NULL. */
 const char* mars_strerror(int code);
 

@@ -107,6 +107,8 @@ def test_host_validation_codes(L):
     assert L.mars_attn_dual_stream_grad(*ga, 96, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_attn_dual_stream_grad(*ga, 64, 0.0, None, P, P, P, 1 << 30, None, None) == mars.EINVAL
     assert L.mars_attn_dual_stream_grad(*ga, 64, 0.0, P, P, P, P, 16, None, None) == mars.ENOSPACE
+    # wait-limit self-check: the status word is required
+    assert L.mars_check_wait_timeout(None, None) == mars.EINVAL
     # forward with row statistics: null lse, misaligned lse, unsupported head dim
     assert L.mars_attn_dual_stream_lse(P, P, P, P, None, 1, 8, 2, 4, 2, 64, 0.0, None, None) == mars.EINVAL
     assert L.mars_attn_dual_stream_lse(P, P, P, P, _p(20), 1, 8, 2, 4, 2, 64, 0.0, None, None) == mars.EALIGN

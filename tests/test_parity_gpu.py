@@ -741,3 +741,24 @@ def test_tiny_decode_step_end_to_end():
         np.testing.assert_array_equal(slots.cpu().numpy(), rs)
         np.testing.assert_array_equal(sl.cpu().numpy(), rl)
     np.testing.assert_array_equal(f64(kp.cpu()), rk)
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_wait_limit_reports_timeout_and_context_stays_usable():
+    """A kernel waiting on an mbarrier that nothing completes gives up after the wait limit,
+    reports ST_TIMEOUT in the status word and exits; the next call runs normally."""
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mars.mars_check_wait_timeout(status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == mars.ST_TIMEOUT
+    cfg = W.DualStreamConfig("after", 1, 130, 16, 2, 1, 64)
+    x = W.make_dual_stream_inputs(cfg, seed=2)
+    st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = torch.empty(x["q"].shape, dtype=torch.float32, device=DEV)
+    mars.mars_attn_dual_stream(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), o, L=cfg.L,
+                               B=cfg.B, status=st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    ref = oracle.attn_dual_stream(f64(x["q"]), f64(x["k"]), f64(x["v"]), cfg.L, cfg.B)
+    assert_attn_close(o.cpu().numpy(), ref)
