@@ -221,8 +221,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (!is_v && lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
     if (st_flags && a.status) atomicOr(a.status, st_flags);
   } else if (warp == 1 || warp == flash::PV_ISSUER_WARP) {
-    if (lane == 0)
-      flash::issuer<D, false>(bar, smem, n_total, tmem, a.status, warp == flash::PV_ISSUER_WARP);
+    // one thread issues both QK^T and PV (short tile lists); the PV warp idles
+    if (warp == 1 && lane == 0) flash::single_issuer<D>(bar, smem, n_total, tmem, a.status);
   } else {
     flash::softmax_loop<D>(bar, smem, pol, n_total, tmem, a.scale_log2, a.status);
   }

@@ -15,9 +15,10 @@
 //               raised lazily: O and l are rescaled (tcgen05.ld / st) only when the max
 //               grows by more than 2^8, which keeps P <= 256 and the result exact up to
 //               rounding.
-// The two issuers run independently, so the softmax of tile j overlaps QK^T of later
-// tiles and the PV of earlier ones. A kernel may instead let warp 1 issue both (S_j, then
-// PV_{j-1}); the decode kernel does, its tile lists being short. The functions take warp
+// The two issuers (s_issuer, pv_issuer) run independently, so the softmax of tile j
+// overlaps QK^T of later tiles and the PV of earlier ones. A kernel may instead let one
+// thread issue both (mma_loop: S_j, then PV_{j-1}); the decode kernel does, its tile lists
+// being short. The functions take warp
 // roles from their caller, and the softmax derives its TMEM lane quadrant from warp & 3,
 // so a kernel may place the roles differently: the persistent dual-stream kernel runs
 // them as warpgroups and adds epilogue warps (staged_epilogue).
@@ -354,29 +355,15 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   mma_commit(&bar.o_final);
 }
 
-// Run by lane 0 of warps 1 and PV_ISSUER_WARP: the issuer's loop, then a wait (bounded)
-// for its own MMAs so none is in flight when the CTA tears down. With kSplit the two warps
-// issue QK^T and PV separately; otherwise warp 1 runs mma_loop and the PV warp idles.
-template <int D, bool kSplit>
-MARS_DEV void issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem, int32_t* status,
-                     bool pv) {
+// Single-issuer form (run by lane 0 of warp 1): mma_loop, then a wait (bounded) for its
+// own MMAs so none is in flight when the CTA tears down.
+template <int D>
+MARS_DEV void single_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
+                            int32_t* status) {
   using namespace sm100;
-  if (!kSplit) {
-    if (pv) return;
-    mma_loop<D>(bar, smem, ntiles, tmem, status);
-    mma_commit(&bar.drain);
-    mbar_wait(&bar.drain, 0, nullptr, status);
-    return;
-  }
-  if (pv) {
-    pv_issuer<D>(bar, smem, ntiles, tmem, status);
-    mma_commit(&bar.drain_pv);
-    mbar_wait(&bar.drain_pv, 0, nullptr, status);
-  } else {
-    s_issuer<D>(bar, smem, ntiles, tmem, status);
-    mma_commit(&bar.drain);
-    mbar_wait(&bar.drain, 0, nullptr, status);
-  }
+  mma_loop<D>(bar, smem, ntiles, tmem, status);
+  mma_commit(&bar.drain);
+  mbar_wait(&bar.drain, 0, nullptr, status);
 }
 
 MARS_DEV float ex2_approx(float x) {
