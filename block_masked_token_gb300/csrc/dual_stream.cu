@@ -337,16 +337,20 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
 // exp2(scale log2(e) S - lse), S = Q K_j^T, dP = dO V_j^T: the row-parallel half of the
 // attention gradient. Work items, their key tiles and the masks are the forward's; per key
 // tile three MMAs (S, dP, dQ += dS K) with dQ accumulated in TMEM and written once per row.
-// TMEM: S in two buffers (columns 0 and 128), dP at 256, dQ at 384. Warps: 0 K loader,
-// 1 TMEM owner and MMA issuer (it also loads each item's Q and dO), 2..9 math (two per
-// TMEM lane quadrant, 64 key columns each), 10 V loader.
+// TMEM: S at column 0, dP at 128, dQ at 256, dS (bf16 pairs, 64 columns) at 384. S and dP
+// are free once the math warps have loaded them, so the next tile's S and dP never wait
+// for a dQ MMA and the tensor pipe does not drain between tiles. Warps: 0 K loader,
+// 1 TMEM owner and S/dP issuer (it also loads each item's Q and dO), 2..9 math (two per
+// TMEM lane quadrant, 64 key columns each), 10 V loader, 11 dQ issuer. The shared-memory
+// operand MMAs (S, dP) and the TMEM-operand ones (dQ) come from two threads on different
+// sub-partitions: one thread alternating the two forms issues them about a quarter slower.
 constexpr int DQ_MATH_WARPS = 8;
-constexpr int DQ_THREADS = 32 * (3 + DQ_MATH_WARPS);
+constexpr int DQ_THREADS = 32 * (4 + DQ_MATH_WARPS);
 constexpr int DQ_V_WARP = 2 + DQ_MATH_WARPS;
+constexpr int DQ_ISSUE_WARP = 3 + DQ_MATH_WARPS;
 
 struct DQBar {
-  uint64_t s_full[2], dq_done[2];
-  uint64_t dp_full, dp_free, ds_full, acc_free;
+  uint64_t s_full, dp_full, sp_free, ds_full, dq_done, acc_free;
 };
 
 struct DQArgs {
@@ -357,10 +361,6 @@ struct DQArgs {
   float* dq;               // [batch][2L][hq][D]
 };
 
-// K-step k (16 keys) of dS in its S buffer: keys [0, 64) over columns [0, 32), keys
-// [64, 128) over [64, 96) (each math warp packs its bf16 values over fp32 columns it has
-// itself already read).
-MARS_DEV uint32_t ds_col(int k) { return (uint32_t)(8 * k + (k >= 4 ? 32 : 0)); }
 
 template <int D>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
@@ -372,7 +372,8 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   using Pol = DualPolicy<D>;
   using S = flash::Smem<D, Pol::kStageBoxes>;     // Q, K ring, V ring; dO over the staging
   static_assert(D * BQ * 2 <= Pol::kStageBoxes * BQ * 128, "dO tile fits the staging area");
-  constexpr int TM_DP = 256, TM_DQ = 384;
+  constexpr int TM_S = 0, TM_DP = BKV, TM_DQ = 2 * BKV, TM_DS = 3 * BKV;
+  static_assert(TM_DQ + D <= TM_DS && TM_DS + BKV / 2 <= 512, "TMEM columns");
   const DualArgs& a = da.f;
   extern __shared__ uint8_t smem_raw[];
   __shared__ flash::Barriers bar;
@@ -381,12 +382,10 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&qb.s_full[i], 1);
-      mbar_init(&qb.dq_done[i], 1);
-    }
+    mbar_init(&qb.s_full, 1);
     mbar_init(&qb.dp_full, 1);
-    mbar_init(&qb.dp_free, 32 * DQ_MATH_WARPS);
+    mbar_init(&qb.dq_done, 1);
+    mbar_init(&qb.sp_free, 32 * DQ_MATH_WARPS);
     mbar_init(&qb.ds_full, 32 * DQ_MATH_WARPS);
     mbar_init(&qb.acc_free, 32 * DQ_MATH_WARPS);
   }
@@ -426,29 +425,28 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BQ, BKV, false);   // S, dP: K-major A and B
-      const uint32_t id_q = idesc_bf16_f32(BQ, D, true);      // dQ: TMEM A, MN-major B
       const uint32_t qa = smem_u32(smem + S::OFF_Q), da_ = smem_u32(smem + S::OFF_STAGE);
       int jg0 = 0, i = 0, nq = 0;
       bool ok = true;
-      auto issue_s = [&](int jg) -> bool {                // S_jg = Q K^T into buffer jg % 2
-        const int st = jg % flash::K_STAGES, sb = jg & 1;
+      auto issue_s = [&](int jg) -> bool {                // S_jg = Q K^T
+        const int st = jg % flash::K_STAGES;
         if (!mbar_wait(&bar.k_full[st], (jg / flash::K_STAGES) & 1, ab, a.status)) return false;
-        if (jg >= 2 && !mbar_wait(&qb.dq_done[sb], ((jg >> 1) - 1) & 1, ab, a.status)) return false;
+        // S and dP of the previous tile have been loaded by the math warps
+        if (jg >= 1 && !mbar_wait(&qb.sp_free, (jg - 1) & 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + sb * BKV, sdesc_sw128(qa + off, 16, 1024),
+          mma_bf16_ss(tmem + TM_S, sdesc_sw128(qa + off, 16, 1024),
                       sdesc_sw128(kb + off, 16, 1024), id_s, k != 0);
         }
-        mma_commit(&qb.s_full[sb]);
+        mma_commit(&qb.s_full);
         return true;
       };
-      auto issue_dp = [&](int jg) -> bool {               // dP_jg = dO V^T
+      auto issue_dp = [&](int jg) -> bool {               // dP_jg = dO V^T (after issue_s(jg))
         const int st = jg % flash::V_STAGES;
         if (!mbar_wait(&bar.v_full[st], (jg / flash::V_STAGES) & 1, ab, a.status)) return false;
-        if (jg >= 1 && !mbar_wait(&qb.dp_free, (jg - 1) & 1, ab, a.status)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
 #pragma unroll
@@ -476,33 +474,50 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         ++nq;
         if (!(ok = mbar_wait(&bar.q_full, i & 1, ab, a.status))) break;
         const int n = pol.n_total;
-        if (!(ok = issue_s(jg0) && issue_dp(jg0))) break;
-        for (int jl = 0; jl < n && ok; ++jl) {
-          const int jg = jg0 + jl, sb = jg & 1;
-          // the next tile's S and dP go ahead of this tile's dQ
-          if (jl + 1 < n && !(ok = issue_s(jg + 1) && issue_dp(jg + 1))) break;
-          if (jl == 0 && i > 0 && !(ok = mbar_wait(&qb.acc_free, (i - 1) & 1, ab, a.status)))
-            break;
-          if (!(ok = mbar_wait(&qb.ds_full, jg & 1, ab, a.status))) break;
-          tc_fence_after();
-          const int st = jg % flash::K_STAGES;
-          const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
-#pragma unroll
-          for (int k = 0; k < BKV / 16; ++k)             // dQ += dS K (K tile MN-major)
-            mma_bf16_ts(tmem + TM_DQ, tmem + sb * BKV + ds_col(k),
-                        sdesc_sw128(kb + k * 2048, BKV * 128, 1024), id_q, (jl | k) != 0);
-          mma_commit(&qb.dq_done[sb]);
-          mma_commit(&bar.k_empty[st]);
-        }
+        for (int jl = 0; jl < n && ok; ++jl) ok = issue_s(jg0 + jl) && issue_dp(jg0 + jl);
         if (!ok) break;
         mma_commit(&bar.q_empty);
-        mma_commit(&bar.o_final);
         jg0 += n;
         ++i;
       }
       mma_commit(&bar.drain);
       mbar_wait(&bar.drain, 0, nullptr, a.status);
       if (nq > 0) mbar_wait(&bar.q_full, (nq - 1) & 1, nullptr, a.status);
+    }
+  } else if (warp == DQ_ISSUE_WARP) {
+    if (lane == 0) {
+      const uint32_t id_q = idesc_bf16_f32(BQ, D, true);      // dQ: TMEM A, MN-major B
+      int jg0 = 0, i = 0;
+      bool ok = true;
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int id = item_id(r);
+        if (id >= total) continue;
+        const int n = make_item<D>(a, id, nullptr).n_total;
+        for (int jl = 0; jl < n; ++jl) {
+          const int jg = jg0 + jl, st = jg % flash::K_STAGES;
+          // the accumulator of the previous item has been read out
+          if (jl == 0 && i > 0 && !(ok = mbar_wait(&qb.acc_free, (i - 1) & 1, ab, a.status)))
+            break;
+          // K_jg has landed (its stage is released below, so this phase is still current)
+          if (!(ok = mbar_wait(&bar.k_full[st], (jg / flash::K_STAGES) & 1, ab, a.status))) break;
+          if (!(ok = mbar_wait(&qb.ds_full, jg & 1, ab, a.status))) break;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+#pragma unroll
+          for (int k = 0; k < BKV / 16; ++k)             // dQ += dS K (K tile MN-major)
+            mma_bf16_ts(tmem + TM_DQ, tmem + TM_DS + 8 * k,
+                        sdesc_sw128(kb + k * 2048, BKV * 128, 1024), id_q, (jl | k) != 0);
+          mma_commit(&qb.dq_done);
+          // S_jg, which also read this stage, completed before the math warps wrote dS_jg
+          mma_commit(&bar.k_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&bar.o_final);
+        jg0 += n;
+        ++i;
+      }
+      mma_commit(&bar.drain_pv);
+      mbar_wait(&bar.drain_pv, 0, nullptr, a.status);
     }
   } else {
     // math: thread = query row (TMEM lane), 64 key columns per warp
@@ -527,23 +542,23 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float dd = rv ? da.drow[srow] : 0.f;
       const int n = pol.n_total;
       for (int jl = 0; jl < n && ok; ++jl) {
-        const int jg = jg0 + jl, sb = jg & 1;
+        const int jg = jg0 + jl;
         const typename Pol::Tile tile = pol.tile(jl);
         const flash::ColRange cr = rv ? pol.cols(vis, tile) : flash::ColRange{0, 0, -1, 0u};
-        if (!(ok = warp_wait(&qb.s_full[sb], (jg >> 1) & 1))) break;
+        if (!(ok = warp_wait(&qb.s_full, jg & 1))) break;
         if (!(ok = warp_wait(&qb.dp_full, jg & 1))) break;
         tc_fence_after();
         uint32_t sv[64], pv[64];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          tmem_ld32(tmem + sb * BKV + 64 * half + 32 * q + lane_off,
+          tmem_ld32(tmem + TM_S + 64 * half + 32 * q + lane_off,
                     *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q));
           tmem_ld32(tmem + TM_DP + 64 * half + 32 * q + lane_off,
                     *reinterpret_cast<uint32_t(*)[32]>(pv + 32 * q));
         }
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive_warp(&qb.dp_free);
+        mbar_arrive_warp(&qb.sp_free);
         // masked keys become -inf (exp2 gives 0) where the tile is not fully visible
         if (!rv || !tile.full) {
 #pragma unroll
@@ -569,7 +584,10 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                  __uint_as_float(pv[e + 1])), nd2));
           ds[e / 2] = flash::pack_bf16x2(x.x, x.y);
         }
-        tmem_st32(tmem + sb * BKV + 64 * half + lane_off, ds);
+        // dS has one buffer: the previous tile's dQ MMA must have read it
+        if (jg > 0 && !(ok = warp_wait(&qb.dq_done, (jg - 1) & 1))) break;
+        tc_fence_after();
+        tmem_st32(tmem + TM_DS + 32 * half + lane_off, ds);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive_warp(&qb.ds_full);
