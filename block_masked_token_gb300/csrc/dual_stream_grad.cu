@@ -13,8 +13,11 @@
 //       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM, bf16 over the
 //                                              fp32 columns they were formed from)
 //     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by two threads per key row
-//     (64 query columns each: with lse known, no row-wide exchange is needed). S^T of the
-//     next pair is issued as soon as dV has read P^T, so it runs under this pair's dS.
+//     (64 query columns each: with lse known, no row-wide exchange is needed). One thread
+//     issues S^T and dP^T (shared-memory operands), another dV and dK (A from TMEM), on
+//     different sub-partitions: one thread alternating the two forms issues them about a
+//     quarter slower. S^T of the next pair is issued as soon as dV has read P^T, so it
+//     runs under this pair's dK.
 //     dK and dV stay in TMEM over the item's pairs and are then added to dK and dV (fp32
 //     vector atomics; the G query heads of a kv group add into the same rows).
 //   - the dQ kernel (with the forward, whose work items and masks it shares): per query
@@ -38,7 +41,10 @@ using namespace sm100;
 
 constexpr int GT = 128;                // keys per key tile, query rows per query tile
 constexpr int MATH_WARPS = 8;          // two per TMEM lane quadrant, 64 query columns each
-constexpr int GRAD_THREADS = 64 + 32 * MATH_WARPS;   // warp 0 loads, warp 1 TMEM + MMAs
+// warp 0 loads, warp 1 owns TMEM and issues S^T and dP^T, warps 2..9 math, warp 10 issues
+// dV and dK
+constexpr int GRAD_THREADS = 96 + 32 * MATH_WARPS;
+constexpr int GRAD_TS_WARP = 2 + MATH_WARPS;
 constexpr int MATH_THREADS = 32 * MATH_WARPS;
 constexpr int NSTAGE = 2;              // Q / dO ring depth
 
@@ -87,7 +93,7 @@ struct GBar {
   uint64_t kv_full, kv_empty;
   uint64_t full[NSTAGE], empty[NSTAGE];
   uint64_t s_full, dp_full, p_full, ds_full, dv_done, dk_done;
-  uint64_t acc_full, acc_free, drain;
+  uint64_t acc_full, acc_free, drain, drain_ts;
   uint32_t tmem_base;
   int abort;
 };
@@ -241,6 +247,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&bar.acc_full, 1);
     mbar_init(&bar.acc_free, MATH_THREADS);
     mbar_init(&bar.drain, 1);
+    mbar_init(&bar.drain_ts, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -312,10 +319,9 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMAs
+    // ------------------------------------------------------- S^T and dP^T MMAs
     if (lane == 0) {
       const uint32_t id_qk = idesc_ab(GT, GT, false, false);   // S^T, dP^T: K-major A, B
-      const uint32_t id_acc = idesc_ab(GT, D, false, true);    // dV, dK: TMEM A, MN-major B
       const uint32_t kb = smem_u32(smem + S::OFF_K), vb = smem_u32(smem + S::OFF_V);
       auto stage_of = [&](int g2) { return smem_u32(smem + S::OFF_RING + (g2 % NSTAGE) * S::STAGE); };
       auto issue_st = [&](int g2) -> bool {            // S^T = K Q^T of pair g2
@@ -352,12 +358,31 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int r = 0; r < rounds && ok; ++r) {
         const int id = item_id(r);
         if (id >= total) continue;
-        const GItem it = grad_item(a, id);
+        const int np = grad_item(a, id).npg;
         if (!(ok = mbar_wait(&bar.kv_full, ii & 1, ab, a.status))) break;
-        const int np = it.npg;
-        if (!(ok = issue_st(gp) && issue_dp(gp))) break;
-        for (int p = 0; p < np && ok; ++p, ++gp) {
-          const uint32_t sb = stage_of(gp);
+        for (int p = 0; p < np && ok; ++p, ++gp) ok = issue_st(gp) && issue_dp(gp);
+        if (!ok) break;
+        mma_commit(&bar.kv_empty);                       // K and V are read by these MMAs only
+        ++ii;
+      }
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0, nullptr, a.status);
+    }
+  } else if (warp == GRAD_TS_WARP) {
+    // -------------------------------------------------------- dV and dK MMAs
+    if (lane == 0) {
+      const uint32_t id_acc = idesc_ab(GT, D, false, true);    // dV, dK: TMEM A, MN-major B
+      int gp = 0, ii = 0;
+      bool ok = true;
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int id = item_id(r);
+        if (id >= total) continue;
+        const int np = grad_item(a, id).npg;
+        for (int p = 0; p < np; ++p, ++gp) {
+          const int st = gp % NSTAGE;
+          const uint32_t sb = smem_u32(smem + S::OFF_RING + st * S::STAGE);
+          // the stage's Q and dO have landed (it is released below, so this phase is current)
+          if (!(ok = mbar_wait(&bar.full[st], (gp / NSTAGE) & 1, ab, a.status))) break;
           if (!(ok = mbar_wait(&bar.p_full, gp & 1, ab, a.status))) break;
           // dV of the item starts from zero: the previous item's dV and dK must be read
           if (p == 0 && ii > 0 && !(ok = mbar_wait(&bar.acc_free, (ii - 1) & 1, ab, a.status)))
@@ -369,13 +394,6 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
                         sdesc_sw128(sb + S::ST_DO + k * 2048, GT * 128, 1024), id_acc,
                         (p | k) != 0);
           mma_commit(&bar.dv_done);
-          // the next pair's S^T runs under this pair's dS when its Q has already landed;
-          // dK (which frees this pair's stage) never waits for the next pair's loads
-          bool next_s = false;
-          if (p + 1 < np && mbar_try_wait(&bar.full[(gp + 1) % NSTAGE], ((gp + 1) / NSTAGE) & 1)) {
-            if (!(ok = issue_st(gp + 1))) break;
-            next_s = true;
-          }
           if (!(ok = mbar_wait(&bar.ds_full, gp & 1, ab, a.status))) break;
           tc_fence_after();
 #pragma unroll
@@ -384,17 +402,16 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
                         sdesc_sw128(sb + S::ST_Q + k * 2048, GT * 128, 1024), id_acc,
                         (p | k) != 0);
           mma_commit(&bar.dk_done);
-          mma_commit(&bar.empty[gp % NSTAGE]);
-          if (p + 1 < np && !next_s && !(ok = issue_st(gp + 1))) break;
-          if (p + 1 < np && !(ok = issue_dp(gp + 1))) break;
+          // S^T and dP^T of this pair completed before the math warps formed dS^T, and the
+          // math warps have read the stage's lse and D rows: the stage is free after dK
+          mma_commit(&bar.empty[st]);
         }
         if (!ok) break;
-        mma_commit(&bar.kv_empty);
         mma_commit(&bar.acc_full);
         ++ii;
       }
-      mma_commit(&bar.drain);
-      mbar_wait(&bar.drain, 0, nullptr, a.status);
+      mma_commit(&bar.drain_ts);
+      mbar_wait(&bar.drain_ts, 0, nullptr, a.status);
     }
   } else {
     // ------------------------------------------------- math (warps 2..9, two per quadrant)
