@@ -394,8 +394,11 @@ def run_gpu(args, rank, world, local):
     # ---- the same step as one CUDA graph (launch overhead removed), rank-local
     graph = run_graph_step(runner, K, Wm)
 
-    # ---- dual-stream training-form attention, same run
-    dual = run_dual(device, peaks, reps=max(3, min(K, 10)), warm=max(3, Wm))
+    # ---- dual-stream training-form attention, same run (with the clocks it ran at: it
+    # follows the head-bound decode loops, and its denominator is the burst rate)
+    with ClockSampler(local) as clk_dual:
+        dual = run_dual(device, peaks, reps=max(3, min(K, 10)), warm=max(3, Wm))
+    dual["clocks"] = clk_dual.summary()
 
     # ---- comparison steps on the same sequences: KV-cached AR (B = 1), and the MARS step
     # at tau = 0 (every block position accepted: the step's ceiling of B tokens)
@@ -404,7 +407,9 @@ def run_gpu(args, rank, world, local):
                             device, K, Wm, seed=rank)
 
     # ---- the training-form loss over the dual stream (forward), same run
-    ce = run_ce(device, peaks, reps=max(3, min(K, 5)), warm=max(3, Wm))
+    with ClockSampler(local) as clk_ce:
+        ce = run_ce(device, peaks, reps=max(3, min(K, 5)), warm=max(3, Wm))
+    ce["clocks"] = clk_ce.summary()
 
     out = None
     if rank == 0:
@@ -729,8 +734,9 @@ def run_case(args):
     elif isinstance(cfg, W.DualStreamConfig):
         x = W.make_dual_stream_inputs(cfg, seed=0, device=device)
         o = torch.empty(x["q"].shape, dtype=torch.float32, device=device)
-        if args.case == "dual_grad":
-            mars.mars_attn_dual_stream(x["q"], x["k"], x["v"], o, L=cfg.L, B=cfg.B)
+        if args.case in ("dual_grad", "dual_grad_lse"):
+            lse = torch.empty(mars.dual_lse_shape(cfg.batch, cfg.hq, cfg.L), device=device)
+            mars.mars_attn_dual_stream_lse(x["q"], x["k"], x["v"], o, lse, L=cfg.L, B=cfg.B)
             d_o = torch.randn(o.shape, device=device)
             b_, _, hq_, d_ = x["q"].shape
             ws = torch.empty(mars.mars_workspace_bytes(mars.OP_DUAL_GRAD, b_, cfg.B, hq_,
@@ -740,9 +746,14 @@ def run_case(args):
             dk = torch.empty(x["k"].shape, dtype=torch.float32, device=device)
             dv = torch.empty(x["v"].shape, dtype=torch.float32, device=device)
 
-            def call():
-                mars.mars_attn_dual_stream_grad(x["q"], x["k"], x["v"], o, d_o, cfg.L, cfg.B,
-                                                dq, dk, dv, ws)
+            if args.case == "dual_grad":
+                def call():
+                    mars.mars_attn_dual_stream_grad(x["q"], x["k"], x["v"], o, d_o, cfg.L,
+                                                    cfg.B, dq, dk, dv, ws)
+            else:                            # from the forward's row statistics
+                def call():
+                    mars.mars_attn_dual_stream_grad_lse(x["q"], x["k"], x["v"], o, d_o, lse,
+                                                        cfg.L, cfg.B, dq, dk, dv, ws)
             work = {"flop": 2.5 * dual_flops(cfg)}
         else:
             def call():
@@ -787,7 +798,7 @@ def run_case(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["head", "decode", "dual", "dual_grad", "ce"], default=None,
+    ap.add_argument("--case", choices=["head", "decode", "dual", "dual_grad", "dual_grad_lse", "ce"], default=None,
                     help="time one entry point on --config instead of the decode step")
     ap.add_argument("--config", default=None, choices=sorted(W.CONFIGS))
     ap.add_argument("--gpus", type=int, default=1)
