@@ -361,7 +361,6 @@ struct DQArgs {
   float* dq;               // [batch][2L][hq][D]
 };
 
-
 template <int D>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
 dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
