@@ -241,6 +241,42 @@ def test_dual_stream_grad_many_items_per_cta():
         assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
 
 
+def test_dual_stream_grad_many_items_per_cta_d128():
+    """d = 128 with about three work items per persistent CTA in both gradient kernels
+    (504 key-tile items, 504 query-tile items), so the two MMA issuer threads of each
+    kernel hand the TMEM accumulators over from item to item; ragged L, blocks of 24 that
+    straddle 128-row tiles."""
+    cfg = W.DualStreamConfig("gm128", 2, 1100, 24, 14, 2, 128)
+    x = W.make_dual_stream_inputs(cfg, seed=6)
+    xd = {kk: vv.to(DEV) for kk, vv in x.items()}
+    d_o, dq, dk, dv = run_dual_grad(xd, cfg.L, cfg.B)
+    rq, rk, rv = oracle.attn_dual_stream_grad(f64(x["q"]), f64(x["k"]), f64(x["v"]),
+                                              d_o.cpu().double().numpy(), cfg.L, cfg.B)
+    for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+        err = _rel(got.cpu().numpy(), ref)
+        assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
+
+
+def test_dual_stream_grad_7b_full_size_one_kv_group():
+    """The timed gradient workload itself (batch 2, 2L = 8192, 28/4 heads, d 128, B 16:
+    3584 items in each kernel, run as the bench launches them), checked on one whole kv
+    group: dQ of its 7 query heads and dK, dV of its kv head, every row."""
+    cfg = W.DUAL_STREAM_7B
+    x = W.make_dual_stream_inputs(cfg, seed=0, device=DEV)
+    d_o, dq, dk, dv = run_dual_grad(x, cfg.L, cfg.B)
+    G = cfg.hq // cfg.hkv
+    bb, kvh = 1, 2
+    hs, ks = slice(kvh * G, (kvh + 1) * G), slice(kvh, kvh + 1)
+    rq, rk, rv = oracle.attn_dual_stream_grad(
+        f64(x["q"][bb:bb + 1, :, hs]), f64(x["k"][bb:bb + 1, :, ks]),
+        f64(x["v"][bb:bb + 1, :, ks]), d_o[bb:bb + 1, :, hs].cpu().double().numpy(),
+        cfg.L, cfg.B)
+    for got, ref, name in ((dq[bb:bb + 1, :, hs], rq, "dq"), (dk[bb:bb + 1, :, ks], rk, "dk"),
+                           (dv[bb:bb + 1, :, ks], rv, "dv")):
+        err = _rel(got.cpu().numpy(), ref)
+        assert err < ATTN_GRAD_TOL, f"{name} relative error {err:.2e}"
+
+
 def test_dual_stream_grad_7b_heads_2l2048():
     """7B head shapes (one kv group of 7 query heads, d 128), 2L = 2048, B = 16."""
     cfg = W.DualStreamConfig("g7", 1, 1024, 16, 7, 1, 128)
