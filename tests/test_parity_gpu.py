@@ -204,6 +204,27 @@ def test_dual_stream_lse_matches_oracle():
     assert (got[:, :, :, cfg.L:] == 0).all()
 
 
+def test_dual_stream_lse_7b_one_head():
+    """The row statistics of the full 2L = 8192 workload (3584 items, several per CTA), for
+    every row of one head, against the oracle; O as the plain forward's."""
+    cfg = W.DUAL_STREAM_7B
+    x = W.make_dual_stream_inputs(cfg, seed=0, device=DEV)
+    q, k, v = x["q"], x["k"], x["v"]
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    lse = torch.empty(mars.dual_lse_shape(cfg.batch, cfg.hq, cfg.L), device=DEV)
+    mars.mars_attn_dual_stream_lse(q, k, v, o, lse, cfg.L, cfg.B)
+    torch.cuda.synchronize()
+    assert torch.equal(o, run_dual(q, k, v, cfg.L, cfg.B))
+    bb, h = 1, 13
+    kvh = h // (cfg.hq // cfg.hkv)
+    ref = oracle.attn_dual_stream_lse(f64(q[bb:bb + 1, :, h:h + 1]),
+                                      f64(k[bb:bb + 1, :, kvh:kvh + 1]), cfg.L, cfg.B)
+    got = lse[bb, h].cpu().double().numpy()                 # [2, Lp]
+    for s_ in range(2):
+        err = np.abs(got[s_, :cfg.L] - ref[0, 0, s_ * cfg.L:(s_ + 1) * cfg.L]).max()
+        assert err < 1e-3, f"stream {s_}: lse max-abs error {err:.2e}"
+
+
 def test_dual_stream_grad_from_lse_matches_plain_grad():
     """The gradient from the forward's statistics equals the plain gradient (which
     recomputes them with the same kernel): dQ bit for bit, dK/dV up to the order of their
