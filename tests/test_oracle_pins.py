@@ -637,3 +637,63 @@ def test_planted_swapped_page_slot_is_caught(monkeypatch):
     monkeypatch.setattr(mars_oracle, "gather_prefix", wrong)
     with pytest.raises(AssertionError):
         test_decode_equals_masked_stream_row(4, 8, 4)
+
+
+def _grad_with(mistake):
+    """The oracle's dual-stream gradient with one planted mistake (the arithmetic of
+    attn_dual_stream_grad otherwise)."""
+    def grad(q, k, v, do, L, B, scale=None):
+        b, n, Hq, D = q.shape
+        g = Hq // k.shape[2]
+        scale = 1.0 / math.sqrt(D) if scale is None else scale
+        vis = mars_oracle.mask_M(L, B)
+        dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+        for bi in range(b):
+            for h in range(Hq):
+                hk = h // g
+                Q, K, V, dO = q[bi, :, h], k[bi, :, hk], v[bi, :, hk], do[bi, :, h]
+                P = mars_oracle._masked_softmax_rows(scale * (Q @ K.T), vis)
+                dP = dO @ V.T
+                if mistake == "no_rowsum":
+                    dS = P * dP
+                else:
+                    dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                dq[bi, :, h] = scale * (dS @ K)
+                dk[bi, :, hk] += scale * ((dS if mistake == "untransposed_dk" else dS.T) @ Q)
+                dv[bi, :, hk] += P.T @ dO
+        return dq, dk, dv
+    return grad
+
+
+@pytest.mark.parametrize("mistake", ["no_rowsum", "untransposed_dk"])
+def test_planted_gradient_mistakes_are_caught(monkeypatch, mistake):
+    monkeypatch.setattr(oracle, "attn_dual_stream_grad", _grad_with(mistake))
+    with pytest.raises(AssertionError):
+        test_dual_stream_grad_matches_finite_differences()
+
+
+def test_planted_natural_log_statistics_are_caught(monkeypatch):
+    real = oracle.attn_dual_stream_lse
+    monkeypatch.setattr(oracle, "attn_dual_stream_lse",
+                        lambda *a, **kw: real(*a, **kw) * math.log(2.0))
+    with pytest.raises(AssertionError):
+        test_dual_stream_lse_zero_queries_counts_visible_keys()
+
+
+def test_planted_single_mean_over_both_streams_is_caught(monkeypatch):
+    real = oracle.ce_loss_dual
+
+    def wrong(h, w, targets, batch, L):
+        _, _, ce = real(h, w, targets, batch, L)
+        m = float(ce[np.asarray(targets) >= 0].mean())
+        return m, m, ce
+    monkeypatch.setattr(oracle, "ce_loss_dual", wrong)
+    with pytest.raises(AssertionError):
+        test_ce_loss_hand_worked_case()
+
+
+def test_gradient_copy_without_a_mistake_passes(monkeypatch):
+    """The copy the planted gradient mistakes are made in passes the same pin unchanged, so
+    each failure above comes from its mistake."""
+    monkeypatch.setattr(oracle, "attn_dual_stream_grad", _grad_with(None))
+    test_dual_stream_grad_matches_finite_differences()
