@@ -697,3 +697,38 @@ def test_gradient_copy_without_a_mistake_passes(monkeypatch):
     each failure above comes from its mistake."""
     monkeypatch.setattr(oracle, "attn_dual_stream_grad", _grad_with(None))
     test_dual_stream_grad_matches_finite_differences()
+
+
+def test_planted_loss_gradient_of_the_sum_is_caught(monkeypatch):
+    """dlogits = softmax - onehot without the 1/N of each stream's mean: the gradient of
+    the summed cross-entropy, not of L_mask + L_AR."""
+    def wrong(h, w, targets, batch, L):
+        logits = h @ w.T
+        p = np.exp(logits - logits.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        y = np.asarray(targets)
+        ok = y >= 0
+        g = np.where(ok[:, None], p, 0.0)
+        g[np.flatnonzero(ok), y[ok]] -= 1.0
+        return g @ w, g.T @ h, None
+    monkeypatch.setattr(oracle, "ce_loss_dual_grad", wrong)
+    with pytest.raises(AssertionError):
+        test_ce_loss_grad_matches_finite_differences()
+
+
+def test_planted_batch_sync_on_the_largest_n_is_caught(monkeypatch):
+    def wrong(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, v_pool, page_size):
+        n_max = max(int(x) for x in n_accept)
+        return oracle.kv_commit(k_blk, v_blk, [n_max] * len(n_accept), seq_lens, block_table,
+                                k_pool, v_pool, page_size)
+    monkeypatch.setattr(oracle, "kv_commit_batch_sync", wrong)
+    with pytest.raises(AssertionError):
+        test_commit_batch_sync_golden_case()
+
+
+def test_planted_first_threshold_for_every_request_is_caught(monkeypatch):
+    real = oracle.head_accept
+    monkeypatch.setattr(oracle, "head_accept_per_request",
+                        lambda h, w, batch, B, taus: real(h, w, batch, B, float(taus[0])))
+    with pytest.raises(AssertionError):
+        test_per_request_thresholds_golden_batch()
