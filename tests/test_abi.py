@@ -119,7 +119,7 @@ def test_host_validation_codes(L):
     assert L.mars_attn_dual_stream_grad_lse(*gl, None, 1, 8, 2, 4, 2, 64, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EINVAL
     assert L.mars_attn_dual_stream_grad_lse(*gl, _p(20), 1, 8, 2, 4, 2, 64, 0.0, P, P, P, P, 1 << 30, None, None) == mars.EALIGN
     assert L.mars_attn_dual_stream_grad_lse(*gl, P, 1, 8, 2, 4, 2, 64, 0.0, P, P, P, P, 16, None, None) == mars.ENOSPACE
-        # loss gradient: vocabulary not a multiple of 8, null row_lse, workspace too small
+    # loss gradient: vocabulary not a multiple of 8, null row_lse, workspace too small
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 100, P, P, P, 1 << 30, None, None) == mars.EUNSUPPORTED
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, None, 1, 4, 64, 96, P, P, P, 1 << 30, None, None) == mars.EINVAL
     assert L.mars_dual_stream_ce_loss_grad(P, P, P, P, 1, 4, 64, 96, P, P, P, 16, None, None) == mars.ENOSPACE
@@ -138,3 +138,65 @@ def test_binding_rejects_cpu_tensors(L):
     o = torch.zeros(1, 8, 2, 64)
     with pytest.raises(ValueError, match="CUDA"):
         mars.mars_attn_dual_stream(q, q[:, :, :1].contiguous(), q[:, :, :1].contiguous(), o, L=4, B=2)
+
+
+def test_every_binding_rejects_cpu_tensors(L):
+    """No entry point has a CPU path: each binding refuses host tensors before anything
+    is launched, and every tensor-taking binding is covered here."""
+    import inspect
+
+    import torch
+
+    def z(*shape, dt=torch.float32):
+        return torch.zeros(*shape, dtype=dt)
+
+    def bf(*shape):
+        return z(*shape, dt=torch.bfloat16)
+
+    def i32(*shape):
+        return z(*shape, dt=torch.int32)
+
+    ws = z(64, dt=torch.uint8)
+    q, kv, o = bf(1, 8, 2, 64), bf(1, 8, 1, 64), z(1, 8, 2, 64)
+    kvf = z(1, 8, 1, 64)
+    lse = z(1, 2, 2, 128)
+    pool = bf(4, 1, 16, 64)
+    blk = bf(1, 4, 1, 64)
+    calls = {
+        "mars_attn_dual_stream": lambda: mars.mars_attn_dual_stream(q, kv, kv, o, 4, 2),
+        "mars_attn_dual_stream_lse":
+            lambda: mars.mars_attn_dual_stream_lse(q, kv, kv, o, lse, 4, 2),
+        "mars_attn_dual_stream_grad":
+            lambda: mars.mars_attn_dual_stream_grad(q, kv, kv, o, o, 4, 2, o, kvf, kvf, ws),
+        "mars_attn_dual_stream_grad_lse":
+            lambda: mars.mars_attn_dual_stream_grad_lse(q, kv, kv, o, o, lse, 4, 2, o, kvf, kvf,
+                                                        ws),
+        "mars_decode_attn":
+            lambda: mars.mars_decode_attn(bf(1, 4, 2, 64), blk, blk, pool, pool, i32(1, 4),
+                                          i32(1), 64, z(1, 4, 2, 64), ws),
+        "mars_head_accept":
+            lambda: mars.mars_head_accept(bf(4, 256), bf(512, 256), 1, 4, 0.9, i32(1, 4),
+                                          z(1, 4), i32(1), ws),
+        "mars_head_accept_per_request":
+            lambda: mars.mars_head_accept_per_request(bf(4, 256), bf(512, 256), 1, 4, z(1),
+                                                      i32(1, 4), z(1, 4), i32(1), ws),
+        "mars_kv_commit":
+            lambda: mars.mars_kv_commit(blk, blk, i32(1), i32(1), i32(1, 4), pool, pool),
+        "mars_kv_commit_batch_sync":
+            lambda: mars.mars_kv_commit_batch_sync(blk, blk, i32(1), i32(1), i32(1, 4), pool,
+                                                   pool),
+        "mars_dual_stream_ce_loss":
+            lambda: mars.mars_dual_stream_ce_loss(bf(8, 64), bf(96, 64), i32(8), 1, 4, z(3), ws),
+        "mars_dual_stream_ce_loss_grad":
+            lambda: mars.mars_dual_stream_ce_loss_grad(bf(8, 64), bf(96, 64), i32(8), z(8), 1,
+                                                       4, ws),
+        "mars_check_wait_timeout": lambda: mars.mars_check_wait_timeout(i32(1)),
+    }
+    scalar_only = {"mars_strerror", "mars_version", "mars_launch_count", "mars_workspace_bytes"}
+    bindings = {n for n, f in vars(mars).items()
+                if n.startswith("mars_") and inspect.isfunction(f)} - scalar_only
+    assert bindings == set(calls), bindings ^ set(calls)
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="CUDA"):
+            call()
+
