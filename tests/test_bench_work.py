@@ -74,3 +74,21 @@ def test_gradient_work_is_two_and_a_half_forwards():
     cfg = W.DUAL_STREAM_7B
     assert torch.isclose(torch.tensor(2.5 * bench.dual_flops(cfg)),
                          torch.tensor(10.0 * cfg.d * cfg.L * (cfg.L + 1) * cfg.batch * cfg.hq))
+
+
+def test_clock_summary_reads_reasons_and_median():
+    """The clock record that decides whether a run is kept: median SM clock over the
+    samples, the maximum clock, and every throttle reason seen Active at least once."""
+    clk = bench.ClockSampler(0)
+    clk.lines = [
+        "2070, 2070, 900.1, Not Active, Not Active, Not Active, Not Active",
+        "1980, 2070, 1390.0, Not Active, Not Active, Not Active, Active",
+        "2070, 2070, 1200.5, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "[N/A], 2070, 0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    s = clk.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    clk.lines = ["1400, 2070, 1000, Active, Not Active, Active, Not Active"]
+    assert bench.ClockSampler.summary(clk)["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
