@@ -92,3 +92,18 @@ def test_clock_summary_reads_reasons_and_median():
     assert s["reasons"] == ["sw_power_cap"]
     clk.lines = ["1400, 2070, 1000, Active, Not Active, Active, Not Active"]
     assert bench.ClockSampler.summary(clk)["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_peaks_come_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
+    """The roofline denominators: the measured copy bandwidth and bf16 rates when the
+    measured-peaks file is present, else the fallback figures, labelled as such."""
+    import json
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    fb = bench.load_peaks()
+    assert fb["source"] == "fallback"
+    assert (fb["hbm_gbs"], fb["bf16_tflops"], fb["bf16_tflops_sustained"]) == (6800.0, 1900.0, 1700.0)
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 6795.1, "bf16_tflops": 1906.6, "bf16_tflops_sustained": 1687.3}))
+    m = bench.load_peaks()
+    assert m["source"] == "measured"
+    assert (m["hbm_gbs"], m["bf16_tflops"], m["bf16_tflops_sustained"]) == (6795.1, 1906.6, 1687.3)
