@@ -11,9 +11,12 @@
 // The scratch is a file-scope __device__ array of MARS_NOALLOC_SCRATCH_BYTES. Every GPU
 // that loads the library keeps that much memory reserved until the process exits. In host
 // code the array's name only stands in for the symbol; its device address is looked up
-// with cudaGetSymbolAddress once per device (on the first call made while that device is
-// current) and that address is what the kernels receive.
+// with cudaGetSymbolAddress once per device and context (on the first call made while
+// that device is current) and that address is what the kernels receive.
 #include <math.h>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -29,20 +32,52 @@ static __device__ __align__(256) unsigned char g_head_scratch[MARS_NOALLOC_SCRAT
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
-// Device address of g_head_scratch on the current device, looked up once per device.
+// The address a device's copy of g_head_scratch has in the context it was looked up in.
+struct ScratchSlot {
+  CUcontext ctx;
+  void* ptr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry-point lookup (no link against libcuda).
+CtxGetCurrentFn ctx_get_current() {
+  static const CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  return fn;
+}
+
+// Device address of g_head_scratch on the current device. It is looked up on the first
+// call made while the device is current, and again whenever the calling thread's current
+// context is not the one of that lookup (after cudaDeviceReset the runtime creates a new
+// primary context, in which the array has a new address).
 int scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MARS_ECUDA;
+  CUcontext ctx = nullptr;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&ctx) != CUDA_SUCCESS) return MARS_ECUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchSlot& slot = g_scratch[dev];
+  if (slot.ptr == nullptr || ctx == nullptr || slot.ctx != ctx) {
+    // the lookup also makes the runtime's context current when none was yet
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_head_scratch) != cudaSuccess || p == nullptr)
       return MARS_ECUDA;
-    g_scratch_ptr[dev] = p;
+    if (ctx == nullptr && (get(&ctx) != CUDA_SUCCESS || ctx == nullptr)) return MARS_ECUDA;
+    slot.ctx = ctx;
+    slot.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return MARS_OK;
 }
 

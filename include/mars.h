@@ -160,7 +160,10 @@ int mars_head_accept_per_request(const mars_bf16* h, const mars_bf16* w, int bat
  * (batch*B*ceil(vocab/256)*16 bytes, i.e. more than 882 rows at vocab 152064) returns
  * MARS_ENOSPACE before anything is launched.
  * The first call on a device (made while that device is current) looks up the array's
- * device address; make that first call before any CUDA stream capture.
+ * device address; make that first call before any CUDA stream capture. The address is
+ * looked up again when the calling thread's current context differs from the one of the
+ * lookup (for example after cudaDeviceReset); such a first call in a new context must
+ * likewise come before any capture.
  * Every call uses the same array and leaves its contents behind: calls whose kernels may
  * overlap on the GPU (different streams without ordering between them) race on it and
  * give wrong results, so order such calls on one stream. */

@@ -8,6 +8,7 @@ from .mars_oracle import (  # noqa: F401
     ar_signal_fraction,
     attn_dual_stream,
     attn_dual_stream_grad,
+    attn_dual_stream_grad_parts,
     attn_dual_stream_lse,
     beta,
     ce_loss_dual,

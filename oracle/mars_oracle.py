@@ -185,31 +185,48 @@ def attn_dual_stream_lse(q, k, L: int, B: int, scale: float | None = None):
     return out
 
 
-def attn_dual_stream_grad(q, k, v, do, L: int, B: int, scale: float | None = None):
-    """Gradient of the dual-stream attention (attn_dual_stream) for an upstream gradient
-    dO [b, 2L, Hq, D]: per (batch, query head h), with kv head h // (Hq/Hkv),
-    P = masked softmax of S = scale Q K^T, dP = dO V^T, dS = P * (dP - rowsum(P * dP)),
-    dQ = scale dS K, and summed over the query heads of a kv head dK = scale dS^T Q,
-    dV = P^T dO. Returns (dq [b, 2L, Hq, D], dk [b, 2L, Hkv, D], dv [b, 2L, Hkv, D])."""
-    b, n, Hq, D = q.shape
+def attn_dual_stream_grad_parts(q, k, v, do, L: int, B: int, scale: float | None = None):
+    """The per-(batch, query head) intermediates of the dual-stream attention gradient, in
+    the order the chain rule forms them ([notes] Key design 1, eq. M: the softmax runs
+    over the keys M leaves visible). For upstream gradient dO [b, 2L, Hq, D], yields
+    (bi, h, hk, P, dP, D, dS) with kv head hk = h // (Hq/Hkv):
+      P  = masked softmax of S = scale Q K^T (0 where M hides the key),
+      dP = dO V^T,
+      D  = rowsum(P * dP) (equal to rowsum(dO * O), O = P V),
+      dS = P * (dP - D)."""
+    b, n, Hq, Dh = q.shape
     Hkv = k.shape[2]
     g = Hq // Hkv
     if scale is None:
-        scale = 1.0 / math.sqrt(D)
+        scale = 1.0 / math.sqrt(Dh)
     vis = mask_M(L, B)
-    dq = np.zeros(q.shape)
-    dk = np.zeros(k.shape)
-    dv = np.zeros(v.shape)
     for bi in range(b):
         for h in range(Hq):
             hk = h // g
             Q, K, V, dO = q[bi, :, h, :], k[bi, :, hk, :], v[bi, :, hk, :], do[bi, :, h, :]
             P = _masked_softmax_rows(scale * (Q @ K.T), vis)
             dP = dO @ V.T
-            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
-            dq[bi, :, h, :] = scale * (dS @ K)
-            dk[bi, :, hk, :] += scale * (dS.T @ Q)
-            dv[bi, :, hk, :] += P.T @ dO
+            D = (P * dP).sum(axis=1, keepdims=True)
+            dS = P * (dP - D)
+            yield bi, h, hk, P, dP, D, dS
+
+
+def attn_dual_stream_grad(q, k, v, do, L: int, B: int, scale: float | None = None):
+    """Gradient of the dual-stream attention (attn_dual_stream) for an upstream gradient
+    dO [b, 2L, Hq, D]: per (batch, query head h), with kv head h // (Hq/Hkv) and P, dS
+    from attn_dual_stream_grad_parts: dQ = scale dS K, and summed over the query heads of
+    a kv head dK = scale dS^T Q, dV = P^T dO. Returns (dq [b, 2L, Hq, D],
+    dk [b, 2L, Hkv, D], dv [b, 2L, Hkv, D])."""
+    Dh = q.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dh)
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for bi, h, hk, P, _, _, dS in attn_dual_stream_grad_parts(q, k, v, do, L, B, scale):
+        dq[bi, :, h, :] = scale * (dS @ k[bi, :, hk, :])
+        dk[bi, :, hk, :] += scale * (dS.T @ q[bi, :, h, :])
+        dv[bi, :, hk, :] += P.T @ do[bi, :, h, :]
     return dq, dk, dv
 
 

@@ -578,6 +578,31 @@ def test_dual_stream_grad_against_torch_autograd():
     np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_dual_stream_grad_parts_identities():
+    """The gradient's intermediates obey what the mathematics fixes: P is the forward
+    oracle's attention (rows sum to 1, zero wherever M hides the key, P V = O), D equals
+    rowsum(dO * O) for that O, and every row of dS sums to 0."""
+    b, L, B, Hq, Hkv, D = 2, 7, 3, 4, 2, 5
+    q = _rand((b, 2 * L, Hq, D), 95)
+    k = _rand((b, 2 * L, Hkv, D), 96)
+    v = _rand((b, 2 * L, Hkv, D), 97)
+    do = _rand((b, 2 * L, Hq, D), 98)
+    o = oracle.attn_dual_stream(q, k, v, L, B)
+    vis = oracle.mask_M(L, B)
+    seen = 0
+    for bi, h, hk, P, dP, Dr, dS in oracle.attn_dual_stream_grad_parts(q, k, v, do, L, B):
+        assert hk == h // (Hq // Hkv)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-13)
+        assert (P[~vis] == 0).all() and (P[vis] > 0).all()
+        np.testing.assert_allclose(P @ v[bi, :, hk], o[bi, :, h], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dP, do[bi, :, h] @ v[bi, :, hk].T, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Dr[:, 0], (do[bi, :, h] * o[bi, :, h]).sum(axis=1),
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dS.sum(axis=1), 0.0, rtol=0, atol=1e-12)
+        seen += 1
+    assert seen == b * Hq
+
+
 # ------------------------------------------- planted mistakes: each must fail some pin
 
 def test_planted_floor_block_index_is_caught(monkeypatch):

@@ -71,6 +71,56 @@ def test_noalloc_matches_workspace_entry_point(batch, B, hidden, vocab, tau):
         np.testing.assert_array_equal(n2.cpu().numpy(), n.cpu().numpy())
 
 
+def _call(fn, h, w, batch, B, hidden, vocab, tau, tok, mp, n, st):
+    stream = torch.cuda.current_stream()
+    return fn(_ptr(h), _ptr(w), batch, B, hidden, vocab, tau, _ptr(tok), _ptr(mp), _ptr(n),
+              _ptr(st), ctypes.c_void_p(stream.cuda_stream))
+
+
+def test_noalloc_at_its_exact_limit_allocates_nothing():
+    """The largest call the scratch holds (882 rows at vocabulary 152064: 882 x 594
+    partials of 16 bytes = 8 382 528 bytes <= 8 MiB) matches the workspace entry point on
+    two calls in a row, and the second call changes neither the device's free memory nor
+    the caching allocator's counters; one row more (883) is refused with ENOSPACE before
+    anything runs."""
+    fn = _noalloc()
+    batch, B, hidden, vocab, tau = 63, 14, 3584, 152064, 0.5
+    assert batch * B * ((vocab + 255) // 256) * 16 <= SCRATCH_BYTES
+    cfg = W.DecodeConfig("lim", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
+                         hidden=hidden, vocab=vocab, taus=(tau,))
+    inp = W.make_decode_inputs(cfg, seed=12, device=DEV, steps=2)
+    ws = torch.empty(mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, batch, B, vocab=vocab),
+                     dtype=torch.uint8, device=DEV)
+    tok2, mp2, n2 = _outputs(batch, B)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for step in range(2):
+        tok, mp, n = _outputs(batch, B)
+        mars.mars_head_accept(inp.h[step], inp.w, batch, B, tau, tok, mp, n, ws)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        stats0 = torch.cuda.memory_stats()
+        rc = _call(fn, inp.h[step], inp.w, batch, B, hidden, vocab, tau, tok2, mp2, n2, st)
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        stats1 = torch.cuda.memory_stats()
+        assert rc == mars.OK, mars.mars_strerror(rc)
+        assert int(st.item()) == 0
+        if step == 1:                      # the first call may set the device up
+            assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+            for key in ("allocation.all.allocated", "segment.all.allocated",
+                        "allocated_bytes.all.allocated", "reserved_bytes.all.allocated"):
+                assert stats1.get(key, 0) == stats0.get(key, 0), key
+        np.testing.assert_array_equal(tok2.cpu().numpy(), tok.cpu().numpy())
+        np.testing.assert_allclose(mp2.cpu().numpy(), mp.cpu().numpy(), rtol=0, atol=1e-4)
+        np.testing.assert_array_equal(n2.cpu().numpy(), n.cpu().numpy())
+    # 883 rows (batch 883, B 1): 16 bytes over
+    assert 883 * ((vocab + 255) // 256) * 16 > SCRATCH_BYTES
+    dummy = torch.empty(16, dtype=torch.uint8, device=DEV)
+    p = _ptr(dummy)
+    rc = fn(p, p, 883, 1, hidden, vocab, tau, p, p, p, None, None)
+    assert rc == mars.ENOSPACE
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     fn = _noalloc()
     batch, B, hidden, vocab = 128, 16, 3584, 152064     # 2048 rows: 19.5 MB of partials
