@@ -14,12 +14,14 @@ from .mars_oracle import (  # noqa: F401
     ce_loss_dual,
     ce_loss_dual_grad,
     decode_attn,
+    decode_attn_staged,
     gather_prefix,
     head_accept,
     head_accept_per_request,
     head_logits,
     kv_commit,
     kv_commit_batch_sync,
+    kv_commit_block,
     mask_M,
     mask_rows,
     maxprob_argmax,

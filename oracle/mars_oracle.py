@@ -30,7 +30,10 @@ Readings taken where the pages are silent:
     tau is a float32 value compared exactly in fp64;
   * commit: each sequence's own N rows are written every step (per-sequence commit);
     kv_commit_batch_sync gives the batch-synchronised alternative, every sequence
-    committing the smallest N of the batch;
+    committing the smallest N of the batch; kv_commit_block the block-level cache with a
+    B_cache boundary (rows held in a per-sequence block buffer until every sequence has
+    filled its block; the block is written at the start of the call after the one that
+    filled the last block);
   * per-request threshold: one float32 tau per sequence (head_accept_per_request).
 
 Every function takes float64 numpy arrays (callers pass bf16-rounded values converted to
@@ -387,6 +390,89 @@ def kv_commit_batch_sync(k_blk, v_blk, n_accept, seq_lens, block_table, k_pool, 
     n_min = min(n) if n else 0
     return kv_commit(k_blk, v_blk, [n_min] * len(n), seq_lens, block_table, k_pool, v_pool,
                      page_size)
+
+
+def kv_commit_block(k_blk, v_blk, n_accept, seq_lens, fill, k_stage, v_stage,
+                    flush_pending: bool, block_table, k_pool, v_pool, page_size: int,
+                    B_cache: int):
+    """Block-level commit with a batch-wide B_cache boundary ([notes] Key design 4: the
+    prefix cache is frozen in blocks of B_cache tokens; within a batch the samples that
+    accept faster wait at the block boundary until every sample has filled the block,
+    and then the whole block is written to the persistent prefix cache; [gist] 2.D: the
+    cache is updated only when a full block has been accepted across all samples).
+
+    State: seq_lens[s] = tokens of sequence s in the persistent cache (the paged pool);
+    fill[s] = accepted tokens of s held in its block buffer stage[s, :fill[s]] (k_stage,
+    v_stage [b, B_cache, Hkv, D]); flush_pending = every block was full after the
+    previous call. One call, in this order:
+      1. if flush_pending, every sequence writes its block, stage[s, 0:B_cache], to the
+         pool at positions seq_lens[s] .. seq_lens[s] + B_cache - 1 (page =
+         block_table[s, pos // page_size], slot = pos % page_size), then
+         seq_lens[s] += B_cache and fill[s] = 0;
+      2. every sequence appends n_s = min(clamp(N_s, 0, B), B_cache - fill[s]) accepted
+         rows (block rows 0..n_s-1) to its block buffer: a sequence whose block is full
+         waits (n_s = 0); commit_slots[s, i] = page * page_size + slot of position
+         seq_lens[s] + fill[s] + i, where row i goes when its block is written, for
+         i < n_s, and -1 otherwise; fill[s] += n_s;
+      3. flush_pending = every fill[s] == B_cache.
+    Pages are assumed mapped. Returns (k_pool, v_pool, seq_lens, fill, k_stage, v_stage,
+    flush_pending, commit_slots); inputs are not modified."""
+    k_pool, v_pool = k_pool.copy(), v_pool.copy()
+    k_stage, v_stage = k_stage.copy(), v_stage.copy()
+    lens = np.array(seq_lens, dtype=np.int64).copy()
+    fill = np.array(fill, dtype=np.int64).copy()
+    b, B = k_blk.shape[0], k_blk.shape[1]
+    if flush_pending:
+        for s in range(b):
+            for i in range(B_cache):
+                pos = int(lens[s]) + i
+                page = int(block_table[s][pos // page_size])
+                k_pool[page, :, pos % page_size, :] = k_stage[s, i]
+                v_pool[page, :, pos % page_size, :] = v_stage[s, i]
+            lens[s] += B_cache
+            fill[s] = 0
+    slots = np.full((b, B), -1, dtype=np.int64)
+    for s in range(b):
+        n = min(min(max(int(n_accept[s]), 0), B), B_cache - int(fill[s]))
+        for i in range(n):
+            pos = int(lens[s]) + int(fill[s]) + i
+            page = int(block_table[s][pos // page_size])
+            slots[s, i] = page * page_size + pos % page_size
+            k_stage[s, int(fill[s]) + i] = k_blk[s, i]
+            v_stage[s, int(fill[s]) + i] = v_blk[s, i]
+        fill[s] += n
+    flush = bool((fill == B_cache).all())
+    return k_pool, v_pool, lens, fill, k_stage, v_stage, flush, slots
+
+
+def decode_attn_staged(q, k_blk, v_blk, k_pool, v_pool, block_table, seq_lens, k_stage,
+                       v_stage, fill, page_size: int, scale: float | None = None, seqs=None):
+    """Decode-form attention over the block-level cache of kv_commit_block: the keys of
+    sequence s are its P_s persistent prefix rows (paged pool), then the fill_s accepted
+    rows of its block buffer (stage[s, :fill_s]), then the B block rows of this step;
+    block query k sees the prefix, the buffered rows and block rows 0..k ([notes] Key
+    design 3 and 4; [gist] 2.C, 2.D). Returns O [b, B, Hq, D] float64 (NaN for
+    sequences not in `seqs`)."""
+    b, B, Hq, D = q.shape
+    Hkv = k_blk.shape[2]
+    g = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.full(q.shape, np.nan)
+    for s in (range(b) if seqs is None else seqs):
+        P, F = int(seq_lens[s]), int(fill[s])
+        K = np.concatenate([gather_prefix(k_pool, block_table[s], P, page_size),
+                            k_stage[s, :F], k_blk[s]])
+        V = np.concatenate([gather_prefix(v_pool, block_table[s], P, page_size),
+                            v_stage[s, :F], v_blk[s]])
+        j = np.arange(P + F + B)[None, :]
+        kq = np.arange(B)[:, None]
+        vis = (j < P + F) | ((j - P - F) <= kq)
+        for h in range(Hq):
+            hk = h // g
+            S = scale * (q[s, :, h, :] @ K[:, hk, :].T)
+            out[s, :, h, :] = _masked_softmax_rows(S, vis) @ V[:, hk, :]
+    return out
 
 
 # ---------------------------------------------------------------------------------------

@@ -66,11 +66,13 @@ def compare_head(tok, p, n, tok_ref, p_ref, n_ref, gap_ref, tau):
 # with fp32 accumulation; the other factor (b: K, Q, dO, W or h) is bf16 input data and
 # exact. Per element, the error of y_c is bounded by three terms:
 #   1. bf16 rounding of a_j: a_j (1 + d_j), |d_j| <= u = 2^-8 (8 significant bits, round
-#      to nearest even: half the spacing 2^-7 of bf16 values in [1, 2)).
-#      Worst case |sum d_j a_j b_jc| <= u * S1, S1 = sum_j |a_j| |b_jc|. With the d_j
-#      independent and zero-mean, Hoeffding's inequality gives |sum| <= 7 u * S2,
-#      S2 = sqrt(sum_j a_j^2 b_jc^2), except with probability 2 exp(-49/2) = 4.6e-11 per
-#      element. The bound takes the smaller of the two.
+#      to nearest even: half the spacing 2^-7 of bf16 values in [1, 2)). With r such
+#      roundings on the way to a_j (r = 2 for dS, which the kernels form from the already
+#      rounded P and round again; r = 1 for P and dlogits), the worst case is
+#      |error| <= r u S1, S1 = sum_j |a_j| |b_jc|. With the roundings independent and
+#      zero-mean, Hoeffding's inequality over the r n bounded terms gives
+#      |error| <= 7 sqrt(r) u S2, S2 = sqrt(sum_j a_j^2 b_jc^2), except with probability
+#      2 exp(-49/2) = 4.6e-11 per element. The bound takes the smaller of the two.
 #   2. fp32 accumulation: m = n/16 + 16 + extra roundings of partial sums no larger than
 #      S1 (one per K = 16 MMA step, up to 16 inside a step, plus the atomic adds of the
 #      query heads of a kv group); independent errors of at most 2^-24 relative give
@@ -88,14 +90,15 @@ U_F32 = 2.0 ** -24
 UPSTREAM_REL = 2.0 ** -14
 
 
-def product_error_bound(a_abs_b, a2_b2, n, upstream=None, extra_roundings=0):
+def product_error_bound(a_abs_b, a2_b2, n, upstream=None, extra_roundings=0, roundings=1):
     """Element-wise bound of the model above from S1 = |a| @ |b| (a_abs_b), the sum of
-    squares S2^2 = a^2 @ b^2 (a2_b2) and the contraction length n; `upstream` is the
-    absolute upstream term beyond 2^-14 * S1 (attention: 2^-14 * S3), or None."""
+    squares S2^2 = a^2 @ b^2 (a2_b2), the contraction length n and the number r of bf16
+    roundings of a (`roundings`); `upstream` is the absolute upstream term beyond
+    2^-14 * S1 (attention: 2^-14 * S3), or None."""
     s1 = np.asarray(a_abs_b, dtype=np.float64)
     s2 = np.sqrt(np.asarray(a2_b2, dtype=np.float64))
     m = n / 16.0 + 16.0 + extra_roundings
-    bound = np.minimum(U_BF16 * s1, 7.0 * U_BF16 * s2)
+    bound = np.minimum(roundings * U_BF16 * s1, 7.0 * math.sqrt(roundings) * U_BF16 * s2)
     bound = bound + (7.0 * U_F32 / math.sqrt(3.0) * math.sqrt(m) + UPSTREAM_REL) * s1
     if upstream is not None:
         bound = bound + np.asarray(upstream, dtype=np.float64)

@@ -444,6 +444,124 @@ def test_commit_batch_sync_properties():
         np.testing.assert_array_equal(x, y)
 
 
+def _block_case():
+    lines = golden_lines("commit_block_case.txt")
+    kv = {}
+    calls, written, staged = [], [], []
+    for ln in lines:
+        if ln.startswith("call"):
+            f = [x.split() for x in ln.split("|")]
+            calls.append({"N": [int(x) for x in f[1]],
+                          "slots": [[int(x) for x in f[2]], [int(x) for x in f[3]]],
+                          "fill": [int(x) for x in f[4]], "seq_len": [int(x) for x in f[5]],
+                          "flush": bool(int(f[6][0]))})
+        elif ln.startswith("written"):
+            written.append([int(x) for x in ln.split()[1:]])
+        elif ln.startswith("staged"):
+            staged.append([int(x) for x in ln.split()[1:]])
+        else:
+            k, v = ln.split(None, 1)
+            kv[k] = v
+    return kv, calls, written, staged
+
+
+def test_commit_block_golden_case():
+    kv, calls, written, staged = _block_case()
+    ps, B, Bc = int(kv["page_size"]), int(kv["B"]), int(kv["B_cache"])
+    bt = np.array([[int(x) for x in kv["block_table_0"].split()],
+                   [int(x) for x in kv["block_table_1"].split()]])
+    lens = np.array([int(x) for x in kv["seq_len"].split()])
+    Hkv, D = 2, 3
+    kp, vp = _rand((10, Hkv, ps, D), 64), _rand((10, Hkv, ps, D), 65)
+    kp0 = kp.copy()
+    ks, vs = np.zeros((2, Bc, Hkv, D)), np.zeros((2, Bc, Hkv, D))
+    fill, flush = np.zeros(2, dtype=np.int64), False
+    blocks = []
+    for c, call in enumerate(calls):
+        kb, vb = _rand((2, B, Hkv, D), 80 + c), _rand((2, B, Hkv, D), 90 + c)
+        blocks.append((kb, vb))
+        kp, vp, lens, fill, ks, vs, flush, slots = oracle.kv_commit_block(
+            kb, vb, np.array(call["N"]), lens, fill, ks, vs, flush, bt, kp, vp, ps, Bc)
+        np.testing.assert_array_equal(slots, call["slots"], err_msg=f"call {c + 1}")
+        np.testing.assert_array_equal(fill, call["fill"], err_msg=f"call {c + 1}")
+        np.testing.assert_array_equal(lens, call["seq_len"], err_msg=f"call {c + 1}")
+        assert flush == call["flush"], f"call {c + 1}"
+        if c < 3:                      # nothing reaches the pool before the block is full
+            np.testing.assert_array_equal(kp, kp0)
+    touched = set()
+    for slot, c, s, row in written:
+        np.testing.assert_array_equal(kp[slot // ps, :, slot % ps], blocks[c - 1][0][s, row])
+        np.testing.assert_array_equal(vp[slot // ps, :, slot % ps], blocks[c - 1][1][s, row])
+        touched.add(slot)
+    for slot in range(10 * ps):
+        if slot not in touched:
+            np.testing.assert_array_equal(kp[slot // ps, :, slot % ps],
+                                          kp0[slot // ps, :, slot % ps])
+    for s, r, c, row in staged:
+        np.testing.assert_array_equal(ks[s, r], blocks[c - 1][0][s, row])
+        np.testing.assert_array_equal(vs[s, r], blocks[c - 1][1][s, row])
+
+
+def test_commit_block_properties():
+    """Over random accepted counts: the persistent lengths of all sequences advance
+    together in whole blocks; the persisted rows followed by the buffered ones are the
+    rows the per-sequence commit writes when each call's count is the number of rows the
+    block could still take; and with every block filled by each call, each call writes
+    the previous call's block."""
+    rng = np.random.default_rng(3)
+    ps, Hkv, D, B, Bc, b = 4, 1, 2, 5, 8, 3
+    lens0 = np.array([2, 9, 4])
+    npg = 12
+    bt = np.array([np.arange(npg) + s * npg for s in range(b)])
+    kp, vp = _rand((b * npg, Hkv, ps, D), 66), _rand((b * npg, Hkv, ps, D), 67)
+    ks, vs = np.zeros((b, Bc, Hkv, D)), np.zeros((b, Bc, Hkv, D))
+    lens, fill, flush = lens0.copy(), np.zeros(b, dtype=np.int64), False
+    rk, rv, rl = kp.copy(), vp.copy(), lens0.copy()       # per-sequence commit reference
+    for c in range(12):
+        kb, vb = _rand((b, B, Hkv, D), 200 + c), _rand((b, B, Hkv, D), 300 + c)
+        n = rng.integers(-1, B + 2, b)
+        took = np.minimum(np.clip(n, 0, B), Bc - np.where(flush, 0, fill))
+        kp, vp, lens, fill, ks, vs, flush, slots = oracle.kv_commit_block(
+            kb, vb, n, lens, fill, ks, vs, flush, bt, kp, vp, ps, Bc)
+        rk, rv, rl, rslots = oracle.kv_commit(kb, vb, took, rl, bt, rk, rv, ps)
+        np.testing.assert_array_equal(slots, rslots)
+        assert ((lens - lens0) % Bc == 0).all() and len(set((lens - lens0).tolist())) == 1
+        np.testing.assert_array_equal(lens + fill, rl)
+        for s in range(b):
+            got = oracle.gather_prefix(kp, bt[s], int(lens[s]), ps)
+            want = oracle.gather_prefix(rk, bt[s], int(lens[s]), ps)
+            np.testing.assert_array_equal(got, want)
+            pending = oracle.gather_prefix(rk, bt[s], int(rl[s]), ps)[int(lens[s]):]
+            np.testing.assert_array_equal(ks[s, :fill[s]], pending)
+    # B = B_cache and every count B: each call fills every block
+    kb, vb = _rand((b, Bc, Hkv, D), 400), _rand((b, Bc, Hkv, D), 401)
+    st = (kp, vp, lens0.copy(), np.zeros(b, dtype=np.int64), ks, vs, False)
+    for c in range(3):
+        kp2, vp2, l2, f2, ks2, vs2, fl2, _ = oracle.kv_commit_block(
+            kb, vb, np.full(b, Bc), st[2], st[3], st[4], st[5], st[6], bt, st[0], st[1], ps, Bc)
+        assert fl2 and (f2 == Bc).all()
+        np.testing.assert_array_equal(l2, lens0 + Bc * c)
+        st = (kp2, vp2, l2, f2, ks2, vs2, fl2)
+
+
+def test_decode_staged_equals_decode_on_the_extended_prefix():
+    """Attention over prefix + buffered block rows + block keys equals the plain decode
+    attention over a prefix that the buffered rows extend (committed into the pool)."""
+    b, B, Hq, Hkv, D, ps, Bc = 3, 4, 4, 2, 8, 4, 8
+    lens = np.array([5, 0, 13])
+    fill = np.array([3, 8, 0])
+    npg = 8
+    bt = np.array([np.arange(npg) + s * npg for s in range(b)])
+    q = _rand((b, B, Hq, D), 500)
+    kb, vb = _rand((b, B, Hkv, D), 501), _rand((b, B, Hkv, D), 502)
+    kp, vp = _rand((b * npg, Hkv, ps, D), 503), _rand((b * npg, Hkv, ps, D), 504)
+    ks, vs = _rand((b, Bc, Hkv, D), 505), _rand((b, Bc, Hkv, D), 506)
+    got = oracle.decode_attn_staged(q, kb, vb, kp, vp, bt, lens, ks, vs, fill, ps)
+    kp2, vp2, lens2, _ = oracle.kv_commit(ks, vs, fill, lens, bt, kp, vp, ps)
+    want = oracle.decode_attn(q, kb, vb, kp2, vp2, bt, lens2, ps)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-13)
+
+
 # --------------------------------------------------------------- dual-stream loss
 
 def test_ce_loss_hand_worked_case():
@@ -749,6 +867,56 @@ def test_planted_batch_sync_on_the_largest_n_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "kv_commit_batch_sync", wrong)
     with pytest.raises(AssertionError):
         test_commit_batch_sync_golden_case()
+
+
+def _block_commit_with(mistake):
+    """The oracle's block-level commit with one planted mistake: "own_flush" writes a
+    sequence's block as soon as that sequence has filled it (no wait for the batch);
+    "no_wait" lets a full block keep taking rows past the boundary."""
+    def commit(k_blk, v_blk, n_accept, seq_lens, fill, k_stage, v_stage, flush_pending,
+               block_table, k_pool, v_pool, page_size, B_cache):
+        k_pool, v_pool = k_pool.copy(), v_pool.copy()
+        k_stage, v_stage = k_stage.copy(), v_stage.copy()
+        lens = np.array(seq_lens, dtype=np.int64).copy()
+        fill = np.array(fill, dtype=np.int64).copy()
+        b, B = k_blk.shape[0], k_blk.shape[1]
+        for s in range(b):
+            if flush_pending or (mistake == "own_flush" and fill[s] == B_cache):
+                for i in range(B_cache):
+                    pos = int(lens[s]) + i
+                    page = int(block_table[s][pos // page_size])
+                    k_pool[page, :, pos % page_size] = k_stage[s, i]
+                    v_pool[page, :, pos % page_size] = v_stage[s, i]
+                lens[s] += B_cache
+                fill[s] = 0
+        slots = np.full((b, B), -1, dtype=np.int64)
+        for s in range(b):
+            room = B if mistake == "no_wait" else B_cache - int(fill[s])
+            n = min(min(max(int(n_accept[s]), 0), B), room)
+            for i in range(n):
+                pos = int(lens[s]) + int(fill[s]) + i
+                page = int(block_table[s][pos // page_size])
+                slots[s, i] = page * page_size + pos % page_size
+                if fill[s] + i < B_cache:
+                    k_stage[s, int(fill[s]) + i] = k_blk[s, i]
+                    v_stage[s, int(fill[s]) + i] = v_blk[s, i]
+            fill[s] = min(int(fill[s]) + n, B_cache)
+        flush = bool((fill == B_cache).all())
+        return k_pool, v_pool, lens, fill, k_stage, v_stage, flush, slots
+    return commit
+
+
+@pytest.mark.parametrize("mistake", ["own_flush", "no_wait"])
+def test_planted_block_commit_mistakes_are_caught(monkeypatch, mistake):
+    monkeypatch.setattr(oracle, "kv_commit_block", _block_commit_with(mistake))
+    with pytest.raises(AssertionError):
+        test_commit_block_golden_case()
+
+
+def test_block_commit_copy_without_a_mistake_passes(monkeypatch):
+    monkeypatch.setattr(oracle, "kv_commit_block", _block_commit_with(None))
+    test_commit_block_golden_case()
+    test_commit_block_properties()
 
 
 def test_planted_first_threshold_for_every_request_is_caught(monkeypatch):

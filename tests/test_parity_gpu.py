@@ -147,8 +147,9 @@ def test_dual_stream_divergent_rescale():
     assert_attn_close(o.cpu().numpy(), ref)
 
 
-# Attention gradient. The kernels round P (for dV) and dS (for dQ, dK) to bf16 before their
-# tensor-core products; each output element is checked against the error bound of that
+# Attention gradient. The kernels round P (for dV) and dS (for dQ, dK; formed from the
+# rounded P) to bf16 before their tensor-core products; each output element is checked
+# against the error bound of that
 # arithmetic (parity_util.product_error_bound), computed from the oracle's own P, dP, D
 # and dS. The cases give the kernels the oracle's forward output as O and an upstream
 # gradient whose values bf16 represents exactly, so that neither the forward's error nor
@@ -201,9 +202,9 @@ def check_dual_grad(q, k, v, do, L, B, dq, dk, dv, what):
         del P, dP, dS, adS, dS2, X
     worst = {}
     for got, ref, bnd, name in (
-            (dq, rq, product_error_bound(s1q, s2q, n, UPSTREAM_REL * s3q), "dq"),
-            (dk, rk, product_error_bound(s1k, s2k, n, UPSTREAM_REL * s3k, extra_roundings=G),
-             "dk"),
+            (dq, rq, product_error_bound(s1q, s2q, n, UPSTREAM_REL * s3q, roundings=2), "dq"),
+            (dk, rk, product_error_bound(s1k, s2k, n, UPSTREAM_REL * s3k, extra_roundings=G,
+                                         roundings=2), "dk"),
             (dv, rv, product_error_bound(s1v, s2v, n, None, extra_roundings=G), "dv")):
         worst[name] = assert_within_bound(np.asarray(got), ref, bnd, f"{what} {name}")
     return worst
