@@ -3,8 +3,8 @@
 Attention outputs: max-abs error <= 1e-2 against the oracle run on the same bf16-rounded
 inputs. Max-probs: |delta| <= 1e-4. Argmax tokens, N and commit slots: bit-exact, except
 positions whose top-2 logit gap (oracle, fp64) is below 1e-3 (token excluded) and
-sequences where a position the acceptance scan examines has |p - tau| < 1e-4 (N and that
-sequence's commit slots excluded). Exclusions are counted and returned.
+sequences where a position the acceptance scan examines has |p - tau| < 1e-4, for
+0 < tau <= 1 (N and that sequence's commit slots excluded). Exclusions are counted and returned.
 
 Gradients are compared element by element against a bound from an error model of the
 kernels' arithmetic (product_error_bound below), not by a norm.
@@ -31,8 +31,12 @@ def assert_attn_close(got, ref, what="attention"):
 
 def scanned_ambiguous(p_ref_row, tau):
     """True when a position the left-to-right scan examines lies within TAU_EXCLUDE of
-    tau (the scan examines positions up to and including the first one below tau)."""
+    tau (the scan examines positions up to and including the first one below tau). A
+    max-prob lies in (0, 1], so with tau <= 0 every position is accepted and with tau > 1
+    none is, on either side: no position is ambiguous then."""
     t = float(np.float32(tau))
+    if t <= 0.0 or t > 1.0:
+        return False
     for p in p_ref_row:
         if abs(p - t) < TAU_EXCLUDE:
             return True
