@@ -47,6 +47,11 @@ struct DecodeArgs {
   int32_t* status;
   int num_pages, max_pages, B, hq, hkv, G, R, split_len, nsplit;
   float scale_log2;
+  // block-level cache: rows accepted into each sequence's block buffer and not yet in the
+  // pool (stage_fill[s] of B_cache), read between the prefix and the block keys; NULL
+  // without a block buffer
+  const int32_t* stage_fill;
+  int B_cache;
 };
 
 MARS_DEV bool page_ok(const DecodeArgs& a, const int32_t* bt_row, int lp) {
@@ -63,6 +68,7 @@ struct DecodePolicy {
   const int32_t* bt_row;
   float* part;           // [R][D + 4] records of this (sequence, kv head, split)
   int P, start, n_prefix;
+  int fill;              // buffered block rows visible before the block keys
   int s_idx, s_kvh;      // sequence and kv head of this CTA
 
   struct Tile {
@@ -92,15 +98,20 @@ struct DecodePolicy {
   }
   MARS_DEV flash::ColRange cols(const flash::RowVis& v, const Tile& t) const {
     flash::ColRange c;
-    if (t.block) {                       // block keys 0..k (k = v.hi2 - P)
+    c.s2 = BKV;
+    c.e2 = -1;
+    if (t.block && a->stage_fill) {      // buffered rows [0, fill), block keys 0..k at B_cache
+      c.e1 = fill;
+      c.s2 = a->B_cache;
+      c.e2 = a->B_cache + (v.hi2 - P);
+      c.pmask = 0xffu;
+    } else if (t.block) {                // block keys 0..k (k = v.hi2 - P)
       c.e1 = v.hi2 - P + 1;
       c.pmask = 0xffu;
     } else {                             // prefix keys below P on mapped pages
       c.e1 = min(P - t.kp0, BKV);
       c.pmask = t.pmask;
     }
-    c.s2 = BKV;
-    c.e2 = -1;
     return c;
   }
   MARS_DEV void store_chunk(int row, int col, const uint32_t (&r)[32], float inv, float m,
@@ -134,7 +145,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_kp,
                  const __grid_constant__ CUtensorMap tm_vp,
                  const __grid_constant__ CUtensorMap tm_kb,
-                 const __grid_constant__ CUtensorMap tm_vb, DecodeArgs a) {
+                 const __grid_constant__ CUtensorMap tm_vb,
+                 const __grid_constant__ CUtensorMap tm_ks,
+                 const __grid_constant__ CUtensorMap tm_vs, DecodeArgs a) {
   using namespace sm100;
   using S = flash::Smem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -148,6 +161,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   pol.bt_row = a.block_table + (size_t)s * a.max_pages;
   pol.part = a.ws + ((((size_t)s * a.hkv + kvh) * a.nsplit + sp) * a.R) * (D + 4);
   pol.P = a.seq_lens[s];
+  pol.fill = a.stage_fill ? min(max(a.stage_fill[s], 0), a.B_cache) : 0;
   pol.s_idx = s;
   pol.s_kvh = kvh;
   pol.start = sp * a.split_len;
@@ -190,9 +204,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     int st_flags = 0;
     // prefix tile j: lane i < 8 copies 16-token page i of the tile (unmapped pages load
     // page 0 and are masked by the softmax); the block tile: lane 0 copies a 128-row box
-    // from row s*B of k_blk / v_blk (rows past the batch read as zeros)
-    auto issue = [&](const CUtensorMap* tm_pool, const CUtensorMap* tm_blk) {
-      return [&, tm_pool, tm_blk](int j, uint8_t* dst, uint64_t* b) {
+    // from row s*B of k_blk / v_blk (rows past the batch read as zeros), or, with a block
+    // buffer, its B_cache rows into tile rows 0..B_cache-1 and a (128 - B_cache)-row box of
+    // k_blk / v_blk after them
+    auto issue = [&](const CUtensorMap* tm_pool, const CUtensorMap* tm_blk,
+                     const CUtensorMap* tm_stage) {
+      return [&, tm_pool, tm_blk, tm_stage](int j, uint8_t* dst, uint64_t* b) {
         if (j < pol.n_prefix) {
           if (lane < kPagesPerTile) {
             const int kp = pol.start + j * BKV + lane * kPageSize;
@@ -209,15 +226,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           row);
           }
         } else if (lane == 0) {
-          for (int x = 0; x < D / 64; ++x)
-            tma_load_3d(dst + x * (BKV * 128), tm_blk, b, x * 64, kvh, s * a.B);
+          for (int x = 0; x < D / 64; ++x) {
+            uint8_t* reg = dst + x * (BKV * 128);
+            if (a.stage_fill) {
+              tma_load_3d(reg, tm_stage, b, x * 64, kvh, s * a.B_cache);
+              tma_load_3d(reg + a.B_cache * 128, tm_blk, b, x * 64, kvh, s * a.B);
+            } else {
+              tma_load_3d(reg, tm_blk, b, x * 64, kvh, s * a.B);
+            }
+          }
         }
       };
     };
     if (is_v)
-      flash::load_ring<D>(bar, smem, n_total, a.status, true, issue(&tm_vp, &tm_vb));
+      flash::load_ring<D>(bar, smem, n_total, a.status, true, issue(&tm_vp, &tm_vb, &tm_vs));
     else
-      flash::load_ring<D>(bar, smem, n_total, a.status, false, issue(&tm_kp, &tm_kb));
+      flash::load_ring<D>(bar, smem, n_total, a.status, false, issue(&tm_kp, &tm_kb, &tm_ks));
     if (!is_v && lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
     if (st_flags && a.status) atomicOr(a.status, st_flags);
   } else if (warp == 1 || warp == flash::PV_ISSUER_WARP) {
@@ -289,8 +313,8 @@ __global__ void __launch_bounds__(1024) decode_order_kernel(const int32_t* __res
 
 template <int D>
 cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
-                      const uint16_t* k_pool, const uint16_t* v_pool, DecodeArgs& a, int batch,
-                      cudaStream_t stream) {
+                      const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* k_stage,
+                      const uint16_t* v_stage, DecodeArgs& a, int batch, cudaStream_t stream) {
   using S = flash::Smem<D>;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
   {
@@ -316,15 +340,24 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* 
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.hkv, (uint64_t)batch * a.B};
     const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.hkv * D * 2};
-    const uint32_t box[3] = {64, 1, BKV};
+    const uint32_t box[3] = {64, 1, (uint32_t)(a.stage_fill ? BKV - a.B_cache : BKV)};
     if (!encode_tmap_bf16(&tkb, k_blk, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (!encode_tmap_bf16(&tvb, v_blk, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  CUtensorMap tks = tkb, tvs = tvb;        // unused without a block buffer
+  if (a.stage_fill) {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.hkv, (uint64_t)batch * a.B_cache};
+    const uint64_t str[2] = {(uint64_t)D * 2, (uint64_t)a.hkv * D * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)a.B_cache};
+    if (!encode_tmap_bf16(&tks, k_stage, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap_bf16(&tvs, v_stage, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(decode_tc_kernel<D>, S::TOTAL, attr);
   if (ea != cudaSuccess) return ea;
   dim3 grid(a.nsplit, a.hkv, batch);
-  decode_tc_kernel<D><<<grid, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tkp, tvp, tkb, tvb, a);
+  decode_tc_kernel<D><<<grid, flash::NUM_THREADS, S::TOTAL, stream>>>(tq, tkp, tvp, tkb, tvb,
+                                                                      tks, tvs, a);
   if (a.nsplit > 1) {
     dim3 cgrid((a.hq * a.B + 7) / 8, batch);
     decode_combine_kernel<D><<<cgrid, 256, 0, stream>>>(a);
@@ -368,7 +401,9 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
                                const int32_t* block_table, int max_pages,
                                const int32_t* seq_lens, const DecodePlan& plan, float* o,
                                int batch, int B, int hq, int hkv, int d, float scale,
-                               void* workspace, int32_t* status, cudaStream_t stream) {
+                               void* workspace, int32_t* status, cudaStream_t stream,
+                               const uint16_t* k_stage, const uint16_t* v_stage,
+                               const int32_t* stage_fill, int B_cache) {
   int32_t* order = plan.ordered ? static_cast<int32_t*>(workspace) : nullptr;
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.order_bytes);
   if (order) {
@@ -377,9 +412,11 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
   }
   DecodeArgs a{block_table, seq_lens, order, part, o, status, num_pages, max_pages, B, hq,
                hkv, hq / hkv, plan.rows, plan.split_len, plan.nsplit,
-               scale * 1.4426950408889634f};
-  const cudaError_t e = d == 64 ? launch_tc<64>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream)
-                                : launch_tc<128>(q, k_blk, v_blk, k_pool, v_pool, a, batch, stream);
+               scale * 1.4426950408889634f, stage_fill, stage_fill ? B_cache : 0};
+  const cudaError_t e =
+      d == 64 ? launch_tc<64>(q, k_blk, v_blk, k_pool, v_pool, k_stage, v_stage, a, batch, stream)
+              : launch_tc<128>(q, k_blk, v_blk, k_pool, v_pool, k_stage, v_stage, a, batch,
+                               stream);
   count_launches(plan.nsplit > 1 ? 2 : 1);
   return e;
 }

@@ -21,6 +21,15 @@ cudaError_t launch_kv_commit(const uint16_t* k_blk, const uint16_t* v_blk,
                              int batch, int B, int hkv, int d, bool batch_sync,
                              int32_t* status, cudaStream_t stream);
 
+// ---- Block-level commit with a B_cache boundary (block buffer, batch-wide flush).
+cudaError_t launch_kv_commit_block(const uint16_t* k_blk, const uint16_t* v_blk,
+                                   const int32_t* n_accept, int32_t* seq_lens, int32_t* fill,
+                                   uint16_t* k_stage, uint16_t* v_stage, int B_cache,
+                                   int32_t* sync, const int32_t* block_table, int max_pages,
+                                   uint16_t* k_pool, uint16_t* v_pool, int num_pages,
+                                   int32_t* commit_slots, int batch, int B, int hkv, int d,
+                                   int32_t* status, cudaStream_t stream);
+
 // ---- Decode attention: split-KV partials then a combine pass.
 struct DecodePlan {
   int split_len;   // keys per split (multiple of 128)
@@ -38,7 +47,10 @@ cudaError_t launch_decode_attn(const uint16_t* q, const uint16_t* k_blk,
                                const int32_t* block_table, int max_pages,
                                const int32_t* seq_lens, const DecodePlan& plan, float* o,
                                int batch, int B, int hq, int hkv, int d, float scale,
-                               void* workspace, int32_t* status, cudaStream_t stream);
+                               void* workspace, int32_t* status, cudaStream_t stream,
+                               const uint16_t* k_stage = nullptr,
+                               const uint16_t* v_stage = nullptr,
+                               const int32_t* stage_fill = nullptr, int B_cache = 0);
 
 // ---- LM head + max-prob/argmax + acceptance.
 size_t head_workspace_bytes(int batch, int B, int vocab);
@@ -48,7 +60,8 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
                                int32_t* tokens, float* maxprob, int32_t* n_accept,
                                void* workspace, int32_t* status, cudaStream_t stream);
 
-// ---- Gradient of the dual-stream attention (cuBLAS products, materialised per kv group).
+// ---- Gradient of the dual-stream attention: a statistics-only forward run, then the
+// tcgen05 dK/dV kernel over key tiles and the row-parallel tcgen05 dQ kernel.
 size_t dual_grad_workspace_bytes(int batch, int L, int B, int hq, int hkv, int d);
 cudaError_t launch_dual_stream_grad(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                     const float* o, const float* d_o, int batch, int L, int B,

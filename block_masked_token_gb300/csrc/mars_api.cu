@@ -140,6 +140,44 @@ int mars_decode_attn(const mars_bf16* q, const mars_bf16* k_blk, const mars_bf16
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int mars_decode_attn_block_cache(const mars_bf16* q, const mars_bf16* k_blk,
+                                 const mars_bf16* v_blk, const mars_bf16* k_pool,
+                                 const mars_bf16* v_pool, int num_pages,
+                                 const int32_t* block_table, int max_pages_per_seq,
+                                 const int32_t* seq_lens, int max_len_hint,
+                                 const mars_bf16* k_stage, const mars_bf16* v_stage,
+                                 const int32_t* block_fill, int B_cache, float* o, int batch,
+                                 int B, int hq, int hkv, int d, int page_size, float scale,
+                                 void* workspace, size_t ws_bytes, int32_t* status,
+                                 void* stream) {
+  if (batch < 0 || B < 1 || B > 32 || max_len_hint < 0 || num_pages < 0 ||
+      max_pages_per_seq < 0)
+    return MARS_EINVAL;
+  if (B_cache < 8 || B_cache > 64 || B_cache % 8) return MARS_EUNSUPPORTED;
+  int rc = check_heads(hq, hkv, d);
+  if (rc) return rc;
+  if (page_size != mars::kPageSize) return MARS_EUNSUPPORTED;
+  if ((hq / hkv) * B > kMaxDecodeRows) return MARS_EUNSUPPORTED;
+  if (batch == 0) return MARS_OK;
+  if (!q || !k_blk || !v_blk || !o || !seq_lens || !workspace || !k_stage || !v_stage ||
+      !block_fill)
+    return MARS_EINVAL;
+  if (max_pages_per_seq > 0 && (!k_pool || !v_pool || !block_table)) return MARS_EINVAL;
+  if (!aligned16(q) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(o) ||
+      !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(workspace) ||
+      !aligned16(k_stage) || !aligned16(v_stage))
+    return MARS_EALIGN;
+  const mars::DecodePlan plan = mars::plan_decode(batch, B, hq, hkv, d, max_len_hint);
+  if (ws_bytes < plan.ws_bytes) return MARS_ENOSPACE;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+  if (isinf(scale)) return MARS_EINVAL;
+  return cuda_rc(mars::launch_decode_attn(q, k_blk, v_blk, k_pool, v_pool, num_pages,
+                                          block_table, max_pages_per_seq, seq_lens, plan, o,
+                                          batch, B, hq, hkv, d, scale, workspace, status,
+                                          static_cast<cudaStream_t>(stream), k_stage, v_stage,
+                                          block_fill, B_cache));
+}
+
 namespace {
 
 int head_accept_checked(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
@@ -216,6 +254,31 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
   return kv_commit_checked(k_blk, v_blk, n_accept, seq_lens, block_table, max_pages_per_seq,
                            k_pool, v_pool, num_pages, commit_slots, batch, B, hkv, d,
                            page_size, true, status, stream);
+}
+
+int mars_kv_commit_block(const mars_bf16* k_blk, const mars_bf16* v_blk,
+                         const int32_t* n_accept, int32_t* seq_lens, int32_t* block_fill,
+                         mars_bf16* k_stage, mars_bf16* v_stage, int B_cache,
+                         int32_t* sync_state, const int32_t* block_table,
+                         int max_pages_per_seq, mars_bf16* k_pool, mars_bf16* v_pool,
+                         int num_pages, int32_t* commit_slots, int batch, int B, int hkv,
+                         int d, int page_size, int32_t* status, void* stream) {
+  if (batch < 0 || B < 1 || B > 32 || hkv < 1 || num_pages < 0 || max_pages_per_seq < 0)
+    return MARS_EINVAL;
+  if (B_cache < 8 || B_cache > 64 || B_cache % 8) return MARS_EUNSUPPORTED;
+  if (d != 64 && d != 128) return MARS_EUNSUPPORTED;
+  if (page_size != mars::kPageSize) return MARS_EUNSUPPORTED;
+  if (batch == 0) return MARS_OK;
+  if (!k_blk || !v_blk || !n_accept || !seq_lens || !block_fill || !k_stage || !v_stage ||
+      !sync_state || !block_table || !k_pool || !v_pool)
+    return MARS_EINVAL;
+  if (!aligned16(k_blk) || !aligned16(v_blk) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      !aligned16(k_stage) || !aligned16(v_stage))
+    return MARS_EALIGN;
+  return cuda_rc(mars::launch_kv_commit_block(
+      k_blk, v_blk, n_accept, seq_lens, block_fill, k_stage, v_stage, B_cache, sync_state,
+      block_table, max_pages_per_seq, k_pool, v_pool, num_pages, commit_slots, batch, B, hkv,
+      d, status, static_cast<cudaStream_t>(stream)));
 }
 
 namespace {

@@ -19,6 +19,7 @@ OK, EINVAL, EALIGN, EUNSUPPORTED, ECUDA, ENOSPACE = 0, -1, -2, -3, -4, -5
 ST_NOPAGE, ST_OVERFLOW, ST_TIMEOUT, ST_BADTARGET = 1, 2, 4, 8
 OP_DECODE_ATTN, OP_HEAD_ACCEPT, OP_CE_LOSS, OP_CE_LOSS_GRAD, OP_DUAL_GRAD = 1, 2, 3, 4, 5
 PAGE_SIZE = 16
+BLOCK_SYNC_WORDS = 4
 
 
 class MarsError(RuntimeError):
@@ -51,6 +52,12 @@ def lib() -> ctypes.CDLL:
         L.mars_kv_commit.argtypes = [P, P, P, P, P, I, P, P, I, P, I, I, I, I, I, P, P]
         L.mars_kv_commit_batch_sync.restype = I
         L.mars_kv_commit_batch_sync.argtypes = L.mars_kv_commit.argtypes
+        L.mars_kv_commit_block.restype = I
+        L.mars_kv_commit_block.argtypes = [P, P, P, P, P, P, P, I, P, P, I, P, P, I, P, I, I, I,
+                                           I, I, P, P]
+        L.mars_decode_attn_block_cache.restype = I
+        L.mars_decode_attn_block_cache.argtypes = [P, P, P, P, P, I, P, I, P, I, P, P, P, I, P,
+                                                   I, I, I, I, I, I, F, P, S, P, P]
         L.mars_dual_stream_ce_loss.restype = I
         L.mars_dual_stream_ce_loss.argtypes = [P, P, P, I, I, I, I, P, P, P, P, S, P, P]
         L.mars_attn_dual_stream_grad.restype = I
@@ -77,7 +84,8 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("mars_workspace_bytes", "mars_attn_dual_stream", "mars_decode_attn",
             "mars_head_accept", "mars_head_accept_per_request", "mars_kv_commit",
-            "mars_kv_commit_batch_sync", "mars_dual_stream_ce_loss",
+            "mars_kv_commit_batch_sync", "mars_kv_commit_block", "mars_decode_attn_block_cache",
+            "mars_dual_stream_ce_loss",
             "mars_dual_stream_ce_loss_grad", "mars_attn_dual_stream_grad",
             "mars_attn_dual_stream_lse", "mars_attn_dual_stream_grad_lse",
             "mars_check_wait_timeout", "mars_strerror",
@@ -238,6 +246,68 @@ def mars_kv_commit_batch_sync(k_blk, v_blk, n_accept, seq_lens, block_table, k_p
                               commit_slots=None, status=None, stream=None):
     _kv_commit(lib().mars_kv_commit_batch_sync, "mars_kv_commit_batch_sync", k_blk, v_blk,
                n_accept, seq_lens, block_table, k_pool, v_pool, commit_slots, status, stream)
+
+
+def mars_kv_commit_block(k_blk, v_blk, n_accept, seq_lens, block_fill, k_stage, v_stage,
+                         sync_state, block_table, k_pool, v_pool, commit_slots=None,
+                         status=None, stream=None):
+    """Block-level commit with a B_cache boundary (B_cache = k_stage.shape[1]); the state
+    tensors seq_lens, block_fill, sync_state (and the stage) persist between calls."""
+    b, B, hkv, d = k_blk.shape
+    B_cache = k_stage.shape[1]
+    num_pages = k_pool.shape[0]
+    _check(k_blk, "k_blk", torch.bfloat16)
+    _check(v_blk, "v_blk", torch.bfloat16, (b, B, hkv, d))
+    _check(n_accept, "n_accept", torch.int32, (b,))
+    _check(seq_lens, "seq_lens", torch.int32, (b,))
+    _check(block_fill, "block_fill", torch.int32, (b,))
+    _check(k_stage, "k_stage", torch.bfloat16, (b, B_cache, hkv, d))
+    _check(v_stage, "v_stage", torch.bfloat16, (b, B_cache, hkv, d))
+    _check(sync_state, "sync_state", torch.int32, (BLOCK_SYNC_WORDS,))
+    _check(block_table, "block_table", torch.int32)
+    _check(k_pool, "k_pool", torch.bfloat16, (num_pages, hkv, PAGE_SIZE, d))
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, hkv, PAGE_SIZE, d))
+    if commit_slots is not None:
+        _check(commit_slots, "commit_slots", torch.int32, (b, B))
+    if status is not None:
+        _check(status, "status", torch.int32, (1,))
+    _rc(lib().mars_kv_commit_block(_ptr(k_blk), _ptr(v_blk), _ptr(n_accept), _ptr(seq_lens),
+                                   _ptr(block_fill), _ptr(k_stage), _ptr(v_stage), B_cache,
+                                   _ptr(sync_state), _ptr(block_table), block_table.shape[1],
+                                   _ptr(k_pool), _ptr(v_pool), num_pages, _ptr(commit_slots),
+                                   b, B, hkv, d, PAGE_SIZE, _ptr(status), _stream(stream)),
+        "mars_kv_commit_block")
+
+
+def mars_decode_attn_block_cache(q, k_blk, v_blk, k_pool, v_pool, block_table, seq_lens,
+                                 max_len_hint: int, k_stage, v_stage, block_fill, o, workspace,
+                                 status=None, scale: float = 0.0, stream=None):
+    """mars_decode_attn with the block buffers of mars_kv_commit_block between the prefix
+    and the block keys (B_cache = k_stage.shape[1])."""
+    b, B, hq, d = q.shape
+    hkv = k_blk.shape[2]
+    num_pages = k_pool.shape[0]
+    B_cache = k_stage.shape[1]
+    _check(q, "q", torch.bfloat16)
+    _check(k_blk, "k_blk", torch.bfloat16, (b, B, hkv, d))
+    _check(v_blk, "v_blk", torch.bfloat16, (b, B, hkv, d))
+    _check(k_pool, "k_pool", torch.bfloat16, (num_pages, hkv, PAGE_SIZE, d))
+    _check(v_pool, "v_pool", torch.bfloat16, (num_pages, hkv, PAGE_SIZE, d))
+    _check(block_table, "block_table", torch.int32)
+    _check(seq_lens, "seq_lens", torch.int32, (b,))
+    _check(k_stage, "k_stage", torch.bfloat16, (b, B_cache, hkv, d))
+    _check(v_stage, "v_stage", torch.bfloat16, (b, B_cache, hkv, d))
+    _check(block_fill, "block_fill", torch.int32, (b,))
+    _check(o, "o", torch.float32, (b, B, hq, d))
+    _check(workspace, "workspace", torch.uint8)
+    if status is not None:
+        _check(status, "status", torch.int32, (1,))
+    _rc(lib().mars_decode_attn_block_cache(
+        _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(k_pool), _ptr(v_pool), num_pages,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_len_hint),
+        _ptr(k_stage), _ptr(v_stage), _ptr(block_fill), B_cache, _ptr(o), b, B, hq, hkv, d,
+        PAGE_SIZE, float(scale), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream(stream)), "mars_decode_attn_block_cache")
 
 
 def mars_dual_stream_ce_loss(h, w, targets, batch: int, L: int, loss, workspace, row_ce=None,

@@ -203,6 +203,66 @@ int mars_kv_commit_batch_sync(const mars_bf16* k_blk, const mars_bf16* v_blk,
                               int32_t* commit_slots, int batch, int B, int hkv, int d,
                               int page_size, int32_t* status, void* stream);
 
+/* Words of the device state that mars_kv_commit_block keeps between calls. */
+#define MARS_BLOCK_SYNC_WORDS 4
+
+/* Block-level commit with a batch-wide B_cache boundary ([notes] Key design 4: the prefix
+ * cache is frozen in blocks of B_cache tokens; within a batch, a sample that has filled
+ * its block waits at the boundary until every sample has filled it, and then the whole
+ * block is written to the persistent prefix cache; [gist] 2.D: the cache is updated only
+ * when a full block of tokens has been accepted across all samples of the batch).
+ * State, all device memory owned by the caller and zeroed by it before the first call:
+ *   seq_lens    [batch] int32   tokens of each sequence in the persistent cache (the pool)
+ *   block_fill  [batch] int32   accepted tokens held in the sequence's block buffer
+ *   k_stage, v_stage [batch, B_cache, hkv, d] bf16   the block buffers (row i = the i-th
+ *               accepted token of the current block); contents need no initialisation
+ *   sync_state  [MARS_BLOCK_SYNC_WORDS] int32        batch-wide flags (zeroed once)
+ * One call, for every sequence s:
+ *   1. if every block was full after the previous call, block rows 0..B_cache-1 are
+ *      written to the pool at positions seq_lens[s] .. seq_lens[s] + B_cache - 1 (page =
+ *      block_table[s][pos / page_size], slot = pos % page_size), seq_lens[s] += B_cache
+ *      and block_fill[s] = 0. (Whether every block is full is known only after every
+ *      sequence of a call has taken its rows; the kernel records it without any wait
+ *      and the next call writes the blocks. The decode attention of the step in between
+ *      reads the full blocks from the buffers, i.e. the same keys.)
+ *   2. it takes n = min(clamp(n_accept[s], 0, B), B_cache - block_fill[s]) accepted rows
+ *      (block rows 0..n-1 of k_blk / v_blk, [batch, B, hkv, d]) into buffer rows
+ *      block_fill[s] .. block_fill[s] + n - 1: a sequence whose block is full takes none
+ *      and waits. commit_slots[s][i] (may be NULL) = page * page_size + slot of position
+ *      seq_lens[s] + block_fill[s] + i, where row i will be written with its block, for
+ *      i < n, and -1 otherwise; block_fill[s] += n.
+ * A page that is unmapped (entry < 0 or >= num_pages, or past max_pages_per_seq) flags
+ * MARS_ST_NOPAGE / MARS_ST_OVERFLOW: a block's write stops before a row on such a page
+ * (seq_lens advances by the rows written, the rest of the block is dropped), and an
+ * accepted row whose position falls on one is not taken, nor are the rows after it.
+ * 8 <= B_cache <= 64, B_cache % 8 == 0; page_size must be 16. Calls must be ordered on one
+ * stream (each reads the state the previous one wrote). The decode attention over this
+ * cache is mars_decode_attn_block_cache. */
+int mars_kv_commit_block(const mars_bf16* k_blk, const mars_bf16* v_blk,
+                         const int32_t* n_accept, int32_t* seq_lens, int32_t* block_fill,
+                         mars_bf16* k_stage, mars_bf16* v_stage, int B_cache,
+                         int32_t* sync_state, const int32_t* block_table,
+                         int max_pages_per_seq, mars_bf16* k_pool, mars_bf16* v_pool,
+                         int num_pages, int32_t* commit_slots, int batch, int B, int hkv,
+                         int d, int page_size, int32_t* status, void* stream);
+
+/* mars_decode_attn over the block-level cache of mars_kv_commit_block ([notes] Key design
+ * 3 and 4; [gist] 2.C, 2.D): the keys of sequence s are its seq_lens[s] prefix tokens in
+ * the paged pool, then the block_fill[s] accepted tokens of its block buffer (k_stage /
+ * v_stage rows 0..block_fill[s]-1), then the B block keys of this step; block query k
+ * sees the prefix, the buffered tokens and block keys 0..k. Arguments, layouts, workspace
+ * and errors as mars_decode_attn; 8 <= B_cache <= 64, B_cache % 8 == 0. */
+int mars_decode_attn_block_cache(const mars_bf16* q, const mars_bf16* k_blk,
+                                 const mars_bf16* v_blk, const mars_bf16* k_pool,
+                                 const mars_bf16* v_pool, int num_pages,
+                                 const int32_t* block_table, int max_pages_per_seq,
+                                 const int32_t* seq_lens, int max_len_hint,
+                                 const mars_bf16* k_stage, const mars_bf16* v_stage,
+                                 const int32_t* block_fill, int B_cache, float* o, int batch,
+                                 int B, int hq, int hkv, int d, int page_size, float scale,
+                                 void* workspace, size_t ws_bytes, int32_t* status,
+                                 void* stream);
+
 /* Gradient of mars_attn_dual_stream (the training step's backward of the attention under
  * M, [notes] Key design 1 and overall framework): for upstream gradient dO, per (batch,
  * query head) with P = softmax(scale Q K^T + M): dQ = scale dS K, and per kv head

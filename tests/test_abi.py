@@ -130,6 +130,22 @@ def test_host_validation_codes(L):
         assert fn(P, P, P, P, P, 4, None, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EINVAL
         assert fn(P, P, P, P, P, 4, P, P, 10, None, 2, 33, 2, 64, 16, None, None) == mars.EINVAL
         assert fn(P, P, P, P, P, 4, P, P, 10, None, 0, 4, 2, 64, 16, None, None) == mars.OK
+    # block-level commit: B_cache range and alignment, null state, page size, misaligned stage
+    cb = L.mars_kv_commit_block
+    for bc in (4, 12, 72):
+        assert cb(P, P, P, P, P, P, P, bc, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EUNSUPPORTED
+    assert cb(P, P, P, P, P, P, P, 16, None, P, 4, P, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EINVAL
+    assert cb(P, P, P, P, None, P, P, 16, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EINVAL
+    assert cb(P, P, P, P, P, P, P, 16, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 8, None, None) == mars.EUNSUPPORTED
+    assert cb(P, P, P, P, P, _p(24), P, 16, P, P, 4, P, P, 10, None, 2, 4, 2, 64, 16, None, None) == mars.EALIGN
+    assert cb(P, P, P, P, P, P, P, 16, P, P, 4, P, P, 10, None, 0, 4, 2, 64, 16, None, None) == mars.OK
+    # decode over the block-level cache: B_cache range, null block_fill, workspace too small
+    da = [P, P, P, P, P, 10, P, 4, P, 64]
+    tail = [P, 2, 4, 4, 2, 64, 16, 0.0, P]
+    assert L.mars_decode_attn_block_cache(*da, P, P, P, 20, *tail, 1 << 30, None, None) == mars.EUNSUPPORTED
+    assert L.mars_decode_attn_block_cache(*da, P, P, None, 16, *tail, 1 << 30, None, None) == mars.EINVAL
+    assert L.mars_decode_attn_block_cache(*da, P, P, P, 16, *tail, 16, None, None) == mars.ENOSPACE
+    assert L.mars_decode_attn_block_cache(*da, _p(20), P, P, 16, *tail, 1 << 30, None, None) == mars.EALIGN
 
 
 def test_binding_rejects_cpu_tensors(L):
@@ -185,6 +201,14 @@ def test_every_binding_rejects_cpu_tensors(L):
         "mars_kv_commit_batch_sync":
             lambda: mars.mars_kv_commit_batch_sync(blk, blk, i32(1), i32(1), i32(1, 4), pool,
                                                    pool),
+        "mars_kv_commit_block":
+            lambda: mars.mars_kv_commit_block(blk, blk, i32(1), i32(1), i32(1), bf(1, 16, 1, 64),
+                                              bf(1, 16, 1, 64), i32(4), i32(1, 4), pool, pool),
+        "mars_decode_attn_block_cache":
+            lambda: mars.mars_decode_attn_block_cache(bf(1, 4, 2, 64), blk, blk, pool, pool,
+                                                      i32(1, 4), i32(1), 64, bf(1, 16, 1, 64),
+                                                      bf(1, 16, 1, 64), i32(1), z(1, 4, 2, 64),
+                                                      ws),
         "mars_dual_stream_ce_loss":
             lambda: mars.mars_dual_stream_ce_loss(bf(8, 64), bf(96, 64), i32(8), 1, 4, z(3), ws),
         "mars_dual_stream_ce_loss_grad":
