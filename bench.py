@@ -224,7 +224,7 @@ def ce_flops(cfg):
 def run_ce(device, peaks, reps=5, warm=3):
     """The dual-stream training loss at the 7B head shape (LM-head GEMM over 2L rows with
     the cross-entropy fused into its epilogue), and its gradient (the GEMM again with a
-    dlogits epilogue, then dh and dW as two cuBLAS GEMMs). W (1.09 GB) and h (117 MB)
+    dlogits epilogue, then dh and dW as two tcgen05 GEMMs). W (1.09 GB) and h (117 MB)
     exceed L2."""
     from block_masked_token_gb300 import mars
     cfg = W.CE_LOSS_7B
@@ -271,7 +271,7 @@ def run_ce(device, peaks, reps=5, warm=3):
            "loss": [float(v) for v in loss.cpu()],
            "grad_ms": tg * 1e3, "grad_tflops": tfg,
            "grad_note": "GEMM with dlogits epilogue (bf16 dlogits written, 5 GB) + dh and dW "
-                        "(cuBLAS); 3 x 2*rows*H*V flop",
+                        "(tcgen05 GEMMs reading dlogits, W and h in place); 3 x 2*rows*H*V flop",
            "l2": "inputs larger than L2 (W 1.09 GB + h 117 MB)"}
     del x, ws, wg, dh, dw
     torch.cuda.empty_cache()
@@ -726,11 +726,27 @@ def run_case(args):
         ws = torch.empty(mars.mars_workspace_bytes(mars.OP_CE_LOSS, cfg.batch, 1,
                                                    vocab=cfg.vocab, max_len=cfg.L),
                          dtype=torch.uint8, device=device)
+        if args.case == "ce_grad":
+            rows = cfg.batch * 2 * cfg.L
+            lse = torch.empty(rows, dtype=torch.float32, device=device)
+            mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L, loss,
+                                          ws, row_lse=lse)
+            del ws
+            wg = torch.empty(mars.mars_workspace_bytes(mars.OP_CE_LOSS_GRAD, cfg.batch, 1,
+                                                       vocab=cfg.vocab, max_len=cfg.L),
+                             dtype=torch.uint8, device=device)
+            dh = torch.empty(rows, cfg.hidden, dtype=torch.float32, device=device)
+            dw = torch.empty(cfg.vocab, cfg.hidden, dtype=torch.float32, device=device)
 
-        def call():
-            mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L,
-                                          loss, ws)
-        work = {"flop": ce_flops(cfg)}
+            def call():
+                mars.mars_dual_stream_ce_loss_grad(x["h"], x["w"], x["targets"], lse, cfg.batch,
+                                                   cfg.L, wg, dh, dw)
+            work = {"flop": 3 * ce_flops(cfg)}
+        else:
+            def call():
+                mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L,
+                                              loss, ws)
+            work = {"flop": ce_flops(cfg)}
     elif isinstance(cfg, W.DualStreamConfig):
         x = W.make_dual_stream_inputs(cfg, seed=0, device=device)
         o = torch.empty(x["q"].shape, dtype=torch.float32, device=device)
@@ -798,7 +814,8 @@ def run_case(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["head", "decode", "dual", "dual_grad", "dual_grad_lse", "ce"], default=None,
+    ap.add_argument("--case", choices=["head", "decode", "dual", "dual_grad", "dual_grad_lse", "ce",
+                                       "ce_grad"], default=None,
                     help="time one entry point on --config instead of the decode step")
     ap.add_argument("--config", default=None, choices=sorted(W.CONFIGS))
     ap.add_argument("--gpus", type=int, default=1)

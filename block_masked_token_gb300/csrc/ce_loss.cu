@@ -18,13 +18,11 @@
 // Gradient: dL/dl_rv = (softmax(l_r)_v - [v = y_r]) / N_x for a row of stream x with a
 // target (N_x = that stream's rows with a target), 0 for the others. The head GEMM is run
 // again with an epilogue that writes this dlogits tile in bf16 (using the forward's
-// per-row log-sum-exp), then two plain GEMMs go to cuBLAS: dh = dlogits W and
-// dW = dlogits^T h, both accumulated in fp32.
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// per-row log-sum-exp), then the tcgen05 GEMM of gemm_tc.cuh forms dh = dlogits W and
+// dW = dlogits^T h from it in place (fp32 accumulation and output): W and h are read as
+// MN-major operands and, for dW, dlogits as well, so nothing is transposed in memory.
 #include "common.cuh"
+#include "gemm_tc.cuh"
 #include "head_gemm_tc.cuh"
 #include "internal.h"
 
@@ -136,15 +134,39 @@ __global__ void __launch_bounds__(256) ce_scale_kernel(const int32_t* __restrict
   if (threadIdx.x < 2) scale[threadIdx.x] = s_cnt[threadIdx.x][0] ? 1.f / s_cnt[threadIdx.x][0] : 0.f;
 }
 
-// One cuBLAS handle per device, created on first use; calls are serialised because a
-// handle carries its stream.
-struct Blas {
-  std::mutex mu;
-  cublasHandle_t h[64] = {};
-};
-Blas& blas() {
-  static Blas b;
-  return b;
+// C [M, N] (ldc = N) = A B with the tcgen05 GEMM; the maps hold A and B in the layouts
+// its template arguments name.
+template <bool A_MN, bool B_MN>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                        float* c, int32_t* status, cudaStream_t stream) {
+  using namespace gemm_tc;
+  Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_m = (M + BM - 1) / BM;
+  p.num_n = (N + BN - 1) / BN;
+  p.num_k = (K + BK - 1) / BK;
+  p.num_tiles = p.num_m * p.num_n;
+  p.c = c;
+  p.ldc = N;
+  p.status = status;
+  static std::atomic<int> attr[64];
+  const cudaError_t ea = set_smem_limit_once(gemm_kernel<A_MN, B_MN>, (int)SMEM_BYTES, attr);
+  if (ea != cudaSuccess) return ea;
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  gemm_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// 2D bf16 tensor map of a row-major [outer, inner] matrix with box {box_inner, box_outer}.
+bool map2d(CUtensorMap* m, const void* base, int inner, int outer, uint32_t box_inner,
+           uint32_t box_outer) {
+  const uint64_t dims[2] = {(uint64_t)inner, (uint64_t)outer};
+  const uint64_t strides[1] = {(uint64_t)inner * 2};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_tmap_bf16(m, base, 2, dims, strides, box);
 }
 
 size_t grad_dlogits_bytes(int batch, int L, int vocab) {
@@ -204,29 +226,26 @@ cudaError_t launch_ce_loss_grad(const uint16_t* h, const uint16_t* w, const int3
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || (!dh && !dw)) return e;
 
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  Blas& b = blas();
-  std::lock_guard<std::mutex> lock(b.mu);
-  if (!b.h[dev] && cublasCreate(&b.h[dev]) != CUBLAS_STATUS_SUCCESS) {
-    b.h[dev] = nullptr;
-    return cudaErrorInitializationError;
+  // dh [rows, H] = dlogits [rows, V] . W [V, H]: A K-major, B (W) MN-major
+  if (dh) {
+    CUtensorMap ta, tb;
+    if (!map2d(&ta, dlogits, vocab, rows, gemm_tc::BK, gemm_tc::BM) ||
+        !map2d(&tb, w, hidden, vocab, 64, gemm_tc::BK))
+      return cudaErrorInvalidValue;
+    if ((e = launch_gemm<false, true>(ta, tb, rows, hidden, vocab, dh, status, stream)) !=
+        cudaSuccess)
+      return e;
   }
-  cublasHandle_t hb = b.h[dev];
-  if (cublasSetStream(hb, stream) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  const float one = 1.f, zero = 0.f;
-  // row-major C = A B is column-major C^T = B^T A^T
-  if (dh &&  // dh [rows, H] = dlogits [rows, V] . W [V, H]
-      cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_N, hidden, rows, vocab, &one, w, CUDA_R_16BF,
-                   hidden, dlogits, CUDA_R_16BF, vocab, &zero, dh, CUDA_R_32F, hidden,
-                   CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorUnknown;
-  if (dw &&  // dW [V, H] = dlogits^T [V, rows] . h [rows, H]
-      cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_T, hidden, vocab, rows, &one, h, CUDA_R_16BF,
-                   hidden, dlogits, CUDA_R_16BF, vocab, &zero, dw, CUDA_R_32F, hidden,
-                   CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorUnknown;
+  // dW [V, H] = dlogits^T [V, rows] . h [rows, H]: both operands MN-major
+  if (dw) {
+    CUtensorMap ta, tb;
+    if (!map2d(&ta, dlogits, vocab, rows, 64, gemm_tc::BK) ||
+        !map2d(&tb, h, hidden, rows, 64, gemm_tc::BK))
+      return cudaErrorInvalidValue;
+    if ((e = launch_gemm<true, true>(ta, tb, vocab, hidden, rows, dw, status, stream)) !=
+        cudaSuccess)
+      return e;
+  }
   return cudaSuccess;
 }
 

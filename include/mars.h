@@ -325,7 +325,8 @@ int mars_dual_stream_ce_loss(const mars_bf16* h, const mars_bf16* w, const int32
  * target (N_x = the rows of that stream with a target) and 0 for the others;
  * dh = dlogits W, dW = dlogits^T h. The logits are recomputed by the LM-head GEMM, whose
  * epilogue writes dlogits in bf16 to the workspace using row_lse from the forward call;
- * the two products are plain cuBLAS GEMMs (bf16 inputs, fp32 accumulate and output).
+ * the two products run on the library's tcgen05 GEMM, which reads dlogits, W and h in
+ * place (bf16 inputs, fp32 accumulate and output).
  *   row_lse   [batch*2L] float          from mars_dual_stream_ce_loss
  *   dh        [batch*2L, hidden] float or NULL (written)
  *   dw        [vocab, hidden] float or NULL    (written)
