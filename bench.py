@@ -37,11 +37,12 @@ from block_masked_token_gb300 import workloads as W  # noqa: E402
 METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TFLOP/s"
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
-# of the kernel as it is now; the summaries and commands are in profiles/. Reset to None
-# whenever the kernel changes, until it is captured again.
-TRAFFIC_HEAD_GEMM = 1124735872         # profiles/head_gemm_sustained_decode_7b_b128_B16.md
-TRAFFIC_DECODE_STEP0 = 1365705088      # profiles/decode_tc_sustained_decode_7b_b128_B16.md
-TRAFFIC_DUAL_STREAM = 330413824        # profiles/dual_stream_persistent_dual_stream_7b_b2_2L8192_B16.md
+# of the kernel as it is now, on the workload named beside each: the LM-head GEMM at 2048
+# rows, decode attention on step 0 of the sustained workload, the dual-stream forward at
+# 2L = 8192. None whenever the kernel has changed since its capture.
+TRAFFIC_HEAD_GEMM = 1124735872         # head_gemm_kernel, sustained decode, 2048 rows
+TRAFFIC_DECODE_STEP0 = None            # decode_tc_kernel, sustained decode, step 0
+TRAFFIC_DUAL_STREAM = 330413824        # dual_stream_persistent_kernel, 2L = 8192
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
 
@@ -372,7 +373,7 @@ def run_gpu(args, rank, world, local):
     elapsed = start.elapsed_time(stop) / 1e3
     n_acc = runner.n_acc[: min(K, cfg.steps)].to(torch.int64)
     steps_done = K
-    tok_local = float(n_acc.sum().item()) if K <= cfg.steps else float("nan")
+    tok_local = float(n_acc.sum().item())          # K <= cfg.steps (checked in main)
     status = int(runner.status.item())
     t_attn = [ev[i][0].elapsed_time(ev[i][1]) / 1e3 for i in range(K)]
     t_head = [ev[i][1].elapsed_time(ev[i][2]) / 1e3 for i in range(K)]
@@ -393,6 +394,9 @@ def run_gpu(args, rank, world, local):
 
     # ---- the same step as one CUDA graph (launch overhead removed), rank-local
     graph = run_graph_step(runner, K, Wm)
+
+    # ---- decode attention of the batch-32 7B decode workload (fewer pairs than SMs)
+    c3 = run_decode_c3(device, peaks, reps=max(5, min(K, 20)), warm=max(3, Wm))
 
     # ---- dual-stream training-form attention, same run (with the clocks it ran at: it
     # follows the head-bound decode loops, and its denominator is the burst rate)
@@ -423,6 +427,10 @@ def run_gpu(args, rank, world, local):
                        "prefix": [cfg.prefix_lo, cfg.prefix_hi], "hq": cfg.hq,
                        "hkv": cfg.hkv, "d": cfg.d, "hidden": cfg.hidden, "vocab": cfg.vocab,
                        "page_size": cfg.page_size, "taus": list(cfg.taus),
+                       "taus_timed": sorted({cfg.tau_at(i) for i in range(min(K, cfg.steps))},
+                                            reverse=True),
+                       "steps_timed": f"workload steps 0..{min(K, cfg.steps) - 1} of "
+                                      f"{cfg.steps}",
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (KV ~1.3 GB + W 1.09 GB read per step)"},
             "decode_step_us": seconds / K * 1e6 if world == 1 else elapsed / K * 1e6,
@@ -444,6 +452,7 @@ def run_gpu(args, rank, world, local):
                             "tflops": head_tflops, "frac_tensor": frac_head},
             "kv_commit": {"us_per_call": statistics.mean(t_commit) * 1e6},
             "decode_step_graph": graph,
+            "decode_attn_b32": c3,
             "dual_stream": dual,
             "ar_baseline": {**ar, "mars_over_ar": (tokens / seconds) / ar["tok_s"] / world,
                             "note": "KV-cached AR step (B=1, tau=1.0) over the same "
@@ -539,6 +548,41 @@ def run_e2e(runner, inp, cfg, K, Wm, device, dist):
     return {"value": tok / sec, "unit": "accepted tok/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "overlap": "input copy of step i+1 on a second stream during step i"}
+
+
+def run_decode_c3(device, peaks, reps=20, warm=3):
+    """Decode attention alone on the batch-32 7B decode workload (128 sequence/kv-head
+    pairs, prefixes 512..2048): CUDA events around each call, L2 flushed before each."""
+    from block_masked_token_gb300 import mars
+    cfg = W.DECODE_7B
+    inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1, with_head=False)
+    r = DecodeRunner(inp, cfg, device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def call():
+        mars.mars_decode_attn(inp.q[0], inp.k_blk[0], inp.v_blk[0], inp.k_pool, inp.v_pool,
+                              r.bt, r.seq_lens, r.max_hint, r.o, r.ws_attn, r.status)
+    for _ in range(warm):
+        call()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = _ev(), _ev()
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / 1e3)
+    t = statistics.median(ts)
+    by = decode_kv_bytes(inp.prefix_lens.tolist(), cfg)
+    gbs = by / t / 1e9
+    out = {"workload": cfg.name, "us_per_call": t * 1e6, "hbm_gbs": gbs,
+           "frac_hbm": gbs / peaks["hbm_gbs"], "algorithmic_bytes": by,
+           "device_status": int(r.status.item()),
+           "l2": "flushed (256 MB write) before each timed call"}
+    del r, inp, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_step_variant(cfg, device, K, Wm, seed):
@@ -742,6 +786,25 @@ def run_case(args):
                 mars.mars_dual_stream_ce_loss_grad(x["h"], x["w"], x["targets"], lse, cfg.batch,
                                                    cfg.L, wg, dh, dw)
             work = {"flop": 3 * ce_flops(cfg)}
+
+            def parts():
+                """Event times of the call with only dlogits, dlogits + dh, dlogits + dW."""
+                out = {}
+                for name, a, b in (("dlogits", None, None), ("dlogits_dh", dh, None),
+                                   ("dlogits_dw", None, dw)):
+                    ts = []
+                    for _ in range(max(args.steps, 2)):
+                        flush.fill_(1)
+                        e0, e1 = _ev(), _ev()
+                        e0.record()
+                        mars.mars_dual_stream_ce_loss_grad(x["h"], x["w"], x["targets"], lse,
+                                                           cfg.batch, cfg.L, wg, a, b)
+                        e1.record()
+                        torch.cuda.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1e3)
+                    out[name + "_us"] = statistics.median(ts)
+                return out
+            work["parts"] = parts
         else:
             def call():
                 mars.mars_dual_stream_ce_loss(x["h"], x["w"], x["targets"], cfg.batch, cfg.L,
@@ -795,16 +858,19 @@ def run_case(args):
     for _ in range(args.warmup):
         call()
     times = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        a, b = _ev(), _ev()
-        a.record()
-        call()
-        b.record()
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b) / 1e3)
+    with ClockSampler(0) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = _ev(), _ev()
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+        extra = work["parts"]() if "parts" in work else {}
     t = statistics.median(times)
-    out = {"case": args.case, "workload": cfg.name, "us": t * 1e6}
+    out = {"case": args.case, "workload": cfg.name, "us": t * 1e6, **extra,
+           "clocks": clk.summary()}
     if "flop" in work:
         out["tflops"] = work["flop"] / t / 1e12
     if "bytes" in work:

@@ -37,6 +37,11 @@ constexpr int kMinSplitKeys = 2048;
 // memory by one CTA); larger batches run in index order.
 constexpr int kMaxOrderBatch = 4096;
 constexpr int kPagesPerTile = BKV / kPageSize;   // 8
+// V-ring depth: one more than the engine's default (the decode CTA has no O staging area,
+// so Q, three K stages and three V stages fill its shared memory). With two, a V slot came
+// free only when the PV two tiles back had completed, and each tile waited about one
+// DRAM round trip of its own.
+constexpr int kVStages = 3;
 
 struct DecodeArgs {
   const int32_t* block_table;
@@ -149,7 +154,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_ks,
                  const __grid_constant__ CUtensorMap tm_vs, DecodeArgs a) {
   using namespace sm100;
-  using S = flash::Smem<D>;
+  using S = flash::Smem<D, 0, kVStages>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ flash::Barriers bar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -202,6 +207,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     s * a.B);
     }
     int st_flags = 0;
+    // block-table entry of this lane's page in prefix tile j (INT_MIN past the table); the
+    // entry of the next tile is read as each tile is issued, so its latency overlaps the
+    // wait for the next free ring slot instead of delaying that tile's copies
+    auto entry = [&](int j) -> int {
+      if (j >= pol.n_prefix || lane >= kPagesPerTile) return 0;
+      const int lp = (pol.start + j * BKV) / kPageSize + lane;
+      return lp < a.max_pages ? pol.bt_row[lp] : INT_MIN;
+    };
+    int next_entry = entry(0);
     // prefix tile j: lane i < 8 copies 16-token page i of the tile (unmapped pages load
     // page 0 and are masked by the softmax); the block tile: lane 0 copies a 128-row box
     // from row s*B of k_blk / v_blk (rows past the batch read as zeros), or, with a block
@@ -210,15 +224,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto issue = [&](const CUtensorMap* tm_pool, const CUtensorMap* tm_blk,
                      const CUtensorMap* tm_stage) {
       return [&, tm_pool, tm_blk, tm_stage](int j, uint8_t* dst, uint64_t* b) {
+        const int e = next_entry;
+        next_entry = entry(j + 1);
         if (j < pol.n_prefix) {
           if (lane < kPagesPerTile) {
             const int kp = pol.start + j * BKV + lane * kPageSize;
-            const int lp = kp / kPageSize;
             int page = 0;
-            if (page_ok(a, pol.bt_row, lp)) {
-              page = pol.bt_row[lp];
+            if (e >= 0 && e < a.num_pages) {
+              page = e;
             } else if (kp < pol.P) {
-              st_flags |= lp >= a.max_pages ? MARS_ST_OVERFLOW : MARS_ST_NOPAGE;
+              st_flags |= e == INT_MIN ? MARS_ST_OVERFLOW : MARS_ST_NOPAGE;
             }
             const int row = (page * a.hkv + kvh) * kPageSize;
             for (int x = 0; x < D / 64; ++x)
@@ -239,14 +254,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       };
     };
     if (is_v)
-      flash::load_ring<D>(bar, smem, n_total, a.status, true, issue(&tm_vp, &tm_vb, &tm_vs));
+      flash::load_ring<D, kVStages>(bar, smem, n_total, a.status, true,
+                                    issue(&tm_vp, &tm_vb, &tm_vs));
     else
-      flash::load_ring<D>(bar, smem, n_total, a.status, false, issue(&tm_kp, &tm_kb, &tm_ks));
+      flash::load_ring<D, kVStages>(bar, smem, n_total, a.status, false,
+                                    issue(&tm_kp, &tm_kb, &tm_ks));
     if (!is_v && lane == 0) mbar_wait(&bar.q_full, 0, nullptr, a.status);
     if (st_flags && a.status) atomicOr(a.status, st_flags);
   } else if (warp == 1 || warp == flash::PV_ISSUER_WARP) {
     // one thread issues both QK^T and PV (short tile lists); the PV warp idles
-    if (warp == 1 && lane == 0) flash::single_issuer<D>(bar, smem, n_total, tmem, a.status);
+    if (warp == 1 && lane == 0)
+      flash::single_issuer<D, kVStages>(bar, smem, n_total, tmem, a.status);
   } else {
     flash::softmax_loop<D>(bar, smem, pol, n_total, tmem, a.scale_log2, a.status);
   }
@@ -315,7 +333,7 @@ template <int D>
 cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* v_blk,
                       const uint16_t* k_pool, const uint16_t* v_pool, const uint16_t* k_stage,
                       const uint16_t* v_stage, DecodeArgs& a, int batch, cudaStream_t stream) {
-  using S = flash::Smem<D>;
+  using S = flash::Smem<D, 0, kVStages>;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.hq, (uint64_t)batch * a.B};

@@ -3,8 +3,8 @@
 // A CTA runs a 128-row query tile held in shared memory over a list of 128-key tiles.
 // Roles, as the decode kernel lays them out (256 threads):
 //   warp 0      Q loader, then K loader: K tiles into a 3-stage ring (TMA, 128-byte
-//               swizzle); warp 6 streams V tiles into their own 2-stage ring, so the two
-//               rings advance independently;
+//               swizzle); warp 6 streams V tiles into their own ring (2 stages, 3 in the
+//               decode kernel), so the two rings advance independently;
 //   warp 1      TMEM owner and QK^T issuer: S_j = Q K_j^T into one of three 128-column
 //               fp32 TMEM buffers; a K stage is released as soon as its QK^T finishes;
 //   warp 7      PV issuer: O += P_j V_j with O and P in TMEM (P is the A operand, read
@@ -48,15 +48,19 @@ constexpr float kRescaleLog2 = 8.0f;       // lazy max: rescale when it grows by
 constexpr int K_STAGES = MARS_K_STAGES;
 constexpr int V_STAGES = MARS_V_STAGES;
 constexpr int NBUF = 3;                    // S/P buffers in TMEM
+constexpr int kMaxVStages = 4;             // V-ring barriers kept (a kernel may use fewer)
 
-template <int D, int STAGE_BOXES = 0>
+// VST: V-ring depth of the kernel (the decode kernel, whose CTAs stream long key lists
+// with no O staging area, runs a deeper V ring than the default).
+template <int D, int STAGE_BOXES = 0, int VST = V_STAGES>
 struct Smem {
+  static_assert(VST >= 1 && VST <= kMaxVStages, "V ring depth");
   static constexpr int Q_BYTES = BQ * D * 2;         // D/64 swizzled regions of [128][64]
   static constexpr int KV_BYTES = BKV * D * 2;       // one K or V tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;                          // K ring
   static constexpr int OFF_V = OFF_K + K_STAGES * KV_BYTES;      // V ring
-  static constexpr int OFF_STAGE = OFF_V + V_STAGES * KV_BYTES;  // O staging (optional)
+  static constexpr int OFF_STAGE = OFF_V + VST * KV_BYTES;       // O staging (optional)
   static constexpr int TOTAL = OFF_STAGE + STAGE_BOXES * BQ * 128 + 1024;   // + alignment slack
   // TMEM columns: three S buffers (fp32) at 0, 128, 256 and O (fp32) at 384. P of a tile
   // (bf16 pairs, 64 columns) is written over the upper half of that tile's S buffer once
@@ -69,7 +73,7 @@ struct Smem {
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[K_STAGES], k_empty[K_STAGES], v_full[V_STAGES], v_empty[V_STAGES];
+  uint64_t k_full[K_STAGES], k_empty[K_STAGES], v_full[kMaxVStages], v_empty[kMaxVStages];
   uint64_t s_full[NBUF];
   uint64_t p_full[NBUF], pv_done[NBUF];
   uint64_t o_final, drain, drain_pv;
@@ -92,7 +96,7 @@ MARS_DEV void init_barriers(Barriers& bar) {
     mbar_init(&bar.k_full[i], 1);
     mbar_init(&bar.k_empty[i], 1);
   }
-  for (int i = 0; i < V_STAGES; ++i) {
+  for (int i = 0; i < kMaxVStages; ++i) {
     mbar_init(&bar.v_full[i], 1);
     mbar_init(&bar.v_empty[i], 1);
   }
@@ -165,13 +169,13 @@ MARS_DEV bool load_ring_item(Barriers& bar, uint8_t* smem, int ntiles, int j0, i
                                     last, drain, status, issue);
 }
 
-template <int D, class Issue>
+template <int D, int VST = V_STAGES, class Issue>
 MARS_DEV void load_ring(Barriers& bar, uint8_t* smem, int ntiles, int32_t* status, bool is_v,
                         Issue issue) {
   if (is_v) {
-    int last[V_STAGES];
-    for (int i = 0; i < V_STAGES; ++i) last[i] = -1;
-    load_ring_item<D, V_STAGES>(bar, smem, ntiles, 0, last, true, status, true, issue);
+    int last[VST];
+    for (int i = 0; i < VST; ++i) last[i] = -1;
+    load_ring_item<D, VST>(bar, smem, ntiles, 0, last, true, status, true, issue);
   } else {
     int last[K_STAGES];
     for (int i = 0; i < K_STAGES; ++i) last[i] = -1;
@@ -304,8 +308,8 @@ MARS_DEV bool pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
 
 // Single-thread alternative: one thread issues S_j, then PV_{j-1}, so the QK^T the softmax
 // waits for is never queued behind PV work (used where the softmax is on the critical
-// path). ntiles >= 1.
-template <int D>
+// path). ntiles >= 1; VST is the V-ring depth the loaders use.
+template <int D, int VST = V_STAGES>
 MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
                        int32_t* status) {
   using namespace sm100;
@@ -316,8 +320,8 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
   volatile int* ab = &bar.abort;
   if (!mbar_wait(&bar.q_full, 0, ab, status)) return;
   auto issue_pv = [&](int j) -> bool {
-    const int pb = j % NBUF, st = j % V_STAGES;
-    if (!mbar_wait(&bar.v_full[st], (j / V_STAGES) & 1, ab, status)) return false;
+    const int pb = j % NBUF, st = j % VST;
+    if (!mbar_wait(&bar.v_full[st], (j / VST) & 1, ab, status)) return false;
     if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return false;
     tc_fence_after();
     const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
@@ -357,11 +361,11 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
 
 // Single-issuer form (run by lane 0 of warp 1): mma_loop, then a wait (bounded) for its
 // own MMAs so none is in flight when the CTA tears down.
-template <int D>
+template <int D, int VST = V_STAGES>
 MARS_DEV void single_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
                             int32_t* status) {
   using namespace sm100;
-  mma_loop<D>(bar, smem, ntiles, tmem, status);
+  mma_loop<D, VST>(bar, smem, ntiles, tmem, status);
   mma_commit(&bar.drain);
   mbar_wait(&bar.drain, 0, nullptr, status);
 }

@@ -101,8 +101,8 @@ extern "C" int mars_head_accept_noalloc(const mars_bf16* h, const mars_bf16* w, 
   void* scratch = nullptr;
   const int rc = mars::scratch_for_current_device(&scratch);
   if (rc != MARS_OK) return rc;
-  // Every partial the finalize step reads is written by the GEMM epilogue of the same
-  // call, so nothing in the scratch has to start at zero.
+  // The row-block counters that must start at zero are cleared on the stream by the
+  // launcher at every call; the partial records are written before they are read.
   const cudaError_t e =
       mars::launch_head_accept(h, w, batch, B, hidden, vocab, tau, nullptr, tokens, maxprob, n_accept,
                                scratch, status, static_cast<cudaStream_t>(stream));

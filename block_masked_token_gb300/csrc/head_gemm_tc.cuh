@@ -17,6 +17,17 @@
 // the group's rows of h (at most 14.7 MB at hidden 3584) stay in L2 while the group sweeps
 // the vocabulary. W therefore streams from HBM once per group (once per call for decode
 // batches), and h once in all.
+//
+// Fused acceptance (the decode step, Params::sync set): within a group a CTA meets only a
+// few row blocks (every gcd(grid, rows of the group)-th), so instead of one partial per
+// tile the epilogue keeps one running partial per row and row block in shared memory
+// over all of the CTA's tiles of the group, and writes it once, as a record, when the CTA
+// leaves the group. Each record adds the number of vocabulary tiles it covers to its row
+// block's count (an atomic ticket): the CTA whose record completes the count merges the
+// row block's records (at most one per CTA), writes tokens and max-probs, and runs the
+// left-to-right scan of every sequence whose rows lie in the block. A sequence whose rows
+// straddle two row blocks is scanned by the second of the two merging CTAs (a second
+// ticket per block boundary). Nothing waits on another CTA, and no second kernel runs.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -37,6 +48,9 @@ constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;   // + alignm
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int GROUP_M = 16;                     // row blocks per tile group
+// running partials of the fused acceptance: [GROUP_M][BM] float4 after the ring
+constexpr size_t SLOT_BYTES = (size_t)GROUP_M * BM * sizeof(float4);   // 32 KB
+constexpr size_t SMEM_FUSED_BYTES = SMEM_BYTES + SLOT_BYTES;
 
 struct Params {
   int rows, hidden, vocab;
@@ -52,7 +66,40 @@ struct Params {
   const float* stream_scale;   // [2]: clean rows, masked rows
   int two_l;
   int32_t* status;
+  // Fused acceptance mode (sync != NULL; part, targets and dlogits unused): counters
+  // sync[0 .. num_m) = vocabulary tiles merged into records per row block, sync[num_m ..
+  // 2 num_m) = records per row block, sync[2 num_m .. 3 num_m) = tickets of the boundary
+  // between row blocks mb - 1 and mb; all zero at launch. rec[mb][i][row] = record i of
+  // row block mb (at most max_rec, one per CTA) {max, sum exp(l - max), first argmax, 0}.
+  uint32_t* sync;
+  float4* rec;
+  int max_rec;
+  int B;                 // block positions per sequence (rows s*B .. s*B + B - 1)
+  float tau;             // threshold, or per sequence from taus when taus != NULL
+  const float* taus;
+  int32_t* tokens;       // [rows]
+  float* maxprob;        // [rows]
+  int32_t* n_accept;     // [rows / B]
 };
+
+// (max, sum exp(l - max), lowest argmax) of the union of two sets of logits
+MARS_DEV void merge_partial(float& m, float& s, int& a, float m2, float s2, int a2) {
+  const float mx = fmaxf(m, m2);
+  if (mx == -INFINITY) return;
+  const float sm = (m == -INFINITY ? 0.f : s * exp2f((m - mx) * kLog2e)) +
+                   (m2 == -INFINITY ? 0.f : s2 * exp2f((m2 - mx) * kLog2e));
+  a = m > m2 ? a : (m2 > m ? a2 : min(a, a2));
+  m = mx;
+  s = sm;
+}
+
+// Left-to-right acceptance of sequence s from its B max-probs p[0..B-1]: the leading run
+// of positions with p >= tau, at least 1 (a NaN threshold compares false).
+MARS_DEV int accept_run(const float* pr, int B, float t) {
+  int n = 0;
+  while (n < B && pr[n] >= t) ++n;
+  return n < 1 ? 1 : n;
+}
 
 // Row block and vocabulary tile of linear tile index `tile` (see the order above).
 MARS_DEV void tile_coords(int tile, const Params& p, int& mb, int& nb) {
@@ -75,16 +122,23 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int issued_s, consumed_s;
+  // fused acceptance: vocabulary tiles per running slot, broadcasts, merged max-probs
+  __shared__ uint32_t slot_tiles_s[GROUP_M];
+  __shared__ int rec_idx_s, last_s;
+  __shared__ float p_s[BM];
+  __shared__ uint64_t epi_bar;               // the four epilogue warps among themselves
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* stage_ptr = smem_raw + (sbase - raw);
+  float4* slots = reinterpret_cast<float4*>(stage_ptr + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     abort_s = 0;
     issued_s = 0;
     consumed_s = 0;
+    for (int i = 0; i < GROUP_M; ++i) slot_tiles_s[i] = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
@@ -94,6 +148,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       mbar_init(&acc_empty[b], EPI_THREADS);
     }
     mbar_init(&drain_bar, 1);
+    mbar_init(&epi_bar, EPI_THREADS);
     fence_barrier_init();
     prefetch_tmap(&tm_h);
     prefetch_tmap(&tm_w);
@@ -164,6 +219,87 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     // ------------------------------------------------------------- epilogue
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int row_in_tile = quad * 32 + lane;
+    const bool leader = threadIdx.x == 64;     // one thread of the four epilogue warps
+
+    // Fused acceptance. The epilogue warps synchronise among themselves on an mbarrier
+    // with the bounded wait (not a named barrier), so that a CTA whose pipeline gave up
+    // cannot leave some of them waiting for ever.
+    uint32_t epi_phase = 0;
+    auto epi_sync = [&]() -> bool {
+      mbar_arrive(&epi_bar);
+      const bool ok = mbar_wait(&epi_bar, epi_phase & 1u, &abort_s, p.status);
+      ++epi_phase;
+      return ok;
+    };
+
+    // All rows of row block mb are merged: write tokens and max-probs, scan the sequences
+    // inside the block, and take the block's boundary tickets.
+    auto merge_block = [&](int mb) -> bool {
+      __threadfence();
+      const int nrec = min((int)atomicAdd(&p.sync[p.num_m + mb], 0u), p.max_rec);
+      float m = -INFINITY, ssum = 0.f;
+      int am = 0x7fffffff;
+      const float4* rb = p.rec + (size_t)mb * p.max_rec * BM + row_in_tile;
+      for (int i = 0; i < nrec; ++i) {
+        const float4 v = __ldcg(rb + (size_t)i * BM);
+        merge_partial(m, ssum, am, v.x, v.y, __float_as_int(v.z));
+      }
+      const float pr = 1.f / ssum;
+      const int r0 = mb * BM;
+      const int row = r0 + row_in_tile;
+      if (row < p.rows) {
+        p.tokens[row] = am;
+        p.maxprob[row] = pr;
+      }
+      p_s[row_in_tile] = pr;
+      __threadfence();
+      if (!epi_sync()) return false;
+      const int r1 = min(p.rows, r0 + BM);
+      for (int sq = (r0 + p.B - 1) / p.B + row_in_tile; sq < r1 / p.B; sq += BM)
+        p.n_accept[sq] = accept_run(p_s + (sq * p.B - r0), p.B, p.taus ? p.taus[sq] : p.tau);
+      if (leader) {
+        // a sequence straddling this block's first or last row: the second of the two
+        // blocks to get here scans it from the max-probs both have written
+        float pr2[32];
+        for (int side = 0; side < 2; ++side) {
+          const int edge = side == 0 ? r0 : r0 + BM;       // first row of the later block
+          if (edge <= 0 || edge >= p.rows || edge % p.B == 0) continue;
+          if (atomicAdd(&p.sync[2 * p.num_m + edge / BM], 1u) != 1u) continue;
+          __threadfence();
+          const int sq = edge / p.B;
+          for (int k = 0; k < p.B; ++k) pr2[k] = __ldcg(p.maxprob + (size_t)sq * p.B + k);
+          p.n_accept[sq] = accept_run(pr2, p.B, p.taus ? p.taus[sq] : p.tau);
+        }
+      }
+      return epi_sync();                 // p_s is rewritten by the next merge
+    };
+
+    // The CTA leaves group g: write its running partials of the group as records and add
+    // their vocabulary tiles to the row blocks' counts.
+    auto flush_group = [&](int g, uint32_t visited) -> bool {
+      for (uint32_t vm = visited; vm; vm &= vm - 1) {
+        const int l = __ffs(vm) - 1;
+        const int mb = g * GROUP_M + l;
+        if (leader) rec_idx_s = (int)atomicAdd(&p.sync[p.num_m + mb], 1u);
+        if (!epi_sync()) return false;
+        const int idx = rec_idx_s;
+        if (idx < p.max_rec)             // one record per CTA and row block: always true
+          p.rec[((size_t)mb * p.max_rec + idx) * BM + row_in_tile] = slots[l * BM + row_in_tile];
+        __threadfence();
+        if (!epi_sync()) return false;
+        if (leader) {
+          const uint32_t n = slot_tiles_s[l];
+          slot_tiles_s[l] = 0;
+          last_s = atomicAdd(&p.sync[mb], n) + n == (uint32_t)p.num_n;
+        }
+        if (!epi_sync()) return false;
+        if (last_s && !merge_block(mb)) return false;
+      }
+      return true;
+    };
+
+    int cur_g = -1;
+    uint32_t visited = 0;
     int t = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++t) {
       int mb, nb;
@@ -260,9 +396,32 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
+      if (p.sync) {
+        // fold this tile's partial into the running slot of its row block
+        const int g = tile / (GROUP_M * p.num_n);
+        const int l = mb - g * GROUP_M;
+        if (g != cur_g) {
+          if (cur_g >= 0 && !flush_group(cur_g, visited)) break;
+          cur_g = g;
+          visited = 0;
+        }
+        float4& sl = slots[l * BM + row_in_tile];
+        if ((visited >> l) & 1u) {
+          float m0 = sl.x, s0 = sl.y;
+          int a0 = __float_as_int(sl.z);
+          merge_partial(m0, s0, a0, m, ssum, am);
+          sl = make_float4(m0, s0, __int_as_float(a0), 0.f);
+        } else {
+          sl = make_float4(m, ssum, __int_as_float(am), 0.f);
+        }
+        visited |= 1u << l;
+        if (leader) ++slot_tiles_s[l];
+        continue;
+      }
       if (row < p.rows)
         p.part[(size_t)nb * p.rows + row] = make_float4(m, ssum, __int_as_float(am), tl);
     }
+    if (p.sync && cur_g >= 0 && !abort_s) flush_group(cur_g, visited);
   }
 
   __syncthreads();

@@ -126,7 +126,10 @@ int mars_decode_attn(const mars_bf16* q, const mars_bf16* k_blk, const mars_bf16
  *   w         [vocab, hidden] bf16     the LM head, vocabulary-major (row v = word v)
  *   tau       the confidence threshold, per call (the live speed knob); finite
  *   tokens    [batch, B] int32, maxprob [batch, B] float, n_accept [batch] int32 (written)
- *   workspace >= mars_workspace_bytes(MARS_OP_HEAD_ACCEPT, ...) bytes
+ *   workspace >= mars_workspace_bytes(MARS_OP_HEAD_ACCEPT, ...) bytes; needs no
+ *             initialisation (the call clears the counters it uses on the stream)
+ * One GEMM kernel does it all: the CTA that completes a block of 128 rows merges its
+ * partial maxima and sums, writes the tokens and max-probs, and runs the scan.
  * hidden % 8 == 0 (row pitch of h and w a multiple of 16 bytes). status may be NULL. */
 int mars_head_accept(const mars_bf16* h, const mars_bf16* w, int batch, int B, int hidden,
                      int vocab, float tau, int32_t* tokens, float* maxprob,
@@ -156,17 +159,19 @@ int mars_head_accept_per_request(const mars_bf16* h, const mars_bf16* w, int bat
  * of mars_head_accept; it allocates nothing (no cudaMalloc, cudaFree or allocating
  * library call).
  * Scratch: one library-owned device array of MARS_NOALLOC_SCRATCH_BYTES per GPU, held
- * from library load until the process exits. A call needing more than that
- * (batch*B*ceil(vocab/256)*16 bytes, i.e. more than 882 rows at vocab 152064) returns
- * MARS_ENOSPACE before anything is launched.
+ * from library load until the process exits. A call needing more than that (the
+ * workspace mars_head_accept would need, mars_workspace_bytes(MARS_OP_HEAD_ACCEPT, ...):
+ * on a 152-SM GB300 at vocab 152064, more than 26 blocks of 128 rows, i.e. 3328 rows)
+ * returns MARS_ENOSPACE before anything is launched.
  * The first call on a device (made while that device is current) looks up the array's
  * device address; make that first call before any CUDA stream capture. The address is
  * looked up again when the calling thread's current context differs from the one of the
  * lookup (for example after cudaDeviceReset); such a first call in a new context must
  * likewise come before any capture.
- * Every call uses the same array and leaves its contents behind: calls whose kernels may
- * overlap on the GPU (different streams without ordering between them) race on it and
- * give wrong results, so order such calls on one stream. */
+ * Every call uses the same array and leaves its contents behind; the counters that must
+ * start at zero are cleared on the stream at the start of every call. Calls whose kernels
+ * may overlap on the GPU (different streams without ordering between them) race on the
+ * array and give wrong results, so order such calls on one stream. */
 int mars_head_accept_noalloc(const mars_bf16* h, const mars_bf16* w, int batch, int B,
                              int hidden, int vocab, float tau, int32_t* tokens,
                              float* maxprob, int32_t* n_accept, int32_t* status,

@@ -503,6 +503,31 @@ def test_head_small(batch, B, hidden, vocab, tau):
         assert (n == B).all()
 
 
+@pytest.mark.parametrize("batch,B,tau", [
+    (60, 5, 0.3),          # 300 rows: sequences straddle the boundaries at rows 128 and 256
+    (20, 24, 0.0),         # whole blocks accepted across two straddles (rows 128, 256)
+    (37, 7, 0.2),          # two straddles and a ragged last row block
+    (9, 32, 0.1),          # B = 32 divides 128: no straddle, several sequences per block
+    (130, 1, 0.5),         # the AR step's head: one row per sequence, two row blocks
+])
+def test_head_sequences_across_row_blocks(batch, B, tau):
+    """The acceptance scan runs where the last partial of a 128-row block is merged; a
+    sequence whose B rows straddle two blocks is scanned once both are merged."""
+    cfg = W.DecodeConfig("hs", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
+                         hidden=128, vocab=1000, taus=(tau,))
+    inp = W.make_decode_inputs(cfg, seed=batch + B)
+    tok, p, n = run_head(inp.h[0].to(DEV), inp.w.to(DEV), batch, B, tau)
+    rt, rp, rn, gap = oracle.head_accept(f64(inp.h[0]), f64(inp.w), batch, B, tau)
+    compare_head(tok, p, n, rt, rp, rn, gap, tau)
+    # the same call with one threshold per sequence (0 or tau, alternating)
+    taus = [0.0 if s % 2 else tau for s in range(batch)]
+    tok2, p2, n2 = run_head_per_request(inp.h[0].to(DEV), inp.w.to(DEV), batch, B, taus)
+    rt2, rp2, rn2, gap2 = oracle.head_accept_per_request(f64(inp.h[0]), f64(inp.w), batch, B,
+                                                         taus)
+    compare_head(tok2, p2, n2, rt2, rp2, rn2, gap2, taus)
+    assert (n2[1::2] == B).all()
+
+
 def test_head_tie_goes_to_lowest_index():
     batch, B, H, V = 1, 2, 64, 700
     h = torch.zeros(batch * B, H, dtype=torch.bfloat16)

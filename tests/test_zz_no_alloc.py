@@ -77,15 +77,26 @@ def _call(fn, h, w, batch, B, hidden, vocab, tau, tok, mp, n, st):
               _ptr(st), ctypes.c_void_p(stream.cuda_stream))
 
 
+def _largest_rows(vocab):
+    """The most rows (a whole number of 128-row blocks) whose workspace fits the scratch,
+    by the library's own workspace size."""
+    rows = 128
+    while mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, rows + 128, 1, vocab=vocab) <= \
+            SCRATCH_BYTES:
+        rows += 128
+    assert mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, rows, 1, vocab=vocab) <= SCRATCH_BYTES
+    return rows
+
+
 def test_noalloc_at_its_exact_limit_allocates_nothing():
-    """The largest call the scratch holds (882 rows at vocabulary 152064: 882 x 594
-    partials of 16 bytes = 8 382 528 bytes <= 8 MiB) matches the workspace entry point on
-    two calls in a row, and the second call changes neither the device's free memory nor
-    the caching allocator's counters; one row more (883) is refused with ENOSPACE before
-    anything runs."""
+    """The largest call the scratch holds (a whole number of row blocks at vocabulary
+    152064, B = 16) matches the workspace entry point on two calls in a row, and the second
+    call changes neither the device's free memory nor the caching allocator's counters;
+    one row more is refused with ENOSPACE before anything runs."""
     fn = _noalloc()
-    batch, B, hidden, vocab, tau = 63, 14, 3584, 152064, 0.5
-    assert batch * B * ((vocab + 255) // 256) * 16 <= SCRATCH_BYTES
+    hidden, vocab, tau, B = 3584, 152064, 0.5, 16
+    rows = _largest_rows(vocab)
+    batch = rows // B
     cfg = W.DecodeConfig("lim", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
                          hidden=hidden, vocab=vocab, taus=(tau,))
     inp = W.make_decode_inputs(cfg, seed=12, device=DEV, steps=2)
@@ -113,19 +124,19 @@ def test_noalloc_at_its_exact_limit_allocates_nothing():
         np.testing.assert_array_equal(tok2.cpu().numpy(), tok.cpu().numpy())
         np.testing.assert_allclose(mp2.cpu().numpy(), mp.cpu().numpy(), rtol=0, atol=1e-4)
         np.testing.assert_array_equal(n2.cpu().numpy(), n.cpu().numpy())
-    # 883 rows (batch 883, B 1): 16 bytes over
-    assert 883 * ((vocab + 255) // 256) * 16 > SCRATCH_BYTES
+    # one row more (batch rows + 1, B 1): one more row block than the scratch holds
+    assert mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, rows + 1, 1, vocab=vocab) > \
+        SCRATCH_BYTES
     dummy = torch.empty(16, dtype=torch.uint8, device=DEV)
     p = _ptr(dummy)
-    rc = fn(p, p, 883, 1, hidden, vocab, tau, p, p, p, None, None)
+    rc = fn(p, p, rows + 1, 1, hidden, vocab, tau, p, p, p, None, None)
     assert rc == mars.ENOSPACE
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     fn = _noalloc()
-    batch, B, hidden, vocab = 128, 16, 3584, 152064     # 2048 rows: 19.5 MB of partials
-    need = batch * B * ((vocab + 255) // 256) * 16
-    assert need > SCRATCH_BYTES
+    batch, B, hidden, vocab = 512, 16, 3584, 152064     # 8192 rows: 64 row blocks
+    assert mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, batch, B, vocab=vocab) > SCRATCH_BYTES
     dummy = torch.empty(16, dtype=torch.uint8, device=DEV)
     p = _ptr(dummy)
     rc = fn(p, p, batch, B, hidden, vocab, 0.9, p, p, p, None, None)
