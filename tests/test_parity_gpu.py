@@ -373,6 +373,13 @@ def _decode_case(cfg, seed=0, steps=1, extra_pages=3):
     # empty prefixes: only the block keys
     W.DecodeConfig("d9", batch=3, prefix_lo=0, prefix_hi=0, prefixes=(0, 0, 0), B=16, hq=4,
                    hkv=1, d=64, hidden=64, vocab=64),
+    # 400 one-tile pairs: several waves of CTAs, ordered longest first
+    W.DecodeConfig("d10", batch=200, prefix_lo=0, prefix_hi=0, prefixes=(0,) * 200, B=4,
+                   hq=4, hkv=2, d=64, hidden=64, vocab=64),
+    # very uneven prefixes, few pairs: the long ones split, some splits past a short end
+    W.DecodeConfig("d11", batch=7, prefix_lo=0, prefix_hi=0,
+                   prefixes=(3000, 5, 130, 0, 700, 4096, 1), B=8, hq=8, hkv=2, d=128,
+                   hidden=64, vocab=64),
 ])
 def test_decode_small(cfg):
     inp = _decode_case(cfg, seed=1)
@@ -413,6 +420,20 @@ def test_decode_hint_smaller_than_length_is_still_correct():
                              f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
                              inp.prefix_lens.numpy(), cfg.page_size)
     assert st == 0
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
+def test_decode_hint_far_above_lengths():
+    """A length hint far above the prefixes plans many splits per pair, most of them past
+    the prefix ends (empty partials that the merge skips)."""
+    cfg = W.DecodeConfig("dh", batch=2, prefix_lo=0, prefix_hi=0, prefixes=(3, 40), B=4,
+                         hq=4, hkv=2, d=64, hidden=64, vocab=64)
+    inp = _decode_case(cfg, seed=4)
+    o, st = run_decode(inp, 0, inp.prefix_lens, cfg, max_len_hint=20000)
+    assert st == 0
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             f64(inp.k_pool), f64(inp.v_pool), inp.block_table.numpy(),
+                             inp.prefix_lens.numpy(), cfg.page_size)
     assert_attn_close(o.cpu().numpy(), ref)
 
 
