@@ -40,8 +40,8 @@ METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TF
 # of the kernel as it is now, on the workload named beside each: the LM-head GEMM at 2048
 # rows, decode attention on step 0 of the sustained workload, the dual-stream forward at
 # 2L = 8192. None whenever the kernel has changed since its capture.
-TRAFFIC_HEAD_GEMM = 1124735872         # head_gemm_kernel, sustained decode, 2048 rows
-TRAFFIC_DECODE_STEP0 = None            # decode_tc_kernel, sustained decode, step 0
+TRAFFIC_HEAD_GEMM = None               # head_gemm_kernel, sustained decode, 2048 rows
+TRAFFIC_DECODE_STEP0 = 1365940864      # decode_tc_kernel, sustained decode, step 0
 TRAFFIC_DUAL_STREAM = 330413824        # dual_stream_persistent_kernel, 2L = 8192
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
@@ -409,6 +409,7 @@ def run_gpu(args, rank, world, local):
     ar = run_step_variant(W.AR_DECODE_7B, device, K, Wm, seed=rank)
     tau0 = run_step_variant(dataclasses.replace(cfg, name=cfg.name + "_tau0", taus=(0.0,)),
                             device, K, Wm, seed=rank)
+    block_cache = run_block_cache_variant(cfg, device, K, Wm, seed=rank)
 
     # ---- the training-form loss over the dual stream (forward), same run
     with ClockSampler(local) as clk_ce:
@@ -460,9 +461,12 @@ def run_gpu(args, rank, world, local):
                                     "is the synthetic analogue of the pages' wall-clock "
                                     "table, with random weights (mean N ~ 1)"},
             "ce_loss": ce,
+            "mars_block_cache": {**block_cache,
+                                 "mars_over_ar": block_cache["tok_s"] / ar["tok_s"]},
             "mars_tau0": {**tau0, "mars_over_ar": tau0["tok_s"] / ar["tok_s"],
                           "note": "coverage run: tau = 0 accepts all B positions"},
-            "roofline": {"kernel": "mars_head_accept (LM head GEMM + fused epilogue)",
+            "roofline": {"kernel": "mars_head_accept (LM-head GEMM; max/sum-exp/argmax and the "
+                                   "acceptance scan in its epilogue)",
                          "bound": "tensor", "achieved": head_tflops,
                          "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                          "frac": frac_head, "traffic": TRAFFIC_HEAD_GEMM,
@@ -606,6 +610,58 @@ def run_step_variant(cfg, device, K, Wm, seed):
            "mean_accepted_per_seq_step": tok / (K * cfg.batch),
            "device_status": int(runner.status.item())}
     del runner, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_block_cache_variant(cfg, device, K, Wm, seed, B_cache=16):
+    """K decode steps with the block-level cache: decode attention over prefix + block
+    buffer, the LM head with acceptance, and the block commit (blocks of B_cache tokens
+    written once every sequence has filled its own). Returns accepted tok/s."""
+    from block_masked_token_gb300 import mars
+    inp = W.make_decode_inputs(cfg, seed=seed, device=device)
+    r = DecodeRunner(inp, cfg, device)
+    b = cfg.batch
+    stage_k = torch.empty(b, B_cache, cfg.hkv, cfg.d, dtype=torch.bfloat16, device=device)
+    stage_v = torch.empty_like(stage_k)
+    fill = torch.zeros(b, dtype=torch.int32, device=device)
+    sync = torch.zeros(mars.BLOCK_SYNC_WORDS, dtype=torch.int32, device=device)
+
+    def reset():
+        r.reset()
+        fill.zero_()
+        sync.zero_()
+
+    def step(i):
+        s_ = i % cfg.steps
+        n = r.n_acc[s_]
+        mars.mars_decode_attn_block_cache(inp.q[s_], inp.k_blk[s_], inp.v_blk[s_], inp.k_pool,
+                                          inp.v_pool, r.bt, r.seq_lens, r.max_hint, stage_k,
+                                          stage_v, fill, r.o, r.ws_attn, r.status)
+        mars.mars_head_accept(inp.h[s_], inp.w, b, cfg.B, cfg.tau_at(s_), r.tokens, r.maxprob,
+                              n, r.ws_head, r.status)
+        mars.mars_kv_commit_block(inp.k_blk[s_], inp.v_blk[s_], n, r.seq_lens, fill, stage_k,
+                                  stage_v, sync, r.bt, inp.k_pool, inp.v_pool, r.slots,
+                                  r.status)
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    reset()
+    a, e = _ev(), _ev()
+    a.record()
+    for i in range(K):
+        step(i)
+    e.record()
+    torch.cuda.synchronize()
+    sec = a.elapsed_time(e) / 1e3
+    tok = float(r.n_acc[: min(K, cfg.steps)].sum().item())
+    out = {"workload": cfg.name + f"_block_cache{B_cache}", "tok_s": tok / sec,
+           "ms_per_step": sec / K * 1e3, "mean_accepted_per_seq_step": tok / (K * b),
+           "device_status": int(r.status.item()),
+           "note": "block-level cache: accepted rows held in a per-sequence block buffer, "
+                   "faster sequences waiting at the boundary; attention reads prefix + "
+                   "buffer + block keys"}
+    del r, inp, stage_k, stage_v
     torch.cuda.empty_cache()
     return out
 

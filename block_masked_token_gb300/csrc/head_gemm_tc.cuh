@@ -82,6 +82,14 @@ struct Params {
   int32_t* n_accept;     // [rows / B]
 };
 
+// 2^x on the special-function unit (ex2.approx.ftz: relative error about 2^-22, -inf -> 0),
+// for the per-logit exponentials of the epilogues.
+MARS_DEV float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // (max, sum exp(l - max), lowest argmax) of the union of two sets of logits
 MARS_DEV void merge_partial(float& m, float& s, int& a, float m2, float s2, int a2) {
   const float mx = fmaxf(m, m2);
@@ -335,8 +343,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
             uint32_t g2[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-              float g0 = exp2f(fmaf(__uint_as_float(r[j]), kLog2e, nl));
-              float g1 = exp2f(fmaf(__uint_as_float(r[j + 1]), kLog2e, nl));
+              float g0 = ex2_fast(fmaf(__uint_as_float(r[j]), kLog2e, nl));
+              float g1 = ex2_fast(fmaf(__uint_as_float(r[j + 1]), kLog2e, nl));
               if (c * 32 + j == tcol) g0 -= 1.f;
               if (c * 32 + j + 1 == tcol) g1 -= 1.f;
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * scale, g1 * scale);
@@ -379,7 +387,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
           if (x > cm) { cm = x; ca = col0 + c * 32 + j; }
         }
         if (cm > m) {
-          ssum *= exp2f((m - cm) * kLog2e);
+          ssum *= ex2_fast((m - cm) * kLog2e);
           m = cm;
           am = ca;
         }
@@ -389,7 +397,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float x = (c * 32 + j < ncols) ? __uint_as_float(r[j]) : -INFINITY;
-            acc += exp2f(fmaf(x, kLog2e, -mb2));
+            acc += ex2_fast(fmaf(x, kLog2e, -mb2));
           }
           ssum += acc;
         }
