@@ -555,11 +555,12 @@ def run_e2e(runner, inp, cfg, K, Wm, device, dist):
 
 
 def run_decode_c3(device, peaks, reps=20, warm=3):
-    """Decode attention alone on the batch-32 7B decode workload (128 sequence/kv-head
-    pairs, prefixes 512..2048): CUDA events around each call, L2 flushed before each."""
+    """Decode attention and the LM head with the acceptance, each alone, on the batch-32
+    7B decode workload (128 sequence/kv-head pairs, prefixes 512..2048; 256 head rows):
+    CUDA events around each call, L2 flushed before each."""
     from block_masked_token_gb300 import mars
     cfg = W.DECODE_7B
-    inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1, with_head=False)
+    inp = W.make_decode_inputs(cfg, seed=0, device=device, steps=1, with_head=True)
     r = DecodeRunner(inp, cfg, device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
@@ -580,11 +581,45 @@ def run_decode_c3(device, peaks, reps=20, warm=3):
     t = statistics.median(ts)
     by = decode_kv_bytes(inp.prefix_lens.tolist(), cfg)
     gbs = by / t / 1e9
+    # the step's LM head at these 256 rows: W streamed once per call
+    rows = cfg.batch * cfg.B
+    tok = torch.empty(cfg.batch, cfg.B, dtype=torch.int32, device=device)
+    mp = torch.empty(cfg.batch, cfg.B, dtype=torch.float32, device=device)
+    na = torch.empty(cfg.batch, dtype=torch.int32, device=device)
+    ws = torch.empty(mars.mars_workspace_bytes(mars.OP_HEAD_ACCEPT, cfg.batch, cfg.B,
+                                               vocab=cfg.vocab), dtype=torch.uint8,
+                     device=device)
+    h0 = inp.h[0].to(device)
+    wt = inp.w.to(device)
+
+    def head():
+        mars.mars_head_accept(h0, wt, cfg.batch, cfg.B, cfg.tau_at(0), tok, mp, na, ws)
+    for _ in range(warm):
+        head()
+    th = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = _ev(), _ev()
+        a.record()
+        head()
+        b.record()
+        torch.cuda.synchronize()
+        th.append(a.elapsed_time(b) / 1e3)
+    tht = statistics.median(th)
+    flop = 2.0 * rows * cfg.hidden * cfg.vocab
+    wbytes = cfg.vocab * cfg.hidden * 2
     out = {"workload": cfg.name, "us_per_call": t * 1e6, "hbm_gbs": gbs,
            "frac_hbm": gbs / peaks["hbm_gbs"], "algorithmic_bytes": by,
            "device_status": int(r.status.item()),
+           "head_accept": {"rows": rows, "us_per_call": tht * 1e6,
+                           "tflops": flop / tht / 1e12,
+                           "frac_tensor": flop / tht / 1e12 / peaks["bf16_tflops"],
+                           "w_gbs": wbytes / tht / 1e9,
+                           "frac_hbm": wbytes / tht / 1e9 / peaks["hbm_gbs"],
+                           "note": "fraction of the burst bf16 rate (timed alone); W read "
+                                   "once per call"},
            "l2": "flushed (256 MB write) before each timed call"}
-    del r, inp, flush
+    del r, inp, flush, ws, h0, wt
     torch.cuda.empty_cache()
     return out
 
