@@ -169,6 +169,13 @@ bool map2d(CUtensorMap* m, const void* base, int inner, int outer, uint32_t box_
   return encode_tmap_bf16(m, base, 2, dims, strides, box);
 }
 
+// Both head launches of this file share one copy of the kernel and so one dynamic
+// shared-memory limit: the larger of the two they use.
+cudaError_t head_smem_limit() {
+  static std::atomic<int> attr[64];
+  return set_smem_limit_once(head_tc::head_gemm_kernel, (int)head_tc::SMEM_FUSED_BYTES, attr);
+}
+
 size_t grad_dlogits_bytes(int batch, int L, int vocab) {
   const size_t n = (size_t)batch * 2 * L * vocab * sizeof(uint16_t);
   return (n + 255) / 256 * 256;
@@ -216,12 +223,14 @@ cudaError_t launch_ce_loss_grad(const uint16_t* h, const uint16_t* w, const int3
   p.stream_scale = scale;
   p.two_l = 2 * L;
   p.status = status;
-  static std::atomic<int> attr[64];
-  const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_BYTES, attr);
+  // dlogits, stored in boxes of 64 columns x 128 rows
+  CUtensorMap tm_d;
+  if (!map2d(&tm_d, dlogits, vocab, rows, 64, BM)) return cudaErrorInvalidValue;
+  const cudaError_t ea = head_smem_limit();
   if (ea != cudaSuccess) return ea;
   ce_scale_kernel<<<1, 256, 0, stream>>>(targets, batch, L, vocab, scale);
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
+  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w, tm_d, p);
   count_launches(2);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || (!dh && !dw)) return e;
@@ -290,11 +299,10 @@ cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* 
   float* ce = row_ce ? row_ce
                      : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                                 (size_t)rows * p.num_n * sizeof(float4));
-  static std::atomic<int> attr[64];
-  const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_BYTES, attr);
+  const cudaError_t ea = head_smem_limit();
   if (ea != cudaSuccess) return ea;
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, p);
+  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, tm_w, p);
   ce_rows_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(p.part, targets, rows, p.num_n, vocab,
                                                       ce, row_lse, status);
   ce_reduce_kernel<<<1, 256, 0, stream>>>(ce, targets, batch, L, vocab, loss);

@@ -107,7 +107,7 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   if (ea != cudaSuccess) return ea;
   cudaError_t e = cudaMemsetAsync(p.sync, 0, (size_t)3 * L.num_m * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
-  head_gemm_kernel<<<L.grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w, p);
+  head_gemm_kernel<<<L.grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w, tm_w, p);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -11,7 +11,8 @@
 //   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (M128 N256 K16) per k-block,
 //               into one of two 256-column fp32 accumulators;
 //   warps 2..5  epilogue: thread = accumulator row (TMEM lane), 256 columns read with
-//               tcgen05.ld, online max / argmax / sum-exp, one 16-byte store per row.
+//               tcgen05.ld, online max / argmax / sum-exp, one 16-byte store per row
+//               (the gradient mode instead stages bf16 dlogits boxes for TMA stores).
 // Tiles are ordered in groups of up to 16 row blocks (2048 rows): inside a group the row
 // block is fastest, so the CTAs running at the same time share one W tile through L2, and
 // the group's rows of h (at most 14.7 MB at hidden 3584) stay in L2 while the group sweeps
@@ -61,6 +62,9 @@ struct Params {
   // dlogits[r, v] = (exp(l_rv - row_lse[r]) - [v == y_r]) * row scale, in bf16, where the
   // row scale is stream_scale[(r % two_l) >= two_l / 2] for rows with a valid target, 0
   // otherwise.
+  // It is written through the kernel's third tensor map (box 64 columns x 128 rows,
+  // 128-byte swizzle, so vocab % 8 == 0), each box staged in the 32 KB after the ring,
+  // which the launch then includes.
   uint16_t* dlogits;       // [rows, vocab] bf16
   const float* row_lse;    // [rows]
   const float* stream_scale;   // [2]: clean rows, masked rows
@@ -122,7 +126,7 @@ MARS_DEV void tile_coords(int tile, const Params& p, int& mb, int& nb) {
 // static: every translation unit that launches it gets its own copy
 static __global__ void __launch_bounds__(NUM_THREADS, 1)
 head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-                 Params p) {
+                 const __grid_constant__ CUtensorMap tm_d, Params p) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
@@ -160,6 +164,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     fence_barrier_init();
     prefetch_tmap(&tm_h);
     prefetch_tmap(&tm_w);
+    if (p.dlogits) prefetch_tmap(&tm_d);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, TMEM_COLS);
@@ -308,6 +313,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 
     int cur_g = -1;
     uint32_t visited = 0;
+    int dl_box = 0;                            // dlogits boxes staged so far (TMA stores)
     int t = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++t) {
       int mb, nb;
@@ -333,34 +339,55 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
             scale = p.stream_scale[(row % p.two_l) >= p.two_l / 2 ? 1 : 0];
         }
         const float nl = -lse * kLog2e;
-        uint16_t* drow = p.dlogits + (size_t)(row < p.rows ? row : 0) * p.vocab + col0;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        // 32 columns c*32 .. c*32 + 31 of this row as 16 packed bf16 pairs
+        auto grad32 = [&](int c, uint32_t (&g2)[16]) {
           uint32_t r[32];
           tmem_ld32(taddr + c * 32, r);
           tmem_ld_wait();
-          if (row < p.rows && c * 32 < ncols) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float g0 = ex2_fast(fmaf(__uint_as_float(r[j]), kLog2e, nl));
+            float g1 = ex2_fast(fmaf(__uint_as_float(r[j + 1]), kLog2e, nl));
+            if (c * 32 + j == tcol) g0 -= 1.f;
+            if (c * 32 + j + 1 == tcol) g1 -= 1.f;
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * scale, g1 * scale);
+            g2[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+        };
+        // Four boxes of 64 columns, each staged as 128 rows x 128 bytes in the layout of
+        // the map's 128-byte swizzle (16-byte unit q of row r at unit q ^ (r & 7)) in one
+        // of two 16 KB halves of the area after the ring, and stored by one thread. Before
+        // the barrier of a box the storing thread waits until its earlier stores have
+        // read their halves, so the next box may overwrite the other half.
+        bool ok = true;
+#pragma unroll 1
+        for (int bi = 0; bi < BN / 64; ++bi, ++dl_box) {
+          uint8_t* half = reinterpret_cast<uint8_t*>(slots) + (dl_box & 1) * (BM * 128);
+          uint8_t* srow = half + row_in_tile * 128;
+#pragma unroll 1
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = bi * 2 + h2;
             uint32_t g2[16];
+            grad32(c, g2);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float g0 = ex2_fast(fmaf(__uint_as_float(r[j]), kLog2e, nl));
-              float g1 = ex2_fast(fmaf(__uint_as_float(r[j + 1]), kLog2e, nl));
-              if (c * 32 + j == tcol) g0 -= 1.f;
-              if (c * 32 + j + 1 == tcol) g1 -= 1.f;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 * scale, g1 * scale);
-              g2[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            if (c * 32 + 32 <= ncols && (p.vocab % 8) == 0) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(drow + c * 32 + q * 8) =
-                    make_uint4(g2[4 * q], g2[4 * q + 1], g2[4 * q + 2], g2[4 * q + 3]);
-            } else {
-              for (int j = 0; j < 32 && c * 32 + j < ncols; ++j)
-                drow[c * 32 + j] = (uint16_t)((g2[j >> 1] >> ((j & 1) * 16)) & 0xffffu);
+            for (int q = 0; q < 4; ++q) {
+              const int u = (h2 * 4 + q) ^ (row_in_tile & 7);
+              *reinterpret_cast<uint4*>(srow + u * 16) =
+                  make_uint4(g2[4 * q], g2[4 * q + 1], g2[4 * q + 2], g2[4 * q + 3]);
             }
           }
+          fence_proxy_async_smem();
+          if (leader) bulk_wait_read_all();
+          if (!epi_sync()) {
+            ok = false;
+            break;
+          }
+          if (leader && col0 + bi * 64 < p.vocab) {
+            tma_store_2d(&tm_d, half, col0 + bi * 64, mb * BM);
+            bulk_commit();
+          }
         }
+        if (!ok) break;
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
         continue;
@@ -430,6 +457,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
         p.part[(size_t)nb * p.rows + row] = make_float4(m, ssum, __int_as_float(am), tl);
     }
     if (p.sync && cur_g >= 0 && !abort_s) flush_group(cur_g, visited);
+    // the dlogits stores must have read shared memory and written global memory before exit
+    if (leader) bulk_wait_all();
   }
 
   __syncthreads();

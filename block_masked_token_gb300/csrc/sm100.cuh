@@ -127,6 +127,14 @@ MARS_DEV void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y
       : "memory");
 }
 
+// Tiled 2D store from shared memory (bulk async-group), as tma_store_4d.
+MARS_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+
 // Tiled 4D reduce-add from shared memory into global (bulk async-group; the element type
 // and the add come from the tensor map). Out-of-range box elements are skipped.
 MARS_DEV void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int x, int y, int z,
@@ -143,6 +151,11 @@ MARS_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "me
 // Wait until every committed bulk store of this thread has finished reading shared memory.
 MARS_DEV void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every committed bulk store of this thread has completed (its writes done).
+MARS_DEV void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Untiled bulk copy global -> shared completing on an mbarrier (both addresses 16-byte
