@@ -161,9 +161,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int sp = blockIdx.x, kvh = blockIdx.y;
   const int s = a.order ? a.order[blockIdx.z] : (int)blockIdx.z;
 
+  // Start what the first tile waits for at once: the loaders' block-table entries of prefix
+  // tile 0 (its pages do not depend on the length) and the tensor maps, so that their
+  // latencies overlap the length's and the set-up below.
+  const int32_t* bt_row = a.block_table + (size_t)s * a.max_pages;
+  int bt0 = INT_MIN;
+  if ((warp == 0 || warp == flash::V_LOADER_WARP) && lane < kPagesPerTile) {
+    const int lp = (sp * a.split_len) / kPageSize + lane;
+    if (lp < a.max_pages) bt0 = bt_row[lp];
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_kp);
+    prefetch_tmap(&tm_vp);
+    prefetch_tmap(&tm_kb);
+    prefetch_tmap(&tm_vb);
+    if (a.stage_fill) {
+      prefetch_tmap(&tm_ks);
+      prefetch_tmap(&tm_vs);
+    }
+  }
+
   DecodePolicy<D> pol;
   pol.a = &a;
-  pol.bt_row = a.block_table + (size_t)s * a.max_pages;
+  pol.bt_row = bt_row;
   pol.part = a.ws + ((((size_t)s * a.hkv + kvh) * a.nsplit + sp) * a.R) * (D + 4);
   pol.P = a.seq_lens[s];
   pol.fill = a.stage_fill ? min(max(a.stage_fill[s], 0), a.B_cache) : 0;
@@ -215,7 +236,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int lp = (pol.start + j * BKV) / kPageSize + lane;
       return lp < a.max_pages ? pol.bt_row[lp] : INT_MIN;
     };
-    int next_entry = entry(0);
+    int next_entry = (pol.n_prefix > 0 && lane < kPagesPerTile) ? bt0 : 0;   // entry(0)
     // prefix tile j: lane i < 8 copies 16-token page i of the tile (unmapped pages load
     // page 0 and are masked by the softmax); the block tile: lane 0 copies a 128-row box
     // from row s*B of k_blk / v_blk (rows past the batch read as zeros), or, with a block
@@ -235,7 +256,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             } else if (kp < pol.P) {
               st_flags |= e == INT_MIN ? MARS_ST_OVERFLOW : MARS_ST_NOPAGE;
             }
-            const int row = (page * a.hkv + kvh) * kPageSize;
+            // with an empty pool the map (over q, one page long) is never read: the box
+            // starts past its end and loads zeros
+            const int row = a.num_pages > 0 ? (page * a.hkv + kvh) * kPageSize : kPageSize;
             for (int x = 0; x < D / 64; ++x)
               tma_load_2d(dst + x * (BKV * 128) + lane * (kPageSize * 128), tm_pool, b, x * 64,
                           row);
@@ -346,7 +369,8 @@ cudaError_t launch_tc(const uint16_t* q, const uint16_t* k_blk, const uint16_t* 
     const uint64_t dims[2] = {(uint64_t)D, rows};
     const uint64_t str[1] = {(uint64_t)D * 2};
     const uint32_t box[2] = {64, (uint32_t)kPageSize};
-    // an empty pool is never read (no prefix keys can be mapped); encode over q instead
+    // an empty pool is never read (its boxes start past the end, see the loader); encode
+    // over q instead
     const void* kp = a.num_pages > 0 ? (const void*)k_pool : (const void*)q;
     const void* vp = a.num_pages > 0 ? (const void*)v_pool : (const void*)q;
     const uint64_t dims_e[2] = {(uint64_t)D, (uint64_t)kPageSize};

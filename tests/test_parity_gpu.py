@@ -446,6 +446,33 @@ def test_decode_unmapped_page_sets_status():
     assert st & mars.ST_NOPAGE
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_empty_pool_leaves_only_block_keys(d):
+    """No pool and no block table while the lengths say there is a prefix: every prefix key
+    is unmapped (flagged), nothing is read for it, and each query attends to the block keys
+    alone, i.e. the oracle's output for an empty prefix."""
+    cfg = W.DecodeConfig("de", batch=3, prefix_lo=0, prefix_hi=0, prefixes=(5, 200, 31),
+                         B=4, hq=8, hkv=2, d=d, hidden=64, vocab=64)
+    inp = W.make_decode_inputs(cfg, seed=2, steps=1, with_head=False)
+    q, kb, vb = inp.q[0].to(DEV), inp.k_blk[0].to(DEV), inp.v_blk[0].to(DEV)
+    pool = torch.empty(0, cfg.hkv, cfg.page_size, d, dtype=torch.bfloat16, device=DEV)
+    bt = torch.empty(cfg.batch, 0, dtype=torch.int32, device=DEV)
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    hint = int(inp.prefix_lens.max())
+    ws = _ws(mars.mars_workspace_bytes(mars.OP_DECODE_ATTN, cfg.batch, cfg.B, cfg.hq, cfg.hkv,
+                                       d, max_len=hint))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mars.mars_decode_attn(q, kb, vb, pool, pool, bt, inp.prefix_lens.to(DEV), hint, o, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mars.ST_OVERFLOW
+    none = np.zeros(cfg.batch, dtype=np.int64)
+    ref = oracle.decode_attn(f64(inp.q[0]), f64(inp.k_blk[0]), f64(inp.v_blk[0]),
+                             np.zeros((0, cfg.hkv, cfg.page_size, d)),
+                             np.zeros((0, cfg.hkv, cfg.page_size, d)),
+                             np.zeros((cfg.batch, 0), dtype=np.int64), none, cfg.page_size)
+    assert_attn_close(o.cpu().numpy(), ref)
+
+
 def test_decode_single_split_direct_output():
     """With at least as many (sequence, kv head) pairs as SMs the kernel runs one split
     per pair and writes the normalised output directly (no merge pass)."""
