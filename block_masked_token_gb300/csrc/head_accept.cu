@@ -24,6 +24,8 @@ namespace {
 // (one per CTA and row block).
 struct HeadLayout {
   int num_m, num_n, grid, max_rec;
+  bool pair;             // the paired (two-SM) kernel: from two row blocks on
+  int pair_grid;         // its CTAs, a whole number of pairs
   size_t sync_bytes, rec_bytes;
 };
 
@@ -35,7 +37,13 @@ HeadLayout head_layout(int batch, int B, int vocab) {
   L.num_n = (vocab + BN - 1) / BN;
   const long long tiles = (long long)L.num_m * L.num_n;
   L.grid = (int)(tiles < num_sms() ? tiles : num_sms());
+  // at most one record per CTA and row block; the paired grid meets a row block with at
+  // most one CTA per pair, min(pair tiles, SMs / 2) <= grid
   L.max_rec = L.grid;
+  L.pair = L.num_m >= 2;
+  const long long pair_tiles = (long long)((L.num_m + 1) / 2) * L.num_n;
+  const long long pairs = num_sms() / 2;
+  L.pair_grid = 2 * (int)(pair_tiles < pairs ? pair_tiles : pairs);
   L.sync_bytes = ((size_t)3 * L.num_m * sizeof(uint32_t) + 255) / 256 * 256;
   L.rec_bytes = (size_t)L.num_m * L.max_rec * BM * sizeof(float4);
   return L;
@@ -76,9 +84,10 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
     if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
+    // paired: each CTA of a pair loads one half (128 vocabulary rows) of the W tile
     const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)vocab};
     const uint64_t strides[1] = {(uint64_t)hidden * 2};
-    const uint32_t box[2] = {BK, BN};
+    const uint32_t box[2] = {BK, (uint32_t)(L.pair ? BN / 2 : BN)};
     if (!encode_tmap_bf16(&tm_w, w, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   Params p{};
@@ -88,7 +97,8 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   p.num_m = L.num_m;
   p.num_n = L.num_n;
   p.num_k = (hidden + BK - 1) / BK;
-  p.num_tiles = p.num_m * p.num_n;
+  p.num_mp = (p.num_m + 1) / 2;
+  p.num_tiles = (L.pair ? p.num_mp : p.num_m) * p.num_n;
   p.part = nullptr;
   p.targets = nullptr;
   p.dlogits = nullptr;
@@ -102,12 +112,17 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   p.tokens = tokens;
   p.maxprob = maxprob;
   p.n_accept = n_accept;
-  static std::atomic<int> attr[64];
-  const cudaError_t ea = set_smem_limit_once(head_gemm_kernel, (int)SMEM_FUSED_BYTES, attr);
-  if (ea != cudaSuccess) return ea;
-  cudaError_t e = cudaMemsetAsync(p.sync, 0, (size_t)3 * L.num_m * sizeof(uint32_t), stream);
+  static std::atomic<int> attr[64], attr_pair[64];
+  cudaError_t e = L.pair ? set_smem_limit_once(head_gemm_pair_kernel, (int)SMEM_FUSED_BYTES, attr_pair)
+                         : set_smem_limit_once(head_gemm_kernel, (int)SMEM_FUSED_BYTES, attr);
   if (e != cudaSuccess) return e;
-  head_gemm_kernel<<<L.grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w, tm_w, p);
+  e = cudaMemsetAsync(p.sync, 0, (size_t)3 * L.num_m * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  if (L.pair)
+    head_gemm_pair_kernel<<<L.pair_grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w,
+                                                                                 tm_w, p);
+  else
+    head_gemm_kernel<<<L.grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w, tm_w, p);
   count_launches(1);
   return cudaGetLastError();
 }

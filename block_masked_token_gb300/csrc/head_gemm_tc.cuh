@@ -53,9 +53,23 @@ constexpr int GROUP_M = 16;                     // row blocks per tile group
 constexpr size_t SLOT_BYTES = (size_t)GROUP_M * BM * sizeof(float4);   // 32 KB
 constexpr size_t SMEM_FUSED_BYTES = SMEM_BYTES + SLOT_BYTES;
 
+// Paired form (head_gemm_pair_kernel): a cluster of two CTAs computes a 256-row x 256-column
+// tile with two-SM MMAs (M256 N256 K16). Each CTA loads its own 128 rows of h and one half
+// (128 vocabulary rows) of the W tile, so a CTA fills 32 KB of shared memory per k-block
+// instead of 48 KB for the same MMA work; the ring then holds six such stages in the same
+// space. The even CTA issues the MMAs; each CTA's epilogue reads its own 128 rows.
+constexpr int GROUP_P = GROUP_M / 2;            // row-block pairs per tile group
+constexpr int STAGES_P = 6;
+constexpr int B_HALF_BYTES = B_BYTES / 2;       // 16 KB
+constexpr int STAGE_BYTES_P = A_BYTES + B_HALF_BYTES;
+static_assert(STAGES_P * STAGE_BYTES_P == STAGES * STAGE_BYTES, "both rings fill the same space");
+constexpr int MAX_STAGES = STAGES_P > STAGES ? STAGES_P : STAGES;
+
 struct Params {
   int rows, hidden, vocab;
-  int num_m, num_n, num_k, num_tiles;
+  // num_tiles counts (row block, vocabulary tile) tiles, or in the paired form (row-block
+  // pair, vocabulary tile) tiles, num_mp = (num_m + 1) / 2 pairs
+  int num_m, num_n, num_k, num_tiles, num_mp;
   float4* part;          // [num_n][rows] {max, sumexp, argmax bits, target logit or 0}
   const int32_t* targets;  // [rows] vocabulary index per row, or NULL (no target logits)
   // Gradient mode (dlogits != NULL): instead of the partials, the epilogue writes
@@ -113,23 +127,30 @@ MARS_DEV int accept_run(const float* pr, int B, float t) {
   return n < 1 ? 1 : n;
 }
 
-// Row block and vocabulary tile of linear tile index `tile` (see the order above).
-MARS_DEV void tile_coords(int tile, const Params& p, int& mb, int& nb) {
-  const int per_group = GROUP_M * p.num_n;
+// Row block (row-block pair when PAIR) and vocabulary tile of linear tile index `tile` (see
+// the order above; a group is 16 row blocks, i.e. 8 pairs).
+template <bool PAIR>
+MARS_DEV void tile_coords(int tile, const Params& p, int& mr, int& nb) {
+  constexpr int GR = PAIR ? GROUP_P : GROUP_M;
+  const int nm = PAIR ? p.num_mp : p.num_m;
+  const int per_group = GR * p.num_n;
   const int g = tile / per_group;
-  const int gm = min(GROUP_M, p.num_m - g * GROUP_M);    // row blocks in this group
+  const int gm = min(GR, nm - g * GR);                   // row blocks (pairs) in this group
   const int local = tile - g * per_group;
-  mb = g * GROUP_M + local % gm;
+  mr = g * GR + local % gm;
   nb = local / gm;
 }
 
-// static: every translation unit that launches it gets its own copy
-static __global__ void __launch_bounds__(NUM_THREADS, 1)
-head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-                 const __grid_constant__ CUtensorMap tm_d, Params p) {
+// The kernel body, one-CTA (PAIR false) or paired form. tm_w's box is 256 vocabulary rows,
+// or 128 in the paired form.
+template <bool PAIR>
+MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
+                             const CUtensorMap& tm_d, const Params& p) {
   using namespace sm100;
+  constexpr int NST = PAIR ? STAGES_P : STAGES;
+  constexpr int SB = PAIR ? STAGE_BYTES_P : STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
   __shared__ uint64_t acc_full[2], acc_empty[2], drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -143,21 +164,27 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* stage_ptr = smem_raw + (sbase - raw);
-  float4* slots = reinterpret_cast<float4*>(stage_ptr + (size_t)STAGES * STAGE_BYTES);
+  float4* slots = reinterpret_cast<float4*>(stage_ptr + (size_t)NST * SB);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the CTA pair (cluster) and this CTA's rank in it: rank 0 issues the MMAs
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int cid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ncl = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     abort_s = 0;
     issued_s = 0;
     consumed_s = 0;
     for (int i = 0; i < GROUP_M; ++i) slot_tiles_s[i] = 0;
-    for (int s = 0; s < STAGES; ++s) {
+    // paired: rank 0's full barriers count the bytes of both CTAs' halves of a stage
+    // (rank 1's are not used); rank 0's acc_empty counts both CTAs' epilogue threads
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], EPI_THREADS);
+      mbar_init(&acc_empty[b], PAIR ? 2 * EPI_THREADS : EPI_THREADS);
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&epi_bar, EPI_THREADS);
@@ -167,12 +194,19 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     if (p.dlogits) prefetch_tmap(&tm_d);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_s, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&tmem_base_s, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_s, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the peer's barriers are initialised before any arrival or commit reaches them
+  if (PAIR) cluster_sync();
   const uint32_t tmem_base = __shfl_sync(0xffffffffu, tmem_base_s, 0);   // warp-uniform
 
   if (warp == 0) {
@@ -180,52 +214,74 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, p, mb, nb);
+      for (int tile = cid; tile < p.num_tiles && ok; tile += ncl) {
+        int mr, nb;
+        tile_coords<PAIR>(tile, p, mr, nb);
+        // this CTA's row block, and its vocabulary rows of the tile (paired: one half;
+        // a row block past the last loads zeros and is skipped by the epilogue)
+        const int mb = PAIR ? 2 * mr + (int)rank : mr;
+        const int wrow = nb * BN + (PAIR ? (int)rank * (BN / 2) : 0);
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1;
           if (!(ok = mbar_wait(&empty_bar[s], ph ^ 1, &abort_s, p.status))) break;
-          uint8_t* a = stage_ptr + s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
-          tma_load_2d(a, &tm_h, &full_bar[s], kb * BK, mb * BM);
-          tma_load_2d(a + A_BYTES, &tm_w, &full_bar[s], kb * BK, nb * BN);
+          uint8_t* a = stage_ptr + s * SB;
+          if (PAIR) {
+            // both halves of the stage land on rank 0's barrier, which expects them both
+            const uint32_t fb = cluster_addr(&full_bar[s], 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * SB);
+            tma_load_2d_pair(a, &tm_h, fb, kb * BK, mb * BM);
+            tma_load_2d_pair(a + A_BYTES, &tm_w, fb, kb * BK, wrow);
+          } else {
+            mbar_arrive_expect_tx(&full_bar[s], SB);
+            tma_load_2d(a, &tm_h, &full_bar[s], kb * BK, mb * BM);
+            tma_load_2d(a + A_BYTES, &tm_w, &full_bar[s], kb * BK, wrow);
+          }
           issued_s = it + 1;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, false);
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, false);
       int it = 0, t = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++t) {
+      for (int tile = cid; tile < p.num_tiles && ok; tile += ncl, ++t) {
         const int buf = t & 1;
         const uint32_t aph = (t >> 1) & 1;
         if (!(ok = mbar_wait(&acc_empty[buf], aph ^ 1, &abort_s, p.status))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1;
           if (!(ok = mbar_wait(&full_bar[s], ph, &abort_s, p.status))) break;
           tc_fence_after();
-          const uint32_t a = smem_u32(stage_ptr + s * STAGE_BYTES);
+          const uint32_t a = smem_u32(stage_ptr + s * SB);
           const uint32_t b = a + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16_ss(d_tmem, sdesc_sw128(a + k * 32, 16, 1024),
-                        sdesc_sw128(b + k * 32, 16, 1024), idesc, (kb | k) != 0);
+            if (PAIR)
+              mma_bf16_ss_pair(d_tmem, sdesc_sw128(a + k * 32, 16, 1024),
+                               sdesc_sw128(b + k * 32, 16, 1024), idesc, (kb | k) != 0);
+            else
+              mma_bf16_ss(d_tmem, sdesc_sw128(a + k * 32, 16, 1024),
+                          sdesc_sw128(b + k * 32, 16, 1024), idesc, (kb | k) != 0);
           }
-          mma_commit(&empty_bar[s]);       // frees the stage once these MMAs finish
+          // frees the stage (in both CTAs) once these MMAs finish
+          if (PAIR) mma_commit_pair(&empty_bar[s], 0x3);
+          else mma_commit(&empty_bar[s]);
           consumed_s = it + 1;
         }
-        if (ok) mma_commit(&acc_full[buf]);
+        if (ok) {
+          if (PAIR) mma_commit_pair(&acc_full[buf], 0x3);
+          else mma_commit(&acc_full[buf]);
+        }
       }
       // make sure no MMA is still in flight when the CTA tears down
-      mma_commit(&drain_bar);
+      if (PAIR) mma_commit_pair(&drain_bar, 0x1);
+      else mma_commit(&drain_bar);
       mbar_wait(&drain_bar, 0, nullptr, p.status);
     }
   } else {
@@ -314,15 +370,31 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     int cur_g = -1;
     uint32_t visited = 0;
     int dl_box = 0;                            // dlogits boxes staged so far (TMA stores)
+    // this tile's accumulator may be overwritten (paired: one arrival per warp of both
+    // CTAs on rank 0's barrier)
+    auto release_acc = [&](int buf) {
+      tc_fence_before();
+      if (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[buf], 0), 32);
+      } else {
+        mbar_arrive(&acc_empty[buf]);
+      }
+    };
     int t = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++t) {
-      int mb, nb;
-      tile_coords(tile, p, mb, nb);
+    for (int tile = cid; tile < p.num_tiles; tile += ncl, ++t) {
+      int mr, nb;
+      tile_coords<PAIR>(tile, p, mr, nb);
+      const int mb = PAIR ? 2 * mr + (int)rank : mr;
       const int buf = t & 1;
       const uint32_t aph = (t >> 1) & 1;
       // warp-uniform result: the tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], aph, &abort_s, p.status))) break;
       tc_fence_after();
+      if (PAIR && mb >= p.num_m) {             // the second half of an odd last pair: no rows
+        release_acc(buf);
+        continue;
+      }
       const uint32_t taddr = tmem_base + buf * BN + ((uint32_t)(quad * 32) << 16);
       const int col0 = nb * BN;
       const int ncols = min(BN, p.vocab - col0);
@@ -388,8 +460,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
           }
         }
         if (!ok) break;
-        tc_fence_before();
-        mbar_arrive(&acc_empty[buf]);
+        release_acc(buf);
         continue;
       }
       float tl = 0.f;
@@ -429,11 +500,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
           ssum += acc;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
+      release_acc(buf);
       if (p.sync) {
         // fold this tile's partial into the running slot of its row block
-        const int g = tile / (GROUP_M * p.num_n);
+        const int g = tile / ((PAIR ? GROUP_P : GROUP_M) * p.num_n);
         const int l = mb - g * GROUP_M;
         if (g != cur_g) {
           if (cur_g >= 0 && !flush_group(cur_g, visited)) break;
@@ -462,17 +532,42 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   }
 
   __syncthreads();
-  // drain: if a wait gave up, wait (bounded) for TMA loads still in flight
+  // drain: if a wait gave up, wait (bounded) for TMA loads still in flight; rank 1's loads
+  // complete on rank 0's barriers, so it gives them a fixed time instead
   if (threadIdx.x == 0 && abort_s) {
-    for (int it = consumed_s; it < issued_s; ++it)
-      mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1, nullptr, p.status);
+    if (PAIR && rank != 0) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 50000) {
+      }
+    } else {
+      for (int it = consumed_s; it < issued_s; ++it)
+        mbar_wait(&full_bar[it % NST], (it / NST) & 1, nullptr, p.status);
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // paired: neither CTA leaves while the other may still arrive on its barriers
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// static: every translation unit that launches them gets its own copy
+static __global__ void __launch_bounds__(NUM_THREADS, 1)
+head_gemm_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+                 const __grid_constant__ CUtensorMap tm_d, Params p) {
+  head_gemm_body<false>(tm_h, tm_w, tm_d, p);
+}
+
+// Paired form: the grid is a whole number of two-CTA clusters.
+static __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+head_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_h,
+                      const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_d, Params p) {
+  head_gemm_body<true>(tm_h, tm_w, tm_d, p);
 }
 
 }  // namespace head_tc

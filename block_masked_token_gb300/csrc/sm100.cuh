@@ -127,6 +127,18 @@ MARS_DEV void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y
       : "memory");
 }
 
+// Tiled 2D load into this CTA's shared memory, whose bytes are counted on an mbarrier of
+// the even CTA of the pair (given by its cluster address): both CTAs' halves of a stage
+// complete one barrier there.
+MARS_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
+                               int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y)
+      : "memory");
+}
+
 // Tiled 2D store from shared memory (bulk async-group), as tma_store_4d.
 MARS_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
   asm volatile(
@@ -209,6 +221,54 @@ MARS_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// ---- Two-SM forms (cta_group::2, a cluster of two CTAs). A kernel uses either these or
+// the one-SM forms above for all of its tcgen05 allocation, MMA and commit instructions.
+// The allocation is collective: one warp of each CTA of the pair executes it, and both
+// get the same TMEM address.
+MARS_DEV void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  __syncwarp();
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+MARS_DEV void tmem_relinquish_pair() {
+  __syncwarp();
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MARS_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  __syncwarp();
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Rank of this CTA in its cluster.
+MARS_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (memory operations before it are visible to
+// all of them after it).
+MARS_DEV void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+MARS_DEV uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+// `count` arrivals on an mbarrier given by its cluster address (this CTA's or a peer's).
+MARS_DEV void mbar_arrive_cluster(uint32_t bar_cluster_addr, uint32_t count) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   bar_cluster_addr),
+               "r"(count)
+               : "memory");
+}
+
 MARS_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MARS_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -237,6 +297,29 @@ MARS_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint
 }
 
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread completed.
+// D[256 x N] (+)= A B^T over the CTA pair, issued by one thread of the even CTA: each CTA
+// holds 128 rows of A and N/2 rows of B at the same shared-memory addresses, and gets its
+// 128 rows of D (all N columns) in its own TMEM at d_tmem.
+MARS_DEV void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One arrival, once the issuing thread's earlier pair MMAs complete, on the mbarrier at the
+// same shared-memory offset in each CTA of `cta_mask`.
+MARS_DEV void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 MARS_DEV void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -557,6 +557,7 @@ def test_head_small(batch, B, hidden, vocab, tau):
     (37, 7, 0.2),          # two straddles and a ragged last row block
     (9, 32, 0.1),          # B = 32 divides 128: no straddle, several sequences per block
     (130, 1, 0.5),         # the AR step's head: one row per sequence, two row blocks
+    (150, 16, 0.4),        # 19 row blocks: a second tile group of 3 (an odd pair count)
 ])
 def test_head_sequences_across_row_blocks(batch, B, tau):
     """The acceptance scan runs where the last partial of a 128-row block is merged; a
