@@ -40,7 +40,7 @@ METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TF
 # of the kernel as it is now, on the workload named beside each: the LM-head GEMM at 2048
 # rows, decode attention on step 0 of the sustained workload, the dual-stream forward at
 # 2L = 8192. None whenever the kernel has changed since its capture.
-TRAFFIC_HEAD_GEMM = 1106327424         # head_gemm_kernel, sustained decode, 2048 rows
+TRAFFIC_HEAD_GEMM = 1106604032         # head_gemm_pair_kernel, sustained decode, 2048 rows
 TRAFFIC_DECODE_STEP0 = 1365940864      # decode_tc_kernel, sustained decode, step 0
 TRAFFIC_DUAL_STREAM = 330413824        # dual_stream_persistent_kernel, 2L = 8192
 CFG = W.SUSTAINED_DECODE_7B
@@ -465,8 +465,9 @@ def run_gpu(args, rank, world, local):
                                  "mars_over_ar": block_cache["tok_s"] / ar["tok_s"]},
             "mars_tau0": {**tau0, "mars_over_ar": tau0["tok_s"] / ar["tok_s"],
                           "note": "coverage run: tau = 0 accepts all B positions"},
-            "roofline": {"kernel": "mars_head_accept (LM-head GEMM; max/sum-exp/argmax and the "
-                                   "acceptance scan in its epilogue)",
+            "roofline": {"kernel": "mars_head_accept (LM-head GEMM on two-SM MMAs over CTA "
+                                   "pairs; max/sum-exp/argmax and the acceptance scan in its "
+                                   "epilogue)",
                          "bound": "tensor", "achieved": head_tflops,
                          "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                          "frac": frac_head, "traffic": TRAFFIC_HEAD_GEMM,
