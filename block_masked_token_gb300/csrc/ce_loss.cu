@@ -176,6 +176,32 @@ cudaError_t head_smem_limit() {
   return set_smem_limit_once(head_tc::head_gemm_kernel, (int)head_tc::SMEM_FUSED_BYTES, attr);
 }
 
+// The LM-head GEMM over h [rows, hidden] and W [vocab, hidden] with p's epilogue (p's
+// mode fields set by the caller; the sizes and tile counts are set here), in its one-SM
+// form: at the loss's 16 384 rows, where the launches run at the power cap, the paired
+// form was slower (forward 10.6-11.0 against 10.3 ms). tm_d is the dlogits map, or NULL.
+cudaError_t launch_head_gemm(const uint16_t* h, const uint16_t* w, int rows, int hidden,
+                             int vocab, head_tc::Params& p, const CUtensorMap* tm_d,
+                             size_t smem, cudaStream_t stream) {
+  using namespace head_tc;
+  p.rows = rows;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.num_m = (rows + BM - 1) / BM;
+  p.num_n = (vocab + BN - 1) / BN;
+  p.num_k = (hidden + BK - 1) / BK;
+  p.num_mp = (p.num_m + 1) / 2;
+  p.num_tiles = p.num_m * p.num_n;
+  CUtensorMap tm_h, tm_w;
+  if (!map2d(&tm_h, h, hidden, rows, BK, BM) || !map2d(&tm_w, w, hidden, vocab, BK, BN))
+    return cudaErrorInvalidValue;
+  const cudaError_t ea = head_smem_limit();
+  if (ea != cudaSuccess) return ea;
+  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  head_gemm_kernel<<<grid, NUM_THREADS, smem, stream>>>(tm_h, tm_w, tm_d ? *tm_d : tm_w, p);
+  return cudaGetLastError();
+}
+
 size_t grad_dlogits_bytes(int batch, int L, int vocab) {
   const size_t n = (size_t)batch * 2 * L * vocab * sizeof(uint16_t);
   return (n + 255) / 256 * 256;
@@ -196,27 +222,7 @@ cudaError_t launch_ce_loss_grad(const uint16_t* h, const uint16_t* w, const int3
   uint16_t* dlogits = static_cast<uint16_t*>(workspace);
   float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                           grad_dlogits_bytes(batch, L, vocab));
-  CUtensorMap tm_h, tm_w;
-  {
-    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)rows};
-    const uint64_t strides[1] = {(uint64_t)hidden * 2};
-    const uint32_t box[2] = {BK, BM};
-    if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)vocab};
-    const uint64_t strides[1] = {(uint64_t)hidden * 2};
-    const uint32_t box[2] = {BK, BN};
-    if (!encode_tmap_bf16(&tm_w, w, 2, dims, strides, box)) return cudaErrorInvalidValue;
-  }
   Params p{};
-  p.rows = rows;
-  p.hidden = hidden;
-  p.vocab = vocab;
-  p.num_m = (rows + BM - 1) / BM;
-  p.num_n = (vocab + BN - 1) / BN;
-  p.num_k = (hidden + BK - 1) / BK;
-  p.num_tiles = p.num_m * p.num_n;
   p.targets = targets;
   p.dlogits = dlogits;
   p.row_lse = row_lse;
@@ -226,14 +232,11 @@ cudaError_t launch_ce_loss_grad(const uint16_t* h, const uint16_t* w, const int3
   // dlogits, stored in boxes of 64 columns x 128 rows
   CUtensorMap tm_d;
   if (!map2d(&tm_d, dlogits, vocab, rows, 64, BM)) return cudaErrorInvalidValue;
-  const cudaError_t ea = head_smem_limit();
-  if (ea != cudaSuccess) return ea;
   ce_scale_kernel<<<1, 256, 0, stream>>>(targets, batch, L, vocab, scale);
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_FUSED_BYTES, stream>>>(tm_h, tm_w, tm_d, p);
+  cudaError_t e = launch_head_gemm(h, w, rows, hidden, vocab, p, &tm_d, SMEM_FUSED_BYTES, stream);
+  if (e != cudaSuccess) return e;
   count_launches(2);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || (!dh && !dw)) return e;
+  if (!dh && !dw) return cudaSuccess;
 
   // dh [rows, H] = dlogits [rows, V] . W [V, H]: A K-major, B (W) MN-major
   if (dh) {
@@ -271,38 +274,17 @@ cudaError_t launch_ce_loss(const uint16_t* h, const uint16_t* w, const int32_t* 
                            cudaStream_t stream) {
   using namespace head_tc;
   const int rows = batch * 2 * L;
-  CUtensorMap tm_h, tm_w;
-  {
-    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)rows};
-    const uint64_t strides[1] = {(uint64_t)hidden * 2};
-    const uint32_t box[2] = {BK, BM};
-    if (!encode_tmap_bf16(&tm_h, h, 2, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[2] = {(uint64_t)hidden, (uint64_t)vocab};
-    const uint64_t strides[1] = {(uint64_t)hidden * 2};
-    const uint32_t box[2] = {BK, BN};
-    if (!encode_tmap_bf16(&tm_w, w, 2, dims, strides, box)) return cudaErrorInvalidValue;
-  }
   Params p{};
-  p.rows = rows;
-  p.hidden = hidden;
-  p.vocab = vocab;
-  p.num_m = (rows + BM - 1) / BM;
-  p.num_n = (vocab + BN - 1) / BN;
-  p.num_k = (hidden + BK - 1) / BK;
-  p.num_tiles = p.num_m * p.num_n;
   p.part = static_cast<float4*>(workspace);
   p.targets = targets;
   p.dlogits = nullptr;
   p.status = status;
+  const cudaError_t e = launch_head_gemm(h, w, rows, hidden, vocab, p, nullptr, SMEM_BYTES,
+                                         stream);
+  if (e != cudaSuccess) return e;
   float* ce = row_ce ? row_ce
                      : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                                 (size_t)rows * p.num_n * sizeof(float4));
-  const cudaError_t ea = head_smem_limit();
-  if (ea != cudaSuccess) return ea;
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  head_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, tm_w, p);
   ce_rows_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(p.part, targets, rows, p.num_n, vocab,
                                                       ce, row_lse, status);
   ce_reduce_kernel<<<1, 256, 0, stream>>>(ce, targets, batch, L, vocab, loss);
