@@ -41,7 +41,7 @@ METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TF
 # rows, decode attention on step 0 of the sustained workload, the dual-stream forward at
 # 2L = 8192. None whenever the kernel has changed since its capture.
 TRAFFIC_HEAD_GEMM = 1106604032         # head_gemm_pair_kernel, sustained decode, 2048 rows
-TRAFFIC_DECODE_STEP0 = 1365940864      # decode_tc_kernel, sustained decode, step 0
+TRAFFIC_DECODE_STEP0 = 1365940480      # decode_tc_kernel, sustained decode, step 0
 TRAFFIC_DUAL_STREAM = 330413824        # dual_stream_persistent_kernel, 2L = 8192
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
