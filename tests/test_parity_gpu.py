@@ -537,6 +537,9 @@ def test_decode_config_7b_sampled():
     (4, 8, 512, 3000, 1.0),         # tau 1: plain AR
     (2, 32, 96, 300, 0.3),
     (1, 4, 64, 1, 1.0),             # one-word vocabulary: p = 1 >= tau = 1, the whole block
+    (20, 16, 128, 77, 0.5),         # 320 rows (paired form) over a vocabulary smaller than
+                                    # one W half: the odd CTA's half is all past the end
+    (17, 16, 64, 1, 1.0),           # paired form, one-word vocabulary
 ])
 def test_head_small(batch, B, hidden, vocab, tau):
     cfg = W.DecodeConfig("h", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
