@@ -126,7 +126,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!(ok = mbar_wait(&empty_bar[s], ph ^ 1, &abort_s, p.status))) break;
+          if (!(ok = mbar_wait_suspending(&empty_bar[s], ph ^ 1, &abort_s, p.status))) break;
           uint8_t* a = stage_ptr + s * STAGE_BYTES;
           mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
           load_operand<A_MN>(a, &tm_a, &full_bar[s], mb * BM, kb, BM);
@@ -144,13 +144,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++t) {
         const int buf = t & 1;
         const uint32_t aph = (t >> 1) & 1;
-        if (!(ok = mbar_wait(&acc_empty[buf], aph ^ 1, &abort_s, p.status))) break;
+        if (!(ok = mbar_wait_suspending(&acc_empty[buf], aph ^ 1, &abort_s, p.status))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!(ok = mbar_wait(&full_bar[s], ph, &abort_s, p.status))) break;
+          if (!(ok = mbar_wait_suspending(&full_bar[s], ph, &abort_s, p.status))) break;
           tc_fence_after();
           const uint32_t a = smem_u32(stage_ptr + s * STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
@@ -165,7 +165,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       }
       // make sure no MMA is still in flight when the CTA tears down
       mma_commit(&drain_bar);
-      mbar_wait(&drain_bar, 0, nullptr, p.status);
+      mbar_wait_suspending(&drain_bar, 0, nullptr, p.status);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -177,7 +177,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
       const int buf = t & 1;
       const uint32_t aph = (t >> 1) & 1;
       // warp-uniform result: the tcgen05.ld below is warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], aph, &abort_s, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_suspending(&acc_full[buf], aph, &abort_s, p.status))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + buf * BN + ((uint32_t)(quad * 32) << 16);
       const int row = mb * BM + row_in_tile;
@@ -212,7 +212,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CU
   // drain: if a wait gave up, wait (bounded) for TMA loads still in flight
   if (threadIdx.x == 0 && abort_s) {
     for (int it = consumed_s; it < issued_s; ++it)
-      mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1, nullptr, p.status);
+      mbar_wait_suspending(&full_bar[it % STAGES], (it / STAGES) & 1, nullptr, p.status);
   }
   tc_fence_before();
   __syncthreads();

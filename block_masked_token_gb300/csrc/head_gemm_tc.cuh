@@ -224,7 +224,7 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
           const int s = it % NST;
           const uint32_t ph = (it / NST) & 1;
-          if (!(ok = mbar_wait(&empty_bar[s], ph ^ 1, &abort_s, p.status))) break;
+          if (!(ok = mbar_wait_suspending(&empty_bar[s], ph ^ 1, &abort_s, p.status))) break;
           uint8_t* a = stage_ptr + s * SB;
           if (PAIR) {
             // both halves of the stage land on rank 0's barrier, which expects them both
@@ -250,13 +250,13 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
       for (int tile = cid; tile < p.num_tiles && ok; tile += ncl, ++t) {
         const int buf = t & 1;
         const uint32_t aph = (t >> 1) & 1;
-        if (!(ok = mbar_wait(&acc_empty[buf], aph ^ 1, &abort_s, p.status))) break;
+        if (!(ok = mbar_wait_suspending(&acc_empty[buf], aph ^ 1, &abort_s, p.status))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int kb = 0; kb < p.num_k; ++kb, ++it) {
           const int s = it % NST;
           const uint32_t ph = (it / NST) & 1;
-          if (!(ok = mbar_wait(&full_bar[s], ph, &abort_s, p.status))) break;
+          if (!(ok = mbar_wait_suspending(&full_bar[s], ph, &abort_s, p.status))) break;
           tc_fence_after();
           const uint32_t a = smem_u32(stage_ptr + s * SB);
           const uint32_t b = a + A_BYTES;
@@ -282,7 +282,7 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
       // make sure no MMA is still in flight when the CTA tears down
       if (PAIR) mma_commit_pair(&drain_bar, 0x1);
       else mma_commit(&drain_bar);
-      mbar_wait(&drain_bar, 0, nullptr, p.status);
+      mbar_wait_suspending(&drain_bar, 0, nullptr, p.status);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -296,7 +296,7 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
     uint32_t epi_phase = 0;
     auto epi_sync = [&]() -> bool {
       mbar_arrive(&epi_bar);
-      const bool ok = mbar_wait(&epi_bar, epi_phase & 1u, &abort_s, p.status);
+      const bool ok = mbar_wait_suspending(&epi_bar, epi_phase & 1u, &abort_s, p.status);
       ++epi_phase;
       return ok;
     };
@@ -389,7 +389,7 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
       const int buf = t & 1;
       const uint32_t aph = (t >> 1) & 1;
       // warp-uniform result: the tcgen05.ld below is warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], aph, &abort_s, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_suspending(&acc_full[buf], aph, &abort_s, p.status))) break;
       tc_fence_after();
       if (PAIR && mb >= p.num_m) {             // the second half of an odd last pair: no rows
         release_acc(buf);
@@ -541,7 +541,7 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
       }
     } else {
       for (int it = consumed_s; it < issued_s; ++it)
-        mbar_wait(&full_bar[it % NST], (it / NST) & 1, nullptr, p.status);
+        mbar_wait_suspending(&full_bar[it % NST], (it / NST) & 1, nullptr, p.status);
     }
   }
   tc_fence_before();

@@ -80,10 +80,25 @@ MARS_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase (much cheaper than try_wait when it has completed).
+MARS_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with `parity` to complete. Gives up (returns false) when
 // *abort is set by another role, or after kWaitNs, flagging MARS_ST_TIMEOUT.
-MARS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                        int32_t* status) {
+// mbar_wait first tests the phase without suspending (a completed phase is seen at a
+// fraction of try_wait's cost); mbar_wait_suspending goes straight to try_wait.
+MARS_DEV bool mbar_wait_suspending(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                   int32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
@@ -96,6 +111,12 @@ MARS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
     }
   }
 }
+
+MARS_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                        int32_t* status) {
+  return mbar_test_wait(bar, parity) || mbar_wait_suspending(bar, parity, abort, status);
+}
+
 
 // ------------------------------------------------------------------------------ TMA
 
