@@ -13,6 +13,10 @@
 //   warps 2..5  epilogue: thread = accumulator row (TMEM lane), 256 columns read with
 //               tcgen05.ld, online max / argmax / sum-exp, one 16-byte store per row
 //               (the gradient mode instead stages bf16 dlogits boxes for TMA stores).
+// Paired form (head_gemm_pair_kernel, two-CTA clusters): the pair computes a 256 x 256
+// tile with tcgen05.mma.cta_group::2 (M256 N256 K16) issued by the even CTA; each CTA
+// loads its own 128 rows of h and half of the W tile into a 6-stage ring of 32 KB, both
+// halves counted on the even CTA's barrier, and each CTA's epilogue reads its own rows.
 // Tiles are ordered in groups of up to 16 row blocks (2048 rows): inside a group the row
 // block is fastest, so the CTAs running at the same time share one W tile through L2, and
 // the group's rows of h (at most 14.7 MB at hidden 3584) stay in L2 while the group sweeps
