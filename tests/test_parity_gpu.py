@@ -540,6 +540,7 @@ def test_decode_config_7b_sampled():
     (20, 16, 128, 77, 0.5),         # 320 rows (paired form) over a vocabulary smaller than
                                     # one W half: the odd CTA's half is all past the end
     (17, 16, 64, 1, 1.0),           # paired form, one-word vocabulary
+    (20, 16, 200, 1000, 0.3),       # paired form, hidden 200: a ragged last k-block
 ])
 def test_head_small(batch, B, hidden, vocab, tau):
     cfg = W.DecodeConfig("h", batch=batch, prefix_lo=1, prefix_hi=1, B=B, hq=1, hkv=1, d=64,
