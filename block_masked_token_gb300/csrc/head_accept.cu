@@ -96,7 +96,7 @@ cudaError_t launch_head_accept(const uint16_t* h, const uint16_t* w, int batch, 
   p.vocab = vocab;
   p.num_m = L.num_m;
   p.num_n = L.num_n;
-  p.num_k = (hidden + BK - 1) / BK;
+  p.num_k = L.pair ? (hidden + BK_P - 1) / BK_P : (hidden + BK - 1) / BK;
   p.num_mp = (p.num_m + 1) / 2;
   p.num_tiles = (L.pair ? p.num_mp : p.num_m) * p.num_n;
   p.part = nullptr;

@@ -15,8 +15,9 @@
 //               (the gradient mode instead stages bf16 dlogits boxes for TMA stores).
 // Paired form (head_gemm_pair_kernel, two-CTA clusters): the pair computes a 256 x 256
 // tile with tcgen05.mma.cta_group::2 (M256 N256 K16) issued by the even CTA; each CTA
-// loads its own 128 rows of h and half of the W tile into a 6-stage ring of 32 KB, both
-// halves counted on the even CTA's barrier, and each CTA's epilogue reads its own rows.
+// loads its own 128 rows of h and half of the W tile, k-blocks of 128 as two 64-column
+// boxes each, into a 3-stage ring of 64 KB, both halves counted on the even CTA's
+// barrier, and each CTA's epilogue reads its own rows.
 // Tiles are ordered in groups of up to 16 row blocks (2048 rows): inside a group the row
 // block is fastest, so the CTAs running at the same time share one W tile through L2, and
 // the group's rows of h (at most 14.7 MB at hidden 3584) stay in L2 while the group sweeps
@@ -59,13 +60,16 @@ constexpr size_t SMEM_FUSED_BYTES = SMEM_BYTES + SLOT_BYTES;
 
 // Paired form (head_gemm_pair_kernel): a cluster of two CTAs computes a 256-row x 256-column
 // tile with two-SM MMAs (M256 N256 K16). Each CTA loads its own 128 rows of h and one half
-// (128 vocabulary rows) of the W tile, so a CTA fills 32 KB of shared memory per k-block
-// instead of 48 KB for the same MMA work; the ring then holds six such stages in the same
-// space. The even CTA issues the MMAs; each CTA's epilogue reads its own 128 rows.
+// (128 vocabulary rows) of the W tile, so a CTA fills a third less shared memory per unit
+// of MMA work. Its k-blocks are 128 wide (two 64-column boxes per operand), three 64 KB
+// stages in the same space: fewer stage hand-offs per tile than six stages of 32 KB. The
+// even CTA issues the MMAs; each CTA's epilogue reads its own 128 rows.
 constexpr int GROUP_P = GROUP_M / 2;            // row-block pairs per tile group
-constexpr int STAGES_P = 6;
-constexpr int B_HALF_BYTES = B_BYTES / 2;       // 16 KB
-constexpr int STAGE_BYTES_P = A_BYTES + B_HALF_BYTES;
+constexpr int STAGES_P = 3;
+constexpr int BK_P = 128;
+constexpr int A_BYTES_P = BM * BK_P * 2;        // 32 KB: two [128][64] regions
+constexpr int B_HALF_BYTES = (BN / 2) * BK_P * 2;       // 32 KB
+constexpr int STAGE_BYTES_P = A_BYTES_P + B_HALF_BYTES;
 static_assert(STAGES_P * STAGE_BYTES_P == STAGES * STAGE_BYTES, "both rings fill the same space");
 constexpr int MAX_STAGES = STAGES_P > STAGES ? STAGES_P : STAGES;
 
@@ -153,6 +157,8 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
   using namespace sm100;
   constexpr int NST = PAIR ? STAGES_P : STAGES;
   constexpr int SB = PAIR ? STAGE_BYTES_P : STAGE_BYTES;
+  constexpr int KB = PAIR ? BK_P : BK;
+  constexpr int AB = PAIR ? A_BYTES_P : A_BYTES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
   __shared__ uint64_t acc_full[2], acc_empty[2], drain_bar;
@@ -234,8 +240,10 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
             // both halves of the stage land on rank 0's barrier, which expects them both
             const uint32_t fb = cluster_addr(&full_bar[s], 0);
             if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * SB);
-            tma_load_2d_pair(a, &tm_h, fb, kb * BK, mb * BM);
-            tma_load_2d_pair(a + A_BYTES, &tm_w, fb, kb * BK, wrow);
+            for (int x = 0; x < KB / 64; ++x) {
+              tma_load_2d_pair(a + x * (BM * 128), &tm_h, fb, kb * KB + x * 64, mb * BM);
+              tma_load_2d_pair(a + AB + x * ((BN / 2) * 128), &tm_w, fb, kb * KB + x * 64, wrow);
+            }
           } else {
             mbar_arrive_expect_tx(&full_bar[s], SB);
             tma_load_2d(a, &tm_h, &full_bar[s], kb * BK, mb * BM);
@@ -263,12 +271,14 @@ MARS_DEV void head_gemm_body(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
           if (!(ok = mbar_wait_suspending(&full_bar[s], ph, &abort_s, p.status))) break;
           tc_fence_after();
           const uint32_t a = smem_u32(stage_ptr + s * SB);
-          const uint32_t b = a + A_BYTES;
+          const uint32_t b = a + AB;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+          for (int k = 0; k < KB / 16; ++k) {
             if (PAIR)
-              mma_bf16_ss_pair(d_tmem, sdesc_sw128(a + k * 32, 16, 1024),
-                               sdesc_sw128(b + k * 32, 16, 1024), idesc, (kb | k) != 0);
+              mma_bf16_ss_pair(d_tmem,
+                               sdesc_sw128(a + (k >> 2) * (BM * 128) + (k & 3) * 32, 16, 1024),
+                               sdesc_sw128(b + (k >> 2) * ((BN / 2) * 128) + (k & 3) * 32, 16, 1024),
+                               idesc, (kb | k) != 0);
             else
               mma_bf16_ss(d_tmem, sdesc_sw128(a + k * 32, 16, 1024),
                           sdesc_sw128(b + k * 32, 16, 1024), idesc, (kb | k) != 0);
