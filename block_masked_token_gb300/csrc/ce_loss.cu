@@ -169,17 +169,19 @@ bool map2d(CUtensorMap* m, const void* base, int inner, int outer, uint32_t box_
   return encode_tmap_bf16(m, base, 2, dims, strides, box);
 }
 
-// Both head launches of this file share one copy of the kernel and so one dynamic
+// Both head launches of this file share one copy of each kernel form and so one dynamic
 // shared-memory limit: the larger of the two they use.
-cudaError_t head_smem_limit() {
-  static std::atomic<int> attr[64];
-  return set_smem_limit_once(head_tc::head_gemm_kernel, (int)head_tc::SMEM_FUSED_BYTES, attr);
+cudaError_t head_smem_limit(bool pair) {
+  static std::atomic<int> attr[64], attr_pair[64];
+  return pair ? set_smem_limit_once(head_tc::head_gemm_pair_kernel,
+                                    (int)head_tc::SMEM_FUSED_BYTES, attr_pair)
+              : set_smem_limit_once(head_tc::head_gemm_kernel, (int)head_tc::SMEM_FUSED_BYTES,
+                                    attr);
 }
 
 // The LM-head GEMM over h [rows, hidden] and W [vocab, hidden] with p's epilogue (p's
-// mode fields set by the caller; the sizes and tile counts are set here), in its one-SM
-// form: at the loss's 16 384 rows, where the launches run at the power cap, the paired
-// form was slower (forward 10.6-11.0 against 10.3 ms). tm_d is the dlogits map, or NULL.
+// mode fields set by the caller; the sizes and tile counts are set here): the paired form
+// from two row blocks on. tm_d is the dlogits map, or NULL.
 cudaError_t launch_head_gemm(const uint16_t* h, const uint16_t* w, int rows, int hidden,
                              int vocab, head_tc::Params& p, const CUtensorMap* tm_d,
                              size_t smem, cudaStream_t stream) {
@@ -189,16 +191,25 @@ cudaError_t launch_head_gemm(const uint16_t* h, const uint16_t* w, int rows, int
   p.vocab = vocab;
   p.num_m = (rows + BM - 1) / BM;
   p.num_n = (vocab + BN - 1) / BN;
-  p.num_k = (hidden + BK - 1) / BK;
+  const bool pair = p.num_m >= 2;
+  p.num_k = pair ? (hidden + BK_P - 1) / BK_P : (hidden + BK - 1) / BK;
   p.num_mp = (p.num_m + 1) / 2;
-  p.num_tiles = p.num_m * p.num_n;
+  p.num_tiles = (pair ? p.num_mp : p.num_m) * p.num_n;
   CUtensorMap tm_h, tm_w;
-  if (!map2d(&tm_h, h, hidden, rows, BK, BM) || !map2d(&tm_w, w, hidden, vocab, BK, BN))
+  if (!map2d(&tm_h, h, hidden, rows, BK, BM) ||
+      !map2d(&tm_w, w, hidden, vocab, BK, pair ? BN / 2 : BN))
     return cudaErrorInvalidValue;
-  const cudaError_t ea = head_smem_limit();
+  const cudaError_t ea = head_smem_limit(pair);
   if (ea != cudaSuccess) return ea;
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  head_gemm_kernel<<<grid, NUM_THREADS, smem, stream>>>(tm_h, tm_w, tm_d ? *tm_d : tm_w, p);
+  if (pair) {
+    const int pairs = num_sms() / 2;
+    const int grid = 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
+    head_gemm_pair_kernel<<<grid, NUM_THREADS, smem, stream>>>(tm_h, tm_w, tm_d ? *tm_d : tm_w,
+                                                                p);
+  } else {
+    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+    head_gemm_kernel<<<grid, NUM_THREADS, smem, stream>>>(tm_h, tm_w, tm_d ? *tm_d : tm_w, p);
+  }
   return cudaGetLastError();
 }
 
