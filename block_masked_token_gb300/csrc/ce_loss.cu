@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(256) ce_scale_kernel(const int32_t* __restrict
   if (threadIdx.x < 2) scale[threadIdx.x] = s_cnt[threadIdx.x][0] ? 1.f / s_cnt[threadIdx.x][0] : 0.f;
 }
 
-// C [M, N] (ldc = N) = A B with the tcgen05 GEMM; the maps hold A and B in the layouts
-// its template arguments name.
+// C [M, N] (ldc = N) = A B with the tcgen05 GEMM, in its paired form from two row blocks
+// on; the maps hold A and B in the layouts its template arguments name (B MN-major).
 template <bool A_MN, bool B_MN>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
                         float* c, int32_t* status, cudaStream_t stream) {
@@ -146,16 +146,25 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int
   p.K = K;
   p.num_m = (M + BM - 1) / BM;
   p.num_n = (N + BN - 1) / BN;
-  p.num_k = (K + BK - 1) / BK;
-  p.num_tiles = p.num_m * p.num_n;
+  const bool pair = p.num_m >= 2;
+  p.num_k = pair ? (K + BK_P - 1) / BK_P : (K + BK - 1) / BK;
+  p.num_tiles = (pair ? (p.num_m + 1) / 2 : p.num_m) * p.num_n;
   p.c = c;
   p.ldc = N;
   p.status = status;
-  static std::atomic<int> attr[64];
-  const cudaError_t ea = set_smem_limit_once(gemm_kernel<A_MN, B_MN>, (int)SMEM_BYTES, attr);
+  static std::atomic<int> attr[64], attr_pair[64];
+  const cudaError_t ea =
+      pair ? set_smem_limit_once(gemm_pair_kernel<A_MN, B_MN>, (int)SMEM_BYTES, attr_pair)
+           : set_smem_limit_once(gemm_kernel<A_MN, B_MN>, (int)SMEM_BYTES, attr);
   if (ea != cudaSuccess) return ea;
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
-  gemm_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  if (pair) {
+    const int pairs = num_sms() / 2;
+    const int grid = 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
+    gemm_pair_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  } else {
+    const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+    gemm_kernel<A_MN, B_MN><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
