@@ -338,8 +338,9 @@ dual_stream_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
 // attention gradient. Work items, their key tiles and the masks are the forward's; per key
 // tile three MMAs (S, dP, dQ += dS K) with dQ accumulated in TMEM and written once per row.
 // TMEM: S at column 0, dP at 128, dQ at 256, dS (bf16 pairs, 64 columns) at 384. S and dP
-// are free once the math warps have loaded them, so the next tile's S and dP never wait
-// for a dQ MMA and the tensor pipe does not drain between tiles. Warps: 0 K loader,
+// are each free once the math warps have loaded them, so the next tile's S and dP never
+// wait for a dQ MMA, and the math warps form P as soon as S has landed, loading dP only
+// for dS: the next tile's S runs under this tile's exponentials. Warps: 0 K loader,
 // 1 TMEM owner and S/dP issuer (it also loads each item's Q and dO), 2..9 math (two per
 // TMEM lane quadrant, 64 key columns each), 10 V loader, 11 dQ issuer. The shared-memory
 // operand MMAs (S, dP) and the TMEM-operand ones (dQ) come from two threads on different
@@ -350,7 +351,7 @@ constexpr int DQ_V_WARP = 2 + DQ_MATH_WARPS;
 constexpr int DQ_ISSUE_WARP = 3 + DQ_MATH_WARPS;
 
 struct DQBar {
-  uint64_t s_full, dp_full, sp_free, ds_full, dq_done, acc_free;
+  uint64_t s_full, dp_full, s_free, dp_free, ds_full, dq_done, acc_free;
 };
 
 struct DQArgs {
@@ -384,7 +385,8 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&qb.s_full, 1);
     mbar_init(&qb.dp_full, 1);
     mbar_init(&qb.dq_done, 1);
-    mbar_init(&qb.sp_free, 32 * DQ_MATH_WARPS);
+    mbar_init(&qb.s_free, 32 * DQ_MATH_WARPS);
+    mbar_init(&qb.dp_free, 32 * DQ_MATH_WARPS);
     mbar_init(&qb.ds_full, 32 * DQ_MATH_WARPS);
     mbar_init(&qb.acc_free, 32 * DQ_MATH_WARPS);
   }
@@ -424,21 +426,21 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(BQ, BKV, false);   // S, dP: K-major A and B
-      const uint32_t qa = smem_u32(smem + S::OFF_Q), da_ = smem_u32(smem + S::OFF_STAGE);
+      const uint64_t qd = sdesc_sw128(smem_u32(smem + S::OFF_Q), 16, 1024);
+      const uint64_t dd = sdesc_sw128(smem_u32(smem + S::OFF_STAGE), 16, 1024);
       int jg0 = 0, i = 0, nq = 0;
       bool ok = true;
       auto issue_s = [&](int jg) -> bool {                // S_jg = Q K^T
         const int st = jg % flash::K_STAGES;
         if (!mbar_wait(&bar.k_full[st], (jg / flash::K_STAGES) & 1, ab, a.status)) return false;
-        // S and dP of the previous tile have been loaded by the math warps
-        if (jg >= 1 && !mbar_wait(&qb.sp_free, (jg - 1) & 1, ab, a.status)) return false;
+        // S of the previous tile has been loaded by the math warps
+        if (jg >= 1 && !mbar_wait(&qb.s_free, (jg - 1) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+        const uint64_t kd = sdesc_sw128(smem_u32(smem + S::OFF_K + st * S::KV_BYTES), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + TM_S, sdesc_sw128(qa + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), id_s, k != 0);
+          mma_bf16_ss(tmem + TM_S, sdesc_advance(qd, off), sdesc_advance(kd, off), id_s, k != 0);
         }
         mma_commit(&qb.s_full);
         return true;
@@ -446,13 +448,14 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
       auto issue_dp = [&](int jg) -> bool {               // dP_jg = dO V^T (after issue_s(jg))
         const int st = jg % flash::V_STAGES;
         if (!mbar_wait(&bar.v_full[st], (jg / flash::V_STAGES) & 1, ab, a.status)) return false;
+        // dP of the previous tile has been loaded by the math warps
+        if (jg >= 1 && !mbar_wait(&qb.dp_free, (jg - 1) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
+        const uint64_t vd = sdesc_sw128(smem_u32(smem + S::OFF_V + st * S::KV_BYTES), 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + TM_DP, sdesc_sw128(da_ + off, 16, 1024),
-                      sdesc_sw128(vb + off, 16, 1024), id_s, k != 0);
+          mma_bf16_ss(tmem + TM_DP, sdesc_advance(dd, off), sdesc_advance(vd, off), id_s, k != 0);
         }
         mma_commit(&qb.dp_full);
         mma_commit(&bar.v_empty[st]);
@@ -501,11 +504,12 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
           if (!(ok = mbar_wait(&bar.k_full[st], (jg / flash::K_STAGES) & 1, ab, a.status))) break;
           if (!(ok = mbar_wait(&qb.ds_full, jg & 1, ab, a.status))) break;
           tc_fence_after();
-          const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+          const uint64_t kd = sdesc_sw128(smem_u32(smem + S::OFF_K + st * S::KV_BYTES),
+                                          BKV * 128, 1024);
 #pragma unroll
           for (int k = 0; k < BKV / 16; ++k)             // dQ += dS K (K tile MN-major)
-            mma_bf16_ts(tmem + TM_DQ, tmem + TM_DS + 8 * k,
-                        sdesc_sw128(kb + k * 2048, BKV * 128, 1024), id_q, (jl | k) != 0);
+            mma_bf16_ts(tmem + TM_DQ, tmem + TM_DS + 8 * k, sdesc_advance(kd, k * 2048), id_q,
+                        (jl | k) != 0);
           mma_commit(&qb.dq_done);
           // S_jg, which also read this stage, completed before the math warps wrote dS_jg
           mma_commit(&bar.k_empty[st]);
@@ -545,19 +549,15 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         const typename Pol::Tile tile = pol.tile(jl);
         const flash::ColRange cr = rv ? pol.cols(vis, tile) : flash::ColRange{0, 0, -1, 0u};
         if (!(ok = warp_wait(&qb.s_full, jg & 1))) break;
-        if (!(ok = warp_wait(&qb.dp_full, jg & 1))) break;
         tc_fence_after();
-        uint32_t sv[64], pv[64];
+        uint32_t sv[64];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < 2; ++q)
           tmem_ld32(tmem + TM_S + 64 * half + 32 * q + lane_off,
                     *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q));
-          tmem_ld32(tmem + TM_DP + 64 * half + 32 * q + lane_off,
-                    *reinterpret_cast<uint32_t(*)[32]>(pv + 32 * q));
-        }
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive_warp(&qb.sp_free);
+        mbar_arrive_warp(&qb.s_free);
         // masked keys become -inf (exp2 gives 0) where the tile is not fully visible
         if (!rv || !tile.full) {
 #pragma unroll
@@ -568,8 +568,8 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
               if (!((mk >> e) & 1u)) sv[32 * q + e] = 0xff800000u;
           }
         }
-        // P = exp2(scale log2e S - lse) rounded to bf16 (as the key-tile kernel's P),
-        // dS = P * (dP - D), in packed f32x2 operations
+        // P = exp2(scale log2e S - lse) rounded to bf16 (as the key-tile kernel's P), then,
+        // once dP has landed, dS = P * (dP - D), in packed f32x2 operations
         uint32_t ds[32];
         const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
         const float2 nl2 = make_float2(-lse, -lse), nd2 = make_float2(-dd, -dd);
@@ -577,8 +577,21 @@ dual_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int e = 0; e < 64; e += 2) {
           const float2 t = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
                                       sc2, nl2);
-          const uint32_t pb = flash::pack_bf16x2(flash::ex2_approx(t.x), flash::ex2_approx(t.y));
-          const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb));
+          ds[e / 2] = flash::pack_bf16x2(flash::ex2_approx(t.x), flash::ex2_approx(t.y));
+        }
+        if (!(ok = warp_wait(&qb.dp_full, jg & 1))) break;
+        tc_fence_after();
+        uint32_t pv[64];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          tmem_ld32(tmem + TM_DP + 64 * half + 32 * q + lane_off,
+                    *reinterpret_cast<uint32_t(*)[32]>(pv + 32 * q));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&qb.dp_free);
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ds[e / 2]));
           const float2 x = __fmul2_rn(pf, __fadd2_rn(make_float2(__uint_as_float(pv[e]),
                                                                  __uint_as_float(pv[e + 1])), nd2));
           ds[e / 2] = flash::pack_bf16x2(x.x, x.y);

@@ -322,19 +322,20 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ------------------------------------------------------- S^T and dP^T MMAs
     if (lane == 0) {
       const uint32_t id_qk = idesc_ab(GT, GT, false, false);   // S^T, dP^T: K-major A, B
-      const uint32_t kb = smem_u32(smem + S::OFF_K), vb = smem_u32(smem + S::OFF_V);
+      const uint64_t kd = sdesc_sw128(smem_u32(smem + S::OFF_K), 16, 1024);
+      const uint64_t vd = sdesc_sw128(smem_u32(smem + S::OFF_V), 16, 1024);
       auto stage_of = [&](int g2) { return smem_u32(smem + S::OFF_RING + (g2 % NSTAGE) * S::STAGE); };
       auto issue_st = [&](int g2) -> bool {            // S^T = K Q^T of pair g2
         if (!mbar_wait(&bar.full[g2 % NSTAGE], (g2 / NSTAGE) & 1, ab, a.status)) return false;
         // the S buffer holds P^T of the previous pair until its dV MMA has read it
         if (g2 > 0 && !mbar_wait(&bar.dv_done, (g2 - 1) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t qb = stage_of(g2) + S::ST_Q;
+        const uint64_t qd = sdesc_sw128(stage_of(g2) + S::ST_Q, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + S::TM_S, sdesc_sw128(kb + off, 16, 1024),
-                      sdesc_sw128(qb + off, 16, 1024), id_qk, k != 0);
+          mma_bf16_ss(tmem + S::TM_S, sdesc_advance(kd, off), sdesc_advance(qd, off), id_qk,
+                      k != 0);
         }
         mma_commit(&bar.s_full);
         return true;
@@ -343,12 +344,12 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         // the dP buffer holds dS^T of the previous pair until its dK MMA has read it
         if (g2 > 0 && !mbar_wait(&bar.dk_done, (g2 - 1) & 1, ab, a.status)) return false;
         tc_fence_after();
-        const uint32_t dob = stage_of(g2) + S::ST_DO;
+        const uint64_t dod = sdesc_sw128(stage_of(g2) + S::ST_DO, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + S::TM_DP, sdesc_sw128(vb + off, 16, 1024),
-                      sdesc_sw128(dob + off, 16, 1024), id_qk, k != 0);
+          mma_bf16_ss(tmem + S::TM_DP, sdesc_advance(vd, off), sdesc_advance(dod, off), id_qk,
+                      k != 0);
         }
         mma_commit(&bar.dp_full);
         return true;
@@ -381,6 +382,8 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int p = 0; p < np; ++p, ++gp) {
           const int st = gp % NSTAGE;
           const uint32_t sb = smem_u32(smem + S::OFF_RING + st * S::STAGE);
+          const uint64_t dod = sdesc_sw128(sb + S::ST_DO, GT * 128, 1024);
+          const uint64_t qd = sdesc_sw128(sb + S::ST_Q, GT * 128, 1024);
           // the stage's Q and dO have landed (it is released below, so this phase is current)
           if (!(ok = mbar_wait(&bar.full[st], (gp / NSTAGE) & 1, ab, a.status))) break;
           if (!(ok = mbar_wait(&bar.p_full, gp & 1, ab, a.status))) break;
@@ -391,7 +394,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int k = 0; k < GT / 16; ++k)                // dV += P^T dO
             mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + p_col(k),
-                        sdesc_sw128(sb + S::ST_DO + k * 2048, GT * 128, 1024), id_acc,
+                        sdesc_advance(dod, k * 2048), id_acc,
                         (p | k) != 0);
           mma_commit(&bar.dv_done);
           if (!(ok = mbar_wait(&bar.ds_full, gp & 1, ab, a.status))) break;
@@ -399,7 +402,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int k = 0; k < GT / 16; ++k)                // dK += dS^T Q
             mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + p_col(k),
-                        sdesc_sw128(sb + S::ST_Q + k * 2048, GT * 128, 1024), id_acc,
+                        sdesc_advance(qd, k * 2048), id_acc,
                         (p | k) != 0);
           mma_commit(&bar.dk_done);
           // S^T and dP^T of this pair completed before the math warps formed dS^T, and the

@@ -257,13 +257,14 @@ MARS_DEV bool s_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status))
       return false;
     tc_fence_after();
-    const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+    const uint64_t qd = sdesc_sw128(q, 16, 1024);
+    const uint64_t kd = sdesc_sw128(smem_u32(smem + S::OFF_K + st * S::KV_BYTES), 16, 1024);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
       const uint32_t koff = (k >> 2) * (BKV * 128) + (k & 3) * 32;
-      mma_bf16_ss(tmem + S::TMEM_S + sb * BKV, sdesc_sw128(q + off, 16, 1024),
-                  sdesc_sw128(kb + koff, 16, 1024), idesc_s, k != 0);
+      mma_bf16_ss(tmem + S::TMEM_S + sb * BKV, sdesc_advance(qd, off), sdesc_advance(kd, koff),
+                  idesc_s, k != 0);
     }
     mma_commit(&bar.s_full[sb]);
     mma_commit(&bar.k_empty[st]);      // K stage free once this QK^T completes
@@ -290,13 +291,13 @@ MARS_DEV bool pv_issuer(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
         !mbar_wait(&bar.o_free, (uint32_t)o_free_parity, ab, status))
       return false;
     tc_fence_after();
-    const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
+    // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
+    const uint64_t vd = sdesc_sw128(smem_u32(smem + S::OFF_V + st * S::KV_BYTES), BKV * 128, 1024);
 #pragma unroll
     for (int k = 0; k < BKV / 16; ++k) {
       // A = P [128 rows x 128 keys] in TMEM: row = lane, 16 keys = 8 columns per K step
       const uint32_t a = tmem + S::TMEM_S + pb * BKV + S::P_OFF + k * 8;
-      // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
-      const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
+      const uint64_t bd = sdesc_advance(vd, k * 2048);
       mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (jl | k) != 0);
     }
     mma_commit(&bar.pv_done[pb]);
@@ -324,13 +325,13 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     if (!mbar_wait(&bar.v_full[st], (j / VST) & 1, ab, status)) return false;
     if (!mbar_wait(&bar.p_full[pb], (j / NBUF) & 1, ab, status)) return false;
     tc_fence_after();
-    const uint32_t v = smem_u32(smem + S::OFF_V + st * S::KV_BYTES);
+    // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
+    const uint64_t vd = sdesc_sw128(smem_u32(smem + S::OFF_V + st * S::KV_BYTES), BKV * 128, 1024);
 #pragma unroll
     for (int k = 0; k < BKV / 16; ++k) {
       // A = P [128 rows x 128 keys] in TMEM: row = lane, 16 keys = 8 columns per K step
       const uint32_t a = tmem + S::TMEM_S + pb * BKV + S::P_OFF + k * 8;
-      // B = V [keys x D], MN-major: D/64 atoms of BKV*128 B, 8-key groups of 1024 B
-      const uint64_t bd = sdesc_sw128(v + k * 2048, BKV * 128, 1024);
+      const uint64_t bd = sdesc_advance(vd, k * 2048);
       mma_bf16_ts(tmem + S::TMEM_O, a, bd, idesc_o, (j | k) != 0);
     }
     mma_commit(&bar.pv_done[pb]);
@@ -343,13 +344,14 @@ MARS_DEV void mma_loop(Barriers& bar, uint8_t* smem, int ntiles, uint32_t tmem,
     // S buffer sb last held tile j-NBUF, whose P the PV of that tile read from it
     if (j >= NBUF && !mbar_wait(&bar.pv_done[sb], ((j / NBUF) - 1) & 1, ab, status)) return;
     tc_fence_after();
-    const uint32_t kb = smem_u32(smem + S::OFF_K + st * S::KV_BYTES);
+    const uint64_t qd = sdesc_sw128(q, 16, 1024);
+    const uint64_t kd = sdesc_sw128(smem_u32(smem + S::OFF_K + st * S::KV_BYTES), 16, 1024);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (BQ * 128) + (k & 3) * 32;
       const uint32_t koff = (k >> 2) * (BKV * 128) + (k & 3) * 32;
-      mma_bf16_ss(tmem + S::TMEM_S + sb * BKV, sdesc_sw128(q + off, 16, 1024),
-                  sdesc_sw128(kb + koff, 16, 1024), idesc_s, k != 0);
+      mma_bf16_ss(tmem + S::TMEM_S + sb * BKV, sdesc_advance(qd, off), sdesc_advance(kd, koff),
+                  idesc_s, k != 0);
     }
     mma_commit(&bar.s_full[sb]);
     mma_commit(&bar.k_empty[st]);      // K stage free once this QK^T completes

@@ -398,6 +398,12 @@ MARS_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on: only the start-address field
+// changes (shared-memory addresses stay below 256 KB, so the field does not carry).
+MARS_DEV uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, A K-major, B K- or MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
   return (1u << 4)                               // D format: f32
