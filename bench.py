@@ -41,8 +41,8 @@ METRIC = "decode-step µs & accepted tok/s; decode HBM GB/s; dual-stream attn TF
 # rows, decode attention on step 0 of the sustained workload, the dual-stream forward at
 # 2L = 8192. None whenever the kernel has changed since its capture.
 TRAFFIC_HEAD_GEMM = 1106390912         # head_gemm_pair_kernel, sustained decode, 2048 rows
-TRAFFIC_DECODE_STEP0 = 1365747200      # decode_tc_kernel, sustained decode, step 0
-TRAFFIC_DUAL_STREAM = 330313344        # dual_stream_persistent_kernel, 2L = 8192
+TRAFFIC_DECODE_STEP0 = 1366012672      # decode_tc_kernel, sustained decode, step 0
+TRAFFIC_DUAL_STREAM = 330302464        # dual_stream_persistent_kernel, 2L = 8192
 CFG = W.SUSTAINED_DECODE_7B
 DUAL = W.DUAL_STREAM_7B
 
