@@ -12,6 +12,8 @@
 //       S^T = K Q^T, dP^T = V dO^T            (keys on TMEM lanes, queries on columns)
 //       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM, bf16 over the
 //                                              fp32 columns they were formed from)
+//     each in two halves of 64 queries with barriers of their own, so that one half's
+//     S^T (or dP^T) of the next pair goes as soon as that half's dV (or dK) has read it.
 //     P^T = exp2(scale log2(e) S^T - lse) and dS^T are formed by two threads per key row
 //     (64 query columns each: with lse known, no row-wide exchange is needed). One thread
 //     issues S^T and dP^T (shared-memory operands), another dV and dK (A from TMEM), on
@@ -92,7 +94,8 @@ struct GSmem {
 struct GBar {
   uint64_t kv_full, kv_empty;
   uint64_t full[NSTAGE], empty[NSTAGE];
-  uint64_t s_full, dp_full, p_full, ds_full, dv_done, dk_done;
+  // per 64-query half of a pair: its S^T and dP^T MMAs, P^T and dS^T, its dV and dK MMAs
+  uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], dv_done[2], dk_done[2];
   uint64_t acc_full, acc_free, drain, drain_ts;
   uint32_t tmem_base;
   int abort;
@@ -238,12 +241,14 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(&bar.full[i], 1);
       mbar_init(&bar.empty[i], 1);
     }
-    mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.dp_full, 1);
-    mbar_init(&bar.p_full, MATH_THREADS);
-    mbar_init(&bar.ds_full, MATH_THREADS);
-    mbar_init(&bar.dv_done, 1);
-    mbar_init(&bar.dk_done, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&bar.s_full[h], 1);
+      mbar_init(&bar.dp_full[h], 1);
+      mbar_init(&bar.p_full[h], MATH_THREADS / 2);
+      mbar_init(&bar.ds_full[h], MATH_THREADS / 2);
+      mbar_init(&bar.dv_done[h], 1);
+      mbar_init(&bar.dk_done[h], 1);
+    }
     mbar_init(&bar.acc_full, 1);
     mbar_init(&bar.acc_free, MATH_THREADS);
     mbar_init(&bar.drain, 1);
@@ -321,37 +326,42 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
   } else if (warp == 1) {
     // ------------------------------------------------------- S^T and dP^T MMAs
     if (lane == 0) {
-      const uint32_t id_qk = idesc_ab(GT, GT, false, false);   // S^T, dP^T: K-major A, B
+      // S^T, dP^T: K-major A and B, one N = 64 group per 64-query half of the pair
+      const uint32_t id_qk = idesc_ab(GT, GT / 2, false, false);
       const uint64_t kd = sdesc_sw128(smem_u32(smem + S::OFF_K), 16, 1024);
       const uint64_t vd = sdesc_sw128(smem_u32(smem + S::OFF_V), 16, 1024);
       auto stage_of = [&](int g2) { return smem_u32(smem + S::OFF_RING + (g2 % NSTAGE) * S::STAGE); };
-      auto issue_st = [&](int g2) -> bool {            // S^T = K Q^T of pair g2
+      auto issue_st = [&](int g2) -> bool {            // S^T = K Q^T of pair g2, by halves
         if (!mbar_wait(&bar.full[g2 % NSTAGE], (g2 / NSTAGE) & 1, ab, a.status)) return false;
-        // the S buffer holds P^T of the previous pair until its dV MMA has read it
-        if (g2 > 0 && !mbar_wait(&bar.dv_done, (g2 - 1) & 1, ab, a.status)) return false;
-        tc_fence_after();
         const uint64_t qd = sdesc_sw128(stage_of(g2) + S::ST_Q, 16, 1024);
+        for (int h = 0; h < 2; ++h) {
+          // half h's S^T buffer holds its P^T of the previous pair until that dV has read it
+          if (g2 > 0 && !mbar_wait(&bar.dv_done[h], (g2 - 1) & 1, ab, a.status)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + S::TM_S, sdesc_advance(kd, off), sdesc_advance(qd, off), id_qk,
-                      k != 0);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
+            mma_bf16_ss(tmem + S::TM_S + (GT / 2) * h, sdesc_advance(kd, off),
+                        sdesc_advance(qd, off + h * (GT / 2) * 128), id_qk, k != 0);
+          }
+          mma_commit(&bar.s_full[h]);
         }
-        mma_commit(&bar.s_full);
         return true;
       };
-      auto issue_dp = [&](int g2) -> bool {            // dP^T = V dO^T of pair g2
-        // the dP buffer holds dS^T of the previous pair until its dK MMA has read it
-        if (g2 > 0 && !mbar_wait(&bar.dk_done, (g2 - 1) & 1, ab, a.status)) return false;
-        tc_fence_after();
+      auto issue_dp = [&](int g2) -> bool {            // dP^T = V dO^T of pair g2, by halves
         const uint64_t dod = sdesc_sw128(stage_of(g2) + S::ST_DO, 16, 1024);
+        for (int h = 0; h < 2; ++h) {
+          // half h's dP^T buffer holds its dS^T of the previous pair until that dK has read it
+          if (g2 > 0 && !mbar_wait(&bar.dk_done[h], (g2 - 1) & 1, ab, a.status)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
-          mma_bf16_ss(tmem + S::TM_DP, sdesc_advance(vd, off), sdesc_advance(dod, off), id_qk,
-                      k != 0);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * (GT * 128) + (k & 3) * 32;
+            mma_bf16_ss(tmem + S::TM_DP + (GT / 2) * h, sdesc_advance(vd, off),
+                        sdesc_advance(dod, off + h * (GT / 2) * 128), id_qk, k != 0);
+          }
+          mma_commit(&bar.dp_full[h]);
         }
-        mma_commit(&bar.dp_full);
         return true;
       };
       int gp = 0, ii = 0;
@@ -386,25 +396,32 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
           const uint64_t qd = sdesc_sw128(sb + S::ST_Q, GT * 128, 1024);
           // the stage's Q and dO have landed (it is released below, so this phase is current)
           if (!(ok = mbar_wait(&bar.full[st], (gp / NSTAGE) & 1, ab, a.status))) break;
-          if (!(ok = mbar_wait(&bar.p_full, gp & 1, ab, a.status))) break;
           // dV of the item starts from zero: the previous item's dV and dK must be read
           if (p == 0 && ii > 0 && !(ok = mbar_wait(&bar.acc_free, (ii - 1) & 1, ab, a.status)))
             break;
-          tc_fence_after();
+          for (int h = 0; h < 2 && ok; ++h) {              // dV += P^T dO, half h's queries
+            if (!(ok = mbar_wait(&bar.p_full[h], gp & 1, ab, a.status))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < GT / 16; ++k)                // dV += P^T dO
-            mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + p_col(k),
-                        sdesc_advance(dod, k * 2048), id_acc,
-                        (p | k) != 0);
-          mma_commit(&bar.dv_done);
-          if (!(ok = mbar_wait(&bar.ds_full, gp & 1, ab, a.status))) break;
-          tc_fence_after();
+            for (int kq = 0; kq < GT / 32; ++kq) {
+              const int k = (GT / 32) * h + kq;
+              mma_bf16_ts(tmem + S::TM_DV, tmem + S::TM_S + p_col(k),
+                          sdesc_advance(dod, k * 2048), id_acc, (p | k) != 0);
+            }
+            mma_commit(&bar.dv_done[h]);
+          }
+          for (int h = 0; h < 2 && ok; ++h) {              // dK += dS^T Q, half h's queries
+            if (!(ok = mbar_wait(&bar.ds_full[h], gp & 1, ab, a.status))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < GT / 16; ++k)                // dK += dS^T Q
-            mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + p_col(k),
-                        sdesc_advance(qd, k * 2048), id_acc,
-                        (p | k) != 0);
-          mma_commit(&bar.dk_done);
+            for (int kq = 0; kq < GT / 32; ++kq) {
+              const int k = (GT / 32) * h + kq;
+              mma_bf16_ts(tmem + S::TM_DK, tmem + S::TM_DP + p_col(k),
+                          sdesc_advance(qd, k * 2048), id_acc, (p | k) != 0);
+            }
+            mma_commit(&bar.dk_done[h]);
+          }
+          if (!ok) break;
           // S^T and dP^T of this pair completed before the math warps formed dS^T, and the
           // math warps have read the stage's lse and D rows: the stage is free after dK
           mma_commit(&bar.empty[st]);
@@ -446,7 +463,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         lo -= HC * half;
         hi -= HC * half;
         // P^T: exp2(scale log2e S - lse) on the visible query columns, 0 elsewhere
-        if (!(ok = warp_wait(&bar.s_full, gp & 1))) break;
+        if (!(ok = warp_wait(&bar.s_full[half], gp & 1))) break;
         tc_fence_after();
         uint32_t v[HC];
 #pragma unroll
@@ -481,9 +498,9 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_st32(tmem + S::TM_S + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(&bar.p_full);
+        mbar_arrive_warp(&bar.p_full[half]);
         // dS^T = P^T * (dP^T - D), over this half's own dP^T columns (the dK MMA's A)
-        if (!(ok = warp_wait(&bar.dp_full, gp & 1))) break;
+        if (!(ok = warp_wait(&bar.dp_full[half], gp & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < HC / 32; ++q)
@@ -507,7 +524,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_st32(tmem + S::TM_DP + HC * half + lane_off, *reinterpret_cast<uint32_t(*)[32]>(pp));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(&bar.ds_full);
+        mbar_arrive_warp(&bar.ds_full[half]);
       }
       if (!ok) break;
       // the item's dV and dK rows (this thread's half of the columns), added to dV and dK
