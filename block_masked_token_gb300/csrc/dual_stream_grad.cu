@@ -112,20 +112,49 @@ struct GArgs {
 };
 
 // Work item: keys [128 jt, 128 jt + 128) of stream ks (0 clean, 1 masked) of (b, kvh),
-// against query head kvh*G + g. Ids run over clean key tiles from the first (seen by most
-// query tiles) to the last, then over the masked key tiles.
+// against query heads kvh*G + g, g in [g0, g0 + ng). A clean key tile is one item per query
+// head. A masked key tile is seen only by the query tiles of its own block (one or two when
+// B <= 128); there one item takes all G heads of the kv group, so that its K and V are
+// loaded, and its dK and dV drained, once for the group instead of once per head. Ids run
+// over the clean key tiles from the first (seen by most query tiles) to the last, then over
+// the masked key tiles.
 struct GItem {
-  int b, kvh, g, ks, jt;
-  int nc, mlo, npg;        // clean keys: clean query tiles [jt, nt), masked [mlo, nt)
+  int b, kvh, g0, ng, ks, jt;
+  int nc, mlo;             // per head: clean query tiles [jt, nt), masked [mlo, nt)
+  int np1, npg;            // pairs per head, pairs of the item (ng * np1)
 };
+
+__host__ __device__ inline bool grad_group_masked(int B) { return B <= GT; }
+
+__host__ __device__ inline long long grad_item_count(int batch, int hkv, int G, int nt, int B) {
+  const long long per = (long long)batch * hkv * G;
+  return per * nt + (grad_group_masked(B) ? (long long)batch * hkv : per) * nt;
+}
 
 MARS_DEV GItem grad_item(const GArgs& a, int id) {
   GItem it;
   const int per = a.batch * a.hkv * a.G;
-  const int kt = id / per;
-  int bk = id % per;
-  it.g = bk % a.G;
-  bk /= a.G;
+  int kt, bk;
+  if (id < a.nt * per) {
+    kt = id / per;
+    bk = id % per;
+    it.g0 = bk % a.G;
+    it.ng = 1;
+    bk /= a.G;
+  } else if (grad_group_masked(a.B)) {
+    const int r = id - a.nt * per, pm = a.batch * a.hkv;
+    kt = a.nt + r / pm;
+    bk = r % pm;
+    it.g0 = 0;
+    it.ng = a.G;
+  } else {
+    const int r = id - a.nt * per;
+    kt = a.nt + r / per;
+    bk = r % per;
+    it.g0 = bk % a.G;
+    it.ng = 1;
+    bk /= a.G;
+  }
   it.b = bk % a.batch;
   it.kvh = bk / a.batch;
   if (kt < a.nt) {
@@ -135,7 +164,7 @@ MARS_DEV GItem grad_item(const GArgs& a, int id) {
     // masked row t sees clean key k iff its block start (t/B)*B > k: t >= (k/B + 1) B
     const int tmin = (GT * kt / a.B + 1) * a.B;
     it.mlo = tmin <= a.L - 1 ? tmin / GT : a.nt;
-    it.npg = it.nc + (a.nt - it.mlo);
+    it.np1 = it.nc + (a.nt - it.mlo);
   } else {
     it.ks = 1;
     it.jt = kt - a.nt;
@@ -144,19 +173,21 @@ MARS_DEV GItem grad_item(const GArgs& a, int id) {
     const int tmax = min(a.L, (umax / a.B + 1) * a.B) - 1;
     it.nc = 0;
     it.mlo = it.jt;
-    it.npg = tmax / GT - it.jt + 1;
+    it.np1 = tmax / GT - it.jt + 1;
   }
+  it.npg = it.ng * it.np1;
   return it;
 }
 
-// Pair p of an item: query stream qs, query tile qi.
+// Pair p of an item: query head kvh*G + g, query stream qs, query tile qi.
 struct GPair {
-  int qs, qi;
+  int g, qs, qi;
 };
 
 MARS_DEV GPair grad_pair(const GItem& it, int p) {
   GPair q;
-  const int r = p;
+  q.g = it.g0 + p / it.np1;
+  const int r = p % it.np1;
   if (r < it.nc) {
     q.qs = 0;
     q.qi = it.jt + r;
@@ -264,7 +295,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = __shfl_sync(0xffffffffu, bar.tmem_base, 0);
 
-  const int total = a.batch * a.hkv * a.G * 2 * a.nt;
+  const int total = (int)grad_item_count(a.batch, a.hkv, a.G, a.nt, a.B);
   const int G = gridDim.x, c = blockIdx.x;
   auto item_id = [&](int r) { return r * G + ((r & 1) ? G - 1 - c : c); };
   const int rounds = (total + G - 1) / G;
@@ -299,7 +330,7 @@ dual_grad_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) ok = mbar_wait(&bar.empty[st], ((gp / NSTAGE) & 1) ^ 1, ab, a.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        const int h = it.kvh * a.G + it.g;
+        const int h = it.kvh * a.G + pr.g;
         if (lane == 0) {
           // lse and D of the tile's 128 rows (one padded row block each), then Q and dO
           const size_t rb = (((size_t)it.b * a.hq + h) * 2 + pr.qs) * (size_t)(GT * a.nt) +
@@ -622,7 +653,7 @@ cudaError_t launch_grad_tc(const uint16_t* q, const uint16_t* k, const uint16_t*
   static std::atomic<int> attr[64];
   const cudaError_t ea = set_smem_limit_once(dual_grad_kernel<D>, S::TOTAL, attr);
   if (ea != cudaSuccess) return ea;
-  const long long items = (long long)batch * hq * 2 * a.nt;
+  const long long items = grad_item_count(batch, hkv, hq / hkv, a.nt, B);
   const long long ctas = std::min<long long>(items, num_sms());
   dual_grad_kernel<D><<<(unsigned)ctas, GRAD_THREADS, S::TOTAL, stream>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();
