@@ -5,8 +5,10 @@
 // With P = softmax(scale * S + M), S = Q K^T, and D_i = rowsum(dO_i * O_i):
 //   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),   dK = scale dS^T Q,   dQ = scale dS K.
 // Two tcgen05 kernels, neither storing a score block:
-//   - dual_grad_kernel (here): a work item is (batch, query head, 128-key tile of one
-//     stream); one persistent CTA per SM runs items heaviest first. The item visits every
+//   - dual_grad_kernel (here): a work item is (batch, query head, 128-key tile of the
+//     clean stream), or (batch, kv head, 128-key tile of the masked stream) for all query
+//     heads of the kv group (see GItem); one persistent CTA per SM runs items heaviest
+//     first. The item visits every
 //     128-row query tile that sees one of its keys under M, and per (key tile, query tile)
 //     pair runs four MMAs with TMEM accumulators:
 //       S^T = K Q^T, dP^T = V dO^T            (keys on TMEM lanes, queries on columns)
