@@ -8,9 +8,8 @@
 //   - dual_grad_kernel (here): a work item is (batch, query head, 128-key tile of the
 //     clean stream), or (batch, kv head, 128-key tile of the masked stream) for all query
 //     heads of the kv group (see GItem); one persistent CTA per SM runs items heaviest
-//     first. The item visits every
-//     128-row query tile that sees one of its keys under M, and per (key tile, query tile)
-//     pair runs four MMAs with TMEM accumulators:
+//     first. The item visits every 128-row query tile that sees one of its keys under M,
+//     and per (key tile, query tile) pair runs four MMAs with TMEM accumulators:
 //       S^T = K Q^T, dP^T = V dO^T            (keys on TMEM lanes, queries on columns)
 //       dV += P^T dO, dK += dS^T Q            (A = P^T / dS^T from TMEM, bf16 over the
 //                                              fp32 columns they were formed from)
